@@ -1,0 +1,213 @@
+/*
+ * int8mp.h -- C ABI of the GB300 (sm_103a) INT8 mixed-precision linear-layer
+ * library (libint8mp.so).
+ *
+ * The method ("Quantized model training" README, section "INT8 mixed
+ * precision training"; "Integrate INT8 mixed-precision from torchao 0.7",
+ * discussion): every matmul of a linear layer -- forward, backward grad-input,
+ * backward grad-weight -- dynamically quantizes both bf16 operands row-wise
+ * along its contraction axis to INT8 codes with one fp32 scale per row,
+ * multiplies the codes with int32 accumulation, and scales the product back to
+ * bf16.  Weights and activations stay bf16 outside the matmul.
+ *
+ * Arithmetic (identical on every entry point):
+ *   scale s   = fp32(max |x| over the group) / 127       (IEEE division)
+ *   code q    = clamp(round(x / s), -127, 127)           (IEEE division)
+ *               round = nearest-even (INT8MP_RNE) or stochastic (INT8MP_SR);
+ *               an all-zero group has s = 0 and all codes 0
+ *   acc[i,j]  = sum_k qA[i,k] * qB[j,k]                   (exact int32)
+ *   out[i,j]  = bf16_RNE((fp32_RN(acc) * sA[i]) * sB[j])
+ * Stochastic rounding: v = x/s, f = floor(v), q = f + (u < v - f) with
+ *   u = (w >> 8) * 2^-24 and w word (n & 3) of Philox4x32-10 (Salmon et al.,
+ *   SC'11) at counter (lo32(n>>2), hi32(n>>2), stream_id, 0) and key
+ *   (lo32(seed), hi32(seed)), n = offset + (r * cols + c) for source element
+ *   (r, c).  Results therefore do not depend on the kernels' tiling.
+ *
+ * Hardware note: sm_103a has no INT8 tcgen05 MMA, and its legacy INT8 tensor
+ * path is an order of magnitude slower than its f16 path.  The library keeps
+ * the INT8 codes and the exact int32 accumulator of the method, but performs
+ * the contraction on the f16 tensor cores: codes in [-127, 127] are exact
+ * fp16 values, every product is exact, and fp32 partial sums are exact while
+ * below 2^24, so the reduction runs in chunks of at most 1024 and each
+ * chunk's sum is added into an int32 total.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are device pointers unless stated; the caller owns every
+ *     buffer.  Nothing here allocates device memory.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
+ *     enqueued asynchronously on it; no entry point synchronizes the host.
+ *   - bf16 tensors are raw 16-bit bf16 arrays, row-major.
+ *   - Host-detected errors return before anything is launched.  Errors of
+ *     the launch itself return INT8MP_ERR_CUDA.  A device-side wait that ran
+ *     out (every wait in the GEMM is bounded) is recorded in a device status
+ *     word, read back by int8mp_poll_device_status().
+ *   - Only sm_103 devices are accepted (INT8MP_ERR_UNSUPPORTED_DEVICE).
+ *   - Entry points may be called from several host threads on different
+ *     streams.
+ */
+#ifndef INT8MP_H
+#define INT8MP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  INT8MP_OK = 0,
+  INT8MP_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, bad size     */
+  INT8MP_ERR_ALIGNMENT = 2,          /* pointer / leading-dim / size rule    */
+  INT8MP_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103         */
+  INT8MP_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed    */
+  INT8MP_ERR_TIMEOUT = 5,            /* a bounded device-side wait ran out   */
+  INT8MP_ERR_WORKSPACE = 6           /* workspace too small                  */
+} int8mp_status;
+
+typedef enum { INT8MP_RNE = 0, INT8MP_SR = 1 } int8mp_round;
+
+/* Operand layouts, named as in the README's matmul benchmark tables. */
+typedef enum {
+  INT8MP_AxBT = 0, /* A [M,K] row-major, B [N,K] row-major  (A @ B.T) */
+  INT8MP_AxB = 1,  /* A [M,K] row-major, B [K,N] row-major  (A @ B)   */
+  INT8MP_ATxB = 2  /* A [K,M] row-major, B [K,N] row-major  (A.T @ B) */
+} int8mp_layout;
+
+/* Storage of INT8 codes.  INT8MP_CODES_S8: one int8_t per code.
+ * INT8MP_CODES_F16: one IEEE binary16 per code holding the same integer
+ * exactly; this is the container the tensor-core GEMM reads directly. */
+typedef enum { INT8MP_CODES_S8 = 0, INT8MP_CODES_F16 = 1 } int8mp_codes;
+
+/* Stochastic-rounding stream ids used by the linear entry points, one per
+ * quantization of a training step, so that the same tensor quantized in two
+ * passes is rounded independently. */
+enum {
+  INT8MP_STREAM_FWD_X = 0, INT8MP_STREAM_FWD_W = 1,
+  INT8MP_STREAM_GI_DY = 2, INT8MP_STREAM_GI_W = 3,
+  INT8MP_STREAM_GW_DY = 4, INT8MP_STREAM_GW_X = 5
+};
+
+/* Largest contraction length: 127 * 127 * K must stay below 2^31. */
+#define INT8MP_MAX_K 133143
+
+/*
+ * int8mp_quantize_rowwise -- dynamic symmetric row-wise quantization
+ * ("Quantized model training" README, "INT8 mixed precision training":
+ * dynamic row-wise quantization; "Add QAT support for distributed
+ * finetuning", summary: x_q = clamp(x / scale + zp), here zp = 0).
+ *
+ *   x       bf16 [rows, cols], row stride `ld` elements (ld >= cols).
+ *   axis    0: one group per row (along cols).  Codes q [rows, cols]
+ *              (row stride cols), scale [rows].
+ *           1: one group per column (along rows).  Codes written transposed,
+ *              q [cols, rows] (row stride rows), scale [cols]; this puts the
+ *              contraction axis innermost for the matmul.
+ *   mode    INT8MP_RNE or INT8MP_SR; seed, offset, stream_id are used by SR
+ *           only (see the header comment for the counter mapping).
+ *   q       output codes, int8_t or binary16 per `codes`.
+ *   scale   output fp32 scales.
+ * Requirements: rows, cols >= 0 (either may be 0: nothing is launched);
+ * cols % 8 == 0, ld % 8 == 0 and x 16-byte aligned (128-bit loads); for
+ * axis 1 also rows % 8 == 0 (128-bit stores of the transposed codes); q 16-byte
+ * aligned; scale 4-byte aligned.  Violations return INT8MP_ERR_ALIGNMENT.
+ */
+int8mp_status int8mp_quantize_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                      int axis, int8mp_round mode, uint64_t seed,
+                                      uint64_t offset, uint32_t stream_id, void* q,
+                                      int8mp_codes codes, float* scale, void* stream);
+
+/*
+ * int8mp_scaled_mm -- scaled INT8 matmul ("Quantized model training" README,
+ * matmul benchmark tables A @ B.T, A @ B, A.T @ B; "Integrate INT8
+ * mixed-precision from torchao 0.7": the INT8 product is scaled back to BF16).
+ *
+ *   out[i,j] = bf16_RNE((fp32_RN(sum_k a(i,k) b(j,k)) * sA[i]) * sB[j])
+ *
+ *   A, B    INT8 codes in the container `codes`, stored per `layout`.  The
+ *           tensor-core path reads K-major operands (INT8MP_AxBT); for AxB and
+ *           ATxB the caller quantizes the K-major operand with axis 1 of
+ *           int8mp_quantize_rowwise, which writes it transposed, and passes
+ *           INT8MP_AxBT.  Other layouts return INT8MP_ERR_INVALID_ARG.
+ *   sA      fp32 [M], sB fp32 [N].
+ *   out     bf16 [M, N], row stride ldo elements (ldo >= N).
+ * Requirements: M, N >= 0; 16 <= K <= INT8MP_MAX_K; K % 16 == 0 (when M or N
+ * is 0 nothing is launched); A, B 16-byte aligned; N % 8 == 0, ldo % 8 == 0
+ * and out 16-byte aligned (128-bit stores).  M and N need not be tile
+ * multiples.  codes must be INT8MP_CODES_F16.
+ */
+int8mp_status int8mp_scaled_mm(const void* A, const float* sA, const void* B, const float* sB,
+                               int64_t M, int64_t N, int64_t K, int8mp_layout layout,
+                               int8mp_codes codes, void* out, int64_t ldo, void* stream);
+
+/*
+ * int8mp_mm_s32 -- the exact integer product alone: acc[i,j] = sum_k
+ * a(i,k) b(j,k) as int32, out int32 [M, N] with row stride ldo.  Same operand
+ * rules as int8mp_scaled_mm.  Exposes the int32 accumulator so that it can be
+ * compared bit for bit.
+ */
+int8mp_status int8mp_mm_s32(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                            int8mp_layout layout, int8mp_codes codes, int32_t* out,
+                            int64_t ldo, void* stream);
+
+/*
+ * Per-pass configuration of a linear layer (the pages' per-matmul INT8
+ * switches and stochastic-rounding switch; "Quantized model training"
+ * README, INT8 mixed precision training table).  This build implements the
+ * INT8 passes: each int8_* flag must be 1 (0 returns INT8MP_ERR_INVALID_ARG).
+ */
+typedef struct {
+  int int8_fwd;
+  int int8_grad_in;
+  int int8_grad_w;
+  int8mp_round mode;
+  uint64_t seed;
+  uint64_t offset;
+} int8mp_linear_cfg;
+
+/* Bytes of device workspace int8mp_linear_fwd / int8mp_linear_bwd need for
+ * these sizes (codes and scales of the quantized operands, 256-byte aligned
+ * sub-buffers).  Returns 0 for invalid sizes. */
+size_t int8mp_linear_workspace_size(int64_t T, int64_t N, int64_t K,
+                                    const int8mp_linear_cfg* cfg);
+
+/*
+ * int8mp_linear_fwd -- Y [T,N] = X [T,K] . W [N,K]^T: X and W quantized
+ * along K (SR streams 0 and 1), scaled matmul, bf16 out.
+ * Requirements: T >= 0, N >= 0, K >= 16; K % 16 == 0, N % 16 == 0,
+ * T % 16 == 0; all pointers 16-byte aligned; workspace at least
+ * int8mp_linear_workspace_size() bytes (INT8MP_ERR_WORKSPACE otherwise).
+ */
+int8mp_status int8mp_linear_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t N,
+                                int64_t K, const int8mp_linear_cfg* cfg, void* workspace,
+                                size_t ws_bytes, void* stream);
+
+/*
+ * int8mp_linear_bwd -- grad-input dX [T,K] = dY [T,N] . W [N,K] (dY along N
+ * by rows, W along N by columns; SR streams 2 and 3) and grad-weight
+ * dW [N,K] = dY^T . X (dY and X along T by columns; SR streams 4 and 5).
+ * dX or dW may be NULL to skip that pass.  Nothing from the forward pass is
+ * reused: both operands are re-quantized from bf16.  Same requirements as
+ * int8mp_linear_fwd.
+ */
+int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, void* dX,
+                                void* dW, int64_t T, int64_t N, int64_t K,
+                                const int8mp_linear_cfg* cfg, void* workspace, size_t ws_bytes,
+                                void* stream);
+
+/* Synchronizes `stream`, then returns and clears the device status word of
+ * the current device: INT8MP_ERR_TIMEOUT if a bounded device wait ran out
+ * since the last poll, INT8MP_ERR_CUDA if the stream reports an error,
+ * INT8MP_OK otherwise. */
+int8mp_status int8mp_poll_device_status(void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* int8mp_status_string(int8mp_status status);
+
+/* Library version as 10000 * major + 100 * minor + patch. */
+int int8mp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* INT8MP_H */

@@ -1,0 +1,33 @@
+/*
+ * int8mp_debug.h -- test-only entry points of libint8mp.so.  Not needed to
+ * use the library; they exist so that the failure paths can be exercised
+ * without faulting or hanging a GPU.
+ */
+#ifndef INT8MP_DEBUG_H
+#define INT8MP_DEBUG_H
+
+#include "int8mp.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Runs the int32 product of int8mp_mm_s32 (INT8MP_AxBT, INT8MP_CODES_F16)
+ * with one deliberate defect injected from the host: the first tile load of
+ * the first CTA is never issued, so the tensor-core warp's bounded wait for
+ * it runs out after `wait_limit_ms` milliseconds (1..5000).  The kernel then
+ * records INT8MP_ERR_TIMEOUT in the device status word, lets its other warps
+ * wind down, waits for its outstanding copies, frees its tensor memory and
+ * returns; the CUDA context stays usable.  Returns INT8MP_OK if the launch
+ * was enqueued; the timeout itself is reported by int8mp_poll_device_status.
+ * Outputs of the first CTA's tiles are left unwritten.
+ */
+int8mp_status int8mp_debug_mm_s32_drop_first_load(const void* A, const void* B, int64_t M,
+                                                  int64_t N, int64_t K, int32_t* out,
+                                                  int64_t ldo, int wait_limit_ms, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* INT8MP_DEBUG_H */

@@ -1,0 +1,218 @@
+"""Thin ctypes binding of libint8mp.so (include/int8mp.h).
+
+Names follow the C entry points.  This module only marshals arguments:
+torch supplies device memory and the current CUDA stream, and every step of
+the computation runs in the library's CUDA kernels.  There is no fallback:
+if the library is missing or the device is not sm_103, calls raise.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+# ---- constants mirrored from include/int8mp.h -----------------------------
+INT8MP_OK = 0
+INT8MP_ERR_INVALID_ARG = 1
+INT8MP_ERR_ALIGNMENT = 2
+INT8MP_ERR_UNSUPPORTED_DEVICE = 3
+INT8MP_ERR_CUDA = 4
+INT8MP_ERR_TIMEOUT = 5
+INT8MP_ERR_WORKSPACE = 6
+
+INT8MP_RNE, INT8MP_SR = 0, 1
+INT8MP_AxBT, INT8MP_AxB, INT8MP_ATxB = 0, 1, 2
+INT8MP_CODES_S8, INT8MP_CODES_F16 = 0, 1
+(INT8MP_STREAM_FWD_X, INT8MP_STREAM_FWD_W, INT8MP_STREAM_GI_DY, INT8MP_STREAM_GI_W,
+ INT8MP_STREAM_GW_DY, INT8MP_STREAM_GW_X) = range(6)
+INT8MP_MAX_K = 133143
+
+# every symbol the public headers declare
+EXPORTED = (
+    "int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
+    "int8mp_linear_workspace_size", "int8mp_linear_fwd", "int8mp_linear_bwd",
+    "int8mp_poll_device_status", "int8mp_status_string", "int8mp_version",
+    "int8mp_debug_mm_s32_drop_first_load",
+)
+
+
+class Int8mpError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {int8mp_status_string(status)} (status {status})")
+
+
+class int8mp_linear_cfg(ctypes.Structure):
+    _fields_ = [("int8_fwd", ctypes.c_int), ("int8_grad_in", ctypes.c_int),
+                ("int8_grad_w", ctypes.c_int), ("mode", ctypes.c_int),
+                ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
+
+
+def linear_cfg(mode=INT8MP_RNE, seed=0, offset=0):
+    return int8mp_linear_cfg(1, 1, 1, int(mode), int(seed), int(offset))
+
+
+_lib = None
+_P, _I64, _U64, _U32, _INT, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64,
+                                   ctypes.c_uint32, ctypes.c_int, ctypes.c_size_t)
+
+
+def library_path():
+    return _build.LIB
+
+
+def load(path=None):
+    """Load libint8mp.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libint8mp.so is not built ({path}); run int8_mixed_precision_row_gb300."
+                           "build.build() or __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    L.int8mp_quantize_rowwise.argtypes = [_P, _I64, _I64, _I64, _INT, _INT, _U64, _U64, _U32, _P,
+                                          _INT, _P, _P]
+    L.int8mp_scaled_mm.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _I64, _P]
+    L.int8mp_mm_s32.argtypes = [_P, _P, _I64, _I64, _I64, _INT, _INT, _P, _I64, _P]
+    L.int8mp_linear_workspace_size.argtypes = [_I64, _I64, _I64, ctypes.POINTER(int8mp_linear_cfg)]
+    L.int8mp_linear_workspace_size.restype = _SZ
+    L.int8mp_linear_fwd.argtypes = [_P, _P, _P, _I64, _I64, _I64, ctypes.POINTER(int8mp_linear_cfg),
+                                    _P, _SZ, _P]
+    L.int8mp_linear_bwd.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64,
+                                    ctypes.POINTER(int8mp_linear_cfg), _P, _SZ, _P]
+    L.int8mp_poll_device_status.argtypes = [_P]
+    L.int8mp_status_string.argtypes = [_INT]
+    L.int8mp_status_string.restype = ctypes.c_char_p
+    L.int8mp_version.argtypes = []
+    L.int8mp_debug_mm_s32_drop_first_load.argtypes = [_P, _P, _I64, _I64, _I64, _P, _I64, _INT, _P]
+    for name in ("int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
+                 "int8mp_linear_fwd", "int8mp_linear_bwd", "int8mp_poll_device_status",
+                 "int8mp_version", "int8mp_debug_mm_s32_drop_first_load"):
+        getattr(L, name).restype = _INT
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status, what):
+    if status != INT8MP_OK:
+        raise Int8mpError(status, what)
+
+
+def _code_dtype(codes):
+    return torch.int8 if codes == INT8MP_CODES_S8 else torch.float16
+
+
+def int8mp_status_string(status):
+    return load().int8mp_status_string(int(status)).decode()
+
+
+def int8mp_version():
+    return load().int8mp_version()
+
+
+def int8mp_quantize_rowwise(x, axis=0, mode=INT8MP_RNE, seed=0, offset=0, stream_id=0,
+                            codes=INT8MP_CODES_S8, cols=None, q=None, scale=None, stream=None):
+    """x: bf16 CUDA tensor [rows, ld] (row stride ld).  Returns (codes, scale);
+    axis 0 codes are [rows, cols], axis 1 codes are [cols, rows]."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda
+    rows = x.shape[0]
+    ld = x.stride(0) if rows > 0 else x.shape[1]
+    cols = x.shape[1] if cols is None else cols
+    groups, glen = (rows, cols) if axis == 0 else (cols, rows)
+    if q is None:
+        q = torch.empty((groups, glen), dtype=_code_dtype(codes), device=x.device)
+    if scale is None:
+        scale = torch.empty((groups,), dtype=torch.float32, device=x.device)
+    _check(load().int8mp_quantize_rowwise(_ptr(x), rows, cols, ld, int(axis), int(mode), int(seed),
+                                          int(offset), int(stream_id), _ptr(q), int(codes),
+                                          _ptr(scale), _stream(stream)), "int8mp_quantize_rowwise")
+    return q, scale
+
+
+def int8mp_scaled_mm(A, sA, B, sB, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, out=None,
+                     stream=None):
+    """A [M,K], B [N,K] codes (f16 containers), sA [M], sB [N] -> bf16 [M,N]."""
+    M, K = A.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    ldo = out.stride(0) if M > 0 else N
+    _check(load().int8mp_scaled_mm(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), M, N, K, int(layout),
+                                   int(codes), _ptr(out), ldo, _stream(stream)), "int8mp_scaled_mm")
+    return out
+
+
+def int8mp_mm_s32(A, B, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, out=None, stream=None):
+    M, K = A.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=A.device)
+    ldo = out.stride(0) if M > 0 else N
+    _check(load().int8mp_mm_s32(_ptr(A), _ptr(B), M, N, K, int(layout), int(codes), _ptr(out), ldo,
+                                _stream(stream)), "int8mp_mm_s32")
+    return out
+
+
+def int8mp_linear_workspace_size(T, N, K, cfg=None):
+    cfg = cfg or linear_cfg()
+    return int(load().int8mp_linear_workspace_size(T, N, K, ctypes.byref(cfg)))
+
+
+def _workspace(T, N, K, cfg, workspace, device):
+    need = int8mp_linear_workspace_size(T, N, K, cfg)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def int8mp_linear_fwd(X, W, cfg=None, Y=None, workspace=None, stream=None):
+    """Y [T,N] = X [T,K] . W [N,K]^T in INT8 mixed precision."""
+    cfg = cfg or linear_cfg()
+    T, K = X.shape
+    N = W.shape[0]
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.bfloat16, device=X.device)
+    ws, nbytes = _workspace(T, N, K, cfg, workspace, X.device)
+    _check(load().int8mp_linear_fwd(_ptr(X), _ptr(W), _ptr(Y), T, N, K, ctypes.byref(cfg), _ptr(ws),
+                                    nbytes, _stream(stream)), "int8mp_linear_fwd")
+    return Y
+
+
+def int8mp_linear_bwd(dY, X, W, cfg=None, dX=None, dW=None, want_dx=True, want_dw=True,
+                      workspace=None, stream=None):
+    """dX [T,K] = dY . W and dW [N,K] = dY^T . X in INT8 mixed precision."""
+    cfg = cfg or linear_cfg()
+    T, K = X.shape
+    N = W.shape[0]
+    if want_dx and dX is None:
+        dX = torch.empty((T, K), dtype=torch.bfloat16, device=X.device)
+    if want_dw and dW is None:
+        dW = torch.empty((N, K), dtype=torch.bfloat16, device=X.device)
+    ws, nbytes = _workspace(T, N, K, cfg, workspace, X.device)
+    _check(load().int8mp_linear_bwd(_ptr(dY), _ptr(X), _ptr(W), _ptr(dX if want_dx else None),
+                                    _ptr(dW if want_dw else None), T, N, K, ctypes.byref(cfg),
+                                    _ptr(ws), nbytes, _stream(stream)), "int8mp_linear_bwd")
+    return (dX if want_dx else None), (dW if want_dw else None)
+
+
+def int8mp_poll_device_status(stream=None):
+    return load().int8mp_poll_device_status(_stream(stream))
+
+
+def int8mp_debug_mm_s32_drop_first_load(A, B, out, wait_limit_ms=200, stream=None):
+    M, K = A.shape
+    N = B.shape[0]
+    return load().int8mp_debug_mm_s32_drop_first_load(_ptr(A), _ptr(B), M, N, K, _ptr(out),
+                                                      out.stride(0), int(wait_limit_ms),
+                                                      _stream(stream))

@@ -1,0 +1,352 @@
+// api.cu -- the extern "C" entry points of libint8mp.so (declared in
+// include/int8mp.h and include/int8mp_debug.h): argument validation,
+// per-device state, workspace carving and the composition of the linear
+// forward / backward passes out of the quantize and GEMM launchers.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/int8mp.h"
+#include "../../include/int8mp_debug.h"
+#include "common.cuh"
+
+namespace {
+
+using int8mp::DeviceInfo;
+
+// Bit 0 set by any kernel whose bounded wait ran out.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int8mp_status status = INT8MP_OK;
+  DeviceInfo info;
+};
+DeviceState g_devices[kMaxDevices];
+
+int8mp_status current_device(DeviceInfo* info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return INT8MP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return INT8MP_ERR_UNSUPPORTED_DEVICE;
+  DeviceState& st = g_devices[dev];
+  std::call_once(st.once, [&st, dev] {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      st.status = INT8MP_ERR_CUDA;
+      return;
+    }
+    if (major != 10 || minor != 3) {
+      st.status = INT8MP_ERR_UNSUPPORTED_DEVICE;
+      return;
+    }
+    void* word = nullptr;
+    if (cudaGetSymbolAddress(&word, g_status_word) != cudaSuccess) {
+      st.status = INT8MP_ERR_CUDA;
+      return;
+    }
+    st.info.sms = sms;
+    st.info.status_word = static_cast<unsigned int*>(word);
+    st.status = INT8MP_OK;
+  });
+  if (st.status == INT8MP_OK) *info = st.info;
+  return st.status;
+}
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+inline int8mp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? INT8MP_OK : INT8MP_ERR_CUDA; }
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// ------------------------------------------------------------ validation
+int8mp_status check_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int axis,
+                             int8mp_round mode, const void* q, int8mp_codes codes,
+                             const float* scale) {
+  if (axis != 0 && axis != 1) return INT8MP_ERR_INVALID_ARG;
+  if (mode != INT8MP_RNE && mode != INT8MP_SR) return INT8MP_ERR_INVALID_ARG;
+  if (codes != INT8MP_CODES_S8 && codes != INT8MP_CODES_F16) return INT8MP_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ld < cols) return INT8MP_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return INT8MP_OK;
+  if (!x || !q || !scale) return INT8MP_ERR_INVALID_ARG;
+  if (axis == 1 && rows > 65535ll * 256) return INT8MP_ERR_INVALID_ARG;
+  if (rows > (int64_t{1} << 31) - 1) return INT8MP_ERR_INVALID_ARG;
+  if (cols % 8 || ld % 8 || !aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4))
+    return INT8MP_ERR_ALIGNMENT;
+  if (axis == 1 && rows % 8) return INT8MP_ERR_ALIGNMENT;
+  return INT8MP_OK;
+}
+
+int8mp_status check_mm(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                       int8mp_layout layout, int8mp_codes codes, const void* out, int64_t ldo) {
+  if (layout != INT8MP_AxBT && layout != INT8MP_AxB && layout != INT8MP_ATxB)
+    return INT8MP_ERR_INVALID_ARG;
+  if (codes != INT8MP_CODES_S8 && codes != INT8MP_CODES_F16) return INT8MP_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || K > INT8MP_MAX_K || ldo < N) return INT8MP_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX) return INT8MP_ERR_INVALID_ARG;
+  // the tensor-core path reads K-major f16 containers
+  if (layout != INT8MP_AxBT || codes != INT8MP_CODES_F16) return INT8MP_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return INT8MP_OK;
+  if (!out || (K > 0 && (!A || !B))) return INT8MP_ERR_INVALID_ARG;
+  if (K % 16 || N % 8 || ldo % 8 || !aligned(out, 16)) return INT8MP_ERR_ALIGNMENT;
+  if (K > 0 && (!aligned(A, 16) || !aligned(B, 16))) return INT8MP_ERR_ALIGNMENT;
+  return INT8MP_OK;
+}
+
+int8mp_status run_mm(const void* A, const float* sA, const void* B, const float* sB, int64_t M,
+                     int64_t N, int64_t K, int8mp::GemmOut mode, void* out, int64_t ldo,
+                     const int8mp::GemmDebug& dbg, cudaStream_t stream) {
+  if (M == 0 || N == 0) return INT8MP_OK;
+  DeviceInfo dev;
+  int8mp_status st = current_device(&dev);
+  if (st != INT8MP_OK) return st;
+  const size_t esize = mode == int8mp::GemmOut::kS32 ? 4 : 2;
+  if (K == 0)  // empty contraction: every accumulator is 0, and so is 0 * sA * sB
+    return from_cuda(cudaMemset2DAsync(out, static_cast<size_t>(ldo) * esize, 0,
+                                       static_cast<size_t>(N) * esize, static_cast<size_t>(M),
+                                       stream));
+  return from_cuda(int8mp::launch_gemm(A, sA, B, sB, M, N, K, mode, out, ldo, dev, dbg, stream));
+}
+
+// ------------------------------------------------------------- workspace
+constexpr size_t kAlign = 256;
+inline size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Carver {
+  char* base;
+  size_t used = 0;
+  void* take(size_t bytes) {
+    void* p = base ? base + used : nullptr;
+    used += round_up(bytes);
+    return p;
+  }
+};
+
+// f16 codes + fp32 scales of one quantized operand
+struct QOperand {
+  void* q;
+  float* s;
+};
+inline QOperand carve_operand(Carver& c, int64_t groups, int64_t glen) {
+  QOperand o;
+  o.q = c.take(static_cast<size_t>(groups) * static_cast<size_t>(glen) * 2);
+  o.s = static_cast<float*>(c.take(static_cast<size_t>(groups) * 4));
+  return o;
+}
+
+size_t fwd_bytes(int64_t T, int64_t N, int64_t K) {
+  Carver c{nullptr};
+  carve_operand(c, T, K);
+  carve_operand(c, N, K);
+  return c.used;
+}
+size_t bwd_bytes(int64_t T, int64_t N, int64_t K) {
+  Carver c{nullptr};
+  carve_operand(c, T, N);  // dY along N (grad input)
+  carve_operand(c, K, N);  // W along N, transposed
+  carve_operand(c, N, T);  // dY along T, transposed (grad weight)
+  carve_operand(c, K, T);  // X along T, transposed
+  return c.used;
+}
+
+int8mp_status check_linear(int64_t T, int64_t N, int64_t K, const int8mp_linear_cfg* cfg) {
+  if (!cfg) return INT8MP_ERR_INVALID_ARG;
+  if (cfg->int8_fwd != 1 || cfg->int8_grad_in != 1 || cfg->int8_grad_w != 1)
+    return INT8MP_ERR_INVALID_ARG;
+  if (cfg->mode != INT8MP_RNE && cfg->mode != INT8MP_SR) return INT8MP_ERR_INVALID_ARG;
+  if (T < 0 || N < 0 || K < 0) return INT8MP_ERR_INVALID_ARG;
+  if (T > INT8MP_MAX_K || N > INT8MP_MAX_K || K > INT8MP_MAX_K) return INT8MP_ERR_INVALID_ARG;
+  if (T % 16 || N % 16 || K % 16) return INT8MP_ERR_ALIGNMENT;
+  return INT8MP_OK;
+}
+
+int8mp::SrArgs sr_of(const int8mp_linear_cfg* cfg, uint32_t stream_id) {
+  return int8mp::SrArgs{cfg->seed, cfg->offset, stream_id};
+}
+
+}  // namespace
+
+extern "C" {
+
+int8mp_status int8mp_quantize_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                      int axis, int8mp_round mode, uint64_t seed,
+                                      uint64_t offset, uint32_t stream_id, void* q,
+                                      int8mp_codes codes, float* scale, void* stream) {
+  int8mp_status st = check_quantize(x, rows, cols, ld, axis, mode, q, codes, scale);
+  if (st != INT8MP_OK || rows == 0 || cols == 0) return st;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != INT8MP_OK) return st;
+  const int8mp::SrArgs sr{seed, offset, stream_id};
+  cudaError_t e = axis == 0
+                      ? int8mp::launch_quantize_rows(x, rows, cols, ld, mode, sr, q, codes, scale,
+                                                     dev, as_stream(stream))
+                      : int8mp::launch_quantize_cols(x, rows, cols, ld, mode, sr, q, codes, scale,
+                                                     dev, as_stream(stream));
+  return from_cuda(e);
+}
+
+int8mp_status int8mp_scaled_mm(const void* A, const float* sA, const void* B, const float* sB,
+                               int64_t M, int64_t N, int64_t K, int8mp_layout layout,
+                               int8mp_codes codes, void* out, int64_t ldo, void* stream) {
+  int8mp_status st = check_mm(A, B, M, N, K, layout, codes, out, ldo);
+  if (st != INT8MP_OK) return st;
+  if (M > 0 && N > 0 && K > 0) {
+    if (!sA || !sB) return INT8MP_ERR_INVALID_ARG;
+    if (!aligned(sA, 4) || !aligned(sB, 4)) return INT8MP_ERR_ALIGNMENT;
+  }
+  return run_mm(A, sA, B, sB, M, N, K, int8mp::GemmOut::kBf16Scaled, out, ldo,
+                int8mp::GemmDebug{}, as_stream(stream));
+}
+
+int8mp_status int8mp_mm_s32(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                            int8mp_layout layout, int8mp_codes codes, int32_t* out, int64_t ldo,
+                            void* stream) {
+  int8mp_status st = check_mm(A, B, M, N, K, layout, codes, out, ldo);
+  if (st != INT8MP_OK) return st;
+  return run_mm(A, nullptr, B, nullptr, M, N, K, int8mp::GemmOut::kS32, out, ldo,
+                int8mp::GemmDebug{}, as_stream(stream));
+}
+
+size_t int8mp_linear_workspace_size(int64_t T, int64_t N, int64_t K, const int8mp_linear_cfg* cfg) {
+  if (check_linear(T, N, K, cfg) != INT8MP_OK) return 0;
+  const size_t f = fwd_bytes(T, N, K), b = bwd_bytes(T, N, K);
+  return f > b ? f : b;
+}
+
+int8mp_status int8mp_linear_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t N,
+                                int64_t K, const int8mp_linear_cfg* cfg, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  int8mp_status st = check_linear(T, N, K, cfg);
+  if (st != INT8MP_OK) return st;
+  if (T == 0 || N == 0) return INT8MP_OK;
+  if (!Y || (K > 0 && (!X || !W || !workspace))) return INT8MP_ERR_INVALID_ARG;
+  if (!aligned(Y, 16) || !aligned(X, 16) || !aligned(W, 16) || !aligned(workspace, 256))
+    return INT8MP_ERR_ALIGNMENT;
+  if (ws_bytes < fwd_bytes(T, N, K)) return INT8MP_ERR_WORKSPACE;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != INT8MP_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  Carver c{static_cast<char*>(workspace)};
+  const QOperand xq = carve_operand(c, T, K);
+  const QOperand wq = carve_operand(c, N, K);
+  if (K > 0) {
+    cudaError_t e = int8mp::launch_quantize_rows(X, T, K, K, cfg->mode, sr_of(cfg, INT8MP_STREAM_FWD_X),
+                                                 xq.q, INT8MP_CODES_F16, xq.s, dev, s);
+    if (e == cudaSuccess)
+      e = int8mp::launch_quantize_rows(W, N, K, K, cfg->mode, sr_of(cfg, INT8MP_STREAM_FWD_W), wq.q,
+                                       INT8MP_CODES_F16, wq.s, dev, s);
+    if (e != cudaSuccess) return INT8MP_ERR_CUDA;
+  }
+  return run_mm(xq.q, xq.s, wq.q, wq.s, T, N, K, int8mp::GemmOut::kBf16Scaled, Y, N,
+                int8mp::GemmDebug{}, s);
+}
+
+int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, void* dX,
+                                void* dW, int64_t T, int64_t N, int64_t K,
+                                const int8mp_linear_cfg* cfg, void* workspace, size_t ws_bytes,
+                                void* stream) {
+  int8mp_status st = check_linear(T, N, K, cfg);
+  if (st != INT8MP_OK) return st;
+  const bool want_dx = dX != nullptr && T > 0 && K > 0;
+  const bool want_dw = dW != nullptr && N > 0 && K > 0;
+  if (!want_dx && !want_dw) return INT8MP_OK;
+  if (!dY || !W || !X || !workspace) return INT8MP_ERR_INVALID_ARG;
+  if (!aligned(dY, 16) || !aligned(X, 16) || !aligned(W, 16) || !aligned(workspace, 256) ||
+      (dX && !aligned(dX, 16)) || (dW && !aligned(dW, 16)))
+    return INT8MP_ERR_ALIGNMENT;
+  if (ws_bytes < bwd_bytes(T, N, K)) return INT8MP_ERR_WORKSPACE;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != INT8MP_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  Carver c{static_cast<char*>(workspace)};
+  const QOperand dyq = carve_operand(c, T, N);
+  const QOperand wqt = carve_operand(c, K, N);
+  const QOperand dyqt = carve_operand(c, N, T);
+  const QOperand xqt = carve_operand(c, K, T);
+  if (want_dx) {
+    // grad input: contraction over N; dY by rows, W by columns (-> [K, N])
+    if (N > 0) {
+      cudaError_t e = int8mp::launch_quantize_rows(dY, T, N, N, cfg->mode,
+                                                   sr_of(cfg, INT8MP_STREAM_GI_DY), dyq.q,
+                                                   INT8MP_CODES_F16, dyq.s, dev, s);
+      if (e == cudaSuccess)
+        e = int8mp::launch_quantize_cols(W, N, K, K, cfg->mode, sr_of(cfg, INT8MP_STREAM_GI_W),
+                                         wqt.q, INT8MP_CODES_F16, wqt.s, dev, s);
+      if (e != cudaSuccess) return INT8MP_ERR_CUDA;
+    }
+    st = run_mm(dyq.q, dyq.s, wqt.q, wqt.s, T, K, N, int8mp::GemmOut::kBf16Scaled, dX, K,
+                int8mp::GemmDebug{}, s);
+    if (st != INT8MP_OK) return st;
+  }
+  if (want_dw) {
+    // grad weight: contraction over T; dY and X by columns (-> [N, T], [K, T])
+    if (T > 0) {
+      cudaError_t e = int8mp::launch_quantize_cols(dY, T, N, N, cfg->mode,
+                                                   sr_of(cfg, INT8MP_STREAM_GW_DY), dyqt.q,
+                                                   INT8MP_CODES_F16, dyqt.s, dev, s);
+      if (e == cudaSuccess)
+        e = int8mp::launch_quantize_cols(X, T, K, K, cfg->mode, sr_of(cfg, INT8MP_STREAM_GW_X),
+                                         xqt.q, INT8MP_CODES_F16, xqt.s, dev, s);
+      if (e != cudaSuccess) return INT8MP_ERR_CUDA;
+    }
+    st = run_mm(dyqt.q, dyqt.s, xqt.q, xqt.s, N, K, T, int8mp::GemmOut::kBf16Scaled, dW, K,
+                int8mp::GemmDebug{}, s);
+  }
+  return st;
+}
+
+int8mp_status int8mp_poll_device_status(void* stream) {
+  DeviceInfo dev;
+  int8mp_status st = current_device(&dev);
+  if (st != INT8MP_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return INT8MP_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, dev.status_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return INT8MP_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemset(dev.status_word, 0, sizeof word) != cudaSuccess) return INT8MP_ERR_CUDA;
+    return INT8MP_ERR_TIMEOUT;
+  }
+  return INT8MP_OK;
+}
+
+const char* int8mp_status_string(int8mp_status status) {
+  switch (status) {
+    case INT8MP_OK: return "ok";
+    case INT8MP_ERR_INVALID_ARG: return "invalid argument";
+    case INT8MP_ERR_ALIGNMENT: return "alignment or size-multiple requirement violated";
+    case INT8MP_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103";
+    case INT8MP_ERR_CUDA: return "CUDA runtime or launch error";
+    case INT8MP_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    case INT8MP_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+int int8mp_version(void) { return 100; }
+
+int8mp_status int8mp_debug_mm_s32_drop_first_load(const void* A, const void* B, int64_t M,
+                                                  int64_t N, int64_t K, int32_t* out,
+                                                  int64_t ldo, int wait_limit_ms, void* stream) {
+  int8mp_status st = check_mm(A, B, M, N, K, INT8MP_AxBT, INT8MP_CODES_F16, out, ldo);
+  if (st != INT8MP_OK) return st;
+  if (M == 0 || N == 0 || K == 0 || wait_limit_ms < 1 || wait_limit_ms > 5000)
+    return INT8MP_ERR_INVALID_ARG;
+  int8mp::GemmDebug dbg;
+  dbg.drop_first_load = 1;
+  dbg.wait_limit_ns = static_cast<uint64_t>(wait_limit_ms) * 1000000ull;
+  return run_mm(A, nullptr, B, nullptr, M, N, K, int8mp::GemmOut::kS32, out, ldo, dbg,
+                as_stream(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// common.cuh -- internal interface between the C-ABI layer (api.cu) and the
+// kernel translation units (quantize.cu, gemm.cu).  Not installed, not part
+// of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/int8mp.h"
+
+namespace int8mp {
+
+// Everything a kernel needs to know about the device it runs on.
+struct DeviceInfo {
+  int sms = 0;
+  unsigned int* status_word = nullptr;  // device address of the status word
+};
+
+// Stochastic-rounding parameters (header of int8mp.h gives the mapping).
+struct SrArgs {
+  uint64_t seed;
+  uint64_t offset;
+  uint32_t stream_id;
+};
+
+// Wait limit for every bounded device-side wait, in nanoseconds of
+// %globaltimer.  Long enough that no healthy wait reaches it.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// ---- quantize (quantize.cu) ------------------------------------------------
+// x bf16 [rows, cols] stride ld.  Row groups: q [rows, cols]; scale [rows].
+cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                 int8mp_round mode, const SrArgs& sr, void* q,
+                                 int8mp_codes codes, float* scale, const DeviceInfo& dev,
+                                 cudaStream_t stream);
+// Column groups, codes written transposed: q [cols, rows]; scale [cols].
+cudaError_t launch_quantize_cols(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                 int8mp_round mode, const SrArgs& sr, void* q,
+                                 int8mp_codes codes, float* scale, const DeviceInfo& dev,
+                                 cudaStream_t stream);
+
+// ---- GEMM (gemm.cu) ---------------------------------------------------------
+enum class GemmOut { kBf16Scaled = 0, kS32 = 1 };
+
+struct GemmDebug {
+  int drop_first_load = 0;        // test only: never issue the first TMA load
+  uint64_t wait_limit_ns = kWaitLimitNs;
+};
+
+// A [M,K], B [N,K]: f16 containers of integer codes, K contiguous.
+cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const float* sB,
+                        int64_t M, int64_t N, int64_t K, GemmOut mode, void* out,
+                        int64_t ldo, const DeviceInfo& dev, const GemmDebug& dbg,
+                        cudaStream_t stream);
+
+}  // namespace int8mp

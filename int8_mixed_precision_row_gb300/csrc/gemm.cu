@@ -1,0 +1,367 @@
+// gemm.cu -- scaled INT8 matmul on the sm_103a tensor cores.
+//
+// What it computes ("Quantized model training" README, INT8 mixed precision
+// training: a scaled INT8 matmul; "Integrate INT8 mixed-precision from
+// torchao 0.7": the product is scaled back to BF16):
+//   acc[i,j] = sum_k qA[i,k] * qB[j,k]                 (exact int32)
+//   out[i,j] = bf16_RNE((fp32_RN(acc) * sA[i]) * sB[j])  or acc itself.
+//
+// How: sm_103a has no INT8 tcgen05 MMA, so the codes arrive as f16 values
+// (exact for |q| <= 127) and the contraction runs on tcgen05.mma.kind::f16
+// with fp32 accumulation in tensor memory.  Every product is exact
+// (|q q'| <= 16129) and so is every fp32 partial sum while its magnitude is
+// below 2^24, which holds for any 1024 consecutive terms (127^2 * 1024 =
+// 16,516,096 < 16,777,216).  The K loop therefore runs in chunks of at most
+// 1024; each chunk lands in one of two TMEM accumulators, and the epilogue
+// warps convert it (exactly) to int32 and add it into per-thread int32
+// totals while the tensor core fills the other accumulator.
+//
+// Structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer (one thread): 4-stage ring of 128x64 A and
+//               256x64 B f16 tiles, 128-byte swizzled, one mbarrier per stage
+//   warp 1      TMEM allocator + MMA issuer (one thread): 4 MMAs of
+//               128x256x16 per stage, commit frees the stage; commit after
+//               each K-chunk hands the accumulator to the epilogue
+//   warps 2-9   epilogue: warp w reads TMEM lanes 32*(w%4).. and one half
+//               (128 columns) of the tile, keeps 128 int32 totals per thread
+// Every mbarrier wait is bounded (wall clock); a wait that runs out raises
+// the CTA abort flag and the device status word, every role winds down,
+// outstanding copies and MMAs are waited for (bounded), TMEM is freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace int8mp {
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64;  // kBK f16 = 128 bytes per row
+constexpr int kStages = 4;
+constexpr int kChunkBlocks = 16;  // 16 * 64 = 1024 terms per exact fp32 chunk
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr uint32_t kTmemCols = 512;  // two 128x256 fp32 accumulators
+constexpr int kBarrierBytes = 256;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes;
+
+struct GemmParams {
+  const float* sA;
+  const float* sB;
+  void* out;
+  int64_t ldo;
+  int M, N, K;
+  int m_tiles, n_tiles, k_blocks;
+  int mode;  // 0: bf16 scaled, 1: int32 accumulators
+  unsigned int* status;
+  uint64_t wait_limit_ns;
+  int drop_first_load;
+};
+
+__device__ __forceinline__ void raise_abort(volatile int* abort, unsigned int* status) {
+  *abort = 1;
+  atomicOr(status, 1u);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_s8f16_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t a_base = sbase;
+  const uint32_t b_base = sbase + kStages * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  const uint32_t bar0 = ptx::smem_addr(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);  // stays 0
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull_bar(b), 1);
+      ptx::mbar_init(tempty_bar(b), kEpiWarps);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort = 0;
+    *never = 0;
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = p.m_tiles * p.n_tiles;
+  const uint64_t limit = p.wait_limit_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ producer
+      uint32_t stage = 0, phase = 0;
+      uint32_t armed = 0u, armed_par = 0u;  // per-stage outstanding copy + its parity
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile / p.n_tiles) * kBM;
+        const int n0 = (tile % p.n_tiles) * kBN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort, limit)) {
+            ok = false;
+            break;
+          }
+          armed &= ~(1u << stage);  // the previous copy into this stage was consumed
+          const bool drop = p.drop_first_load && tile == static_cast<int>(blockIdx.x) && kb == 0;
+          if (!drop) {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+            ptx::tma_load_2d(a_base + stage * kABytes, &tmA, full_bar(stage), kb * kBK, m0);
+            ptx::tma_load_2d(b_base + stage * kBBytes, &tmB, full_bar(stage), kb * kBK, n0);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) raise_abort(abort, p.status);
+      // never leave a copy in flight into shared memory of an exiting CTA
+      for (int s = 0; s < kStages; ++s)
+        if (armed & (1u << s))
+          if (!ptx::mbar_wait_bounded(full_bar(s), (armed_par >> s) & 1u, never, limit))
+            raise_abort(abort, p.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------- MMA
+      constexpr uint32_t idesc = ptx::idesc_f16_f32(kBM, kBN);
+      uint32_t stage = 0, phase = 0, chunk = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int kb0 = 0; kb0 < p.k_blocks && ok; kb0 += kChunkBlocks) {
+          const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
+          if (!ptx::mbar_wait_bounded(tempty_bar(buf), aph ^ 1u, abort, limit)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * kBN;
+          const int kb_end = min(kb0 + kChunkBlocks, p.k_blocks);
+          for (int kb = kb0; kb < kb_end; ++kb) {
+            if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort, limit)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t adesc = ptx::smem_desc_kmajor_sw128(a_base + stage * kABytes);
+            const uint64_t bdesc = ptx::smem_desc_kmajor_sw128(b_base + stage * kBBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // advance 16 f16 = 32 bytes along K inside the swizzled row
+              ptx::mma_f16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                           (kb > kb0 || kk > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(empty_bar(stage));
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          ptx::mma_commit(tfull_bar(buf));
+          ++chunk;
+        }
+      }
+      if (!ok) raise_abort(abort, p.status);
+      // every MMA issued above completes before TMEM is released
+      ptx::mma_commit(drain_bar);
+      if (!ptx::mbar_wait_bounded(drain_bar, 0u, never, limit)) raise_abort(abort, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;           // TMEM lanes this warp may access
+    const int half = (warp - 2) >> 2;    // which 128 columns of the tile
+    uint32_t chunk = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const int m0 = (tile / p.n_tiles) * kBM;
+      const int n0 = (tile % p.n_tiles) * kBN;
+      int32_t tot[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) tot[i] = 0;
+      for (int kb0 = 0; kb0 < p.k_blocks; kb0 += kChunkBlocks) {
+        const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
+        int got = 1;
+        if (lane == 0) got = ptx::mbar_wait_bounded(tfull_bar(buf), aph, abort, limit) ? 1 : 0;
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kBN +
+                               static_cast<uint32_t>(half * 128);
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub) {
+          uint32_t r[32];
+          ptx::tmem_ld_32cols(taddr + sub * 32, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) tot[sub * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
+        ++chunk;
+      }
+      if (!ok) break;
+      const int64_t row = static_cast<int64_t>(m0) + quad * 32 + lane;
+      const int64_t col0 = static_cast<int64_t>(n0) + half * 128;
+      if (row < p.M) {
+        if (p.mode == 1) {
+          int32_t* orow = static_cast<int32_t*>(p.out) + row * p.ldo;
+#pragma unroll
+          for (int v = 0; v < 32; ++v) {
+            const int64_t col = col0 + v * 4;
+            if (col < p.N)
+              *reinterpret_cast<int4*>(orow + col) =
+                  make_int4(tot[4 * v], tot[4 * v + 1], tot[4 * v + 2], tot[4 * v + 3]);
+          }
+        } else {
+          const float sa = __ldg(p.sA + row);
+          uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.ldo;
+#pragma unroll
+          for (int v = 0; v < 16; ++v) {
+            const int64_t col = col0 + v * 8;
+            if (col < p.N) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float o0 = __fmul_rn(__fmul_rn(__int2float_rn(tot[v * 8 + 2 * e]), sa),
+                                           __ldg(p.sB + col + 2 * e));
+                const float o1 = __fmul_rn(__fmul_rn(__int2float_rn(tot[v * 8 + 2 * e + 1]), sa),
+                                           __ldg(p.sB + col + 2 * e + 1));
+                const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
+                w[e] = *reinterpret_cast<const uint32_t*>(&h);
+              }
+              *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+    }
+    if (!ok && lane == 0) raise_abort(abort, p.status);
+  }
+
+  // ------------------------------------------------------------ teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// K-major f16 operand [rows, K]: box of 64 (K) x box_rows, 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2u};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const float* sB,
+                        int64_t M, int64_t N, int64_t K, GemmOut mode, void* out, int64_t ldo,
+                        const DeviceInfo& dev, const GemmDebug& dbg, cudaStream_t stream) {
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int device = 0;
+  cudaError_t err = cudaGetDevice(&device);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[device]) {
+      err = cudaFuncSetAttribute(gemm_s8f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+      if (err != cudaSuccess) return err;
+      attr_set[device] = true;
+    }
+  }
+  CUtensorMap mapA, mapB;
+  if (!make_kmajor_map(&mapA, A, M, K, kBM) || !make_kmajor_map(&mapB, B, N, K, kBN))
+    return cudaErrorInvalidValue;
+  GemmParams p;
+  p.sA = sA;
+  p.sB = sB;
+  p.out = out;
+  p.ldo = ldo;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.m_tiles = static_cast<int>((M + kBM - 1) / kBM);
+  p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
+  p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
+  p.mode = mode == GemmOut::kS32 ? 1 : 0;
+  p.status = dev.status_word;
+  p.wait_limit_ns = dbg.wait_limit_ns;
+  p.drop_first_load = dbg.drop_first_load;
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  const int grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
+  gemm_s8f16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mapA, mapB, p);
+  return cudaGetLastError();
+}
+
+}  // namespace int8mp

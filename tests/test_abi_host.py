@@ -1,0 +1,103 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+public headers declare, and rejects bad arguments on the host before it
+touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import int8_mixed_precision_row_gb300 as m
+from int8_mixed_precision_row_gb300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return m.load()
+
+
+def _declared_symbols():
+    names = set()
+    for h in ("int8mp.h", "int8mp_debug.h"):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(int8mp_\w+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_symbols()
+    assert declared == set(m.EXPORTED), declared ^ set(m.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert m.int8mp_version() >= 100
+    for st in range(7):
+        assert m.int8mp_status_string(st) != "unknown status"
+    assert m.int8mp_status_string(99) == "unknown status"
+
+
+P = ctypes.c_void_p
+
+
+def _q(lib, x, rows, cols, ld, axis, mode=0, codes=0, q=16, scale=16):
+    return lib.int8mp_quantize_rowwise(P(x), rows, cols, ld, axis, mode, 0, 0, 0, P(q), codes,
+                                       P(scale), None)
+
+
+def test_quantize_host_validation(lib):
+    assert _q(lib, 16, 8, 8, 8, axis=2) == m.INT8MP_ERR_INVALID_ARG
+    assert _q(lib, 16, 8, 8, 8, axis=0, mode=3) == m.INT8MP_ERR_INVALID_ARG
+    assert _q(lib, 16, 8, 8, 8, axis=0, codes=5) == m.INT8MP_ERR_INVALID_ARG
+    assert _q(lib, 16, 8, 16, 8, axis=0) == m.INT8MP_ERR_INVALID_ARG      # ld < cols
+    assert _q(lib, 0, 8, 8, 8, axis=0) == m.INT8MP_ERR_INVALID_ARG        # null x
+    assert _q(lib, 16, 0, 8, 8, axis=0, q=0, scale=0) == m.INT8MP_OK      # empty: nothing to do
+    assert _q(lib, 16, 8, 12, 16, axis=0) == m.INT8MP_ERR_ALIGNMENT       # cols % 8
+    assert _q(lib, 24, 8, 8, 8, axis=0) == m.INT8MP_ERR_ALIGNMENT         # x not 16-byte aligned
+    assert _q(lib, 16, 12, 8, 8, axis=1) == m.INT8MP_ERR_ALIGNMENT        # axis 1 needs rows % 8
+
+
+def _mm(lib, M, N, K, layout=0, codes=1, A=16, B=16, out=16, ldo=None):
+    return lib.int8mp_mm_s32(P(A), P(B), M, N, K, layout, codes, P(out), N if ldo is None else ldo,
+                             None)
+
+
+def test_matmul_host_validation(lib):
+    assert _mm(lib, 8, 8, 16, layout=1) == m.INT8MP_ERR_INVALID_ARG       # tensor core needs A@B.T
+    assert _mm(lib, 8, 8, 16, codes=0) == m.INT8MP_ERR_INVALID_ARG        # and f16 containers
+    assert _mm(lib, 8, 8, m.INT8MP_MAX_K + 1) == m.INT8MP_ERR_INVALID_ARG
+    assert _mm(lib, 8, 8, 24) == m.INT8MP_ERR_ALIGNMENT                   # K % 16
+    assert _mm(lib, 8, 12, 16) == m.INT8MP_ERR_ALIGNMENT                  # N % 8
+    assert _mm(lib, 8, 8, 16, A=8) == m.INT8MP_ERR_ALIGNMENT
+    assert _mm(lib, 8, 8, 16, out=0) == m.INT8MP_ERR_INVALID_ARG
+    assert _mm(lib, 0, 8, 16, A=0, B=0, out=0) == m.INT8MP_OK             # empty
+
+
+def test_linear_host_validation(lib):
+    cfg = m.linear_cfg()
+    ref = ctypes.byref(cfg)
+    f = lib.int8mp_linear_fwd
+    assert f(P(16), P(16), P(16), 32, 32, 32, None, P(256), 1 << 20, None) == m.INT8MP_ERR_INVALID_ARG
+    assert f(P(16), P(16), P(16), 32, 32, 24, ref, P(256), 1 << 20, None) == m.INT8MP_ERR_ALIGNMENT
+    assert f(P(16), P(16), P(16), 32, 32, 32, ref, P(256), 16, None) == m.INT8MP_ERR_WORKSPACE
+    bad = m.int8mp_linear_cfg(0, 1, 1, 0, 0, 0)   # BF16 passes are not part of this build
+    assert f(P(16), P(16), P(16), 32, 32, 32, ctypes.byref(bad), P(256), 1 << 20, None) == \
+        m.INT8MP_ERR_INVALID_ARG
+    need = m.int8mp_linear_workspace_size(32, 48, 64, cfg)
+    assert need >= 2 * (32 * 64 + 48 * 64) and need % 256 == 0
+    assert m.int8mp_linear_workspace_size(32, 48, 24, cfg) == 0
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    pkg = os.path.join(ROOT, "int8_mixed_precision_row_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
+                assert "liboracle" not in text and "oracle.h" not in text, fn
