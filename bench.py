@@ -1,0 +1,513 @@
+#!/usr/bin/env python
+"""Benchmark of the INT8 mixed-precision linear-layer hot path on GB300.
+
+One step = forward + backward (grad-input and grad-weight) of the seven
+linear layers of one Llama2-1B-shaped decoder layer (q, k, v, o 2048x2048;
+gate, up 5632x2048; down 2048x5632) over 16 x 2048 = 32768 tokens, every
+matmul in INT8 with dynamic row-wise quantization along its contraction axis
+("Quantized model training" README, INT8 mixed precision training; LM head
+excluded).  Activations N(0,1), weights N(0,0.02), output gradients
+N(0,1e-3), round to nearest even.  Inputs are resident in HBM before the
+timed region; every step touches about 5 GB, far more than the 129 MB L2.
+
+Output: one JSON line (rank 0).  `value` is whole-job tokens/s; `e2e` is the
+same metric through int8mp_linear_fwd/bwd with inputs copied from pinned
+host memory and dW copied back inside the timed region; `roofline` describes
+the dominant kernel (the tensor-core GEMM); `cpu_baseline` times the plain-C
+oracle on a bounded token sample on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quant+INT8 scaled-mm TOPS; fwd+bwd linear tok/s at Llama2-1B shapes"
+WORKLOAD = ("llama2-1b decoder-layer linears (q,k,v,o 2048x2048; gate,up 5632x2048; "
+            "down 2048x5632) fwd+grad_in+grad_w, all INT8, T=16x2048 tokens")
+ORACLE_SAMPLE_TOKENS = 512
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-steps", action="store_true",
+                    help="short run for a profiler: no extras, no e2e, no CPU baseline")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value, world, device=None):
+    """Largest value over all ranks (the job takes as long as its slowest
+    rank).  No data-path collective: the replicas share nothing else."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------- workload
+class LayerStep:
+    """Device-resident inputs, outputs and code/scale buffers of one decoder
+    layer's linears, and the step composed of the public C-ABI calls."""
+
+    def __init__(self, spec, mode, device, T=None):
+        import torch
+        from int8_mixed_precision_row_gb300 import synth
+        import int8_mixed_precision_row_gb300 as m
+        self.m = m
+        self.spec = spec
+        self.T = spec["T"] if T is None else T
+        self.mode = mode
+        self.device = device
+        host = synth.layer_inputs(spec, T=self.T)
+        self.host = host
+        dev_cache = {}
+
+        def on_dev(t):
+            key = id(t)
+            if key not in dev_cache:
+                dev_cache[key] = t.to(device)
+            return dev_cache[key]
+        self.linears = []
+        T = self.T
+        for name, (X, W, dY) in host.items():
+            N, K = W.shape
+            self.linears.append({
+                "name": name, "N": N, "K": K, "X": on_dev(X), "W": on_dev(W), "dY": on_dev(dY),
+                "Y": torch.empty((T, N), dtype=torch.bfloat16, device=device),
+                "dX": torch.empty((T, K), dtype=torch.bfloat16, device=device),
+                "dW": torch.empty((N, K), dtype=torch.bfloat16, device=device)})
+        nmax = max(l["N"] for l in self.linears)
+        kmax = max(l["K"] for l in self.linears)
+        big = max(T * kmax, T * nmax, nmax * kmax)
+        f16 = torch.float16
+        # code buffers (f16 containers) and scales, reused linear after linear
+        self.qa = torch.empty(big, dtype=f16, device=device)
+        self.qb = torch.empty(big, dtype=f16, device=device)
+        self.sa = torch.empty(max(T, nmax, kmax), dtype=torch.float32, device=device)
+        self.sb = torch.empty(max(T, nmax, kmax), dtype=torch.float32, device=device)
+        self.flops = 6.0 * T * sum(l["N"] * l["K"] for l in self.linears)
+        self.gemms_per_step = 3 * len(self.linears)
+        # kernels of this library per step: row quantize 1, column quantize 3
+        # (absmax, codes, scales), GEMM 1
+        self.kernels_per_step = len(self.linears) * (3 * 1 + 3 * 3 + 3 * 1)
+        # algorithmic quantize bytes: bf16 read once, code (f16 container) and scale written
+        self.quant_elems = sum(2 * (T * l["K"] + l["N"] * l["K"] + T * l["N"]) for l in self.linears)
+
+    def _q(self, x, axis, sid, qbuf, sbuf, cfg_seed, cfg_off):
+        m = self.m
+        rows, cols = x.shape
+        groups, glen = (rows, cols) if axis == 0 else (cols, rows)
+        q = qbuf[:groups * glen].view(groups, glen)
+        s = sbuf[:groups]
+        m.int8mp_quantize_rowwise(x, axis=axis, mode=self.mode, seed=cfg_seed, offset=cfg_off,
+                                  stream_id=sid, codes=m.INT8MP_CODES_F16, q=q, scale=s)
+        return q, s
+
+    def run(self, timers=None, seed=0, offset=0):
+        """One step.  timers: optional dict of kernel class -> list of
+        (start, end) CUDA event pairs recorded around each call."""
+        m = self.m
+        import torch
+
+        def rec(kind, fn):
+            if timers is None:
+                return fn()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            r = fn()
+            b.record()
+            timers.setdefault(kind, []).append((a, b))
+            return r
+        for l in self.linears:
+            X, W, dY = l["X"], l["W"], l["dY"]
+            # forward: X and W along K (their rows)
+            qx, sx = rec("quant_rows", lambda: self._q(X, 0, m.INT8MP_STREAM_FWD_X, self.qa, self.sa, seed, offset))
+            qw, sw = rec("quant_rows", lambda: self._q(W, 0, m.INT8MP_STREAM_FWD_W, self.qb, self.sb, seed, offset))
+            rec("gemm", lambda: m.int8mp_scaled_mm(qx, sx, qw, sw, out=l["Y"]))
+            # grad input: dY along N (rows), W along N (columns -> [K, N])
+            qg, sg = rec("quant_rows", lambda: self._q(dY, 0, m.INT8MP_STREAM_GI_DY, self.qa, self.sa, seed, offset))
+            qwt, swt = rec("quant_cols", lambda: self._q(W, 1, m.INT8MP_STREAM_GI_W, self.qb, self.sb, seed, offset))
+            rec("gemm", lambda: m.int8mp_scaled_mm(qg, sg, qwt, swt, out=l["dX"]))
+            # grad weight: dY and X along T (columns -> [N, T], [K, T])
+            qgt, sgt = rec("quant_cols", lambda: self._q(dY, 1, m.INT8MP_STREAM_GW_DY, self.qa, self.sa, seed, offset))
+            qxt, sxt = rec("quant_cols", lambda: self._q(X, 1, m.INT8MP_STREAM_GW_X, self.qb, self.sb, seed, offset))
+            rec("gemm", lambda: m.int8mp_scaled_mm(qgt, sgt, qxt, sxt, out=l["dW"]))
+
+
+def time_steps(step, steps, warmup, world, device):
+    import torch
+    for _ in range(warmup):
+        step.run()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    timers = {}
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step.run(timers=timers)
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    elapsed_ms = start.elapsed_time(end)
+    per_kind = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in timers.items()}
+    counts = {k: len(v) for k, v in timers.items()}
+    return elapsed_ms, per_kind, counts
+
+
+def time_e2e(step, steps, warmup):
+    """Same step through int8mp_linear_fwd / int8mp_linear_bwd, inputs copied
+    from pinned host memory each step and dW copied back."""
+    import torch
+    m = step.m
+    cfg = m.linear_cfg(mode=step.mode)
+    pinned = {}
+    for l, (name, (X, W, dY)) in zip(step.linears, step.host.items()):
+        for key, t in (("X", X), ("W", W), ("dY", dY)):
+            if id(t) not in pinned:
+                pinned[id(t)] = t.pin_memory()
+        l["hX"], l["hW"], l["hdY"] = pinned[id(X)], pinned[id(W)], pinned[id(dY)]
+        l["hdW"] = torch.empty(l["dW"].shape, dtype=torch.bfloat16).pin_memory()
+    ws_bytes = max(m.int8mp_linear_workspace_size(step.T, l["N"], l["K"], cfg) for l in step.linears)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=step.device)
+    h2d = sum(t.numel() * 2 for t in pinned.values())
+    d2h = sum(l["dW"].numel() * 2 for l in step.linears)
+
+    def one():
+        copied = set()
+        for l in step.linears:
+            for dkey, hkey in (("X", "hX"), ("W", "hW"), ("dY", "hdY")):
+                if id(l[hkey]) not in copied:
+                    l[dkey].copy_(l[hkey], non_blocking=True)
+                    copied.add(id(l[hkey]))
+        for l in step.linears:
+            m.int8mp_linear_fwd(l["X"], l["W"], cfg, Y=l["Y"], workspace=ws)
+            m.int8mp_linear_bwd(l["dY"], l["X"], l["W"], cfg, dX=l["dX"], dW=l["dW"], workspace=ws)
+            l["hdW"].copy_(l["dW"], non_blocking=True)
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    if m.int8mp_poll_device_status() != m.INT8MP_OK:
+        raise RuntimeError("device status reported a timeout during the e2e run")
+    return a.elapsed_time(b), h2d, d2h
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_layer_sample(spec, T_sample, mode=0, nthreads=None):
+    """Seconds the oracle takes for the step's arithmetic on the first
+    T_sample tokens of the same layer inputs (all seven linears, fwd + bwd)."""
+    import numpy as np
+    import torch
+    import oracle
+    from int8_mixed_precision_row_gb300 import synth
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    host = synth.layer_inputs(spec, T=T_sample)
+    arrays = [(bits(X), bits(W), bits(dY)) for X, W, dY in host.values()]
+    nthreads = nthreads or oracle.default_threads()
+    oracle.lib()
+    t0 = time.perf_counter()
+    for X, W, dY in arrays:
+        oracle.linear_fwd(X, W, mode=mode, nthreads=nthreads)
+        oracle.linear_bwd(dY, X, W, mode=mode, nthreads=nthreads)
+    return time.perf_counter() - t0, nthreads
+
+
+def cpu_baseline(spec):
+    secs, cores = oracle_layer_sample(spec, ORACLE_SAMPLE_TOKENS)
+    return {"value": ORACLE_SAMPLE_TOKENS / secs, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {ORACLE_SAMPLE_TOKENS} tokens of the same layer inputs, all 7 linears "
+                      f"fwd+grad_in+grad_w, RNE ({secs:.1f} s)"}
+
+
+# ------------------------------------------------------------------ extras
+def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
+    """Square quant+scaled-mm in the three layouts: quantize A and B along K
+    (columns for the operands stored K-first), then the matmul.  L2 flushed
+    between iterations (256 MB write)."""
+    import torch
+    import int8_mixed_precision_row_gb300 as m
+    from int8_mixed_precision_row_gb300 import synth
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    out = {}
+    for S in sizes:
+        A, B = synth.square_inputs(S, "AxBT")
+        A, B = A.to(device), B.to(device)
+        qa = torch.empty((S, S), dtype=torch.float16, device=device)
+        qb = torch.empty((S, S), dtype=torch.float16, device=device)
+        sa = torch.empty(S, dtype=torch.float32, device=device)
+        sb = torch.empty(S, dtype=torch.float32, device=device)
+        Y = torch.empty((S, S), dtype=torch.bfloat16, device=device)
+        for layout, (ax_a, ax_b) in (("A@B.T", (0, 0)), ("A@B", (0, 1)), ("A.T@B", (1, 1))):
+            tq, tm = [], []
+            for it in range(iters + 3):
+                flush.fill_(it & 0xFF)
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record()
+                m.int8mp_quantize_rowwise(A, axis=ax_a, codes=m.INT8MP_CODES_F16, q=qa, scale=sa)
+                m.int8mp_quantize_rowwise(B, axis=ax_b, codes=m.INT8MP_CODES_F16, q=qb, scale=sb)
+                e[1].record()
+                m.int8mp_scaled_mm(qa, sa, qb, sb, out=Y)
+                e[2].record()
+                torch.cuda.synchronize()
+                if it >= 3:
+                    tq.append(e[0].elapsed_time(e[1]))
+                    tm.append(e[1].elapsed_time(e[2]))
+            q_ms, mm_ms = statistics.median(tq), statistics.median(tm)
+            ops = 2.0 * S ** 3
+            out[f"{S}:{layout}"] = {
+                "quant_mm_tops": round(ops / ((q_ms + mm_ms) * 1e-3) / 1e12, 1),
+                "mm_tops": round(ops / (mm_ms * 1e-3) / 1e12, 1),
+                "quant_ms": round(q_ms, 4), "mm_ms": round(mm_ms, 4),
+                "quant_gbs_f16codes": round(2 * S * S * 4 / (q_ms * 1e-3) / 1e9, 1)}
+    return out
+
+
+def layer_tok_s(spec, mode, device, steps=5, warmup=2):
+    import torch
+    step = LayerStep(spec, mode, device)
+    el, per_kind, _ = time_steps(step, steps, warmup, 1, device)
+    r = {"tok_s": round(step.T * steps / (el * 1e-3), 1), "ms_per_step": round(el / steps, 3),
+         "gemm_tflops": round(step.flops * steps / (per_kind.get("gemm", el) * 1e-3) / 1e12, 1)}
+    del step
+    torch.cuda.empty_cache()
+    return r
+
+
+# -------------------------------------------------------------------- main
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p.get("hbm_gbs"), p.get("bf16_tflops"), p.get("bf16_tflops_sustained"), "measured"
+    except (OSError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands on the host cores, each step a bounded sample
+    of the same workload.  Under torchrun only rank 0 works."""
+    if rank != 0:
+        return
+    from int8_mixed_precision_row_gb300 import synth
+    spec = synth.LLAMA2_1B
+    T_s = 32
+    for _ in range(args.warmup):
+        oracle_layer_sample(spec, T_s)
+    secs = 0.0
+    cores = 1
+    for _ in range(args.steps):
+        s, cores = oracle_layer_sample(spec, T_s)
+        secs += s
+    value = T_s * args.steps / secs
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": T_s, "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {T_s} tokens of the llama2-1b layer per step"},
+        "e2e": {"value": round(value, 3), "unit": "tok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        init_dist(world, "gloo")
+        run_reference(args, world, rank)
+        return
+    import torch
+    from int8_mixed_precision_row_gb300 import build, synth
+    import int8_mixed_precision_row_gb300 as m
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    build.build()
+    m.load()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    spec = synth.LLAMA2_1B
+    step = LayerStep(spec, m.INT8MP_RNE, device)
+    with ClockSampler(local) as clk:
+        elapsed_ms, per_kind, counts = time_steps(step, args.steps, args.warmup, world, device)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, device)
+    if m.int8mp_poll_device_status() != m.INT8MP_OK:
+        raise RuntimeError("a bounded device wait ran out during the timed region")
+    tokens = step.T * args.steps * world
+    value = tokens / (elapsed_ms * 1e-3)
+    hbm, bf16_burst, bf16_sust, peak_src = measured_peaks()
+    gemm_ms = per_kind.get("gemm", 0.0)
+    gemm_launches = counts.get("gemm", 1)
+    gemm_tflops = step.flops * args.steps / (gemm_ms * 1e-3) / 1e12
+    quant_ms = per_kind.get("quant_rows", 0.0) + per_kind.get("quant_cols", 0.0)
+    quant_bytes = step.quant_elems * 4 * args.steps  # bf16 read + f16 code written per element
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": step.T, "hidden": spec["hidden"],
+                   "intermediate": spec["inter"], "linears": len(step.linears), "rounding": "RNE",
+                   "l2": "inputs larger than L2 (about 5 GB touched per step, L2 129 MB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_s8f16_kernel (tcgen05 kind::f16, exact int)",
+                     "achieved": round(gemm_tflops, 1), "peak": bf16_sust, "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / bf16_sust, 3), "traffic": None,
+                     "peak_source": f"{peak_src} dense bf16 sustained (f16 runs at the bf16 rate)",
+                     "launches_timed": gemm_launches,
+                     "avg_launch_ms": round(gemm_ms / gemm_launches, 4)},
+        "kernels": {
+            "gemm_ms_per_step": round(gemm_ms / args.steps, 3),
+            "quant_rows_ms_per_step": round(per_kind.get("quant_rows", 0.0) / args.steps, 3),
+            "quant_cols_ms_per_step": round(per_kind.get("quant_cols", 0.0) / args.steps, 3),
+            "quant_gbs_f16codes": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1) if quant_ms else None,
+            "hbm_peak_gbs": hbm},
+        "gpu_launches": step.kernels_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.profile_steps:
+        e2e_steps = max(2, min(args.steps, 5))
+        e2e_ms, h2d, d2h = time_e2e(step, e2e_steps, 1)
+        e2e_ms = max_over_ranks(e2e_ms, world, device)
+        line["e2e"] = {"value": round(step.T * e2e_steps * world / (e2e_ms * 1e-3), 1), "unit": "tok/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del step
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.profile_steps and not args.no_extra:
+        line["extra"] = {
+            "square_quant_scaled_mm": square_sweep(device),
+            "llama2-1b_stochastic_rounding": layer_tok_s(synth.LLAMA2_1B, m.INT8MP_SR, device),
+            "llama3-8b_T16384": layer_tok_s(synth.LLAMA3_8B, m.INT8MP_RNE, device),
+        }
+    if rank == 0 and not args.profile_steps and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
