@@ -195,6 +195,33 @@ int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, vo
                                 const int8mp_linear_cfg* cfg, void* workspace, size_t ws_bytes,
                                 void* stream);
 
+/*
+ * int8mp_linear_fwd_noalloc -- the same forward pass as int8mp_linear_fwd
+ * (same arguments, requirements and results, bit for bit) for callers that
+ * cannot allocate device memory: programs that hand out all device memory
+ * through their own pool or have reserved it up front, and latency-critical
+ * code that may not call cudaMalloc/cudaFree (which can synchronize the
+ * device).  The pages have no counterpart; this is a property of the library.
+ *
+ * The workspace is a library-owned array of INT8MP_NOALLOC_SCRATCH_BYTES on
+ * every device that loads the library, held until the process exits.  Sizes
+ * needing more, i.e. round256(2*T*K) + round256(4*T) + round256(2*N*K) +
+ * round256(4*N) bytes above the maximum, return INT8MP_ERR_WORKSPACE before
+ * anything is launched.  Nothing is allocated by the call.
+ *
+ * The first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  All calls on a device share the array and it keeps the
+ * last call's contents (nothing in it needs to start at zero: every byte a
+ * call reads it has written first).  Calls that overlap on the GPU -- on
+ * different streams, or from several host threads -- race on the array and
+ * must be serialized by the caller.
+ */
+#define INT8MP_NOALLOC_SCRATCH_BYTES (32u << 20)
+int8mp_status int8mp_linear_fwd_noalloc(const void* X, const void* W, void* Y, int64_t T,
+                                        int64_t N, int64_t K, const int8mp_linear_cfg* cfg,
+                                        void* stream);
+
 /* Synchronizes `stream`, then returns and clears the device status word of
  * the current device: INT8MP_ERR_TIMEOUT if a bounded device wait ran out
  * since the last poll, INT8MP_ERR_CUDA if the stream reports an error,

@@ -33,8 +33,9 @@ EXPORTED = (
     "int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
     "int8mp_linear_workspace_size", "int8mp_linear_fwd", "int8mp_linear_bwd",
     "int8mp_poll_device_status", "int8mp_status_string", "int8mp_version",
-    "int8mp_debug_mm_s32_drop_first_load",
+    "int8mp_debug_mm_s32_drop_first_load", "int8mp_linear_fwd_noalloc",
 )
+INT8MP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class Int8mpError(RuntimeError):
@@ -87,9 +88,12 @@ def load(path=None):
     L.int8mp_status_string.restype = ctypes.c_char_p
     L.int8mp_version.argtypes = []
     L.int8mp_debug_mm_s32_drop_first_load.argtypes = [_P, _P, _I64, _I64, _I64, _P, _I64, _INT, _P]
+    L.int8mp_linear_fwd_noalloc.argtypes = [_P, _P, _P, _I64, _I64, _I64,
+                                            ctypes.POINTER(int8mp_linear_cfg), _P]
     for name in ("int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
                  "int8mp_linear_fwd", "int8mp_linear_bwd", "int8mp_poll_device_status",
-                 "int8mp_version", "int8mp_debug_mm_s32_drop_first_load"):
+                 "int8mp_version", "int8mp_debug_mm_s32_drop_first_load",
+                 "int8mp_linear_fwd_noalloc"):
         getattr(L, name).restype = _INT
     _lib = L
     return L
@@ -216,3 +220,18 @@ def int8mp_debug_mm_s32_drop_first_load(A, B, out, wait_limit_ms=200, stream=Non
     return load().int8mp_debug_mm_s32_drop_first_load(_ptr(A), _ptr(B), M, N, K, _ptr(out),
                                                       out.stride(0), int(wait_limit_ms),
                                                       _stream(stream))
+
+
+def int8mp_linear_fwd_noalloc(X, W, cfg=None, Y=None, stream=None):
+    """Y [T,N] = X [T,K] . W [N,K]^T like int8mp_linear_fwd, with the
+    workspace in the library's fixed per-device scratch array instead of a
+    caller-provided buffer (for callers that cannot allocate device memory).
+    Y is allocated here only when the caller passes none."""
+    cfg = cfg or linear_cfg()
+    T, K = X.shape
+    N = W.shape[0]
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.bfloat16, device=X.device)
+    _check(load().int8mp_linear_fwd_noalloc(_ptr(X), _ptr(W), _ptr(Y), T, N, K, ctypes.byref(cfg),
+                                            _stream(stream)), "int8mp_linear_fwd_noalloc")
+    return Y

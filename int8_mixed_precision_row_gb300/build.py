@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libint8mp.so")
 
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "philox.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
