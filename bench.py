@@ -47,6 +47,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", action="store_true",
                     help="short run for a profiler: no extras, no e2e, no CPU baseline")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="profiling cases only: tokens per step instead of 16x2048")
+    ap.add_argument("--linears", default=None,
+                    help="profiling cases only: comma-separated subset of q,k,v,o,gate,up,down")
     return ap.parse_args()
 
 
@@ -154,7 +158,7 @@ class LayerStep:
     """Device-resident inputs, outputs and code/scale buffers of one decoder
     layer's linears, and the step composed of the public C-ABI calls."""
 
-    def __init__(self, spec, mode, device, T=None):
+    def __init__(self, spec, mode, device, T=None, only=None):
         import torch
         from int8_mixed_precision_row_gb300 import synth
         import int8_mixed_precision_row_gb300 as m
@@ -163,6 +167,9 @@ class LayerStep:
         self.T = spec["T"] if T is None else T
         self.mode = mode
         self.device = device
+        if only:
+            spec = dict(spec, linears=[l for l in spec["linears"] if l[0] in only])
+            self.spec = spec
         host = synth.layer_inputs(spec, T=self.T)
         self.host = host
         dev_cache = {}
@@ -448,7 +455,10 @@ def main():
     device = torch.device("cuda", local)
     init_dist(world, "nccl")
     spec = synth.LLAMA2_1B
-    step = LayerStep(spec, m.INT8MP_RNE, device)
+    only = set(args.linears.split(",")) if args.linears else None
+    if (args.tokens or only) and not args.profile_steps:
+        raise SystemExit("--tokens/--linears select profiling cases and need --profile-steps")
+    step = LayerStep(spec, m.INT8MP_RNE, device, T=args.tokens, only=only)
     with ClockSampler(local) as clk:
         elapsed_ms, per_kind, counts = time_steps(step, args.steps, args.warmup, world, device)
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)

@@ -34,6 +34,7 @@ EXPORTED = (
     "int8mp_linear_workspace_size", "int8mp_linear_fwd", "int8mp_linear_bwd",
     "int8mp_poll_device_status", "int8mp_status_string", "int8mp_version",
     "int8mp_debug_mm_s32_drop_first_load", "int8mp_linear_fwd_noalloc",
+    "int8mp_debug_check_division",
 )
 INT8MP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -90,10 +91,11 @@ def load(path=None):
     L.int8mp_debug_mm_s32_drop_first_load.argtypes = [_P, _P, _I64, _I64, _I64, _P, _I64, _INT, _P]
     L.int8mp_linear_fwd_noalloc.argtypes = [_P, _P, _P, _I64, _I64, _I64,
                                             ctypes.POINTER(int8mp_linear_cfg), _P]
+    L.int8mp_debug_check_division.argtypes = [_P, _P, _P, _P]
     for name in ("int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
                  "int8mp_linear_fwd", "int8mp_linear_bwd", "int8mp_poll_device_status",
                  "int8mp_version", "int8mp_debug_mm_s32_drop_first_load",
-                 "int8mp_linear_fwd_noalloc"):
+                 "int8mp_linear_fwd_noalloc", "int8mp_debug_check_division"):
         getattr(L, name).restype = _INT
     _lib = L
     return L
@@ -212,6 +214,16 @@ def int8mp_linear_bwd(dY, X, W, cfg=None, dX=None, dW=None, want_dx=True, want_d
 
 def int8mp_poll_device_status(stream=None):
     return load().int8mp_poll_device_status(_stream(stream))
+
+
+def int8mp_debug_check_division():
+    """(mismatches, pairs, fast_pairs, (absmax_bits, x_bits, max_abs_x_bits))
+    of the exhaustive division check."""
+    vals = [ctypes.c_uint64() for _ in range(3)]
+    first = (ctypes.c_uint32 * 3)()
+    _check(load().int8mp_debug_check_division(*(ctypes.byref(v) for v in vals), first),
+           "int8mp_debug_check_division")
+    return vals[0].value, vals[1].value, vals[2].value, (first[0], first[1], first[2])
 
 
 def int8mp_debug_mm_s32_drop_first_load(A, B, out, wait_limit_ms=200, stream=None):

@@ -17,8 +17,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libint8mp.so")
 
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "ptx.cuh", "philox.cuh"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "tma.cu", "noalloc.cu", "debug.cu"]
+HEADERS = ["common.cuh", "ptx.cuh", "philox.cuh", "divide.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

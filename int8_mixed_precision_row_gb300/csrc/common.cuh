@@ -3,6 +3,7 @@
 // of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,6 +27,13 @@ struct SrArgs {
 // Wait limit for every bounded device-side wait, in nanoseconds of
 // %globaltimer.  Long enough that no healthy wait reaches it.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// ---- TMA tensor maps (tma.cu) -----------------------------------------------
+// Row-major [rows, cols] matrix of `esize`-byte elements, row stride ld
+// elements; boxes of box_rows x box_cols; zero fill outside the matrix.
+bool encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                          int esize, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                          int box_rows, CUtensorMapSwizzle swizzle);
 
 // ---- quantize (quantize.cu) ------------------------------------------------
 // x bf16 [rows, cols] stride ld.  Row groups: q [rows, cols]; scale [rows].

@@ -6,25 +6,37 @@
 // finetuning", summary: x_q = clamp(x / scale + zp) -- here zp = 0 and
 // scale = absmax / 127.
 //
-// Two groupings:
+// Two groupings, both HBM-bound and both fed by TMA:
 //   rows    one group per row of x [rows, cols] (the contraction axis is
-//           contiguous): the row is held in registers, reduced by warp
-//           shuffles, and quantized without a second read.
+//           contiguous).  Each warp streams whole rows into a double-buffered
+//           shared-memory slot with a bulk copy (cp.async.bulk), reduces the
+//           absmax from shared memory, and writes the codes; the copy of the
+//           row after next is issued as soon as a slot is free.
 //   columns one group per column (the contraction axis is the leading one):
 //           pass 1 reduces column absmax over row blocks into the scale
 //           buffer (atomic max on the fp32 bit pattern, valid for values
-//           >= 0); pass 2 re-reads 256x64 tiles, quantizes, and writes the
-//           codes transposed [cols, rows] through a swizzled shared-memory
-//           tile; pass 3 turns the stored absmax into absmax / 127.
+//           >= 0); pass 2 turns it into absmax / 127 in place; pass 3 streams
+//           256x64 tiles into a two-deep shared-memory ring with 2-D TMA
+//           loads, quantizes them, and writes the codes transposed
+//           [cols, rows] through a swizzled shared-memory tile.
 //
 // Arithmetic per element (identical to the header of int8mp.h):
-//   v = x / s (IEEE division), q = clamp(rint(v)) or, stochastically,
-//   q = clamp(floor(v) + (u < v - floor(v))), u from Philox4x32-10.
+//   v = x / s rounded as an IEEE division (div8_*: a reciprocal and two FMAs,
+//   certified against IEEE division over all bf16 inputs), then
+//   q = clamp(rint(v)) or, stochastically, q = clamp(floor(v) + (u < v -
+//   floor(v))) with u from Philox4x32-10.
+// Every wait on a copy is bounded; a wait that runs out sets the device
+// status word and the warp or block stops after its copies have landed.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "common.cuh"
+#include "divide.cuh"
 #include "philox.cuh"
+#include "ptx.cuh"
 
 namespace int8mp {
 namespace {
@@ -53,35 +65,30 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
-// One code as an exact float in [-127, 127] (never -0).  s > 0.
-template <bool SR>
-__device__ __forceinline__ float code_of(float x, float s, uint32_t word) {
-  const float v = __fdiv_rn(x, s);
-  float q;
-  if (SR) {
-    const float f = floorf(v);
-    const float fr = __fsub_rn(v, f);
-    q = (sr_uniform(word) < fr) ? __fadd_rn(f, 1.0f) : f;
-  } else {
-    q = rintf(v);
-  }
-  q = fminf(fmaxf(q, -127.0f), 127.0f);
-  return __fadd_rn(q, 0.0f);  // -0 -> +0
+// Code from an exact quotient v: an exact float in [-127, 127], never -0.
+__device__ __forceinline__ float code_rne(float v) {
+  return __fadd_rn(fminf(fmaxf(rintf(v), -127.0f), 127.0f), 0.0f);
+}
+__device__ __forceinline__ float code_sr(float v, uint32_t word) {
+  const float f = floorf(v);
+  const float fr = __fsub_rn(v, f);
+  const float q = (sr_uniform(word) < fr) ? __fadd_rn(f, 1.0f) : f;
+  return __fadd_rn(fminf(fmaxf(q, -127.0f), 127.0f), 0.0f);
 }
 
-// Eight codes of one vector (elements n0 .. n0+7 of the SR stream).
+// Eight codes from eight quotients (elements n0 .. n0+7 of the SR stream).
 template <bool SR>
-__device__ __forceinline__ void codes8(const float (&f)[8], float s, const SrArgs& sr, uint64_t n0,
-                                       float (&c)[8]) {
-  uint32_t w[8];
+__device__ __forceinline__ void codes_of(const float (&v)[8], const SrArgs& sr, uint64_t n0,
+                                         float (&c)[8]) {
   if (SR) {
+    uint32_t w[8];
     philox_words8(sr.seed, n0, sr.stream_id, w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = code_sr(v[i], w[i]);
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = 0u;
+    for (int i = 0; i < 8; ++i) c[i] = code_rne(v[i]);
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) c[i] = (s != 0.0f) ? code_of<SR>(f[i], s, w[i]) : 0.0f;
 }
 
 template <typename CodeT>
@@ -112,59 +119,91 @@ struct Pack8<__half> {
 };
 
 // ------------------------------------------------------------ row groups
-// A team of `wpr` warps owns one row; lane t of the team holds vectors
-// t, t + 32*wpr, ... (VPL of them) in registers.
-template <typename CodeT, int VPL, bool SR>
+// Each warp owns two row slots of `slot_bytes` in dynamic shared memory and
+// walks the rows gw, gw + nw, ... (gw = its global warp index, nw = warps in
+// the grid).  Lane 0 issues the bulk copies and waits for them.
+template <typename CodeT, bool SR>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, CodeT* __restrict__ q,
-    float* __restrict__ scale, int wpr, SrArgs sr) {
-  __shared__ float red[kThreads / 32];
+    float* __restrict__ scale, SrArgs sr, uint32_t slot_bytes, unsigned int* status,
+    uint64_t limit_ns) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t bars[kThreads / 32][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int teams = (kThreads / 32) / wpr;
-  const int team = warp / wpr, wit = warp % wpr;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * teams + team;
-  const bool active = row < rows;
+  const int wpc = blockDim.x >> 5;
+  const uint32_t row_bytes = static_cast<uint32_t>(cols) * 2u;
   const int nvec = static_cast<int>(cols >> 3);
-  const int tl = wit * 32 + lane, stride = wpr * 32;
-
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (active ? row : 0) * ld);
-  uint4 v[VPL];
-  float amax = 0.0f;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int vi = tl + j * stride;
-    v[j] = (active && vi < nvec) ? __ldg(xr + vi) : make_uint4(0u, 0u, 0u, 0u);
-  }
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) amax = absmax8(amax, v[j]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-  if (wpr > 1) {
-    if (lane == 0) red[warp] = amax;
-    __syncthreads();
-    amax = red[team * wpr];
-    for (int w = 1; w < wpr; ++w) amax = fmaxf(amax, red[team * wpr + w]);
-  }
-  const float s = __fdiv_rn(amax, 127.0f);
-  if (active && tl == 0) scale[row] = s;
-  if (!active) return;
-
+  const uint8_t* slots = smem + static_cast<size_t>(warp) * 2 * slot_bytes;
+  const uint32_t slot_addr = ptx::smem_addr(slots);
+  const uint32_t bar[2] = {ptx::smem_addr(&bars[warp][0]), ptx::smem_addr(&bars[warp][1])};
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * wpc + warp;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * wpc;
   using P = Pack8<CodeT>;
-  typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + row * cols);
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int vi = tl + j * stride;
-    if (vi < nvec) {
-      float f[8], c[8];
-      unpack8(v[j], f);
-      codes8<SR>(f, s, sr, sr.offset + static_cast<uint64_t>(row * cols + vi * 8), c);
-      qr[vi] = P::pack(c);
+
+  uint32_t pending = 0u, pend_par = 0u;  // lane 0: copies in flight per slot, their parity
+  if (lane == 0) {
+    ptx::mbar_init(bar[0], 1);
+    ptx::mbar_init(bar[1], 1);
+    ptx::fence_mbar_init();
+    for (int k = 0; k < 2; ++k) {
+      const int64_t r = gw + k * nw;
+      if (r < rows) {
+        ptx::mbar_arrive_expect_tx(bar[k], row_bytes);
+        ptx::bulk_load(slot_addr + k * slot_bytes, x + r * ld, row_bytes, bar[k]);
+        pending |= 1u << k;
+      }
     }
+  }
+  __syncwarp();
+  int it = 0;
+  for (int64_t r = gw; r < rows; r += nw, ++it) {
+    const int b = it & 1;
+    int got = 1;
+    if (lane == 0) got = ptx::mbar_wait_timeout(bar[b], (it >> 1) & 1, limit_ns) ? 1 : 0;
+    got = __shfl_sync(0xFFFFFFFFu, got, 0);
+    if (!got) {
+      if (lane == 0) atomicOr(status, 1u);
+      break;
+    }
+    if (lane == 0) pending &= ~(1u << b);
+    const uint4* rowv = reinterpret_cast<const uint4*>(slots + b * slot_bytes);
+    float amax = 0.0f;
+    for (int v = lane; v < nvec; v += 32) amax = absmax8(amax, rowv[v]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (lane == 0) scale[r] = s;
+    const ScaleDiv d = make_scale_div(s);
+    typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + r * cols);
+    for (int v = lane; v < nvec; v += 32) {
+      float f[8], quo[8], c[8];
+      unpack8(rowv[v], f);
+      div8_same(f, d, quo);
+      codes_of<SR>(quo, sr, sr.offset + static_cast<uint64_t>(r * cols + v * 8), c);
+      qr[v] = P::pack(c);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const int64_t r2 = r + 2 * nw;
+      if (r2 < rows) {
+        ptx::fence_proxy_async_smem();  // the slot's reads above precede the copy into it
+        ptx::mbar_arrive_expect_tx(bar[b], row_bytes);
+        ptx::bulk_load(slot_addr + b * slot_bytes, x + r2 * ld, row_bytes, bar[b]);
+        pending |= 1u << b;
+        pend_par = (pend_par & ~(1u << b)) | (static_cast<uint32_t>(((it + 2) >> 1) & 1) << b);
+      }
+    }
+  }
+  // after a timeout: never leave a copy in flight into this block's memory
+  if (lane == 0) {
+    for (int k = 0; k < 2; ++k)
+      if (pending & (1u << k))
+        if (!ptx::mbar_wait_timeout(bar[k], (pend_par >> k) & 1u, limit_ns)) atomicOr(status, 1u);
   }
 }
 
-// Rows too long for registers: one block per row, two sweeps (the second
-// re-reads the row, which is still in L2).
+// Rows too long for two shared-memory slots: one block per row, two sweeps
+// over global memory (the second hits L2).
 template <typename CodeT, bool SR>
 __global__ void __launch_bounds__(kThreads) quant_rows_long_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, CodeT* __restrict__ q,
@@ -185,12 +224,14 @@ __global__ void __launch_bounds__(kThreads) quant_rows_long_kernel(
   for (int w = 1; w < kThreads / 32; ++w) amax = fmaxf(amax, red[w]);
   const float s = __fdiv_rn(amax, 127.0f);
   if (threadIdx.x == 0) scale[row] = s;
+  const ScaleDiv d = make_scale_div(s);
   using P = Pack8<CodeT>;
   typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + row * cols);
   for (int64_t vi = threadIdx.x; vi < nvec; vi += kThreads) {
-    float f[8], c[8];
+    float f[8], quo[8], c[8];
     unpack8(__ldg(xr + vi), f);
-    codes8<SR>(f, s, sr, sr.offset + static_cast<uint64_t>(row * cols + vi * 8), c);
+    div8_same(f, d, quo);
+    codes_of<SR>(quo, sr, sr.offset + static_cast<uint64_t>(row * cols + vi * 8), c);
     qr[vi] = P::pack(c);
   }
 }
@@ -198,7 +239,8 @@ __global__ void __launch_bounds__(kThreads) quant_rows_long_kernel(
 // --------------------------------------------------------- column groups
 // Pass 1: absmax of each column over this block's rows, merged by atomic max
 // on the bit pattern (absolute values are >= +0, whose bits order as
-// unsigned integers).  Lane = one 8-column vector, warp = row phase.
+// unsigned integers).  Lane = one 8-column vector, warp = row phase; eight
+// rows in flight per thread.
 __global__ void __launch_bounds__(kThreads) col_absmax_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
     int64_t rows_per_block, unsigned int* __restrict__ amax_bits) {
@@ -214,12 +256,13 @@ __global__ void __launch_bounds__(kThreads) col_absmax_kernel(
   if (vi < nvec) {
     const uint16_t* base = x + vi * 8;
     int64_t r = r0 + warp;
-    for (; r + 3 * 8 < r1; r += 4 * 8) {
-      uint4 a[4];
+    constexpr int U = 8;
+    for (; r + (U - 1) * 8 < r1; r += U * 8) {
+      uint4 a[U];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] = __ldg(reinterpret_cast<const uint4*>(base + (r + u * 8) * ld));
+      for (int u = 0; u < U; ++u) a[u] = __ldg(reinterpret_cast<const uint4*>(base + (r + u * 8) * ld));
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < U; ++u) {
         float f[8];
         unpack8(a[u], f);
 #pragma unroll
@@ -247,117 +290,217 @@ __global__ void __launch_bounds__(kThreads) col_absmax_kernel(
   }
 }
 
-// Pass 2: a 256-row x 64-column tile.  Thread (rg, cg) loads rows
-// rg*8 .. rg*8+7 of column group cg (8 columns, one 16-byte vector each),
-// quantizes the 8x8 block, transposes it in registers, and stores the 8
-// column vectors into the shared tile [64 cols][256 rows]; the 16-byte (f16)
-// or 8-byte (int8) slot of row group rg in column row rho is placed at slot
-// rg ^ (rho / 8) so that both the writes and the row-wise read-out spread
-// over the banks.  The read-out stores whole rows of the transposed codes.
+// Pass 2: scale = absmax / 127, in place, before any code is computed.
+__global__ void col_scale_kernel(unsigned int* __restrict__ amax_bits, int64_t cols) {
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c < cols) amax_bits[c] = __float_as_uint(__fdiv_rn(__uint_as_float(amax_bits[c]), 127.0f));
+}
+
+// Pass 3: codes of 256-row x 64-column tiles.  Thread 0 keeps a two-deep ring
+// of input tiles filled with 2-D TMA loads (rows of 128 bytes, no swizzle).
+// Thread (rg, cg) reads rows rg*8 .. rg*8+7 of column group cg (8 columns,
+// one 16-byte vector per row) from the ring, quantizes the 8x8 block, packs
+// the codes column by column, and stores the 8 column vectors into the
+// output tile [64 cols][256 rows]; the slot of row group rg in column row rho
+// is placed at rg ^ (rho / 8) so that both the writes and the row-wise
+// read-out spread over the banks.  The read-out stores whole rows of the
+// transposed codes.
+constexpr int kColTileRows = 256, kColTileCols = 64;
+constexpr uint32_t kColTileBytes = kColTileRows * kColTileCols * 2;
+
+template <typename CodeT>
+struct ColPack;
+template <>
+struct ColPack<int8_t> {
+  using Vec = uint2;
+  // rows 2p, 2p+1 of the 8-row block: bytes 2p, 2p+1 of the column vector
+  __device__ __forceinline__ static void put2(Vec& v, int p, float a, float b) {
+    const uint32_t two = (static_cast<uint32_t>(__float2int_rn(a)) & 0xFFu) |
+                         ((static_cast<uint32_t>(__float2int_rn(b)) & 0xFFu) << 8);
+    if (p < 2) v.x |= two << (16 * p); else v.y |= two << (16 * (p - 2));
+  }
+};
+template <>
+struct ColPack<__half> {
+  using Vec = uint4;
+  __device__ __forceinline__ static void put2(Vec& v, int p, float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(&h);
+    switch (p) {
+      case 0: v.x = u; break;
+      case 1: v.y = u; break;
+      case 2: v.z = u; break;
+      default: v.w = u; break;
+    }
+  }
+};
+
 template <typename CodeT, bool SR>
 __global__ void __launch_bounds__(kThreads) quant_cols_kernel(
-    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-    const unsigned int* __restrict__ amax_bits, CodeT* __restrict__ q, SrArgs sr) {
-  using P = Pack8<CodeT>;
-  using Vec = typename P::Vec;
-  __shared__ Vec tile[64][32];
+    const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
+    const float* __restrict__ scale, CodeT* __restrict__ q, int64_t col_tiles, int64_t tiles,
+    SrArgs sr, unsigned int* status, uint64_t limit_ns) {
+  using CP = ColPack<CodeT>;
+  using Vec = typename CP::Vec;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint64_t bars[2];
+  __shared__ int got_tile;
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
+  const uint32_t in_addr = ptx::smem_addr(smem);
+  Vec(*out)[32] = reinterpret_cast<Vec(*)[32]>(smem + 2 * kColTileBytes);
   const int t = threadIdx.x;
   const int cg = t & 7, rg = t >> 3;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 256;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;
-  const int64_t c = c0 + cg * 8;
-  const int64_t rb = r0 + rg * 8;
-  if (c < cols) {
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      v[i] = (rb + i < rows) ? __ldg(reinterpret_cast<const uint4*>(x + (rb + i) * ld + c))
-                             : make_uint4(0u, 0u, 0u, 0u);
-    float s[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) s[j] = __fdiv_rn(__uint_as_float(__ldg(amax_bits + c + j)), 127.0f);
-    float cd[8][8];  // [row i][col j]
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float f[8], out[8];
-      unpack8(v[i], f);
-      uint32_t w[8];
-      if (SR) {
-        philox_words8(sr.seed, sr.offset + static_cast<uint64_t>((rb + i) * cols + c), sr.stream_id, w);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = 0u;
+  const int warp = t >> 5, lane = t & 31;
+  const uint32_t bar[2] = {ptx::smem_addr(&bars[0]), ptx::smem_addr(&bars[1])};
+
+  uint32_t pending = 0u, pend_par = 0u;  // thread 0 only
+  auto issue = [&](int b, int64_t tix) {
+    ptx::mbar_arrive_expect_tx(bar[b], kColTileBytes);
+    ptx::tma_load_2d(in_addr + b * kColTileBytes, &tmx, bar[b],
+                     static_cast<int32_t>((tix % col_tiles) * kColTileCols),
+                     static_cast<int32_t>((tix / col_tiles) * kColTileRows));
+  };
+  if (t == 0) {
+    ptx::mbar_init(bar[0], 1);
+    ptx::mbar_init(bar[1], 1);
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tmx);
+    for (int k = 0; k < 2; ++k) {
+      const int64_t tix = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
+      if (tix < tiles) {
+        issue(k, tix);
+        pending |= 1u << k;
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) out[j] = (s[j] != 0.0f) ? code_of<SR>(f[j], s[j], w[j]) : 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) cd[i][j] = out[j];
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float colv[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) colv[i] = cd[i][j];
-      const int rho = cg * 8 + j;
-      tile[rho][rg ^ cg] = P::pack(colv);
     }
   }
   __syncthreads();
-  // read-out: warp w handles rows rho = w, w+8, ..., lane = row-group slot
-  const int warp = t >> 5, lane = t & 31;
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int rho = warp + it * 8;
-    const int64_t cc = c0 + rho;
-    const int64_t rr = r0 + lane * 8;
-    if (cc < cols && rr < rows) {
-      Vec* dst = reinterpret_cast<Vec*>(q + cc * rows + rr);
-      *dst = tile[rho][lane ^ (rho >> 3)];
+  int it = 0;
+  for (int64_t tix = blockIdx.x; tix < tiles; tix += gridDim.x, ++it) {
+    const int b = it & 1;
+    if (t == 0) {
+      got_tile = ptx::mbar_wait_timeout(bar[b], (it >> 1) & 1, limit_ns) ? 1 : 0;
+      if (got_tile) pending &= ~(1u << b);
+      else atomicOr(status, 1u);
     }
+    __syncthreads();
+    if (!got_tile) break;
+    const int64_t r0 = (tix / col_tiles) * kColTileRows, c0 = (tix % col_tiles) * kColTileCols;
+    const int64_t c = c0 + cg * 8, rb = r0 + rg * 8;
+    if (c < cols) {
+      float s[8], r[8];
+      bool all_fast = true;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        s[j] = __ldg(scale + c + j);
+        all_fast = all_fast && scale_is_fast(s[j]);
+        r[j] = __frcp_rn(s[j]);
+      }
+      const uint8_t* in = smem + b * kColTileBytes + (rg * 8) * 128 + cg * 16;
+      Vec colv[8];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {  // rows 2p and 2p+1 of the 8-row block
+        float cd[2][8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = 2 * p + h;
+          float f[8], quo[8];
+          unpack8(*reinterpret_cast<const uint4*>(in + i * 128), f);
+          div8_each(f, s, r, all_fast, quo);
+          codes_of<SR>(quo, sr, sr.offset + static_cast<uint64_t>((rb + i) * cols + c), cd[h]);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (p == 0) colv[j] = Vec{};
+          CP::put2(colv[j], p, cd[0][j], cd[1][j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) out[cg * 8 + j][rg ^ cg] = colv[j];
+    }
+    __syncthreads();  // the input slot is consumed and the output tile complete
+    if (t == 0) {
+      const int64_t nt = tix + 2 * static_cast<int64_t>(gridDim.x);
+      if (nt < tiles) {
+        ptx::fence_proxy_async_smem();
+        issue(b, nt);
+        pending |= 1u << b;
+        pend_par = (pend_par & ~(1u << b)) | (static_cast<uint32_t>(((it + 2) >> 1) & 1) << b);
+      }
+    }
+    // read-out: warp w handles rows rho = w, w+8, ..., lane = row-group slot
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int rho = warp + k * 8;
+      const int64_t cc = c0 + rho;
+      const int64_t rr = r0 + lane * 8;
+      if (cc < cols && rr < rows)
+        *reinterpret_cast<Vec*>(q + cc * rows + rr) = out[rho][lane ^ (rho >> 3)];
+    }
+    __syncthreads();  // the output tile may be rewritten
+  }
+  if (t == 0) {
+    for (int k = 0; k < 2; ++k)
+      if (pending & (1u << k))
+        if (!ptx::mbar_wait_timeout(bar[k], (pend_par >> k) & 1u, limit_ns)) atomicOr(status, 1u);
   }
 }
 
-// Pass 3: scale = absmax / 127, in place.
-__global__ void col_scale_kernel(unsigned int* __restrict__ amax_bits, int64_t cols) {
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (c < cols) {
-    const float s = __fdiv_rn(__uint_as_float(amax_bits[c]), 127.0f);
-    amax_bits[c] = __float_as_uint(s);
+// ------------------------------------------------------------------ host
+// Resident blocks per SM of a kernel at a given dynamic shared-memory size.
+template <typename Kernel>
+int blocks_per_sm(Kernel k, int threads, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem) != cudaSuccess || n < 1)
+    n = 1;
+  return n;
+}
+
+constexpr size_t kMaxDynSmem = 200 * 1024;
+
+// per-device "dynamic shared memory attribute set" flags, one set per kernel
+template <typename Kernel>
+cudaError_t allow_smem(Kernel k, bool* done) {
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxDynSmem));
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
   }
+  return cudaSuccess;
 }
 
 template <typename CodeT, bool SR>
 cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
-                          float* scale, const SrArgs& sr, cudaStream_t stream) {
-  const int64_t nvec = cols >> 3;
+                          float* scale, const SrArgs& sr, const DeviceInfo& dev,
+                          cudaStream_t stream) {
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   CodeT* qp = static_cast<CodeT*>(q);
-  int wpr = 0, vpl = 0;
-  for (int w = 1; w <= 8 && !wpr; w <<= 1)
-    for (int p = 2; p <= 8; p <<= 1)
-      if (static_cast<int64_t>(w) * 32 * p >= nvec) {
-        wpr = w;
-        vpl = p;
-        break;
-      }
-  if (!wpr) {
+  const uint32_t slot = static_cast<uint32_t>((cols * 2 + 127) / 128 * 128);
+  if (2ull * slot > kMaxDynSmem) {
     quant_rows_long_kernel<CodeT, SR><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(
         xp, rows, cols, ld, qp, scale, sr);
     return cudaGetLastError();
   }
-  const int64_t teams = (kThreads / 32) / wpr;
-  const unsigned blocks = static_cast<unsigned>((rows + teams - 1) / teams);
-  switch (vpl) {
-    case 2:
-      quant_rows_kernel<CodeT, 2, SR><<<blocks, kThreads, 0, stream>>>(xp, rows, cols, ld, qp, scale, wpr, sr);
-      break;
-    case 4:
-      quant_rows_kernel<CodeT, 4, SR><<<blocks, kThreads, 0, stream>>>(xp, rows, cols, ld, qp, scale, wpr, sr);
-      break;
-    default:
-      quant_rows_kernel<CodeT, 8, SR><<<blocks, kThreads, 0, stream>>>(xp, rows, cols, ld, qp, scale, wpr, sr);
-      break;
-  }
+  static bool attr[64] = {};
+  cudaError_t e = allow_smem(quant_rows_kernel<CodeT, SR>, attr);
+  if (e != cudaSuccess) return e;
+  // warps per block: as many as fit two slots each in ~100 KB (at least one)
+  int wpc = static_cast<int>((100u * 1024u) / (2u * slot));
+  if (wpc > kThreads / 32) wpc = kThreads / 32;
+  if (wpc < 1) wpc = 1;
+  const size_t smem = static_cast<size_t>(wpc) * 2 * slot;
+  const int occ = blocks_per_sm(quant_rows_kernel<CodeT, SR>, wpc * 32, smem);
+  const int sms = dev.sms > 0 ? dev.sms : 148;
+  const int64_t need = (rows + wpc - 1) / wpc;
+  const int64_t cap = static_cast<int64_t>(sms) * occ;
+  const unsigned blocks = static_cast<unsigned>(need < cap ? need : cap);
+  quant_rows_kernel<CodeT, SR><<<blocks, wpc * 32, smem, stream>>>(
+      xp, rows, cols, ld, qp, scale, sr, slot, dev.status_word, kWaitLimitNs);
   return cudaGetLastError();
 }
 
@@ -367,27 +510,44 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
                           cudaStream_t stream) {
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   unsigned int* amax = reinterpret_cast<unsigned int*>(scale);
-  cudaError_t err = cudaMemsetAsync(amax, 0, static_cast<size_t>(cols) * sizeof(float), stream);
+  CUtensorMap tmx;
+  if (!encode_tensor_map_2d(&tmx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, cols, ld,
+                            kColTileCols, kColTileRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  static bool attr[64] = {};
+  cudaError_t err = allow_smem(quant_cols_kernel<CodeT, SR>, attr);
   if (err != cudaSuccess) return err;
+  err = cudaMemsetAsync(amax, 0, static_cast<size_t>(cols) * sizeof(float), stream);
+  if (err != cudaSuccess) return err;
+  const int sms = dev.sms > 0 ? dev.sms : 148;
+  // pass 1: one wave of blocks
   const int64_t nvec = cols >> 3;
   const int64_t gx = (nvec + 31) / 32;
-  const int64_t target = static_cast<int64_t>(dev.sms > 0 ? dev.sms : 148) * 8;
+  static const int occ1 = blocks_per_sm(col_absmax_kernel, kThreads, 0);
+  const int64_t target = static_cast<int64_t>(sms) * occ1;
   int64_t gy = target / gx;
-  if (gy < 1) gy = 1;
   const int64_t max_gy = (rows + 63) / 64;
   if (gy > max_gy) gy = max_gy;
+  if (gy < 1) gy = 1;
   if (gy > 65535) gy = 65535;
   const int64_t rpb = (rows + gy - 1) / gy;
   col_absmax_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), kThreads, 0, stream>>>(
       xp, rows, cols, ld, rpb, amax);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const dim3 grid2(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 255) / 256));
-  quant_cols_kernel<CodeT, SR><<<grid2, kThreads, 0, stream>>>(xp, rows, cols, ld, amax,
-                                                               static_cast<CodeT*>(q), sr);
+  col_scale_kernel<<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(amax, cols);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  col_scale_kernel<<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(amax, cols);
+  // pass 3
+  const int64_t col_tiles = (cols + kColTileCols - 1) / kColTileCols;
+  const int64_t tiles = col_tiles * ((rows + kColTileRows - 1) / kColTileRows);
+  const size_t smem = 1024 + 2 * kColTileBytes + 64 * 32 * sizeof(typename ColPack<CodeT>::Vec);
+  static const int occ3 = blocks_per_sm(quant_cols_kernel<CodeT, SR>, kThreads, smem);
+  const int64_t cap = static_cast<int64_t>(sms) * occ3;
+  const unsigned blocks = static_cast<unsigned>(tiles < cap ? tiles : cap);
+  quant_cols_kernel<CodeT, SR><<<blocks, kThreads, smem, stream>>>(
+      tmx, rows, cols, scale, static_cast<CodeT*>(q), col_tiles, tiles, sr, dev.status_word,
+      kWaitLimitNs);
   return cudaGetLastError();
 }
 
@@ -395,14 +555,14 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
 
 cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                  int8mp_round mode, const SrArgs& sr, void* q,
-                                 int8mp_codes codes, float* scale, const DeviceInfo&,
+                                 int8mp_codes codes, float* scale, const DeviceInfo& dev,
                                  cudaStream_t stream) {
   const bool s = mode == INT8MP_SR;
   if (codes == INT8MP_CODES_S8)
-    return s ? rows_dispatch<int8_t, true>(x, rows, cols, ld, q, scale, sr, stream)
-             : rows_dispatch<int8_t, false>(x, rows, cols, ld, q, scale, sr, stream);
-  return s ? rows_dispatch<__half, true>(x, rows, cols, ld, q, scale, sr, stream)
-           : rows_dispatch<__half, false>(x, rows, cols, ld, q, scale, sr, stream);
+    return s ? rows_dispatch<int8_t, true>(x, rows, cols, ld, q, scale, sr, dev, stream)
+             : rows_dispatch<int8_t, false>(x, rows, cols, ld, q, scale, sr, dev, stream);
+  return s ? rows_dispatch<__half, true>(x, rows, cols, ld, q, scale, sr, dev, stream)
+           : rows_dispatch<__half, false>(x, rows, cols, ld, q, scale, sr, dev, stream);
 }
 
 cudaError_t launch_quantize_cols(const void* x, int64_t rows, int64_t cols, int64_t ld,

@@ -73,7 +73,8 @@ def _edge_input(rows, cols, seed):
     return x.to(torch.bfloat16)
 
 
-ROW_SHAPES = [(256, 512), (8, 8), (77, 136), (300, 5632), (40, 14336), (9, 24576), (1, 2048)]
+ROW_SHAPES = [(256, 512), (8, 8), (77, 136), (300, 5632), (40, 14336), (9, 24576), (1, 2048),
+              (3, 53248)]
 COL_SHAPES = [(256, 512), (8, 8), (264, 136), (1032, 64), (520, 2048), (16, 4096)]
 
 
@@ -252,3 +253,13 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     acc = m.int8mp_mm_s32(ad, bd).cpu().numpy()
     np.testing.assert_array_equal(acc, oracle.mm_s32(a.numpy(), b.numpy(), M, N, K))
     assert m.int8mp_poll_device_status() == m.INT8MP_OK
+
+
+def test_division_matches_ieee_for_every_bf16_pair():
+    # the quantizers' reciprocal-and-FMA quotient against __fdiv_rn on every
+    # (absmax, x) pair of bf16 values with absmax > 0 finite and |x| <= absmax
+    bad, pairs, fast, first = m.int8mp_debug_check_division()
+    assert pairs > 1_000_000_000
+    print(f"division check: {pairs} pairs, {fast} on the fast path, {bad} differ")
+    assert fast > 300_000_000  # the fast path (scales in [2^-100, 2^10]) is exercised
+    assert bad == 0, f"{bad} quotients differ; (absmax, x, largest |x|) bf16 bits = {first}"
