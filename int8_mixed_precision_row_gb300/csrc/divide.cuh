@@ -16,8 +16,9 @@
 // every intermediate is a normal number.  Otherwise IEEE division is used.
 // div_scale() is that rule for one element; int8mp_debug_check_division()
 // compares it with __fdiv_rn over every such (x, absmax) pair of bf16 values.
-// The vector forms below give, element by element, the same results: they
-// take the fast path for all elements or fall back to IEEE division for all.
+// The vector forms below give, element by element, the same results: a batch
+// of elements takes the fast path only if every element of it qualifies, and
+// is otherwise recomputed with IEEE division.
 #pragma once
 
 namespace int8mp {
@@ -56,33 +57,42 @@ __device__ __forceinline__ float div_scale(float x, const ScaleDiv& d) {
   return __fdiv_rn(x, d.s);
 }
 
-// v[i] = x[i] / s for eight elements of one group (s >= 0; s = 0 gives 0)
-__device__ __forceinline__ void div8_same(const float (&x)[8], const ScaleDiv& d, float (&v)[8]) {
+// Fast quotients of eight elements of one group; returns whether all of them
+// took the fast path (otherwise redo them with div8_ieee).
+__device__ __forceinline__ bool div8_try(const float (&x)[8], const ScaleDiv& d, float (&v)[8]) {
   bool ok = d.fast;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     v[i] = div_fast(x[i], d.s, d.r);
     ok = ok && fast_element(x[i]);
   }
-  if (!ok) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = d.s != 0.0f ? __fdiv_rn(x[i], d.s) : 0.0f;
-  }
+  return ok;
 }
 
-// v[i] = x[i] / s[i] for eight elements of eight groups (s[i] >= 0)
-__device__ __forceinline__ void div8_each(const float (&x)[8], const float (&s)[8],
-                                          const float (&r)[8], bool all_fast, float (&v)[8]) {
+// Same for eight elements of eight groups (scales s[i], reciprocals r[i]).
+__device__ __forceinline__ bool div8_each_try(const float (&x)[8], const float (&s)[8],
+                                              const float (&r)[8], bool all_fast,
+                                              float (&v)[8]) {
   bool ok = all_fast;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     v[i] = div_fast(x[i], s[i], r[i]);
     ok = ok && fast_element(x[i]);
   }
-  if (!ok) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = s[i] != 0.0f ? __fdiv_rn(x[i], s[i]) : 0.0f;
-  }
+  return ok;
 }
+
+// IEEE quotients (a zero scale gives 0: the group is all zero).
+__device__ __forceinline__ void div8_ieee(const float (&x)[8], float s, float (&v)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = s != 0.0f ? __fdiv_rn(x[i], s) : 0.0f;
+}
+__device__ __forceinline__ void div8_each_ieee(const float (&x)[8], const float (&s)[8],
+                                               float (&v)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = s[i] != 0.0f ? __fdiv_rn(x[i], s[i]) : 0.0f;
+}
+
+__device__ __forceinline__ bool scale_is_normal(float s) { return s >= 0x1p-126f; }
 
 }  // namespace int8mp

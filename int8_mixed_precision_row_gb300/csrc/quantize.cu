@@ -46,16 +46,13 @@ constexpr int kThreads = 256;
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// max(m, |v_0|, ..., |v_7|) as a tree: a dependency depth of 4, not 8
 __device__ __forceinline__ float absmax8(float m, const uint4& v) {
-  m = fmaxf(m, fabsf(bf16_lo(v.x)));
-  m = fmaxf(m, fabsf(bf16_hi(v.x)));
-  m = fmaxf(m, fabsf(bf16_lo(v.y)));
-  m = fmaxf(m, fabsf(bf16_hi(v.y)));
-  m = fmaxf(m, fabsf(bf16_lo(v.z)));
-  m = fmaxf(m, fabsf(bf16_hi(v.z)));
-  m = fmaxf(m, fabsf(bf16_lo(v.w)));
-  m = fmaxf(m, fabsf(bf16_hi(v.w)));
-  return m;
+  const float a = fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x)));
+  const float b = fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)));
+  const float c = fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z)));
+  const float d = fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)));
+  return fmaxf(m, fmaxf(fmaxf(a, b), fmaxf(c, d)));
 }
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -69,6 +66,12 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 __device__ __forceinline__ float code_rne(float v) {
   return __fadd_rn(fminf(fmaxf(rintf(v), -127.0f), 127.0f), 0.0f);
 }
+// Same when the group scale is a normal number s = RN(absmax / 127): then
+// s >= (absmax / 127)(1 - 2^-24), so |v| <= 127 (1 + 2^-23) < 127.5 and
+// rounding cannot leave [-127, 127]; the clamp is dropped.
+__device__ __forceinline__ float code_rne_normal_scale(float v) {
+  return __fadd_rn(rintf(v), 0.0f);
+}
 __device__ __forceinline__ float code_sr(float v, uint32_t word) {
   const float f = floorf(v);
   const float fr = __fsub_rn(v, f);
@@ -77,14 +80,18 @@ __device__ __forceinline__ float code_sr(float v, uint32_t word) {
 }
 
 // Eight codes from eight quotients (elements n0 .. n0+7 of the SR stream).
+// normal_scales: every element's group scale is at least 2^-126.
 template <bool SR>
 __device__ __forceinline__ void codes_of(const float (&v)[8], const SrArgs& sr, uint64_t n0,
-                                         float (&c)[8]) {
+                                         bool normal_scales, float (&c)[8]) {
   if (SR) {
     uint32_t w[8];
     philox_words8(sr.seed, n0, sr.stream_id, w);
 #pragma unroll
     for (int i = 0; i < 8; ++i) c[i] = code_sr(v[i], w[i]);
+  } else if (normal_scales) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = code_rne_normal_scale(v[i]);
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) c[i] = code_rne(v[i]);
@@ -119,34 +126,77 @@ struct Pack8<__half> {
 };
 
 // ------------------------------------------------------------ row groups
-// Each warp owns two row slots of `slot_bytes` in dynamic shared memory and
-// walks the rows gw, gw + nw, ... (gw = its global warp index, nw = warps in
-// the grid).  Lane 0 issues the bulk copies and waits for them.
+// The block's warps form teams of T warps (T = 1, 2, 4 or 8).  Each team owns
+// two row slots of `slot_bytes` in dynamic shared memory and walks the rows
+// g, g + n, ... (g = its global team index, n = teams in the grid).  The
+// team's first lane issues the bulk copies, waits for them and publishes the
+// outcome; each warp of the team reduces and quantizes a strided share of the
+// row's 16-byte vectors, and the partial absmax values meet in shared memory.
+// The copy of the next row starts as soon as every warp of the team has left
+// the previous one.
+__device__ __forceinline__ void team_sync(int team, int T) {
+  if (T == 1) {
+    __syncwarp();
+  } else {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(T * 32) : "memory");
+  }
+}
+
+// Codes of two 16-byte vectors a, b of one row (b absent when !has_b): exact
+// quotients (fast form, or IEEE division for both vectors if either has an
+// element outside the fast form's range), then the rounding.
+template <typename CodeT, bool SR>
+__device__ __forceinline__ void quantize_two(const uint4& a, const uint4& b, bool has_b,
+                                             const ScaleDiv& d, bool normal, const SrArgs& sr,
+                                             uint64_t na, uint64_t nb,
+                                             typename Pack8<CodeT>::Vec* qa,
+                                             typename Pack8<CodeT>::Vec* qb) {
+  float fa[8], fb[8], va[8], vb[8], c[8];
+  unpack8(a, fa);
+  unpack8(b, fb);
+  const bool ok_a = div8_try(fa, d, va);
+  const bool ok_b = div8_try(fb, d, vb);
+  if (!(ok_a && ok_b)) {
+    div8_ieee(fa, d.s, va);
+    div8_ieee(fb, d.s, vb);
+  }
+  codes_of<SR>(va, sr, na, normal, c);
+  *qa = Pack8<CodeT>::pack(c);
+  if (has_b) {
+    codes_of<SR>(vb, sr, nb, normal, c);
+    *qb = Pack8<CodeT>::pack(c);
+  }
+}
+
 template <typename CodeT, bool SR>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, CodeT* __restrict__ q,
-    float* __restrict__ scale, SrArgs sr, uint32_t slot_bytes, unsigned int* status,
+    float* __restrict__ scale, SrArgs sr, uint32_t slot_bytes, int T, unsigned int* status,
     uint64_t limit_ns) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t bars[kThreads / 32][2];
+  __shared__ float red[kThreads / 32];
+  __shared__ int got_row[kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wpc = blockDim.x >> 5;
+  const int team = warp / T, wt = warp % T;
+  const int teams = (blockDim.x >> 5) / T;
+  const bool leader = wt == 0 && lane == 0;
   const uint32_t row_bytes = static_cast<uint32_t>(cols) * 2u;
   const int nvec = static_cast<int>(cols >> 3);
-  const uint8_t* slots = smem + static_cast<size_t>(warp) * 2 * slot_bytes;
+  const uint8_t* slots = smem + static_cast<size_t>(team) * 2 * slot_bytes;
   const uint32_t slot_addr = ptx::smem_addr(slots);
-  const uint32_t bar[2] = {ptx::smem_addr(&bars[warp][0]), ptx::smem_addr(&bars[warp][1])};
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * wpc + warp;
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * wpc;
+  const uint32_t bar[2] = {ptx::smem_addr(&bars[team][0]), ptx::smem_addr(&bars[team][1])};
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * teams + team;
+  const int64_t n = static_cast<int64_t>(gridDim.x) * teams;
   using P = Pack8<CodeT>;
 
-  uint32_t pending = 0u, pend_par = 0u;  // lane 0: copies in flight per slot, their parity
-  if (lane == 0) {
+  uint32_t pending = 0u, pend_par = 0u;  // leader: copies in flight per slot, their parity
+  if (leader) {
     ptx::mbar_init(bar[0], 1);
     ptx::mbar_init(bar[1], 1);
     ptx::fence_mbar_init();
     for (int k = 0; k < 2; ++k) {
-      const int64_t r = gw + k * nw;
+      const int64_t r = g + k * n;
       if (r < rows) {
         ptx::mbar_arrive_expect_tx(bar[k], row_bytes);
         ptx::bulk_load(slot_addr + k * slot_bytes, x + r * ld, row_bytes, bar[k]);
@@ -154,48 +204,55 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
       }
     }
   }
-  __syncwarp();
   int it = 0;
-  for (int64_t r = gw; r < rows; r += nw, ++it) {
+  for (int64_t r = g; r < rows; r += n, ++it) {
     const int b = it & 1;
-    int got = 1;
-    if (lane == 0) got = ptx::mbar_wait_timeout(bar[b], (it >> 1) & 1, limit_ns) ? 1 : 0;
-    got = __shfl_sync(0xFFFFFFFFu, got, 0);
-    if (!got) {
-      if (lane == 0) atomicOr(status, 1u);
-      break;
+    if (leader) {
+      const bool ok = ptx::mbar_wait_timeout(bar[b], (it >> 1) & 1, limit_ns);
+      got_row[team] = ok ? 1 : 0;
+      if (ok) pending &= ~(1u << b);
+      else atomicOr(status, 1u);
     }
-    if (lane == 0) pending &= ~(1u << b);
+    team_sync(team, T);  // the row has landed; every warp has left row it-1
+    if (!got_row[team]) break;
+    if (leader && it >= 1 && r + n < rows) {
+      // slot (it+1)&1 held row it-1, which every warp of the team has left
+      const int nb = (it + 1) & 1;
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive_expect_tx(bar[nb], row_bytes);
+      ptx::bulk_load(slot_addr + nb * slot_bytes, x + (r + n) * ld, row_bytes, bar[nb]);
+      pending |= 1u << nb;
+      pend_par = (pend_par & ~(1u << nb)) | (static_cast<uint32_t>(((it + 1) >> 1) & 1) << nb);
+    }
     const uint4* rowv = reinterpret_cast<const uint4*>(slots + b * slot_bytes);
+    const int first = wt * 32 + lane, step = T * 32;
     float amax = 0.0f;
-    for (int v = lane; v < nvec; v += 32) amax = absmax8(amax, rowv[v]);
+    for (int v = first; v < nvec; v += step) amax = absmax8(amax, rowv[v]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const float s = __fdiv_rn(amax, 127.0f);
-    if (lane == 0) scale[r] = s;
-    const ScaleDiv d = make_scale_div(s);
-    typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + r * cols);
-    for (int v = lane; v < nvec; v += 32) {
-      float f[8], quo[8], c[8];
-      unpack8(rowv[v], f);
-      div8_same(f, d, quo);
-      codes_of<SR>(quo, sr, sr.offset + static_cast<uint64_t>(r * cols + v * 8), c);
-      qr[v] = P::pack(c);
+    if (T > 1) {
+      if (lane == 0) red[warp] = amax;
+      team_sync(team, T);
+      amax = red[team * T];
+      for (int w = 1; w < T; ++w) amax = fmaxf(amax, red[team * T + w]);
     }
-    __syncwarp();
-    if (lane == 0) {
-      const int64_t r2 = r + 2 * nw;
-      if (r2 < rows) {
-        ptx::fence_proxy_async_smem();  // the slot's reads above precede the copy into it
-        ptx::mbar_arrive_expect_tx(bar[b], row_bytes);
-        ptx::bulk_load(slot_addr + b * slot_bytes, x + r2 * ld, row_bytes, bar[b]);
-        pending |= 1u << b;
-        pend_par = (pend_par & ~(1u << b)) | (static_cast<uint32_t>(((it + 2) >> 1) & 1) << b);
-      }
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (leader) scale[r] = s;
+    const ScaleDiv d = make_scale_div(s);
+    const bool normal = scale_is_normal(s);
+    typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + r * cols);
+    const uint64_t nrow = sr.offset + static_cast<uint64_t>(r * cols);
+    for (int v = first; v < nvec; v += 2 * step) {
+      const int v2 = v + step;
+      const bool has2 = v2 < nvec;
+      const uint4 a = rowv[v];
+      const uint4 bb = has2 ? rowv[v2] : make_uint4(0u, 0u, 0u, 0u);
+      quantize_two<CodeT, SR>(a, bb, has2, d, normal, sr, nrow + 8u * v, nrow + 8u * v2,
+                              qr + v, qr + (has2 ? v2 : v));
     }
   }
   // after a timeout: never leave a copy in flight into this block's memory
-  if (lane == 0) {
+  if (leader) {
     for (int k = 0; k < 2; ++k)
       if (pending & (1u << k))
         if (!ptx::mbar_wait_timeout(bar[k], (pend_par >> k) & 1u, limit_ns)) atomicOr(status, 1u);
@@ -225,14 +282,13 @@ __global__ void __launch_bounds__(kThreads) quant_rows_long_kernel(
   const float s = __fdiv_rn(amax, 127.0f);
   if (threadIdx.x == 0) scale[row] = s;
   const ScaleDiv d = make_scale_div(s);
+  const bool normal = scale_is_normal(s);
   using P = Pack8<CodeT>;
   typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + row * cols);
   for (int64_t vi = threadIdx.x; vi < nvec; vi += kThreads) {
-    float f[8], quo[8], c[8];
-    unpack8(__ldg(xr + vi), f);
-    div8_same(f, d, quo);
-    codes_of<SR>(quo, sr, sr.offset + static_cast<uint64_t>(row * cols + vi * 8), c);
-    qr[vi] = P::pack(c);
+    const uint64_t n0 = sr.offset + static_cast<uint64_t>(row * cols + vi * 8);
+    quantize_two<CodeT, SR>(__ldg(xr + vi), make_uint4(0u, 0u, 0u, 0u), false, d, normal, sr,
+                            n0, n0, qr + vi, qr + vi);
   }
 }
 
@@ -336,7 +392,7 @@ struct ColPack<__half> {
 };
 
 template <typename CodeT, bool SR>
-__global__ void __launch_bounds__(kThreads) quant_cols_kernel(
+__global__ void __launch_bounds__(kThreads, 2) quant_cols_kernel(
     const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
     const float* __restrict__ scale, CodeT* __restrict__ q, int64_t col_tiles, int64_t tiles,
     SrArgs sr, unsigned int* status, uint64_t limit_ns) {
@@ -388,30 +444,48 @@ __global__ void __launch_bounds__(kThreads) quant_cols_kernel(
     const int64_t c = c0 + cg * 8, rb = r0 + rg * 8;
     if (c < cols) {
       float s[8], r[8];
-      bool all_fast = true;
+      bool all_fast = true, all_normal = true;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         s[j] = __ldg(scale + c + j);
         all_fast = all_fast && scale_is_fast(s[j]);
+        all_normal = all_normal && scale_is_normal(s[j]);
         r[j] = __frcp_rn(s[j]);
       }
+      const bool normal = all_normal;
       const uint8_t* in = smem + b * kColTileBytes + (rg * 8) * 128 + cg * 16;
       Vec colv[8];
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {  // rows 2p and 2p+1 of the 8-row block
-        float cd[2][8];
+      for (int j = 0; j < 8; ++j) colv[j] = Vec{};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int i = 2 * p + h;
-          float f[8], quo[8];
-          unpack8(*reinterpret_cast<const uint4*>(in + i * 128), f);
-          div8_each(f, s, r, all_fast, quo);
-          codes_of<SR>(quo, sr, sr.offset + static_cast<uint64_t>((rb + i) * cols + c), cd[h]);
+      for (int h = 0; h < 2; ++h) {  // rows 4h .. 4h+3 of the 8-row block
+        float quo[4][8];             // [row][column]
+        bool ok = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float f[8];
+          unpack8(*reinterpret_cast<const uint4*>(in + (4 * h + i) * 128), f);
+          ok = div8_each_try(f, s, r, all_fast, quo[i]) && ok;
+        }
+        if (!ok) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4*>(in + (4 * h + i) * 128), f);
+            div8_each_ieee(f, s, quo[i]);
+          }
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (p == 0) colv[j] = Vec{};
-          CP::put2(colv[j], p, cd[0][j], cd[1][j]);
+        for (int p = 0; p < 2; ++p) {  // row pairs (4h+2p, 4h+2p+1)
+          float cd[2][8];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i = 4 * h + 2 * p + e;
+            codes_of<SR>(quo[2 * p + e], sr, sr.offset + static_cast<uint64_t>((rb + i) * cols + c),
+                         normal, cd[e]);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) CP::put2(colv[j], 2 * h + p, cd[0][j], cd[1][j]);
         }
       }
 #pragma unroll
@@ -489,18 +563,19 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   static bool attr[64] = {};
   cudaError_t e = allow_smem(quant_rows_kernel<CodeT, SR>, attr);
   if (e != cudaSuccess) return e;
-  // warps per block: as many as fit two slots each in ~100 KB (at least one)
-  int wpc = static_cast<int>((100u * 1024u) / (2u * slot));
-  if (wpc > kThreads / 32) wpc = kThreads / 32;
-  if (wpc < 1) wpc = 1;
-  const size_t smem = static_cast<size_t>(wpc) * 2 * slot;
-  const int occ = blocks_per_sm(quant_rows_kernel<CodeT, SR>, wpc * 32, smem);
+  // 8 warps per block in teams of T: the smallest T whose slots (two per
+  // team) fit in 72 KB, so that at least three blocks share an SM
+  int T = 1;
+  while (T < 8 && static_cast<size_t>(kThreads / 32 / T) * 2 * slot > 72u * 1024u) T <<= 1;
+  const size_t smem = static_cast<size_t>(kThreads / 32 / T) * 2 * slot;
+  const int occ = blocks_per_sm(quant_rows_kernel<CodeT, SR>, kThreads, smem);
   const int sms = dev.sms > 0 ? dev.sms : 148;
-  const int64_t need = (rows + wpc - 1) / wpc;
+  const int64_t teams = kThreads / 32 / T;
+  const int64_t need = (rows + teams - 1) / teams;
   const int64_t cap = static_cast<int64_t>(sms) * occ;
   const unsigned blocks = static_cast<unsigned>(need < cap ? need : cap);
-  quant_rows_kernel<CodeT, SR><<<blocks, wpc * 32, smem, stream>>>(
-      xp, rows, cols, ld, qp, scale, sr, slot, dev.status_word, kWaitLimitNs);
+  quant_rows_kernel<CodeT, SR><<<blocks, kThreads, smem, stream>>>(
+      xp, rows, cols, ld, qp, scale, sr, slot, T, dev.status_word, kWaitLimitNs);
   return cudaGetLastError();
 }
 

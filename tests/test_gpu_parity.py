@@ -263,3 +263,22 @@ def test_division_matches_ieee_for_every_bf16_pair():
     print(f"division check: {pairs} pairs, {fast} on the fast path, {bad} differ")
     assert fast > 300_000_000  # the fast path (scales in [2^-100, 2^10]) is exercised
     assert bad == 0, f"{bad} quotients differ; (absmax, x, largest |x|) bf16 bits = {first}"
+
+
+@pytest.mark.parametrize("axis", [0, 1])
+def test_quantize_division_ties_bit_exact(axis):
+    # bf16 pairs where x / s sits on (or within rounding of) k + 1/2 and a
+    # reciprocal multiply would round the other way than IEEE division
+    from test_oracle_quantize import DIVISION_TIES
+    rows = np.zeros((len(DIVISION_TIES), 8), dtype=np.float32)
+    for i, (amax, xv) in enumerate(DIVISION_TIES):
+        rows[i, 0], rows[i, 1] = amax, xv
+        rows[i, 2:] = np.float32(xv) * np.array([1, -1, 0.5, -0.5, 0.25, 3], dtype=np.float32)
+    x = torch.from_numpy(rows).to(torch.bfloat16)
+    if axis == 1:
+        x = x.t().contiguous()
+    for codes in (m.INT8MP_CODES_S8, m.INT8MP_CODES_F16):
+        q, s = m.int8mp_quantize_rowwise(_dev(x), axis=axis, codes=codes)
+        qr, sr = oracle.quantize(bf16_bits(x), axis=axis)
+        np.testing.assert_array_equal(_f32_bits(s), sr.view(np.int32))
+        np.testing.assert_array_equal(_codes_np(q), qr)
