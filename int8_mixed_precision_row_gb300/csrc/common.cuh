@@ -52,6 +52,7 @@ enum class GemmOut { kBf16Scaled = 0, kS32 = 1 };
 
 struct GemmDebug {
   int drop_first_load = 0;        // test only: never issue the first TMA load
+  int single_cta = 0;             // test only: use the single-CTA kernel for any M
   uint64_t wait_limit_ns = kWaitLimitNs;
 };
 

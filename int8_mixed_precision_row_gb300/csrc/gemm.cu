@@ -69,6 +69,58 @@ __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned int* s
   atomicOr(status, 1u);
 }
 
+// One thread's output: row `row`, columns col0 .. col0+127, from its int32
+// totals.  bf16: (fp32(acc) * sA[row]) * sB[col], round to nearest even;
+// int32: the totals themselves.  Columns are 16-byte vectors (N % 8 == 0).
+__device__ __forceinline__ void store_rows(const GemmParams& p, int64_t row, int64_t col0,
+                                           const int32_t (&tot)[128]) {
+  if (row >= p.M) return;
+  if (p.mode == 1) {
+    int32_t* orow = static_cast<int32_t*>(p.out) + row * p.ldo;
+#pragma unroll
+    for (int v = 0; v < 32; ++v) {
+      const int64_t col = col0 + v * 4;
+      if (col < p.N)
+        *reinterpret_cast<int4*>(orow + col) =
+            make_int4(tot[4 * v], tot[4 * v + 1], tot[4 * v + 2], tot[4 * v + 3]);
+    }
+  } else {
+    const float sa = __ldg(p.sA + row);
+    uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.ldo;
+#pragma unroll
+    for (int v = 0; v < 16; ++v) {
+      const int64_t col = col0 + v * 8;
+      if (col < p.N) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float o0 = __fmul_rn(__fmul_rn(__int2float_rn(tot[v * 8 + 2 * e]), sa),
+                                     __ldg(p.sB + col + 2 * e));
+          const float o1 = __fmul_rn(__fmul_rn(__int2float_rn(tot[v * 8 + 2 * e + 1]), sa),
+                                     __ldg(p.sB + col + 2 * e + 1));
+          const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
+          w[e] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+}
+
+// Drain one 128-column half of a chunk accumulator (this warp's 32 lanes)
+// from tensor memory into the int32 totals; every fp32 value is an exact
+// integer below 2^24 in magnitude.
+__device__ __forceinline__ void drain_chunk(uint32_t taddr, int32_t (&tot)[128]) {
+#pragma unroll
+  for (int sub = 0; sub < 4; ++sub) {
+    uint32_t r[32];
+    ptx::tmem_ld_32cols(taddr + sub * 32, r);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) tot[sub * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_s8f16_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
@@ -224,54 +276,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kBN +
                                static_cast<uint32_t>(half * 128);
-#pragma unroll
-        for (int sub = 0; sub < 4; ++sub) {
-          uint32_t r[32];
-          ptx::tmem_ld_32cols(taddr + sub * 32, r);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) tot[sub * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
-        }
+        drain_chunk(taddr, tot);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
         ++chunk;
       }
       if (!ok) break;
-      const int64_t row = static_cast<int64_t>(m0) + quad * 32 + lane;
-      const int64_t col0 = static_cast<int64_t>(n0) + half * 128;
-      if (row < p.M) {
-        if (p.mode == 1) {
-          int32_t* orow = static_cast<int32_t*>(p.out) + row * p.ldo;
-#pragma unroll
-          for (int v = 0; v < 32; ++v) {
-            const int64_t col = col0 + v * 4;
-            if (col < p.N)
-              *reinterpret_cast<int4*>(orow + col) =
-                  make_int4(tot[4 * v], tot[4 * v + 1], tot[4 * v + 2], tot[4 * v + 3]);
-          }
-        } else {
-          const float sa = __ldg(p.sA + row);
-          uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.ldo;
-#pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            const int64_t col = col0 + v * 8;
-            if (col < p.N) {
-              uint32_t w[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float o0 = __fmul_rn(__fmul_rn(__int2float_rn(tot[v * 8 + 2 * e]), sa),
-                                           __ldg(p.sB + col + 2 * e));
-                const float o1 = __fmul_rn(__fmul_rn(__int2float_rn(tot[v * 8 + 2 * e + 1]), sa),
-                                           __ldg(p.sB + col + 2 * e + 1));
-                const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
-                w[e] = *reinterpret_cast<const uint32_t*>(&h);
-              }
-              *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-        }
-      }
+      store_rows(p, static_cast<int64_t>(m0) + quad * 32 + lane,
+                 static_cast<int64_t>(n0) + half * 128, tot);
     }
     if (!ok && lane == 0) raise_abort(abort, p.status);
   }
@@ -282,6 +295,209 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------ CTA-pair kernel
+// Same computation on 256x256 tiles by a cluster of two CTAs (one per SM of
+// a pair).  CTA r loads rows r*128 .. r*128+127 of the tile's A block and
+// columns r*128 .. r*128+127 of its B block (32 KB per stage instead of
+// 48 KB, so six stages fit); the even CTA's MMA thread issues
+// tcgen05.mma.cta_group::2, which reads both CTAs' shared memory and writes
+// each CTA's 128 accumulator rows into that CTA's tensor memory.  Both CTAs'
+// loads complete on the even CTA's full barrier; the MMA commits arrive on
+// both CTAs' empty and accumulator-full barriers; the odd CTA's epilogue warps
+// arrive on the even CTA's accumulator-empty barrier.  K runs in exact
+// 1024-term chunks drained into int32 totals, as in the single-CTA kernel.
+constexpr int kPairStages = 6;
+constexpr int kPairABytes = 128 * kBK * 2;
+constexpr int kPairBBytes = 128 * kBK * 2;
+constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
+constexpr int kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + kBarrierBytes;
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_s8f16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t a_base = sbase;
+  const uint32_t b_base = sbase + kPairStages * kPairABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes);
+  const uint32_t bar0 = ptx::smem_addr(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kPairStages + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kPairStages + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kPairStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kPairStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool even = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull_bar(b), 1);
+      ptx::mbar_init(tempty_bar(b), 2 * kEpiWarps);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort = 0;
+    *never = 0;
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // both CTAs' barriers exist before any remote use
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int num_tiles = p.m_tiles * p.n_tiles;  // 256 x 256 tiles
+  const uint64_t limit = p.wait_limit_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ producer
+      uint32_t stage = 0, phase = 0;
+      uint32_t armed = 0u, armed_par = 0u;  // even CTA: stages whose full barrier it armed
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+        const int m0 = (tile / p.n_tiles) * 256 + static_cast<int>(rank) * 128;
+        const int n0 = (tile % p.n_tiles) * 256 + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort, limit)) {
+            ok = false;
+            break;
+          }
+          armed &= ~(1u << stage);
+          const bool drop = p.drop_first_load && even && tile == pair && kb == 0;
+          if (!drop) {
+            const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);
+            if (even) {
+              ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * kPairStageBytes);
+              armed |= 1u << stage;
+              armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+            }
+            ptx::tma_load_2d_pair(a_base + stage * kPairABytes, &tmA, fb, kb * kBK, m0);
+            ptx::tma_load_2d_pair(b_base + stage * kPairBBytes, &tmB, fb, kb * kBK, n0);
+          }
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) raise_abort(abort, p.status);
+      for (int s = 0; s < kPairStages; ++s)
+        if (armed & (1u << s))
+          if (!ptx::mbar_wait_bounded(full_bar(s), (armed_par >> s) & 1u, never, limit))
+            raise_abort(abort, p.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && even) {
+      // ----------------------------------------------------------- MMA
+      constexpr uint32_t idesc = ptx::idesc_f16_f32(256, 256);
+      uint32_t stage = 0, phase = 0, chunk = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+        for (int kb0 = 0; kb0 < p.k_blocks && ok; kb0 += kChunkBlocks) {
+          const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
+          if (!ptx::mbar_wait_bounded(tempty_bar(buf), aph ^ 1u, abort, limit)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * kBN;
+          const int kb_end = min(kb0 + kChunkBlocks, p.k_blocks);
+          for (int kb = kb0; kb < kb_end; ++kb) {
+            if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort, limit)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t adesc = ptx::smem_desc_kmajor_sw128(a_base + stage * kPairABytes);
+            const uint64_t bdesc = ptx::smem_desc_kmajor_sw128(b_base + stage * kPairBBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              ptx::mma_f16_pair(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                (kb > kb0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit_pair(empty_bar(stage), 0x3);
+            if (++stage == kPairStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          ptx::mma_commit_pair(tfull_bar(buf), 0x3);
+          ++chunk;
+        }
+      }
+      if (!ok) raise_abort(abort, p.status);
+      ptx::mma_commit_pair(drain_bar, 0x1);
+      if (!ptx::mbar_wait_bounded(drain_bar, 0u, never, limit)) raise_abort(abort, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint32_t chunk = 0;
+    bool ok = true;
+    for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+      const int m0 = (tile / p.n_tiles) * 256 + static_cast<int>(rank) * 128;
+      const int n0 = (tile % p.n_tiles) * 256;
+      int32_t tot[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) tot[i] = 0;
+      for (int kb0 = 0; kb0 < p.k_blocks; kb0 += kChunkBlocks) {
+        const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
+        int got = 1;
+        if (lane == 0) got = ptx::mbar_wait_bounded(tfull_bar(buf), aph, abort, limit) ? 1 : 0;
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kBN +
+                               static_cast<uint32_t>(half * 128);
+        drain_chunk(taddr, tot);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(buf), 0));
+        ++chunk;
+      }
+      if (!ok) break;
+      store_rows(p, static_cast<int64_t>(m0) + quad * 32 + lane,
+                 static_cast<int64_t>(n0) + half * 128, tot);
+    }
+    if (!ok && lane == 0) raise_abort(abort, p.status);
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort) {
+    // after a timeout, give copies issued by either CTA time to land
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 200000ull) {
+    }
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // the pair's MMAs, copies and remote arrivals are done
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -309,12 +525,19 @@ cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const flo
     if (!attr_set[device]) {
       err = cudaFuncSetAttribute(gemm_s8f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes);
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
       if (err != cudaSuccess) return err;
       attr_set[device] = true;
     }
   }
+  // CTA pairs (256x256 tiles) when they still give every pair of SMs a
+  // tile; otherwise single CTAs (128x256 tiles), which spread better
+  const int64_t pair_tiles = ((M + 255) / 256) * ((N + kBN - 1) / kBN);
+  const bool pair = M > kBM && pair_tiles >= dev.sms / 2 && !dbg.single_cta;
   CUtensorMap mapA, mapB;
-  if (!make_kmajor_map(&mapA, A, M, K, kBM) || !make_kmajor_map(&mapB, B, N, K, kBN))
+  if (!make_kmajor_map(&mapA, A, M, K, kBM) || !make_kmajor_map(&mapB, B, N, K, pair ? 128 : kBN))
     return cudaErrorInvalidValue;
   GemmParams p;
   p.sA = sA;
@@ -324,7 +547,7 @@ cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const flo
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.m_tiles = static_cast<int>((M + kBM - 1) / kBM);
+  p.m_tiles = static_cast<int>((M + (pair ? 255 : kBM - 1)) / (pair ? 256 : kBM));
   p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
   p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
   p.mode = mode == GemmOut::kS32 ? 1 : 0;
@@ -332,8 +555,14 @@ cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const flo
   p.wait_limit_ns = dbg.wait_limit_ns;
   p.drop_first_load = dbg.drop_first_load;
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-  const int grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
-  gemm_s8f16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mapA, mapB, p);
+  if (pair) {
+    const int64_t pairs_max = dev.sms / 2;
+    const int grid = static_cast<int>(2 * (tiles < pairs_max ? tiles : pairs_max));
+    gemm_s8f16_pair_kernel<<<grid, kThreads, kPairSmemBytes, stream>>>(mapA, mapB, p);
+  } else {
+    const int grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
+    gemm_s8f16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mapA, mapB, p);
+  }
   return cudaGetLastError();
 }
 

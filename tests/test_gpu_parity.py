@@ -127,7 +127,7 @@ def _rand_codes(M, K, seed, extreme=False):
 
 
 MM_SHAPES = [(256, 256, 512), (128, 256, 16), (200, 264, 144), (130, 520, 1040),
-             (256, 512, 3072), (64, 96, 4096)]
+             (256, 512, 3072), (64, 96, 4096), (1000, 776, 2096), (100, 1024, 64)]
 
 
 @pytest.mark.parametrize("shape", MM_SHAPES)
@@ -139,10 +139,11 @@ def test_mm_s32_bit_exact(shape):
     np.testing.assert_array_equal(acc.cpu().numpy(), ref)
 
 
-def test_mm_s32_chunking_keeps_large_sums_exact():
+@pytest.mark.parametrize("M", [128, 256])  # single-CTA and CTA-pair kernels
+def test_mm_s32_chunking_keeps_large_sums_exact(M):
     # all codes +-127 with K = 8192: partial sums reach 127^2 * 8192 = 1.3e8,
     # far above 2^24, so a single fp32 accumulation would round
-    M, N, K = 128, 256, 8192
+    N, K = 256, 8192
     a = _rand_codes(M, K, 3, extreme=True)
     b = _rand_codes(N, K, 4, extreme=True)
     b[0] = a[0]          # row 0 of the output hits 127^2 * K exactly
