@@ -30,17 +30,18 @@ int8mp_status int8mp_debug_mm_s32_drop_first_load(const void* A, const void* B, 
 /*
  * Certifies the quantizers' division.  The quantizers compute x / s for the
  * group scale s = RN(absmax / 127) with a reciprocal and two FMAs
- * (Markstein's correction) instead of an IEEE division; this runs that
- * function and IEEE division (__fdiv_rn) on every pair of bf16 values with
- * absmax > 0 finite and |x| <= absmax (about 1.07e9 pairs) and reports how
- * many quotients differ (compared as floats, so +0 and -0 are equal: both
- * give code 0), how many pairs were checked, how many of them took the fast
- * path, the bf16 bit patterns (absmax, x) of one differing pair, and the
- * largest |x| bit pattern among differing pairs (first_bad has 3 entries).
- * Synchronizes the device.  Test use only.
+ * (Markstein's correction) when s is in [2^-60, 2^10], and by IEEE division
+ * otherwise.  This runs that rule and IEEE division (__fdiv_rn) on every pair
+ * of bf16 values with absmax > 0 finite and |x| <= absmax (about 1.07e9
+ * pairs) and compares the codes the two quotients give: the nearest-even code
+ * bit for bit, and for stochastic rounding floor(v) and the number of draws
+ * u = k 2^-24 below v - floor(v), which fix the code for every u.
+ * results[0] = pairs whose codes differ, [1] = pairs checked, [2] = pairs on
+ * the fast path, [3] = pairs whose quotients differ in any bit (informative:
+ * tiny x only).  first_bad[0..1] = bf16 bits (absmax, x) of one pair whose
+ * codes differ.  Synchronizes the device.  Test use only.
  */
-int8mp_status int8mp_debug_check_division(uint64_t* mismatches, uint64_t* pairs,
-                                          uint64_t* fast_pairs, uint32_t* first_bad);
+int8mp_status int8mp_debug_check_division(uint64_t* results, uint32_t* first_bad);
 
 #ifdef __cplusplus
 }

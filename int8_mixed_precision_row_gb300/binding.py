@@ -91,7 +91,7 @@ def load(path=None):
     L.int8mp_debug_mm_s32_drop_first_load.argtypes = [_P, _P, _I64, _I64, _I64, _P, _I64, _INT, _P]
     L.int8mp_linear_fwd_noalloc.argtypes = [_P, _P, _P, _I64, _I64, _I64,
                                             ctypes.POINTER(int8mp_linear_cfg), _P]
-    L.int8mp_debug_check_division.argtypes = [_P, _P, _P, _P]
+    L.int8mp_debug_check_division.argtypes = [_P, _P]
     for name in ("int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
                  "int8mp_linear_fwd", "int8mp_linear_bwd", "int8mp_poll_device_status",
                  "int8mp_version", "int8mp_debug_mm_s32_drop_first_load",
@@ -217,13 +217,12 @@ def int8mp_poll_device_status(stream=None):
 
 
 def int8mp_debug_check_division():
-    """(mismatches, pairs, fast_pairs, (absmax_bits, x_bits, max_abs_x_bits))
-    of the exhaustive division check."""
-    vals = [ctypes.c_uint64() for _ in range(3)]
-    first = (ctypes.c_uint32 * 3)()
-    _check(load().int8mp_debug_check_division(*(ctypes.byref(v) for v in vals), first),
-           "int8mp_debug_check_division")
-    return vals[0].value, vals[1].value, vals[2].value, (first[0], first[1], first[2])
+    """(code_mismatches, pairs, fast_pairs, quotient_differences,
+    (absmax_bits, x_bits)) of the exhaustive division check."""
+    res = (ctypes.c_uint64 * 4)()
+    first = (ctypes.c_uint32 * 2)()
+    _check(load().int8mp_debug_check_division(res, first), "int8mp_debug_check_division")
+    return res[0], res[1], res[2], res[3], (first[0], first[1])
 
 
 def int8mp_debug_mm_s32_drop_first_load(A, B, out, wait_limit_ms=200, stream=None):

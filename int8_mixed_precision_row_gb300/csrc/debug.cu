@@ -7,20 +7,34 @@
 #include "../../include/int8mp_debug.h"
 #include "divide.cuh"
 
-static __device__ unsigned long long g_div_counts[3];  // mismatches, pairs, fast-path pairs
-static __device__ unsigned int g_div_first[3];  // a mismatch (absmax bits, x bits); largest |x| bits
+// code mismatches, pairs, fast-path pairs, quotients differing from IEEE
+static __device__ unsigned long long g_div_counts[4];
+static __device__ unsigned int g_div_first[2];  // first code mismatch: absmax bits, x bits
 
 namespace {
 
+// nearest-even code of a quotient: clamp(rint(v)), +0 for zero
+__device__ __forceinline__ float rne_code_of(float v) {
+  return __fadd_rn(fminf(fmaxf(rintf(v), -127.0f), 127.0f), 0.0f);
+}
+
+// What fixes the stochastic code for every draw u = k 2^-24: floor(v) and
+// the number of draws below v - floor(v).
+__device__ __forceinline__ void sr_signature(float v, float& f, float& below) {
+  f = floorf(v);
+  below = ceilf(__fmul_rn(__fsub_rn(v, f), 0x1p24f));
+}
+
 // One block per positive finite bf16 absmax (bit patterns 0x0001..0x7F7F);
 // its threads sweep every bf16 x with |x| <= absmax (magnitude bits <= the
-// absmax bits, both signs) and compare div_scale with IEEE division.
+// absmax bits, both signs) and compare the codes from div_scale with the
+// codes from IEEE division.
 __global__ void __launch_bounds__(256) check_division_kernel() {
   const uint32_t a = blockIdx.x + 1u;
   const float amax = __uint_as_float(a << 16);
   const float s = __fdiv_rn(amax, 127.0f);
   const int8mp::ScaleDiv d = int8mp::make_scale_div(s);
-  unsigned long long bad = 0, pairs = 0;
+  unsigned long long bad = 0, pairs = 0, qdiff = 0;
   for (uint32_t m = threadIdx.x; m <= a; m += blockDim.x) {
     for (uint32_t sign = 0; sign < 2; ++sign) {
       const uint32_t xb = (sign << 15) | m;
@@ -28,47 +42,49 @@ __global__ void __launch_bounds__(256) check_division_kernel() {
       const float got = int8mp::div_scale(x, d);
       const float ref = __fdiv_rn(x, s);
       ++pairs;
-      if (!(got == ref)) {  // float equality: +0 == -0, which give the same code
+      if (!(got == ref)) ++qdiff;
+      float fg, bg, fr, br;
+      sr_signature(got, fg, bg);
+      sr_signature(ref, fr, br);
+      const bool same = __float_as_uint(rne_code_of(got)) == __float_as_uint(rne_code_of(ref)) &&
+                        fg == fr && bg == br;
+      if (!same) {
         ++bad;
         if (atomicCAS(&g_div_first[0], 0u, a) == 0u) g_div_first[1] = xb;
-        atomicMax(&g_div_first[2], m);
       }
     }
   }
   if (bad) atomicAdd(&g_div_counts[0], bad);
   atomicAdd(&g_div_counts[1], pairs);
   if (d.fast) atomicAdd(&g_div_counts[2], pairs);
+  if (qdiff) atomicAdd(&g_div_counts[3], qdiff);
 }
 
 }  // namespace
 
-extern "C" int8mp_status int8mp_debug_check_division(uint64_t* mismatches, uint64_t* pairs,
-                                                     uint64_t* fast_pairs, uint32_t* first_bad) {
-  if (!mismatches || !pairs || !fast_pairs || !first_bad) return INT8MP_ERR_INVALID_ARG;
+extern "C" int8mp_status int8mp_debug_check_division(uint64_t* results, uint32_t* first_bad) {
+  if (!results || !first_bad) return INT8MP_ERR_INVALID_ARG;
   int major = 0, minor = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return INT8MP_ERR_CUDA;
   if (major != 10 || minor != 3) return INT8MP_ERR_UNSUPPORTED_DEVICE;
-  const unsigned long long zero3[3] = {0, 0, 0};
-  const unsigned int zero2[3] = {0, 0, 0};
-  if (cudaMemcpyToSymbol(g_div_counts, zero3, sizeof zero3) != cudaSuccess ||
+  const unsigned long long zero4[4] = {0, 0, 0, 0};
+  const unsigned int zero2[2] = {0, 0};
+  if (cudaMemcpyToSymbol(g_div_counts, zero4, sizeof zero4) != cudaSuccess ||
       cudaMemcpyToSymbol(g_div_first, zero2, sizeof zero2) != cudaSuccess)
     return INT8MP_ERR_CUDA;
   check_division_kernel<<<0x7F7F, 256>>>();
   if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
     return INT8MP_ERR_CUDA;
-  unsigned long long counts[3];
-  unsigned int first[3];
+  unsigned long long counts[4];
+  unsigned int first[2];
   if (cudaMemcpyFromSymbol(counts, g_div_counts, sizeof counts) != cudaSuccess ||
       cudaMemcpyFromSymbol(first, g_div_first, sizeof first) != cudaSuccess)
     return INT8MP_ERR_CUDA;
-  *mismatches = counts[0];
-  *pairs = counts[1];
-  *fast_pairs = counts[2];
+  for (int i = 0; i < 4; ++i) results[i] = counts[i];
   first_bad[0] = first[0];
   first_bad[1] = first[1];
-  first_bad[2] = first[2];
   return INT8MP_OK;
 }

@@ -1,5 +1,5 @@
-// divide.cuh -- x / s for a fixed per-group scale s, rounded exactly like an
-// IEEE round-to-nearest division, in three fused operations.
+// divide.cuh -- x / s for a fixed per-group scale s, in three fused
+// operations, for the quantizers' codes.
 //
 // Method: Markstein's correction (P. W. Markstein, "Computation of elementary
 // functions on the IBM RISC System/6000 processor", IBM J. Res. Develop.
@@ -7,18 +7,18 @@
 // remainder x - q0 s is exactly representable and an FMA computes it
 // exactly; q = RN(q0 + rem r) is then the correctly rounded quotient, as long
 // as nothing over- or underflows.  The remainder is a multiple of about
-// |x| 2^-46, so it stays exact only while that quantum is not below the
-// smallest subnormal 2^-149.
+// |x| 2^-46, so the quotient is exact while |x| >= 2^-103.
 //
-// Domain used by the quantizers: s = RN(absmax / 127) for a bf16 absmax and
-// |x| <= absmax.  The fast path is taken when 2^-100 <= s <= 2^10 (group
-// flag) and x = 0 or |x| >= 2^-100 (element test); then |x/s| >= 2^-110 and
-// every intermediate is a normal number.  Otherwise IEEE division is used.
-// div_scale() is that rule for one element; int8mp_debug_check_division()
-// compares it with __fdiv_rn over every such (x, absmax) pair of bf16 values.
-// The vector forms below give, element by element, the same results: a batch
-// of elements takes the fast path only if every element of it qualifies, and
-// is otherwise recomputed with IEEE division.
+// The quantizers use the fast form for every element of a group whose scale
+// s = RN(absmax / 127) lies in [2^-60, 2^10], and IEEE division otherwise.
+// Below |x| = 2^-103 the fast quotient may differ from the IEEE one in its
+// last bits, but then |x/s| < 2^-43 and both have the same sign and are
+// nonzero together, so every code is the same: nearest-even gives 0, and the
+// stochastic draw floor(v) + (u < v - floor(v)) with u a multiple of 2^-24
+// gives the same result for every u.  int8mp_debug_check_division() verifies
+// that the codes agree -- the nearest-even code bit for bit, and for the
+// stochastic code floor(v) and the number of draws u below v - floor(v) --
+// over every (x, absmax) pair of bf16 values.
 #pragma once
 
 namespace int8mp {
@@ -29,7 +29,7 @@ struct ScaleDiv {
   bool fast;
 };
 
-__device__ __forceinline__ bool scale_is_fast(float s) { return s >= 0x1p-100f && s <= 0x1p10f; }
+__device__ __forceinline__ bool scale_is_fast(float s) { return s >= 0x1p-60f && s <= 0x1p10f; }
 
 __device__ __forceinline__ ScaleDiv make_scale_div(float s) {
   ScaleDiv d;
@@ -39,47 +39,33 @@ __device__ __forceinline__ ScaleDiv make_scale_div(float s) {
   return d;
 }
 
-// element test of the fast path: 0 or at least 2^-100 in magnitude
-__device__ __forceinline__ bool fast_element(float x) {
-  const float a = fabsf(x);
-  return a >= 0x1p-100f || a == 0.0f;
-}
-
 __device__ __forceinline__ float div_fast(float x, float s, float r) {
   const float q0 = __fmul_rn(x, r);
   const float rem = __fmaf_rn(-q0, s, x);
   return __fmaf_rn(rem, r, q0);
 }
 
-// x / s for s > 0, equal to __fdiv_rn(x, s)
+// x / s for s > 0 as the quantizers compute it
 __device__ __forceinline__ float div_scale(float x, const ScaleDiv& d) {
-  if (d.fast && fast_element(x)) return div_fast(x, d.s, d.r);
-  return __fdiv_rn(x, d.s);
+  return d.fast ? div_fast(x, d.s, d.r) : __fdiv_rn(x, d.s);
 }
 
-// Fast quotients of eight elements of one group; returns whether all of them
-// took the fast path (otherwise redo them with div8_ieee).
+// Fast quotients of eight elements of one group; returns d.fast (otherwise
+// redo them with div8_ieee).
 __device__ __forceinline__ bool div8_try(const float (&x)[8], const ScaleDiv& d, float (&v)[8]) {
-  bool ok = d.fast;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[i] = div_fast(x[i], d.s, d.r);
-    ok = ok && fast_element(x[i]);
-  }
-  return ok;
+  for (int i = 0; i < 8; ++i) v[i] = div_fast(x[i], d.s, d.r);
+  return d.fast;
 }
 
-// Same for eight elements of eight groups (scales s[i], reciprocals r[i]).
+// Same for eight elements of eight groups (scales s[i], reciprocals r[i]);
+// all_fast: every s[i] is in the fast range.
 __device__ __forceinline__ bool div8_each_try(const float (&x)[8], const float (&s)[8],
                                               const float (&r)[8], bool all_fast,
                                               float (&v)[8]) {
-  bool ok = all_fast;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[i] = div_fast(x[i], s[i], r[i]);
-    ok = ok && fast_element(x[i]);
-  }
-  return ok;
+  for (int i = 0; i < 8; ++i) v[i] = div_fast(x[i], s[i], r[i]);
+  return all_fast;
 }
 
 // IEEE quotients (a zero scale gives 0: the group is all zero).

@@ -532,10 +532,11 @@ cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const flo
       attr_set[device] = true;
     }
   }
-  // CTA pairs (256x256 tiles) when they still give every pair of SMs a
-  // tile; otherwise single CTAs (128x256 tiles), which spread better
+  // CTA pairs (256x256 tiles) when they give every pair of SMs a tile or
+  // the contraction is long (each tile then runs long enough for the pair's
+  // per-tile efficiency to win); otherwise single CTAs (128x256 tiles)
   const int64_t pair_tiles = ((M + 255) / 256) * ((N + kBN - 1) / kBN);
-  const bool pair = M > kBM && pair_tiles >= dev.sms / 2 && !dbg.single_cta;
+  const bool pair = M > kBM && (pair_tiles >= dev.sms / 2 || K >= 8192) && !dbg.single_cta;
   CUtensorMap mapA, mapB;
   if (!make_kmajor_map(&mapA, A, M, K, kBM) || !make_kmajor_map(&mapB, B, N, K, pair ? 128 : kBN))
     return cudaErrorInvalidValue;
