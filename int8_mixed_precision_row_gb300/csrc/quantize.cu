@@ -15,10 +15,10 @@
 //   columns one group per column (the contraction axis is the leading one):
 //           pass 1 reduces column absmax over row blocks into the scale
 //           buffer (atomic max on the fp32 bit pattern, valid for values
-//           >= 0); pass 2 turns it into absmax / 127 in place; pass 3 streams
-//           256x64 tiles into a two-deep shared-memory ring with 2-D TMA
-//           loads, quantizes them, and writes the codes transposed
-//           [cols, rows] through a swizzled shared-memory tile.
+//           >= 0); pass 2 turns it into absmax / 127 in place; pass 3 has
+//           each warp stream 32x64 sub-tiles through its own two-slot ring
+//           of 2-D TMA loads, quantize them, and write the codes transposed
+//           [cols, rows] through its own staging tile.
 //
 // Arithmetic per element (identical to the header of int8mp.h):
 //   v = x / s rounded as an IEEE division (div8_*: a reciprocal and two FMAs,
@@ -352,17 +352,20 @@ __global__ void col_scale_kernel(unsigned int* __restrict__ amax_bits, int64_t c
   if (c < cols) amax_bits[c] = __float_as_uint(__fdiv_rn(__uint_as_float(amax_bits[c]), 127.0f));
 }
 
-// Pass 3: codes of 256-row x 64-column tiles.  Thread 0 keeps a two-deep ring
-// of input tiles filled with 2-D TMA loads (rows of 128 bytes, no swizzle).
-// Thread (rg, cg) reads rows rg*8 .. rg*8+7 of column group cg (8 columns,
-// one 16-byte vector per row) from the ring, quantizes the 8x8 block, packs
-// the codes column by column, and stores the 8 column vectors into the
-// output tile [64 cols][256 rows]; the slot of row group rg in column row rho
-// is placed at rg ^ (rho / 8) so that both the writes and the row-wise
-// read-out spread over the banks.  The read-out stores whole rows of the
-// transposed codes.
-constexpr int kColTileRows = 256, kColTileCols = 64;
-constexpr uint32_t kColTileBytes = kColTileRows * kColTileCols * 2;
+// Pass 3: codes, one warp per 32-row x 64-column sub-tile at a time.  Each
+// warp keeps its own two-slot ring of sub-tiles filled by 2-D TMA loads
+// (rows of 128 bytes, no swizzle) and its own staging tile for the
+// transposed codes, so warps never wait for one another.  Lane (rg, cg)
+// reads rows rg*8 .. rg*8+7 of column group cg (8 columns, one 16-byte
+// vector per row), quantizes the 8x8 block, packs the codes column by
+// column, and writes the 8 column vectors to staging rows cg*8 .. cg*8+7
+// (one per column of x, i.e. per row of the transposed output).  Shared
+// memory serves 16-byte accesses eight lanes at a time and 8-byte accesses
+// sixteen at a time; the staging row and slot permutations below give every
+// such group distinct banks, for the writes and for the row-wise read-out.
+// The read-out stores 8-code vectors of the transposed rows.
+constexpr int kCwRows = 32, kCwCols = 64;
+constexpr uint32_t kCwInBytes = kCwRows * kCwCols * 2;
 
 template <typename CodeT>
 struct ColPack;
@@ -391,6 +394,25 @@ struct ColPack<__half> {
   }
 };
 
+template <typename CodeT>
+__host__ __device__ constexpr uint32_t col_warp_bytes() {
+  return 2 * kCwInBytes + 64 * 4 * static_cast<uint32_t>(sizeof(typename ColPack<CodeT>::Vec));
+}
+
+// staging position of (row rho, slot) of the transposed output
+template <typename CodeT>
+struct Staging;
+template <>
+struct Staging<__half> {  // 64-byte rows of four 16-byte slots
+  __device__ __forceinline__ static int row(int rho) { return rho ^ ((rho >> 3) & 1); }
+  __device__ __forceinline__ static int slot(int rho, int sl) { return sl ^ ((rho >> 4) & 3); }
+};
+template <>
+struct Staging<int8_t> {  // 32-byte rows of four 8-byte slots
+  __device__ __forceinline__ static int row(int rho) { return rho ^ ((rho >> 3) & 3); }
+  __device__ __forceinline__ static int slot(int rho, int sl) { return sl ^ (((rho >> 5) & 1) << 1); }
+};
+
 template <typename CodeT, bool SR>
 __global__ void __launch_bounds__(kThreads, 2) quant_cols_kernel(
     const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
@@ -399,64 +421,70 @@ __global__ void __launch_bounds__(kThreads, 2) quant_cols_kernel(
   using CP = ColPack<CodeT>;
   using Vec = typename CP::Vec;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ uint64_t bars[2];
-  __shared__ int got_tile;
+  __shared__ uint64_t bars[kThreads / 32][2];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
-  const uint32_t in_addr = ptx::smem_addr(smem);
-  Vec(*out)[32] = reinterpret_cast<Vec(*)[32]>(smem + 2 * kColTileBytes);
-  const int t = threadIdx.x;
-  const int cg = t & 7, rg = t >> 3;
-  const int warp = t >> 5, lane = t & 31;
-  const uint32_t bar[2] = {ptx::smem_addr(&bars[0]), ptx::smem_addr(&bars[1])};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cg = lane & 7, rg = lane >> 3;
+  uint8_t* in = smem + warp * col_warp_bytes<CodeT>();
+  const uint32_t in_addr = ptx::smem_addr(in);
+  Vec(*out)[4] = reinterpret_cast<Vec(*)[4]>(in + 2 * kCwInBytes);
+  const uint32_t bar[2] = {ptx::smem_addr(&bars[warp][0]), ptx::smem_addr(&bars[warp][1])};
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
 
-  uint32_t pending = 0u, pend_par = 0u;  // thread 0 only
-  auto issue = [&](int b, int64_t tix) {
-    ptx::mbar_arrive_expect_tx(bar[b], kColTileBytes);
-    ptx::tma_load_2d(in_addr + b * kColTileBytes, &tmx, bar[b],
-                     static_cast<int32_t>((tix % col_tiles) * kColTileCols),
-                     static_cast<int32_t>((tix / col_tiles) * kColTileRows));
+  uint32_t pending = 0u, pend_par = 0u;  // lane 0 only
+  auto issue = [&](int b, int64_t t) {
+    ptx::mbar_arrive_expect_tx(bar[b], kCwInBytes);
+    ptx::tma_load_2d(in_addr + b * kCwInBytes, &tmx, bar[b],
+                     static_cast<int32_t>((t % col_tiles) * kCwCols),
+                     static_cast<int32_t>((t / col_tiles) * kCwRows));
   };
-  if (t == 0) {
+  if (lane == 0) {
     ptx::mbar_init(bar[0], 1);
     ptx::mbar_init(bar[1], 1);
     ptx::fence_mbar_init();
-    ptx::tma_prefetch_desc(&tmx);
     for (int k = 0; k < 2; ++k) {
-      const int64_t tix = blockIdx.x + static_cast<int64_t>(k) * gridDim.x;
-      if (tix < tiles) {
-        issue(k, tix);
+      const int64_t t = gw + k * nw;
+      if (t < tiles) {
+        issue(k, t);
         pending |= 1u << k;
       }
     }
   }
-  __syncthreads();
+  __syncwarp();
+  int64_t cur_cb = -1;
+  float s[8], r[8];
+  bool all_fast = false, normal = false;
   int it = 0;
-  for (int64_t tix = blockIdx.x; tix < tiles; tix += gridDim.x, ++it) {
+  for (int64_t t = gw; t < tiles; t += nw, ++it) {
     const int b = it & 1;
-    if (t == 0) {
-      got_tile = ptx::mbar_wait_timeout(bar[b], (it >> 1) & 1, limit_ns) ? 1 : 0;
-      if (got_tile) pending &= ~(1u << b);
+    int got = 1;
+    if (lane == 0) {
+      got = ptx::mbar_wait_timeout(bar[b], (it >> 1) & 1, limit_ns) ? 1 : 0;
+      if (got) pending &= ~(1u << b);
       else atomicOr(status, 1u);
     }
-    __syncthreads();
-    if (!got_tile) break;
-    const int64_t r0 = (tix / col_tiles) * kColTileRows, c0 = (tix % col_tiles) * kColTileCols;
+    got = __shfl_sync(0xFFFFFFFFu, got, 0);
+    if (!got) break;
+    const int64_t cb = t % col_tiles, r0 = (t / col_tiles) * kCwRows, c0 = cb * kCwCols;
     const int64_t c = c0 + cg * 8, rb = r0 + rg * 8;
-    if (c < cols) {
-      float s[8], r[8];
-      bool all_fast = true, all_normal = true;
+    if (cb != cur_cb) {
+      cur_cb = cb;
+      all_fast = true;
+      normal = true;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        s[j] = __ldg(scale + c + j);
+        s[j] = c < cols ? __ldg(scale + c + j) : 1.0f;
         all_fast = all_fast && scale_is_fast(s[j]);
-        all_normal = all_normal && scale_is_normal(s[j]);
+        normal = normal && scale_is_normal(s[j]);
         r[j] = __frcp_rn(s[j]);
       }
-      const bool normal = all_normal;
-      const uint8_t* in = smem + b * kColTileBytes + (rg * 8) * 128 + cg * 16;
-      Vec colv[8];
+    }
+    Vec colv[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) colv[j] = Vec{};
+    for (int j = 0; j < 8; ++j) colv[j] = Vec{};
+    if (c < cols) {
+      const uint8_t* src = in + b * kCwInBytes + (rg * 8) * 128 + cg * 16;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // rows 4h .. 4h+3 of the 8-row block
         float quo[4][8];             // [row][column]
@@ -464,14 +492,14 @@ __global__ void __launch_bounds__(kThreads, 2) quant_cols_kernel(
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float f[8];
-          unpack8(*reinterpret_cast<const uint4*>(in + (4 * h + i) * 128), f);
+          unpack8(*reinterpret_cast<const uint4*>(src + (4 * h + i) * 128), f);
           ok = div8_each_try(f, s, r, all_fast, quo[i]) && ok;
         }
         if (!ok) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float f[8];
-            unpack8(*reinterpret_cast<const uint4*>(in + (4 * h + i) * 128), f);
+            unpack8(*reinterpret_cast<const uint4*>(src + (4 * h + i) * 128), f);
             div8_each_ieee(f, s, quo[i]);
           }
         }
@@ -488,12 +516,10 @@ __global__ void __launch_bounds__(kThreads, 2) quant_cols_kernel(
           for (int j = 0; j < 8; ++j) CP::put2(colv[j], 2 * h + p, cd[0][j], cd[1][j]);
         }
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) out[cg * 8 + j][rg ^ cg] = colv[j];
     }
-    __syncthreads();  // the input slot is consumed and the output tile complete
-    if (t == 0) {
-      const int64_t nt = tix + 2 * static_cast<int64_t>(gridDim.x);
+    __syncwarp();  // every lane has read slot b
+    if (lane == 0) {
+      const int64_t nt = t + 2 * nw;
       if (nt < tiles) {
         ptx::fence_proxy_async_smem();
         issue(b, nt);
@@ -501,18 +527,24 @@ __global__ void __launch_bounds__(kThreads, 2) quant_cols_kernel(
         pend_par = (pend_par & ~(1u << b)) | (static_cast<uint32_t>(((it + 2) >> 1) & 1) << b);
       }
     }
-    // read-out: warp w handles rows rho = w, w+8, ..., lane = row-group slot
+    using SG = Staging<CodeT>;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int rho = cg * 8 + j;
+      out[SG::row(rho)][SG::slot(rho, rg)] = colv[j];
+    }
+    __syncwarp();
+    // read-out: 8 staging rows per step, 4 lanes (32 codes) per row
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int rho = warp + k * 8;
-      const int64_t cc = c0 + rho;
-      const int64_t rr = r0 + lane * 8;
+      const int rho = k * 8 + (lane >> 2), slot = lane & 3;
+      const int64_t cc = c0 + rho, rr = r0 + slot * 8;
       if (cc < cols && rr < rows)
-        *reinterpret_cast<Vec*>(q + cc * rows + rr) = out[rho][lane ^ (rho >> 3)];
+        *reinterpret_cast<Vec*>(q + cc * rows + rr) = out[SG::row(rho)][SG::slot(rho, slot)];
     }
-    __syncthreads();  // the output tile may be rewritten
+    __syncwarp();  // the staging tile may be rewritten
   }
-  if (t == 0) {
+  if (lane == 0) {
     for (int k = 0; k < 2; ++k)
       if (pending & (1u << k))
         if (!ptx::mbar_wait_timeout(bar[k], (pend_par >> k) & 1u, limit_ns)) atomicOr(status, 1u);
@@ -587,7 +619,7 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   unsigned int* amax = reinterpret_cast<unsigned int*>(scale);
   CUtensorMap tmx;
   if (!encode_tensor_map_2d(&tmx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, cols, ld,
-                            kColTileCols, kColTileRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+                            kCwCols, kCwRows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   static bool attr[64] = {};
   cudaError_t err = allow_smem(quant_cols_kernel<CodeT, SR>, attr);
@@ -613,14 +645,28 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   col_scale_kernel<<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(amax, cols);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  // pass 3
-  const int64_t col_tiles = (cols + kColTileCols - 1) / kColTileCols;
-  const int64_t tiles = col_tiles * ((rows + kColTileRows - 1) / kColTileRows);
-  const size_t smem = 1024 + 2 * kColTileBytes + 64 * 32 * sizeof(typename ColPack<CodeT>::Vec);
+  // pass 3: persistent warps over 32x64 sub-tiles, column-block fastest
+  const int64_t col_tiles = (cols + kCwCols - 1) / kCwCols;
+  const int64_t tiles = col_tiles * ((rows + kCwRows - 1) / kCwRows);
+  const size_t smem = 1024 + (kThreads / 32) * col_warp_bytes<CodeT>();
   static const int occ3 = blocks_per_sm(quant_cols_kernel<CodeT, SR>, kThreads, smem);
+  const int64_t need = (tiles + kThreads / 32 - 1) / (kThreads / 32);
   const int64_t cap = static_cast<int64_t>(sms) * occ3;
-  const unsigned blocks = static_cast<unsigned>(tiles < cap ? tiles : cap);
-  quant_cols_kernel<CodeT, SR><<<blocks, kThreads, smem, stream>>>(
+  int64_t blocks = need < cap ? need : cap;
+  // a warp count that is a multiple of the column blocks keeps every warp on
+  // one column block (its scales are loaded once)
+  const int64_t wpb = kThreads / 32;
+  if (blocks * wpb >= col_tiles) {
+    const int64_t warps = blocks * wpb / col_tiles * col_tiles;
+    blocks = (warps + wpb - 1) / wpb;
+    if (blocks * wpb != warps) {
+      // round down to whole blocks whose warp count is still a multiple
+      int64_t b = blocks;
+      while (b > 1 && (b * wpb) % col_tiles != 0) --b;
+      if ((b * wpb) % col_tiles == 0) blocks = b;
+    }
+  }
+  quant_cols_kernel<CodeT, SR><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(
       tmx, rows, cols, scale, static_cast<CodeT*>(q), col_tiles, tiles, sr, dev.status_word,
       kWaitLimitNs);
   return cudaGetLastError();
