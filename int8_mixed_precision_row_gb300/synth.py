@@ -64,6 +64,20 @@ def layer_shapes(spec):
     return [(name, N, K) for name, N, K, _ in spec["linears"]]
 
 
+def linear_inputs(spec, name, T=None):
+    """(X [T,K], W [N,K], dY [T,N]) of one linear of the layer, drawn exactly
+    as layer_inputs draws it."""
+    T = spec["T"] if T is None else T
+    frac, scale = spec["x_outliers"]
+    for i, (lname, N, K, act) in enumerate(spec["linears"]):
+        if lname == name:
+            X = bf16_normal((T, K), ACT_SEEDS[act], outlier_frac=frac, outlier_scale=scale)
+            W = bf16_normal((N, K), 20 + i, std=0.02)
+            dY = bf16_normal((T, N), 30 + i, std=1e-3)
+            return X, W, dY
+    raise KeyError(name)
+
+
 def layer_inputs(spec, T=None):
     """Activations (shared where the decoder layer shares them), weights and
     output gradients of one decoder layer's linears:
