@@ -40,10 +40,15 @@ def _load(path):
     L.orc_scaled_mm.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _int, _p, _int]
     L.orc_linear_fwd.argtypes = [_p, _p, _i64, _i64, _i64, _int, _u64, _u64, _p, _int]
     L.orc_linear_bwd.argtypes = [_p, _p, _p, _i64, _i64, _i64, _int, _u64, _u64, _p, _p, _int]
+    L.orc_matmul_bf16.argtypes = [_p, _p, _i64, _i64, _i64, _int, _p, _int]
+    L.orc_linear_fwd_cfg.argtypes = [_p, _p, _i64, _i64, _i64, _int, _int, _u64, _u64, _p, _int]
+    L.orc_linear_bwd_cfg.argtypes = [_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _u64, _u64,
+                                     _p, _p, _int]
     L.orc_f32_to_bf16_rne.argtypes = [ctypes.c_float]
     L.orc_f32_to_bf16_rne.restype = ctypes.c_uint16
     for name in ("orc_quantize", "orc_mm_s32", "orc_rescale_bf16", "orc_scaled_mm",
-                 "orc_linear_fwd", "orc_linear_bwd"):
+                 "orc_linear_fwd", "orc_linear_bwd", "orc_matmul_bf16", "orc_linear_fwd_cfg",
+                 "orc_linear_bwd_cfg"):
         getattr(L, name).restype = _int
     return L
 
@@ -160,4 +165,38 @@ def linear_bwd(dY, X, W, mode=RNE, seed=0, offset=0, nthreads=None, want_dx=True
     dW = np.zeros((N, K), dtype=np.uint16) if want_dw else None
     _check(lib().orc_linear_bwd(_ptr(dY), _ptr(X), _ptr(W), T, N, K, mode, seed, offset,
                                 _ptr(dX), _ptr(dW), nthreads or default_threads()), "linear_bwd")
+    return dX, dW
+
+
+def matmul_bf16(A, B, M, N, K, layout=AxBT, nthreads=None):
+    """BF16 pass: bf16_RNE(fp32_RN(sum in fp64)), operands as bf16 bits."""
+    out = np.zeros((M, N), dtype=np.uint16)
+    _check(lib().orc_matmul_bf16(_ptr(_c(A, np.uint16)), _ptr(_c(B, np.uint16)), M, N, K, layout,
+                                 _ptr(out), nthreads or default_threads()), "matmul_bf16")
+    return out
+
+
+def linear_fwd_cfg(X, W, int8_fwd=1, mode=RNE, seed=0, offset=0, nthreads=None):
+    X = _c(X, np.uint16)
+    W = _c(W, np.uint16)
+    T, K = X.shape
+    N = W.shape[0]
+    Y = np.zeros((T, N), dtype=np.uint16)
+    _check(lib().orc_linear_fwd_cfg(_ptr(X), _ptr(W), T, N, K, int8_fwd, mode, seed, offset,
+                                    _ptr(Y), nthreads or default_threads()), "linear_fwd_cfg")
+    return Y
+
+
+def linear_bwd_cfg(dY, X, W, int8_grad_in=1, int8_grad_w=1, mode=RNE, seed=0, offset=0,
+                   nthreads=None):
+    dY = _c(dY, np.uint16)
+    X = _c(X, np.uint16)
+    W = _c(W, np.uint16)
+    T, K = X.shape
+    N = W.shape[0]
+    dX = np.zeros((T, K), dtype=np.uint16)
+    dW = np.zeros((N, K), dtype=np.uint16)
+    _check(lib().orc_linear_bwd_cfg(_ptr(dY), _ptr(X), _ptr(W), T, N, K, int8_grad_in, int8_grad_w,
+                                    mode, seed, offset, _ptr(dX), _ptr(dW),
+                                    nthreads or default_threads()), "linear_bwd_cfg")
     return dX, dW

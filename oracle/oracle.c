@@ -271,3 +271,80 @@ int orc_linear_bwd(const uint16_t* dY, const uint16_t* X, const uint16_t* W,
   }
   return rc;
 }
+
+/* ------------------------------------------------------------ BF16 passes */
+
+typedef struct {
+  const uint16_t* A;
+  const uint16_t* B;
+  int64_t M, N, K;
+  int layout;
+  uint16_t* out;
+  int64_t i0, i1;
+} bf_job;
+
+static void* bf_rows(void* arg) {
+  bf_job* j = (bf_job*)arg;
+  for (int64_t i = j->i0; i < j->i1; ++i) {
+    for (int64_t n = 0; n < j->N; ++n) {
+      double s = 0.0;
+      for (int64_t k = 0; k < j->K; ++k) {
+        uint16_t a = j->layout == ORC_ATxB ? j->A[k * j->M + i] : j->A[i * j->K + k];
+        uint16_t b = j->layout == ORC_AxBT ? j->B[n * j->K + k] : j->B[k * j->N + n];
+        s += (double)orc_bf16_to_f32(a) * (double)orc_bf16_to_f32(b);
+      }
+      j->out[i * j->N + n] = orc_f32_to_bf16_rne((float)s);
+    }
+  }
+  return NULL;
+}
+
+int orc_matmul_bf16(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                    int layout, uint16_t* out, int nthreads) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  if (layout != ORC_AxBT && layout != ORC_AxB && layout != ORC_ATxB) return -1;
+  if (M == 0 || N == 0) return 0;
+  if (!out || (K > 0 && (!A || !B))) return -1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > M) nthreads = (int)M;
+  if (nthreads > 256) nthreads = 256;
+  bf_job jobs[256];
+  pthread_t tids[256];
+  for (int t = 0; t < nthreads; ++t)
+    jobs[t] = (bf_job){A, B, M, N, K, layout, out, M * t / nthreads, M * (t + 1) / nthreads};
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&tids[t], NULL, bf_rows, &jobs[t]) != 0) break;
+    started = t;
+  }
+  bf_rows(&jobs[0]);
+  for (int t = started + 1; t < nthreads; ++t) bf_rows(&jobs[t]);
+  for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
+  return 0;
+}
+
+int orc_linear_fwd_cfg(const uint16_t* X, const uint16_t* W, int64_t T, int64_t N, int64_t K,
+                       int int8_fwd, int mode, uint64_t seed, uint64_t offset, uint16_t* Y,
+                       int nthreads) {
+  if (int8_fwd) return orc_linear_fwd(X, W, T, N, K, mode, seed, offset, Y, nthreads);
+  return orc_matmul_bf16(X, W, T, N, K, ORC_AxBT, Y, nthreads); /* Y = X . W^T */
+}
+
+int orc_linear_bwd_cfg(const uint16_t* dY, const uint16_t* X, const uint16_t* W, int64_t T,
+                       int64_t N, int64_t K, int int8_grad_in, int int8_grad_w, int mode,
+                       uint64_t seed, uint64_t offset, uint16_t* dX, uint16_t* dW,
+                       int nthreads) {
+  int rc = 0;
+  if (dX) {
+    rc = int8_grad_in
+             ? orc_linear_bwd(dY, X, W, T, N, K, mode, seed, offset, dX, NULL, nthreads)
+             : orc_matmul_bf16(dY, W, T, K, N, ORC_AxB, dX, nthreads); /* dX = dY . W */
+    if (rc) return rc;
+  }
+  if (dW) {
+    rc = int8_grad_w
+             ? orc_linear_bwd(dY, X, W, T, N, K, mode, seed, offset, NULL, dW, nthreads)
+             : orc_matmul_bf16(dY, X, N, K, T, ORC_ATxB, dW, nthreads); /* dW = dY^T . X */
+  }
+  return rc;
+}

@@ -94,6 +94,24 @@ int orc_linear_bwd(const uint16_t* dY, const uint16_t* X, const uint16_t* W,
                    int64_t T, int64_t N, int64_t K, int mode, uint64_t seed,
                    uint64_t offset, uint16_t* dX, uint16_t* dW, int nthreads);
 
+/* A BF16 pass (the "BF16" entries of the INT8 mixed precision training
+ * table in the "Quantized model training" README): the plain product of the
+ * bf16 operands, out[i,j] = bf16_RNE(fp32_RN(sum_k a(i,k) b(j,k))) with the
+ * sum taken in fp64 (every product of two bf16 values is exact in fp64).
+ * Operands stored per layout as in orc_mm_s32. */
+int orc_matmul_bf16(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                    int layout, uint16_t* out, int nthreads);
+
+/* Linear passes with per-pass switches: int8_* = 1 runs the pass as
+ * orc_linear_fwd / orc_linear_bwd do, 0 runs it as a BF16 pass. */
+int orc_linear_fwd_cfg(const uint16_t* X, const uint16_t* W, int64_t T, int64_t N, int64_t K,
+                       int int8_fwd, int mode, uint64_t seed, uint64_t offset, uint16_t* Y,
+                       int nthreads);
+int orc_linear_bwd_cfg(const uint16_t* dY, const uint16_t* X, const uint16_t* W, int64_t T,
+                       int64_t N, int64_t K, int int8_grad_in, int int8_grad_w, int mode,
+                       uint64_t seed, uint64_t offset, uint16_t* dX, uint16_t* dW,
+                       int nthreads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -125,3 +125,51 @@ def test_relative_error_against_fp64_product():
     for name, e in errs.items():
         # about 0.9% expected for N(0,1)-like rows (s/sqrt(12) per operand)
         assert 0.002 < e < 0.03, (name, e)
+
+
+# ------------------------------------------------------------ BF16 passes
+# "BF16" entries of the INT8 mixed precision training table ("Quantized
+# model training" README): the pass is the plain bf16 product.
+
+def _exact_bf16_product(a, b):
+    """bf16_RNE(fp32_RN(exact sum)) of a @ b.T, exact rationals."""
+    from fractions import Fraction
+    from helpers import rn_f32, rn_bf16
+    M, K = a.shape
+    N = b.shape[0]
+    out = np.zeros((M, N))
+    for i in range(M):
+        for j in range(N):
+            s = sum(Fraction(float(a[i, k])) * Fraction(float(b[j, k])) for k in range(K))
+            out[i, j] = float(rn_bf16(rn_f32(s)))
+    return out
+
+
+@pytest.mark.parametrize("layout", [oracle.AxBT, oracle.AxB, oracle.ATxB])
+def test_bf16_matmul_matches_exact_rational_product(layout):
+    M, N, K = 5, 7, 33
+    A = bf16_bits(synth.bf16_normal((M, K), 5))
+    B = bf16_bits(synth.bf16_normal((N, K), 6))
+    a, bb = bits_to_f32(A), bits_to_f32(B)
+    As = A if layout != oracle.ATxB else np.ascontiguousarray(A.T)
+    Bs = B if layout == oracle.AxBT else np.ascontiguousarray(B.T)
+    got = bits_to_f32(oracle.matmul_bf16(As, Bs, M, N, K, layout=layout, nthreads=2))
+    np.testing.assert_array_equal(got, _exact_bf16_product(a, bb))
+
+
+def test_bf16_passes_in_the_linear_layer():
+    T, N, K = 16, 8, 24
+    X = bf16_bits(synth.bf16_normal((T, K), 7))
+    W = bf16_bits(synth.bf16_normal((N, K), 8, std=0.02))
+    dY = bf16_bits(synth.bf16_normal((T, N), 9, std=1e-3))
+    x, w, g = bits_to_f32(X), bits_to_f32(W), bits_to_f32(dY)
+    np.testing.assert_array_equal(bits_to_f32(oracle.linear_fwd_cfg(X, W, int8_fwd=0)),
+                                  _exact_bf16_product(x, w))
+    dX, dW = oracle.linear_bwd_cfg(dY, X, W, int8_grad_in=0, int8_grad_w=0)
+    np.testing.assert_array_equal(bits_to_f32(dX), _exact_bf16_product(g, np.ascontiguousarray(w.T)))
+    np.testing.assert_array_equal(bits_to_f32(dW), _exact_bf16_product(np.ascontiguousarray(g.T),
+                                                                       np.ascontiguousarray(x.T)))
+    # switches are per pass: INT8 grad-input with BF16 grad-weight
+    dX8, dWb = oracle.linear_bwd_cfg(dY, X, W, int8_grad_in=1, int8_grad_w=0)
+    np.testing.assert_array_equal(dX8, oracle.linear_bwd(dY, X, W, want_dw=False)[0])
+    np.testing.assert_array_equal(dWb, dW)

@@ -30,6 +30,10 @@ MUTATIONS = {
                                      "X, T, K, 1, ORC_STREAM_GW_X, dY, T, N, 1, ORC_STREAM_GW_DY"),
     "rescale_drops_column_scale": ("float o = t * sB[j];", "float o = t;"),
     "bf16_truncates": ("bits += 0x7fffu + lsb;", "bits += 0u * lsb;"),
+    "bf16_grad_input_untransposed": ("orc_matmul_bf16(dY, W, T, K, N, ORC_AxB, dX, nthreads)",
+                                     "orc_matmul_bf16(dY, W, T, K, N, ORC_AxBT, dX, nthreads)"),
+    "bf16_pass_rounds_in_fp64_to_bf16_by_truncation": ("j->out[i * j->N + n] = orc_f32_to_bf16_rne((float)s);",
+                                                        "j->out[i * j->N + n] = (uint16_t)(orc_f32_to_bf16_rne((float)s) & 0xFFFEu);"),
     "scale_floored_at_epsilon": ("float s = amax / 127.0f;", "float s = fmaxf(amax / 127.0f, 1e-12f);"),
 }
 
@@ -46,6 +50,8 @@ PINS = [
     lambda: L.test_forward_closed_form(oracle.RNE),
     lambda: L.test_grad_input_closed_form(oracle.RNE),
     lambda: L.test_grad_weight_closed_form(oracle.RNE),
+    lambda: L.test_bf16_matmul_matches_exact_rational_product(oracle.AxB),
+    L.test_bf16_passes_in_the_linear_layer,
 ]
 
 
