@@ -7,3 +7,4 @@ is loaded on first use and raises if it has not been built.
 from .binding import *  # noqa: F401,F403
 from .binding import (EXPORTED, Int8mpError, int8mp_linear_cfg, linear_cfg, load,  # noqa: F401
                       library_path)
+from .autograd import Int8MixedPrecisionLinear, Int8MixedPrecisionLinearFunction  # noqa: F401,E402
