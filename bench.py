@@ -397,6 +397,43 @@ def layer_tok_s(spec, mode, device, steps=5, warmup=2):
     return r
 
 
+def pass_switch_table(spec, device, steps=5, warmup=2):
+    """The rows of the pages' INT8 mixed precision training table (forward /
+    grad-input / grad-weight each INT8 or BF16, nearest-even) on this GPU,
+    for the decoder layer's linears, through int8mp_linear_fwd/bwd."""
+    import torch
+    import int8_mixed_precision_row_gb300 as m
+    step = LayerStep(spec, m.INT8MP_RNE, device)
+    ws_bytes = max(m.int8mp_linear_workspace_size(step.T, l["N"], l["K"]) for l in step.linears)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    rows = {}
+    for flags in ((0, 0, 0), (1, 0, 0), (1, 1, 0), (1, 1, 1)):
+        cfg = m.linear_cfg(int8_fwd=flags[0], int8_grad_in=flags[1], int8_grad_w=flags[2])
+
+        def one():
+            for l in step.linears:
+                m.int8mp_linear_fwd(l["X"], l["W"], cfg, Y=l["Y"], workspace=ws)
+                m.int8mp_linear_bwd(l["dY"], l["X"], l["W"], cfg, dX=l["dX"], dW=l["dW"],
+                                    workspace=ws)
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            one()
+        b.record()
+        torch.cuda.synchronize()
+        name = "/".join("INT8" if f else "BF16" for f in flags)
+        rows[name] = round(step.T * steps / (a.elapsed_time(b) * 1e-3), 1)
+    base = rows["BF16/BF16/BF16"]
+    out = {k: {"tok_s": v, "speedup_vs_bf16": round(v / base, 3)} for k, v in rows.items()}
+    del step, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 # -------------------------------------------------------------------- main
 def measured_peaks():
     try:
@@ -512,6 +549,8 @@ def main():
             "square_quant_scaled_mm": square_sweep(device),
             "llama2-1b_stochastic_rounding": layer_tok_s(synth.LLAMA2_1B, m.INT8MP_SR, device),
             "llama3-8b_T16384": layer_tok_s(synth.LLAMA3_8B, m.INT8MP_RNE, device),
+            "llama2-1b_pass_switches (forward/grad-input/grad-weight)":
+                pass_switch_table(synth.LLAMA2_1B, device),
         }
     if rank == 0 and not args.profile_steps and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec)

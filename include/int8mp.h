@@ -153,8 +153,12 @@ int8mp_status int8mp_mm_s32(const void* A, const void* B, int64_t M, int64_t N, 
 /*
  * Per-pass configuration of a linear layer (the pages' per-matmul INT8
  * switches and stochastic-rounding switch; "Quantized model training"
- * README, INT8 mixed precision training table).  This build implements the
- * INT8 passes: each int8_* flag must be 1 (0 returns INT8MP_ERR_INVALID_ARG).
+ * README, INT8 mixed precision training table).  int8_* = 1 runs that pass
+ * in INT8 as described above; 0 runs it in BF16: the plain product of the
+ * bf16 operands with fp32 accumulation and a bf16 result, computed by
+ * cuBLASLt (a library GEMM; cuBLASLt keeps a per-device handle, created on
+ * first use).  Other values return INT8MP_ERR_INVALID_ARG.  mode, seed and
+ * offset apply to the INT8 passes.
  */
 typedef struct {
   int int8_fwd;
@@ -209,6 +213,8 @@ int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, vo
  * round256(4*N) bytes above the maximum, return INT8MP_ERR_WORKSPACE before
  * anything is launched.  Nothing is allocated by the call.
  *
+ * The forward pass must be the INT8 one (cfg->int8_fwd = 1; the BF16 pass runs
+ * in a library GEMM that may allocate, so it returns INT8MP_ERR_INVALID_ARG).
  * The first call on a device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress); make that first call before
  * any stream capture.  All calls on a device share the array and it keeps the

@@ -51,8 +51,10 @@ class int8mp_linear_cfg(ctypes.Structure):
                 ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
 
 
-def linear_cfg(mode=INT8MP_RNE, seed=0, offset=0):
-    return int8mp_linear_cfg(1, 1, 1, int(mode), int(seed), int(offset))
+def linear_cfg(mode=INT8MP_RNE, seed=0, offset=0, int8_fwd=1, int8_grad_in=1, int8_grad_w=1):
+    """int8_* = 1: that pass in INT8; 0: in BF16 (plain bf16 product)."""
+    return int8mp_linear_cfg(int(int8_fwd), int(int8_grad_in), int(int8_grad_w), int(mode),
+                             int(seed), int(offset))
 
 
 _lib = None

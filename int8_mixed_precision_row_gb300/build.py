@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libint8mp.so")
 
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "tma.cu", "noalloc.cu", "debug.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "tma.cu", "blas.cu", "noalloc.cu", "debug.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "philox.cuh", "divide.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
@@ -59,7 +59,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
+    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-lcublasLt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -157,7 +157,8 @@ size_t bwd_bytes(int64_t T, int64_t N, int64_t K) {
 
 int8mp_status check_linear(int64_t T, int64_t N, int64_t K, const int8mp_linear_cfg* cfg) {
   if (!cfg) return INT8MP_ERR_INVALID_ARG;
-  if (cfg->int8_fwd != 1 || cfg->int8_grad_in != 1 || cfg->int8_grad_w != 1)
+  auto flag = [](int v) { return v == 0 || v == 1; };
+  if (!flag(cfg->int8_fwd) || !flag(cfg->int8_grad_in) || !flag(cfg->int8_grad_w))
     return INT8MP_ERR_INVALID_ARG;
   if (cfg->mode != INT8MP_RNE && cfg->mode != INT8MP_SR) return INT8MP_ERR_INVALID_ARG;
   if (T < 0 || N < 0 || K < 0) return INT8MP_ERR_INVALID_ARG;
@@ -234,6 +235,13 @@ int8mp_status int8mp_linear_fwd(const void* X, const void* W, void* Y, int64_t T
   st = current_device(&dev);
   if (st != INT8MP_OK) return st;
   cudaStream_t s = as_stream(stream);
+  if (!cfg->int8_fwd) {
+    // BF16 pass: Y [T,N] = X W^T, i.e. column-major Y^T [N,T] = W X^T
+    if (K == 0)
+      return from_cuda(cudaMemset2DAsync(Y, static_cast<size_t>(N) * 2, 0,
+                                         static_cast<size_t>(N) * 2, static_cast<size_t>(T), s));
+    return from_cuda(int8mp::bf16_gemm_colmajor(W, X, Y, N, T, K, true, false, K, K, N, s));
+  }
   Carver c{static_cast<char*>(workspace)};
   const QOperand xq = carve_operand(c, T, K);
   const QOperand wq = carve_operand(c, N, K);
@@ -272,7 +280,15 @@ int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, vo
   const QOperand wqt = carve_operand(c, K, N);
   const QOperand dyqt = carve_operand(c, N, T);
   const QOperand xqt = carve_operand(c, K, T);
-  if (want_dx) {
+  if (want_dx && !cfg->int8_grad_in) {
+    // BF16 pass: dX [T,K] = dY W, i.e. column-major dX^T [K,T] = W^T dY^T
+    if (N == 0)
+      st = from_cuda(cudaMemset2DAsync(dX, static_cast<size_t>(K) * 2, 0,
+                                       static_cast<size_t>(K) * 2, static_cast<size_t>(T), s));
+    else
+      st = from_cuda(int8mp::bf16_gemm_colmajor(W, dY, dX, K, T, N, false, false, K, N, K, s));
+    if (st != INT8MP_OK) return st;
+  } else if (want_dx) {
     // grad input: contraction over N; dY by rows, W by columns (-> [K, N])
     if (N > 0) {
       cudaError_t e = int8mp::launch_quantize_rows(dY, T, N, N, cfg->mode,
@@ -287,7 +303,14 @@ int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, vo
                 int8mp::GemmDebug{}, s);
     if (st != INT8MP_OK) return st;
   }
-  if (want_dw) {
+  if (want_dw && !cfg->int8_grad_w) {
+    // BF16 pass: dW [N,K] = dY^T X, i.e. column-major dW^T [K,N] = X^T dY
+    if (T == 0)
+      st = from_cuda(cudaMemset2DAsync(dW, static_cast<size_t>(K) * 2, 0,
+                                       static_cast<size_t>(K) * 2, static_cast<size_t>(N), s));
+    else
+      st = from_cuda(int8mp::bf16_gemm_colmajor(X, dY, dW, K, N, T, false, true, K, N, K, s));
+  } else if (want_dw) {
     // grad weight: contraction over T; dY and X by columns (-> [N, T], [K, T])
     if (T > 0) {
       cudaError_t e = int8mp::launch_quantize_cols(dY, T, N, N, cfg->mode,

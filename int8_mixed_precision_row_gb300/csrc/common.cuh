@@ -62,4 +62,10 @@ cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const flo
                         int64_t ldo, const DeviceInfo& dev, const GemmDebug& dbg,
                         cudaStream_t stream);
 
+// ---- BF16 passes (blas.cu) --------------------------------------------------
+// Column-major C [m, n] = op(A) op(B), bf16 in and out, fp32 accumulation.
+cudaError_t bf16_gemm_colmajor(const void* A, const void* B, void* C, int64_t m, int64_t n,
+                               int64_t k, bool transa, bool transb, int64_t lda, int64_t ldb,
+                               int64_t ldc, cudaStream_t stream);
+
 }  // namespace int8mp

@@ -61,6 +61,8 @@ extern "C" int8mp_status int8mp_linear_fwd_noalloc(const void* X, const void* W,
                                                    const int8mp_linear_cfg* cfg, void* stream) {
   if (T < 0 || N < 0 || K < 0 || T > INT8MP_MAX_K || N > INT8MP_MAX_K || K > INT8MP_MAX_K)
     return INT8MP_ERR_INVALID_ARG;
+  // the BF16 forward pass runs in a library GEMM that may allocate: not here
+  if (cfg && cfg->int8_fwd != 1) return INT8MP_ERR_INVALID_ARG;
   // the forward pass's workspace: codes (2 bytes each) and scales of X and W
   const uint64_t need = round256(2ull * T * K) + round256(4ull * T) + round256(2ull * N * K) +
                         round256(4ull * N);

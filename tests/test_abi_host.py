@@ -85,9 +85,12 @@ def test_linear_host_validation(lib):
     assert f(P(16), P(16), P(16), 32, 32, 32, None, P(256), 1 << 20, None) == m.INT8MP_ERR_INVALID_ARG
     assert f(P(16), P(16), P(16), 32, 32, 24, ref, P(256), 1 << 20, None) == m.INT8MP_ERR_ALIGNMENT
     assert f(P(16), P(16), P(16), 32, 32, 32, ref, P(256), 16, None) == m.INT8MP_ERR_WORKSPACE
-    bad = m.int8mp_linear_cfg(0, 1, 1, 0, 0, 0)   # BF16 passes are not part of this build
+    bad = m.int8mp_linear_cfg(2, 1, 1, 0, 0, 0)   # a pass switch is 0 (BF16) or 1 (INT8)
     assert f(P(16), P(16), P(16), 32, 32, 32, ctypes.byref(bad), P(256), 1 << 20, None) == \
         m.INT8MP_ERR_INVALID_ARG
+    bf16_fwd = m.int8mp_linear_cfg(0, 1, 1, 0, 0, 0)  # the no-alloc forward is INT8 only
+    assert lib.int8mp_linear_fwd_noalloc(P(16), P(16), P(16), 32, 32, 32, ctypes.byref(bf16_fwd),
+                                         None) == m.INT8MP_ERR_INVALID_ARG
     need = m.int8mp_linear_workspace_size(32, 48, 64, cfg)
     assert need >= 2 * (32 * 64 + 48 * 64) and need % 256 == 0
     assert m.int8mp_linear_workspace_size(32, 48, 24, cfg) == 0

@@ -286,3 +286,45 @@ def test_quantize_division_ties_bit_exact(axis):
         qr, sr = oracle.quantize(bf16_bits(x), axis=axis)
         np.testing.assert_array_equal(_f32_bits(s), sr.view(np.int32))
         np.testing.assert_array_equal(_codes_np(q), qr)
+
+
+def _bf16_pass_close(got_t, ref_bits, a, b, what):
+    """BF16 pass: cuBLASLt accumulates in fp32 in its own order, the oracle
+    in fp64; allow two bf16 ulps plus the fp32 accumulation bound
+    K 2^-23 sum |a||b| per output."""
+    got = got_t.cpu().float().double()
+    ref = torch.from_numpy(bits_to_f32(ref_bits).astype(np.float64))
+    K = a.shape[1]
+    bound = 2.0 ** -7 * ref.abs() + K * 2.0 ** -23 * (a.abs().double() @ b.abs().double().T)
+    bad = (got - ref).abs() > bound
+    assert not bool(bad.any()), f"{what}: {int(bad.sum())} outputs outside the bound"
+
+
+@pytest.mark.parametrize("flags", [(0, 0, 0), (1, 0, 0), (1, 1, 0), (0, 1, 1), (1, 0, 1)])
+def test_linear_per_pass_switches(flags):
+    T, N, K = 256, 192, 320
+    X = synth.bf16_normal((T, K), 40)
+    W = synth.bf16_normal((N, K), 41, std=0.02)
+    dY = synth.bf16_normal((T, N), 42, std=1e-3)
+    f, gi, gw = flags
+    cfg = m.linear_cfg(mode=m.INT8MP_SR, seed=3, offset=7, int8_fwd=f, int8_grad_in=gi,
+                       int8_grad_w=gw)
+    Y = m.int8mp_linear_fwd(_dev(X), _dev(W), cfg)
+    dX, dW = m.int8mp_linear_bwd(_dev(dY), _dev(X), _dev(W), cfg)
+    kw = dict(mode=oracle.SR, seed=3, offset=7)
+    Yr = oracle.linear_fwd_cfg(bf16_bits(X), bf16_bits(W), int8_fwd=f, **kw)
+    dXr, dWr = oracle.linear_bwd_cfg(bf16_bits(dY), bf16_bits(X), bf16_bits(W), int8_grad_in=gi,
+                                     int8_grad_w=gw, **kw)
+    xf, wf, gf = X.float(), W.float(), dY.float()
+    if f:
+        assert_bf16_equal(Y, Yr, "INT8 forward")
+    else:
+        _bf16_pass_close(Y, Yr, xf, wf, "BF16 forward")
+    if gi:
+        assert_bf16_equal(dX, dXr, "INT8 grad input")
+    else:
+        _bf16_pass_close(dX, dXr, gf, wf.T.contiguous(), "BF16 grad input")
+    if gw:
+        assert_bf16_equal(dW, dWr, "INT8 grad weight")
+    else:
+        _bf16_pass_close(dW, dWr, gf.T.contiguous(), xf.T.contiguous(), "BF16 grad weight")
