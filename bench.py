@@ -11,7 +11,8 @@ N(0,1e-3), round to nearest even.  Inputs are resident in HBM before the
 timed region; every step touches about 5 GB, far more than the 129 MB L2.
 
 Output: one JSON line (rank 0).  `value` is whole-job tokens/s; `e2e` is the
-same metric through int8mp_linear_fwd/bwd with inputs copied from pinned
+same metric through the layer API (int8mp_linear_fwd_save /
+int8mp_linear_bwd_saved) with inputs copied from pinned
 host memory and dW copied back inside the timed region; `roofline` describes
 the dominant kernel (the tensor-core GEMM); `cpu_baseline` times the plain-C
 oracle on a bounded token sample on the host cores.
@@ -197,22 +198,33 @@ class LayerStep:
         self.qb = torch.empty(big, dtype=f16, device=device)
         self.sa = torch.empty(max(T, nmax, kmax), dtype=torch.float32, device=device)
         self.sb = torch.empty(max(T, nmax, kmax), dtype=torch.float32, device=device)
+        # column absmax of X, W (recorded by their forward row passes) and dY
+        # (by its grad-input row pass), per linear: [K | K | N]
+        for l in self.linears:
+            l["colmax"] = torch.empty(2 * l["K"] + l["N"], dtype=torch.float32, device=device)
         self.flops = 6.0 * T * sum(l["N"] * l["K"] for l in self.linears)
         self.gemms_per_step = 3 * len(self.linears)
-        # kernels of this library per step: row quantize 1, column quantize 3
-        # (absmax, codes, scales), GEMM 1
-        self.kernels_per_step = len(self.linears) * (3 * 1 + 3 * 3 + 3 * 1)
+        # kernels of this library per step and linear: three row quantizations
+        # (each also recording column absmax), three column quantizations
+        # (codes from that absmax), three GEMMs
+        self.kernels_per_step = len(self.linears) * (3 + 3 + 3)
         # algorithmic quantize bytes: bf16 read once, code (f16 container) and scale written
         self.quant_elems = sum(2 * (T * l["K"] + l["N"] * l["K"] + T * l["N"]) for l in self.linears)
 
-    def _q(self, x, axis, sid, qbuf, sbuf, cfg_seed, cfg_off):
+    def _q(self, x, axis, sid, qbuf, sbuf, cfg_seed, cfg_off, colmax):
+        """axis 0: row groups, recording each column's absmax into colmax;
+        2: column groups, codes in x's layout, from that absmax."""
         m = self.m
         rows, cols = x.shape
-        groups, glen = (rows, cols) if axis == 0 else (cols, rows)
-        q = qbuf[:groups * glen].view(groups, glen)
-        s = sbuf[:groups]
-        m.int8mp_quantize_rowwise(x, axis=axis, mode=self.mode, seed=cfg_seed, offset=cfg_off,
-                                  stream_id=sid, codes=m.INT8MP_CODES_F16, q=q, scale=s)
+        q = qbuf[:rows * cols].view(rows, cols)
+        kw = dict(mode=self.mode, seed=cfg_seed, offset=cfg_off, stream_id=sid,
+                  codes=m.INT8MP_CODES_F16, q=q)
+        if axis == 0:
+            s = sbuf[:rows]
+            m.int8mp_quantize_rows_colmax(x, colmax, scale=s, **kw)
+        else:
+            s = sbuf[:cols]
+            m.int8mp_quantize_cols_absmax(x, colmax, scale=s, **kw)
         return q, s
 
     def run(self, timers=None, seed=0, offset=0):
@@ -233,18 +245,22 @@ class LayerStep:
             return r
         for l in self.linears:
             X, W, dY = l["X"], l["W"], l["dY"]
-            # forward: X and W along K (their rows)
-            qx, sx = rec("quant_rows", lambda: self._q(X, 0, m.INT8MP_STREAM_FWD_X, self.qa, self.sa, seed, offset))
-            qw, sw = rec("quant_rows", lambda: self._q(W, 0, m.INT8MP_STREAM_FWD_W, self.qb, self.sb, seed, offset))
+            K = l["K"]
+            cm = l["colmax"]
+            cx, cw, cg = cm[:K], cm[K:2 * K], cm[2 * K:]
+            cm.zero_()
+            # forward: X and W along K (their rows); their column absmax on the way
+            qx, sx = rec("quant_rows", lambda: self._q(X, 0, m.INT8MP_STREAM_FWD_X, self.qa, self.sa, seed, offset, cx))
+            qw, sw = rec("quant_rows", lambda: self._q(W, 0, m.INT8MP_STREAM_FWD_W, self.qb, self.sb, seed, offset, cw))
             rec("gemm", lambda: m.int8mp_scaled_mm(qx, sx, qw, sw, out=l["Y"]))
-            # grad input: dY along N (rows), W along N (columns -> [K, N])
-            qg, sg = rec("quant_rows", lambda: self._q(dY, 0, m.INT8MP_STREAM_GI_DY, self.qa, self.sa, seed, offset))
-            qwt, swt = rec("quant_cols", lambda: self._q(W, 1, m.INT8MP_STREAM_GI_W, self.qb, self.sb, seed, offset))
-            rec("gemm", lambda: m.int8mp_scaled_mm(qg, sg, qwt, swt, out=l["dX"]))
-            # grad weight: dY and X along T (columns -> [N, T], [K, T])
-            qgt, sgt = rec("quant_cols", lambda: self._q(dY, 1, m.INT8MP_STREAM_GW_DY, self.qa, self.sa, seed, offset))
-            qxt, sxt = rec("quant_cols", lambda: self._q(X, 1, m.INT8MP_STREAM_GW_X, self.qb, self.sb, seed, offset))
-            rec("gemm", lambda: m.int8mp_scaled_mm(qgt, sgt, qxt, sxt, out=l["dW"]))
+            # grad input: dY along N (rows), W along N (columns, codes [N, K]): A @ B
+            qg, sg = rec("quant_rows", lambda: self._q(dY, 0, m.INT8MP_STREAM_GI_DY, self.qa, self.sa, seed, offset, cg))
+            qwc, swc = rec("quant_cols", lambda: self._q(W, 2, m.INT8MP_STREAM_GI_W, self.qb, self.sb, seed, offset, cw))
+            rec("gemm", lambda: m.int8mp_scaled_mm(qg, sg, qwc, swc, layout=m.INT8MP_AxB, out=l["dX"]))
+            # grad weight: dY and X along T (columns, codes [T, N], [T, K]): A.T @ B
+            qgc, sgc = rec("quant_cols", lambda: self._q(dY, 2, m.INT8MP_STREAM_GW_DY, self.qa, self.sa, seed, offset, cg))
+            qxc, sxc = rec("quant_cols", lambda: self._q(X, 2, m.INT8MP_STREAM_GW_X, self.qb, self.sb, seed, offset, cx))
+            rec("gemm", lambda: m.int8mp_scaled_mm(qgc, sgc, qxc, sxc, layout=m.INT8MP_ATxB, out=l["dW"]))
 
 
 def time_steps(step, steps, warmup, world, device):
@@ -271,8 +287,10 @@ def time_steps(step, steps, warmup, world, device):
 
 
 def time_e2e(step, steps, warmup):
-    """Same step through int8mp_linear_fwd / int8mp_linear_bwd, inputs copied
-    from pinned host memory each step and dW copied back."""
+    """Same step through int8mp_linear_fwd_save / int8mp_linear_bwd_saved (the
+    layer API: the forward pass keeps X's and W's column absmax for the
+    backward pass), inputs copied from pinned host memory each step and dW
+    copied back."""
     import torch
     m = step.m
     cfg = m.linear_cfg(mode=step.mode)
@@ -296,8 +314,11 @@ def time_e2e(step, steps, warmup):
                     l[dkey].copy_(l[hkey], non_blocking=True)
                     copied.add(id(l[hkey]))
         for l in step.linears:
-            m.int8mp_linear_fwd(l["X"], l["W"], cfg, Y=l["Y"], workspace=ws)
-            m.int8mp_linear_bwd(l["dY"], l["X"], l["W"], cfg, dX=l["dX"], dW=l["dW"], workspace=ws)
+            K = l["K"]
+            am = l["colmax"][:2 * K]
+            m.int8mp_linear_fwd_save(l["X"], l["W"], am, cfg, Y=l["Y"], workspace=ws)
+            m.int8mp_linear_bwd_saved(l["dY"], l["X"], l["W"], am, cfg, dX=l["dX"], dW=l["dW"],
+                                      workspace=ws)
             l["hdW"].copy_(l["dW"], non_blocking=True)
     for _ in range(warmup):
         one()
@@ -346,8 +367,9 @@ def cpu_baseline(spec):
 # ------------------------------------------------------------------ extras
 def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
     """Square quant+scaled-mm in the three layouts: quantize A and B along K
-    (columns for the operands stored K-first), then the matmul.  L2 flushed
-    between iterations (256 MB write)."""
+    (by columns, codes left in place, for the operands stored K-first), then
+    the matmul in the stored layout.  L2 flushed between iterations (256 MB
+    write)."""
     import torch
     import int8_mixed_precision_row_gb300 as m
     from int8_mixed_precision_row_gb300 import synth
@@ -361,7 +383,8 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
         sa = torch.empty(S, dtype=torch.float32, device=device)
         sb = torch.empty(S, dtype=torch.float32, device=device)
         Y = torch.empty((S, S), dtype=torch.bfloat16, device=device)
-        for layout, (ax_a, ax_b) in (("A@B.T", (0, 0)), ("A@B", (0, 1)), ("A.T@B", (1, 1))):
+        for layout, (ax_a, ax_b, lay) in (("A@B.T", (0, 0, m.INT8MP_AxBT)), ("A@B", (0, 2, m.INT8MP_AxB)),
+                                          ("A.T@B", (2, 2, m.INT8MP_ATxB))):
             tq, tm = [], []
             for it in range(iters + 3):
                 flush.fill_(it & 0xFF)
@@ -370,7 +393,7 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
                 m.int8mp_quantize_rowwise(A, axis=ax_a, codes=m.INT8MP_CODES_F16, q=qa, scale=sa)
                 m.int8mp_quantize_rowwise(B, axis=ax_b, codes=m.INT8MP_CODES_F16, q=qb, scale=sb)
                 e[1].record()
-                m.int8mp_scaled_mm(qa, sa, qb, sb, out=Y)
+                m.int8mp_scaled_mm(qa, sa, qb, sb, layout=lay, out=Y)
                 e[2].record()
                 torch.cuda.synchronize()
                 if it >= 3:
@@ -400,7 +423,8 @@ def layer_tok_s(spec, mode, device, steps=5, warmup=2):
 def pass_switch_table(spec, device, steps=5, warmup=2):
     """The rows of the pages' INT8 mixed precision training table (forward /
     grad-input / grad-weight each INT8 or BF16, nearest-even) on this GPU,
-    for the decoder layer's linears, through int8mp_linear_fwd/bwd."""
+    for the decoder layer's linears, through int8mp_linear_fwd_save /
+    int8mp_linear_bwd_saved."""
     import torch
     import int8_mixed_precision_row_gb300 as m
     step = LayerStep(spec, m.INT8MP_RNE, device)
@@ -412,9 +436,10 @@ def pass_switch_table(spec, device, steps=5, warmup=2):
 
         def one():
             for l in step.linears:
-                m.int8mp_linear_fwd(l["X"], l["W"], cfg, Y=l["Y"], workspace=ws)
-                m.int8mp_linear_bwd(l["dY"], l["X"], l["W"], cfg, dX=l["dX"], dW=l["dW"],
-                                    workspace=ws)
+                am = l["colmax"][:2 * l["K"]]
+                m.int8mp_linear_fwd_save(l["X"], l["W"], am, cfg, Y=l["Y"], workspace=ws)
+                m.int8mp_linear_bwd_saved(l["dY"], l["X"], l["W"], am, cfg, dX=l["dX"],
+                                          dW=l["dW"], workspace=ws)
         for _ in range(warmup):
             one()
         torch.cuda.synchronize()

@@ -88,6 +88,13 @@ enum {
   INT8MP_STREAM_GW_DY = 4, INT8MP_STREAM_GW_X = 5
 };
 
+/* Groups and code layout of int8mp_quantize_rowwise (its `axis`). */
+enum {
+  INT8MP_GROUP_ROWS = 0,   /* one group per row; codes [rows, cols]               */
+  INT8MP_GROUP_COLS_T = 1, /* one group per column; codes transposed [cols, rows] */
+  INT8MP_GROUP_COLS = 2    /* one group per column; codes [rows, cols]            */
+};
+
 /* Largest contraction length: 127 * 127 * K must stay below 2^31. */
 #define INT8MP_MAX_K 133143
 
@@ -98,11 +105,17 @@ enum {
  * finetuning", summary: x_q = clamp(x / scale + zp), here zp = 0).
  *
  *   x       bf16 [rows, cols], row stride `ld` elements (ld >= cols).
- *   axis    0: one group per row (along cols).  Codes q [rows, cols]
- *              (row stride cols), scale [rows].
- *           1: one group per column (along rows).  Codes written transposed,
- *              q [cols, rows] (row stride rows), scale [cols]; this puts the
- *              contraction axis innermost for the matmul.
+ *   axis    INT8MP_GROUP_ROWS (0): one group per row (along cols).  Codes
+ *              q [rows, cols] (row stride cols), scale [rows].
+ *           INT8MP_GROUP_COLS_T (1): one group per column (along rows).
+ *              Codes written transposed, q [cols, rows] (row stride rows),
+ *              scale [cols]: the contraction axis innermost (K-major).
+ *           INT8MP_GROUP_COLS (2): one group per column (along rows).  Codes
+ *              in the input's layout, q [rows, cols] (row stride cols), scale
+ *              [cols]: the operand enters int8mp_scaled_mm as the [K, M] or
+ *              [K, N] operand of the A @ B and A.T @ B layouts.
+ *           The codes of 1 and 2 are the same numbers (the stochastic
+ *           counter follows the source element), only their layout differs.
  *   mode    INT8MP_RNE or INT8MP_SR; seed, offset, stream_id are used by SR
  *           only (see the header comment for the counter mapping).
  *   q       output codes, int8_t or binary16 per `codes`.
@@ -110,12 +123,50 @@ enum {
  * Requirements: rows, cols >= 0 (either may be 0: nothing is launched);
  * cols % 8 == 0, ld % 8 == 0 and x 16-byte aligned (128-bit loads); for
  * axis 1 also rows % 8 == 0 (128-bit stores of the transposed codes); q 16-byte
- * aligned; scale 4-byte aligned.  Violations return INT8MP_ERR_ALIGNMENT.
+ * aligned; scale 4-byte aligned.  Violations return INT8MP_ERR_ALIGNMENT.  A
+ * column-grouped call writes `scale` twice (absmax first, then the scale):
+ * nothing else may read it until the call's work on `stream` is done.
  */
 int8mp_status int8mp_quantize_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                       int axis, int8mp_round mode, uint64_t seed,
                                       uint64_t offset, uint32_t stream_id, void* q,
                                       int8mp_codes codes, float* scale, void* stream);
+
+/*
+ * int8mp_quantize_rows_colmax -- row groups exactly as int8mp_quantize_rowwise
+ * with INT8MP_GROUP_ROWS, and in the same pass over x the absmax of every
+ * column merged into colmax:
+ *   colmax[c] = max(colmax[c], max_r |x[r, c]|)      (fp32 [cols])
+ * The caller initializes colmax with non-negative values (zeros for one
+ * matrix; calls over row blocks of one matrix can accumulate into the same
+ * array).  This is the
+ * pass that feeds int8mp_quantize_cols_absmax when the same matrix is
+ * quantized along both axes (the output gradient of a linear layer, whose
+ * rows feed grad-input and whose columns feed grad-weight), so that the
+ * column groups need no absmax pass of their own.
+ * Requirements: those of INT8MP_GROUP_ROWS; colmax non-NULL, 4-byte aligned
+ * (INT8MP_ERR_INVALID_ARG / INT8MP_ERR_ALIGNMENT).  While the call runs on
+ * `stream`, colmax is updated by atomic max.
+ */
+int8mp_status int8mp_quantize_rows_colmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                          int8mp_round mode, uint64_t seed, uint64_t offset,
+                                          uint32_t stream_id, void* q, int8mp_codes codes,
+                                          float* scale, float* colmax, void* stream);
+
+/*
+ * int8mp_quantize_cols_absmax -- column groups with the codes in the input's
+ * layout (as INT8MP_GROUP_COLS), given each column's absmax (fp32 [cols],
+ * e.g. from int8mp_quantize_rows_colmax over the same x): scale[c] =
+ * colmax[c] / 127 and codes q [rows, cols].  When colmax holds the true
+ * column absmax the results are those of int8mp_quantize_rowwise with
+ * INT8MP_GROUP_COLS, bit for bit; otherwise codes are still clamped to
+ * [-127, 127].  Requirements: those of INT8MP_GROUP_COLS; colmax non-NULL,
+ * 4-byte aligned.
+ */
+int8mp_status int8mp_quantize_cols_absmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                          const float* colmax, int8mp_round mode, uint64_t seed,
+                                          uint64_t offset, uint32_t stream_id, void* q,
+                                          int8mp_codes codes, float* scale, void* stream);
 
 /*
  * int8mp_scaled_mm -- scaled INT8 matmul ("Quantized model training" README,
@@ -124,17 +175,19 @@ int8mp_status int8mp_quantize_rowwise(const void* x, int64_t rows, int64_t cols,
  *
  *   out[i,j] = bf16_RNE((fp32_RN(sum_k a(i,k) b(j,k)) * sA[i]) * sB[j])
  *
- *   A, B    INT8 codes in the container `codes`, stored per `layout`.  The
- *           tensor-core path reads K-major operands (INT8MP_AxBT); for AxB and
- *           ATxB the caller quantizes the K-major operand with axis 1 of
- *           int8mp_quantize_rowwise, which writes it transposed, and passes
- *           INT8MP_AxBT.  Other layouts return INT8MP_ERR_INVALID_ARG.
+ *   A, B    INT8 codes in the container `codes`, stored per `layout`
+ *           (dense: row stride = row length): AxBT A [M,K], B [N,K]; AxB
+ *           A [M,K], B [K,N]; ATxB A [K,M], B [K,N].  Operands quantized
+ *           along K come from int8mp_quantize_rowwise: a [.., K] operand with
+ *           INT8MP_GROUP_ROWS, a [K, ..] operand with INT8MP_GROUP_COLS (or
+ *           with INT8MP_GROUP_COLS_T and the AxBT layout).
  *   sA      fp32 [M], sB fp32 [N].
  *   out     bf16 [M, N], row stride ldo elements (ldo >= N).
  * Requirements: M, N >= 0; 16 <= K <= INT8MP_MAX_K; K % 16 == 0 (when M or N
  * is 0 nothing is launched); A, B 16-byte aligned; N % 8 == 0, ldo % 8 == 0
- * and out 16-byte aligned (128-bit stores).  M and N need not be tile
- * multiples.  codes must be INT8MP_CODES_F16.
+ * and out 16-byte aligned (128-bit stores); for ATxB also M % 8 == 0.  M and
+ * N need not be tile multiples.  codes must be INT8MP_CODES_F16 (the
+ * tensor-core container; INT8MP_CODES_S8 returns INT8MP_ERR_INVALID_ARG).
  */
 int8mp_status int8mp_scaled_mm(const void* A, const float* sA, const void* B, const float* sB,
                                int64_t M, int64_t N, int64_t K, int8mp_layout layout,
@@ -198,6 +251,29 @@ int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, vo
                                 void* dW, int64_t T, int64_t N, int64_t K,
                                 const int8mp_linear_cfg* cfg, void* workspace, size_t ws_bytes,
                                 void* stream);
+
+/*
+ * int8mp_linear_fwd_save / int8mp_linear_bwd_saved -- the same passes, with
+ * the same results bit for bit, sharing one thing across them: the forward
+ * pass, which reads X and W row by row anyway, also records their column
+ * absmax -- absmax[0..K) for X over its T rows, absmax[K..2K) for W over its
+ * N rows (fp32, 2K values, caller-owned) -- and the backward pass uses them
+ * for the column groups of grad-weight (X along T) and grad-input (W along
+ * N) instead of reading X and W once more.  X's half is filled only when
+ * cfg->int8_grad_w is 1 and W's only when cfg->int8_grad_in is 1 (the other
+ * half is set to 0); the backward pass must get the same cfg, X and W as the
+ * forward pass that filled `absmax`.  Requirements:
+ * those of int8mp_linear_fwd / int8mp_linear_bwd; absmax non-NULL and
+ * 4-byte aligned.  (The 2K floats are the only state kept between the passes;
+ * the INT8 codes are still recomputed from bf16.)
+ */
+int8mp_status int8mp_linear_fwd_save(const void* X, const void* W, void* Y, int64_t T, int64_t N,
+                                     int64_t K, const int8mp_linear_cfg* cfg, float* absmax,
+                                     void* workspace, size_t ws_bytes, void* stream);
+int8mp_status int8mp_linear_bwd_saved(const void* dY, const void* X, const void* W, void* dX,
+                                      void* dW, int64_t T, int64_t N, int64_t K,
+                                      const int8mp_linear_cfg* cfg, const float* absmax,
+                                      void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * int8mp_linear_fwd_noalloc -- the same forward pass as int8mp_linear_fwd

@@ -5,8 +5,14 @@ forward and backward matmuls run in INT8 while the weight and the saved
 activation stay bf16 (memory does not change).  Int8MixedPrecisionLinear
 is a bias-free drop-in for nn.Linear with a bf16 weight [out, in]; both
 passes call the library (int8mp_linear_fwd / int8mp_linear_bwd) and do
-nothing else.  Requirements of the library apply to the flattened input:
-the token count, in_features and out_features must be multiples of 16.
+nothing else.  The forward pass keeps one thing for the backward pass
+besides X and W: their column absmax (2 x in_features floats, recorded while
+the forward pass reads them), so that the backward pass's column
+quantizations of X and W need no extra pass over them
+(int8mp_linear_fwd_save / int8mp_linear_bwd_saved; results are those of the
+plain passes bit for bit).  Requirements of the library apply to the
+flattened input: the token count, in_features and out_features must be
+multiples of 16.
 """
 import torch
 
@@ -22,23 +28,25 @@ class Int8MixedPrecisionLinearFunction(torch.autograd.Function):
         if not x2.is_contiguous():
             x2 = x2.contiguous()
         cfg = b.linear_cfg(mode=mode, seed=seed, offset=offset)
-        y = b.int8mp_linear_fwd(x2, weight, cfg)
-        ctx.save_for_backward(x2, weight)
+        absmax = torch.empty((2 * K,), dtype=torch.float32, device=x.device)
+        y = b.int8mp_linear_fwd_save(x2, weight, absmax, cfg)
+        ctx.save_for_backward(x2, weight, absmax)
         ctx.cfg = (mode, seed, offset)
         ctx.in_shape = x.shape
         return y.reshape(*x.shape[:-1], N)
 
     @staticmethod
     def backward(ctx, dy):
-        x2, weight = ctx.saved_tensors
+        x2, weight, absmax = ctx.saved_tensors
         N = weight.shape[0]
         dy2 = dy.reshape(-1, N)
         if not dy2.is_contiguous():
             dy2 = dy2.contiguous()
         mode, seed, offset = ctx.cfg
         cfg = b.linear_cfg(mode=mode, seed=seed, offset=offset)
-        dx, dw = b.int8mp_linear_bwd(dy2, x2, weight, cfg, want_dx=ctx.needs_input_grad[0],
-                                     want_dw=ctx.needs_input_grad[1])
+        dx, dw = b.int8mp_linear_bwd_saved(dy2, x2, weight, absmax, cfg,
+                                           want_dx=ctx.needs_input_grad[0],
+                                           want_dw=ctx.needs_input_grad[1])
         if dx is not None:
             dx = dx.reshape(ctx.in_shape)
         return dx, dw, None, None, None

@@ -23,6 +23,7 @@ INT8MP_ERR_WORKSPACE = 6
 
 INT8MP_RNE, INT8MP_SR = 0, 1
 INT8MP_AxBT, INT8MP_AxB, INT8MP_ATxB = 0, 1, 2
+INT8MP_GROUP_ROWS, INT8MP_GROUP_COLS_T, INT8MP_GROUP_COLS = 0, 1, 2
 INT8MP_CODES_S8, INT8MP_CODES_F16 = 0, 1
 (INT8MP_STREAM_FWD_X, INT8MP_STREAM_FWD_W, INT8MP_STREAM_GI_DY, INT8MP_STREAM_GI_W,
  INT8MP_STREAM_GW_DY, INT8MP_STREAM_GW_X) = range(6)
@@ -34,7 +35,8 @@ EXPORTED = (
     "int8mp_linear_workspace_size", "int8mp_linear_fwd", "int8mp_linear_bwd",
     "int8mp_poll_device_status", "int8mp_status_string", "int8mp_version",
     "int8mp_debug_mm_s32_drop_first_load", "int8mp_linear_fwd_noalloc",
-    "int8mp_debug_check_division",
+    "int8mp_debug_check_division", "int8mp_quantize_rows_colmax", "int8mp_quantize_cols_absmax",
+    "int8mp_linear_fwd_save", "int8mp_linear_bwd_saved",
 )
 INT8MP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -94,10 +96,20 @@ def load(path=None):
     L.int8mp_linear_fwd_noalloc.argtypes = [_P, _P, _P, _I64, _I64, _I64,
                                             ctypes.POINTER(int8mp_linear_cfg), _P]
     L.int8mp_debug_check_division.argtypes = [_P, _P]
+    L.int8mp_quantize_rows_colmax.argtypes = [_P, _I64, _I64, _I64, _INT, _U64, _U64, _U32, _P,
+                                              _INT, _P, _P, _P]
+    L.int8mp_quantize_cols_absmax.argtypes = [_P, _I64, _I64, _I64, _P, _INT, _U64, _U64, _U32, _P,
+                                              _INT, _P, _P]
+    L.int8mp_linear_fwd_save.argtypes = [_P, _P, _P, _I64, _I64, _I64,
+                                         ctypes.POINTER(int8mp_linear_cfg), _P, _P, _SZ, _P]
+    L.int8mp_linear_bwd_saved.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64,
+                                          ctypes.POINTER(int8mp_linear_cfg), _P, _P, _SZ, _P]
     for name in ("int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
                  "int8mp_linear_fwd", "int8mp_linear_bwd", "int8mp_poll_device_status",
                  "int8mp_version", "int8mp_debug_mm_s32_drop_first_load",
-                 "int8mp_linear_fwd_noalloc", "int8mp_debug_check_division"):
+                 "int8mp_linear_fwd_noalloc", "int8mp_debug_check_division",
+                 "int8mp_quantize_rows_colmax", "int8mp_quantize_cols_absmax",
+                 "int8mp_linear_fwd_save", "int8mp_linear_bwd_saved"):
         getattr(L, name).restype = _INT
     _lib = L
     return L
@@ -132,27 +144,75 @@ def int8mp_version():
 def int8mp_quantize_rowwise(x, axis=0, mode=INT8MP_RNE, seed=0, offset=0, stream_id=0,
                             codes=INT8MP_CODES_S8, cols=None, q=None, scale=None, stream=None):
     """x: bf16 CUDA tensor [rows, ld] (row stride ld).  Returns (codes, scale);
-    axis 0 codes are [rows, cols], axis 1 codes are [cols, rows]."""
+    axis 0 (row groups) and 2 (column groups) codes are [rows, cols], axis 1
+    (column groups) codes are [cols, rows]."""
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda
     rows = x.shape[0]
     ld = x.stride(0) if rows > 0 else x.shape[1]
     cols = x.shape[1] if cols is None else cols
-    groups, glen = (rows, cols) if axis == 0 else (cols, rows)
+    shape = (cols, rows) if axis == INT8MP_GROUP_COLS_T else (rows, cols)
     if q is None:
-        q = torch.empty((groups, glen), dtype=_code_dtype(codes), device=x.device)
+        q = torch.empty(shape, dtype=_code_dtype(codes), device=x.device)
     if scale is None:
-        scale = torch.empty((groups,), dtype=torch.float32, device=x.device)
+        scale = torch.empty((rows if axis == INT8MP_GROUP_ROWS else cols,), dtype=torch.float32,
+                            device=x.device)
     _check(load().int8mp_quantize_rowwise(_ptr(x), rows, cols, ld, int(axis), int(mode), int(seed),
                                           int(offset), int(stream_id), _ptr(q), int(codes),
                                           _ptr(scale), _stream(stream)), "int8mp_quantize_rowwise")
     return q, scale
 
 
+def _mm_sizes(A, B, layout):
+    if layout == INT8MP_AxBT:
+        return A.shape[0], B.shape[0], A.shape[1]
+    if layout == INT8MP_AxB:
+        return A.shape[0], B.shape[1], A.shape[1]
+    return A.shape[1], B.shape[1], A.shape[0]
+
+
+def int8mp_quantize_rows_colmax(x, colmax, mode=INT8MP_RNE, seed=0, offset=0, stream_id=0,
+                                codes=INT8MP_CODES_S8, q=None, scale=None, stream=None):
+    """Row groups of x [rows, cols] (codes [rows, cols], scale [rows]) and,
+    in the same pass, colmax [cols] (fp32, caller-initialized) max-merged
+    with each column's absmax."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda
+    rows, cols = x.shape
+    ld = x.stride(0) if rows > 0 else cols
+    if q is None:
+        q = torch.empty((rows, cols), dtype=_code_dtype(codes), device=x.device)
+    if scale is None:
+        scale = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    _check(load().int8mp_quantize_rows_colmax(_ptr(x), rows, cols, ld, int(mode), int(seed),
+                                              int(offset), int(stream_id), _ptr(q), int(codes),
+                                              _ptr(scale), _ptr(colmax), _stream(stream)),
+           "int8mp_quantize_rows_colmax")
+    return q, scale
+
+
+def int8mp_quantize_cols_absmax(x, colmax, mode=INT8MP_RNE, seed=0, offset=0, stream_id=0,
+                                codes=INT8MP_CODES_S8, q=None, scale=None, stream=None):
+    """Column groups of x [rows, cols] with each column's absmax given:
+    codes [rows, cols], scale [cols]."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda
+    rows, cols = x.shape
+    ld = x.stride(0) if rows > 0 else cols
+    if q is None:
+        q = torch.empty((rows, cols), dtype=_code_dtype(codes), device=x.device)
+    if scale is None:
+        scale = torch.empty((cols,), dtype=torch.float32, device=x.device)
+    _check(load().int8mp_quantize_cols_absmax(_ptr(x), rows, cols, ld, _ptr(colmax), int(mode),
+                                              int(seed), int(offset), int(stream_id), _ptr(q),
+                                              int(codes), _ptr(scale), _stream(stream)),
+           "int8mp_quantize_cols_absmax")
+    return q, scale
+
+
 def int8mp_scaled_mm(A, sA, B, sB, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, out=None,
                      stream=None):
-    """A [M,K], B [N,K] codes (f16 containers), sA [M], sB [N] -> bf16 [M,N]."""
-    M, K = A.shape
-    N = B.shape[0]
+    """Codes (f16 containers) A, B stored per layout -- A@B.T: A [M,K], B [N,K];
+    A@B: A [M,K], B [K,N]; A.T@B: A [K,M], B [K,N] -- sA [M], sB [N] -> bf16
+    [M,N]."""
+    M, N, K = _mm_sizes(A, B, layout)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     ldo = out.stride(0) if M > 0 else N
@@ -162,8 +222,7 @@ def int8mp_scaled_mm(A, sA, B, sB, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, o
 
 
 def int8mp_mm_s32(A, B, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, out=None, stream=None):
-    M, K = A.shape
-    N = B.shape[0]
+    M, N, K = _mm_sizes(A, B, layout)
     if out is None:
         out = torch.empty((M, N), dtype=torch.int32, device=A.device)
     ldo = out.stride(0) if M > 0 else N
@@ -211,6 +270,39 @@ def int8mp_linear_bwd(dY, X, W, cfg=None, dX=None, dW=None, want_dx=True, want_d
     _check(load().int8mp_linear_bwd(_ptr(dY), _ptr(X), _ptr(W), _ptr(dX if want_dx else None),
                                     _ptr(dW if want_dw else None), T, N, K, ctypes.byref(cfg),
                                     _ptr(ws), nbytes, _stream(stream)), "int8mp_linear_bwd")
+    return (dX if want_dx else None), (dW if want_dw else None)
+
+
+def int8mp_linear_fwd_save(X, W, absmax, cfg=None, Y=None, workspace=None, stream=None):
+    """int8mp_linear_fwd that also fills absmax (fp32 [2K]) with the column
+    absmax of X and of W for int8mp_linear_bwd_saved."""
+    cfg = cfg or linear_cfg()
+    T, K = X.shape
+    N = W.shape[0]
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.bfloat16, device=X.device)
+    ws, nbytes = _workspace(T, N, K, cfg, workspace, X.device)
+    _check(load().int8mp_linear_fwd_save(_ptr(X), _ptr(W), _ptr(Y), T, N, K, ctypes.byref(cfg),
+                                         _ptr(absmax), _ptr(ws), nbytes, _stream(stream)),
+           "int8mp_linear_fwd_save")
+    return Y
+
+
+def int8mp_linear_bwd_saved(dY, X, W, absmax, cfg=None, dX=None, dW=None, want_dx=True,
+                            want_dw=True, workspace=None, stream=None):
+    """int8mp_linear_bwd given the absmax saved by int8mp_linear_fwd_save."""
+    cfg = cfg or linear_cfg()
+    T, K = X.shape
+    N = W.shape[0]
+    if want_dx and dX is None:
+        dX = torch.empty((T, K), dtype=torch.bfloat16, device=X.device)
+    if want_dw and dW is None:
+        dW = torch.empty((N, K), dtype=torch.bfloat16, device=X.device)
+    ws, nbytes = _workspace(T, N, K, cfg, workspace, X.device)
+    _check(load().int8mp_linear_bwd_saved(_ptr(dY), _ptr(X), _ptr(W), _ptr(dX if want_dx else None),
+                                          _ptr(dW if want_dw else None), T, N, K,
+                                          ctypes.byref(cfg), _ptr(absmax), _ptr(ws), nbytes,
+                                          _stream(stream)), "int8mp_linear_bwd_saved")
     return (dX if want_dx else None), (dW if want_dw else None)
 
 

@@ -69,7 +69,7 @@ inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 int8mp_status check_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int axis,
                              int8mp_round mode, const void* q, int8mp_codes codes,
                              const float* scale) {
-  if (axis != 0 && axis != 1) return INT8MP_ERR_INVALID_ARG;
+  if (axis != 0 && axis != 1 && axis != 2) return INT8MP_ERR_INVALID_ARG;
   if (mode != INT8MP_RNE && mode != INT8MP_SR) return INT8MP_ERR_INVALID_ARG;
   if (codes != INT8MP_CODES_S8 && codes != INT8MP_CODES_F16) return INT8MP_ERR_INVALID_ARG;
   if (rows < 0 || cols < 0 || ld < cols) return INT8MP_ERR_INVALID_ARG;
@@ -90,18 +90,21 @@ int8mp_status check_mm(const void* A, const void* B, int64_t M, int64_t N, int64
   if (codes != INT8MP_CODES_S8 && codes != INT8MP_CODES_F16) return INT8MP_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || K > INT8MP_MAX_K || ldo < N) return INT8MP_ERR_INVALID_ARG;
   if (M > INT32_MAX || N > INT32_MAX) return INT8MP_ERR_INVALID_ARG;
-  // the tensor-core path reads K-major f16 containers
-  if (layout != INT8MP_AxBT || codes != INT8MP_CODES_F16) return INT8MP_ERR_INVALID_ARG;
+  // the tensor-core path reads f16 containers
+  if (codes != INT8MP_CODES_F16) return INT8MP_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return INT8MP_OK;
   if (!out || (K > 0 && (!A || !B))) return INT8MP_ERR_INVALID_ARG;
   if (K % 16 || N % 8 || ldo % 8 || !aligned(out, 16)) return INT8MP_ERR_ALIGNMENT;
+  if (layout == INT8MP_ATxB && M % 8) return INT8MP_ERR_ALIGNMENT;  // rows of A^T are M long
   if (K > 0 && (!aligned(A, 16) || !aligned(B, 16))) return INT8MP_ERR_ALIGNMENT;
   return INT8MP_OK;
 }
 
+// layout AxBT: both operands K-major; AxB: B MN-major ([K,N]); ATxB: both
+// MN-major (A [K,M], B [K,N]).
 int8mp_status run_mm(const void* A, const float* sA, const void* B, const float* sB, int64_t M,
-                     int64_t N, int64_t K, int8mp::GemmOut mode, void* out, int64_t ldo,
-                     const int8mp::GemmDebug& dbg, cudaStream_t stream) {
+                     int64_t N, int64_t K, int8mp_layout layout, int8mp::GemmOut mode, void* out,
+                     int64_t ldo, const int8mp::GemmDebug& dbg, cudaStream_t stream) {
   if (M == 0 || N == 0) return INT8MP_OK;
   DeviceInfo dev;
   int8mp_status st = current_device(&dev);
@@ -111,7 +114,9 @@ int8mp_status run_mm(const void* A, const float* sA, const void* B, const float*
     return from_cuda(cudaMemset2DAsync(out, static_cast<size_t>(ldo) * esize, 0,
                                        static_cast<size_t>(N) * esize, static_cast<size_t>(M),
                                        stream));
-  return from_cuda(int8mp::launch_gemm(A, sA, B, sB, M, N, K, mode, out, ldo, dev, dbg, stream));
+  const bool a_mn = layout == INT8MP_ATxB, b_mn = layout != INT8MP_AxBT;
+  return from_cuda(
+      int8mp::launch_gemm(A, a_mn, sA, B, b_mn, sB, M, N, K, mode, out, ldo, dev, dbg, stream));
 }
 
 // ------------------------------------------------------------- workspace
@@ -146,12 +151,27 @@ size_t fwd_bytes(int64_t T, int64_t N, int64_t K) {
   carve_operand(c, N, K);
   return c.used;
 }
+// backward codes: dY by rows [T,N] + s[T] (grad input, along N); W by
+// columns [N,K] + s[K] (along N); dY by columns [T,N] + s[N] (grad weight,
+// along T); X by columns [T,K] + s[K] (along T).  Column codes keep the
+// input's layout and enter the matmul MN-major.  Then the column absmax of
+// dY [N], X [K] and W [K] (contiguous, cleared by one memset).
+struct BwdOperands {
+  QOperand dy_rows, w_cols, dy_cols, x_cols;
+  float* absmax;  // dY [N], then X [K], then W [K]
+};
+BwdOperands carve_bwd(Carver& c, int64_t T, int64_t N, int64_t K) {
+  BwdOperands o;
+  o.dy_rows = carve_operand(c, T, N);
+  o.w_cols = carve_operand(c, K, N);
+  o.dy_cols = carve_operand(c, N, T);
+  o.x_cols = carve_operand(c, K, T);
+  o.absmax = static_cast<float*>(c.take(static_cast<size_t>(N + 2 * K) * 4));
+  return o;
+}
 size_t bwd_bytes(int64_t T, int64_t N, int64_t K) {
   Carver c{nullptr};
-  carve_operand(c, T, N);  // dY along N (grad input)
-  carve_operand(c, K, N);  // W along N, transposed
-  carve_operand(c, N, T);  // dY along T, transposed (grad weight)
-  carve_operand(c, K, T);  // X along T, transposed
+  carve_bwd(c, T, N, K);
   return c.used;
 }
 
@@ -187,10 +207,43 @@ int8mp_status int8mp_quantize_rowwise(const void* x, int64_t rows, int64_t cols,
   const int8mp::SrArgs sr{seed, offset, stream_id};
   cudaError_t e = axis == 0
                       ? int8mp::launch_quantize_rows(x, rows, cols, ld, mode, sr, q, codes, scale,
-                                                     dev, as_stream(stream))
+                                                     nullptr, dev, as_stream(stream))
                       : int8mp::launch_quantize_cols(x, rows, cols, ld, mode, sr, q, codes, scale,
-                                                     dev, as_stream(stream));
+                                                     axis == 1, dev, as_stream(stream));
   return from_cuda(e);
+}
+
+int8mp_status int8mp_quantize_rows_colmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                          int8mp_round mode, uint64_t seed, uint64_t offset,
+                                          uint32_t stream_id, void* q, int8mp_codes codes,
+                                          float* scale, float* colmax, void* stream) {
+  int8mp_status st = check_quantize(x, rows, cols, ld, 0, mode, q, codes, scale);
+  if (st != INT8MP_OK || rows == 0 || cols == 0) return st;
+  if (!colmax) return INT8MP_ERR_INVALID_ARG;
+  if (!aligned(colmax, 4)) return INT8MP_ERR_ALIGNMENT;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != INT8MP_OK) return st;
+  const int8mp::SrArgs sr{seed, offset, stream_id};
+  return from_cuda(int8mp::launch_quantize_rows(x, rows, cols, ld, mode, sr, q, codes, scale,
+                                                colmax, dev, as_stream(stream)));
+}
+
+int8mp_status int8mp_quantize_cols_absmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                          const float* colmax, int8mp_round mode, uint64_t seed,
+                                          uint64_t offset, uint32_t stream_id, void* q,
+                                          int8mp_codes codes, float* scale, void* stream) {
+  int8mp_status st = check_quantize(x, rows, cols, ld, 2, mode, q, codes, scale);
+  if (st != INT8MP_OK || rows == 0 || cols == 0) return st;
+  if (!colmax) return INT8MP_ERR_INVALID_ARG;
+  if (!aligned(colmax, 4)) return INT8MP_ERR_ALIGNMENT;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != INT8MP_OK) return st;
+  const int8mp::SrArgs sr{seed, offset, stream_id};
+  return from_cuda(int8mp::launch_quantize_cols_from_absmax(x, rows, cols, ld, colmax, mode, sr,
+                                                            q, codes, scale, dev,
+                                                            as_stream(stream)));
 }
 
 int8mp_status int8mp_scaled_mm(const void* A, const float* sA, const void* B, const float* sB,
@@ -202,7 +255,7 @@ int8mp_status int8mp_scaled_mm(const void* A, const float* sA, const void* B, co
     if (!sA || !sB) return INT8MP_ERR_INVALID_ARG;
     if (!aligned(sA, 4) || !aligned(sB, 4)) return INT8MP_ERR_ALIGNMENT;
   }
-  return run_mm(A, sA, B, sB, M, N, K, int8mp::GemmOut::kBf16Scaled, out, ldo,
+  return run_mm(A, sA, B, sB, M, N, K, layout, int8mp::GemmOut::kBf16Scaled, out, ldo,
                 int8mp::GemmDebug{}, as_stream(stream));
 }
 
@@ -211,7 +264,7 @@ int8mp_status int8mp_mm_s32(const void* A, const void* B, int64_t M, int64_t N, 
                             void* stream) {
   int8mp_status st = check_mm(A, B, M, N, K, layout, codes, out, ldo);
   if (st != INT8MP_OK) return st;
-  return run_mm(A, nullptr, B, nullptr, M, N, K, int8mp::GemmOut::kS32, out, ldo,
+  return run_mm(A, nullptr, B, nullptr, M, N, K, layout, int8mp::GemmOut::kS32, out, ldo,
                 int8mp::GemmDebug{}, as_stream(stream));
 }
 
@@ -221,12 +274,26 @@ size_t int8mp_linear_workspace_size(int64_t T, int64_t N, int64_t K, const int8m
   return f > b ? f : b;
 }
 
-int8mp_status int8mp_linear_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t N,
-                                int64_t K, const int8mp_linear_cfg* cfg, void* workspace,
-                                size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Forward pass.  save_absmax (optional, fp32 [2K]): the column absmax of X
+// (over T) and of W (over N), for a later backward pass over the same X, W;
+// X's only when grad-weight runs in INT8, W's only when grad-input does (the
+// other half stays 0).
+int8mp_status linear_fwd_impl(const void* X, const void* W, void* Y, int64_t T, int64_t N,
+                              int64_t K, const int8mp_linear_cfg* cfg, float* save_absmax,
+                              void* workspace, size_t ws_bytes, void* stream) {
   int8mp_status st = check_linear(T, N, K, cfg);
   if (st != INT8MP_OK) return st;
-  if (T == 0 || N == 0) return INT8MP_OK;
+  if (save_absmax && !aligned(save_absmax, 4)) return INT8MP_ERR_ALIGNMENT;
+  if (T == 0 || N == 0) {
+    if (save_absmax && K > 0)  // the absmax of an empty group is 0
+      return from_cuda(cudaMemsetAsync(save_absmax, 0, static_cast<size_t>(2 * K) * 4,
+                                       as_stream(stream)));
+    return INT8MP_OK;
+  }
   if (!Y || (K > 0 && (!X || !W || !workspace))) return INT8MP_ERR_INVALID_ARG;
   if (!aligned(Y, 16) || !aligned(X, 16) || !aligned(W, 16) || !aligned(workspace, 256))
     return INT8MP_ERR_ALIGNMENT;
@@ -235,7 +302,16 @@ int8mp_status int8mp_linear_fwd(const void* X, const void* W, void* Y, int64_t T
   st = current_device(&dev);
   if (st != INT8MP_OK) return st;
   cudaStream_t s = as_stream(stream);
+  if (save_absmax && K > 0 &&
+      cudaMemsetAsync(save_absmax, 0, static_cast<size_t>(2 * K) * 4, s) != cudaSuccess)
+    return INT8MP_ERR_CUDA;
+  float* x_absmax = save_absmax && K > 0 && cfg->int8_grad_w ? save_absmax : nullptr;
+  float* w_absmax = save_absmax && K > 0 && cfg->int8_grad_in ? save_absmax + K : nullptr;
   if (!cfg->int8_fwd) {
+    cudaError_t e = cudaSuccess;
+    if (x_absmax) e = int8mp::launch_column_absmax(X, T, K, K, x_absmax, dev, s);
+    if (e == cudaSuccess && w_absmax) e = int8mp::launch_column_absmax(W, N, K, K, w_absmax, dev, s);
+    if (e != cudaSuccess) return INT8MP_ERR_CUDA;
     // BF16 pass: Y [T,N] = X W^T, i.e. column-major Y^T [N,T] = W X^T
     if (K == 0)
       return from_cuda(cudaMemset2DAsync(Y, static_cast<size_t>(N) * 2, 0,
@@ -247,20 +323,22 @@ int8mp_status int8mp_linear_fwd(const void* X, const void* W, void* Y, int64_t T
   const QOperand wq = carve_operand(c, N, K);
   if (K > 0) {
     cudaError_t e = int8mp::launch_quantize_rows(X, T, K, K, cfg->mode, sr_of(cfg, INT8MP_STREAM_FWD_X),
-                                                 xq.q, INT8MP_CODES_F16, xq.s, dev, s);
+                                                 xq.q, INT8MP_CODES_F16, xq.s, x_absmax, dev, s);
     if (e == cudaSuccess)
       e = int8mp::launch_quantize_rows(W, N, K, K, cfg->mode, sr_of(cfg, INT8MP_STREAM_FWD_W), wq.q,
-                                       INT8MP_CODES_F16, wq.s, dev, s);
+                                       INT8MP_CODES_F16, wq.s, w_absmax, dev, s);
     if (e != cudaSuccess) return INT8MP_ERR_CUDA;
   }
-  return run_mm(xq.q, xq.s, wq.q, wq.s, T, N, K, int8mp::GemmOut::kBf16Scaled, Y, N,
+  return run_mm(xq.q, xq.s, wq.q, wq.s, T, N, K, INT8MP_AxBT, int8mp::GemmOut::kBf16Scaled, Y, N,
                 int8mp::GemmDebug{}, s);
 }
 
-int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, void* dX,
-                                void* dW, int64_t T, int64_t N, int64_t K,
-                                const int8mp_linear_cfg* cfg, void* workspace, size_t ws_bytes,
-                                void* stream) {
+// Backward pass.  saved_absmax (optional, fp32 [2K]): what the forward pass
+// saved for these X and W; otherwise their column absmax is computed here.
+int8mp_status linear_bwd_impl(const void* dY, const void* X, const void* W, void* dX, void* dW,
+                              int64_t T, int64_t N, int64_t K, const int8mp_linear_cfg* cfg,
+                              const float* saved_absmax, void* workspace, size_t ws_bytes,
+                              void* stream) {
   int8mp_status st = check_linear(T, N, K, cfg);
   if (st != INT8MP_OK) return st;
   const bool want_dx = dX != nullptr && T > 0 && K > 0;
@@ -268,7 +346,8 @@ int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, vo
   if (!want_dx && !want_dw) return INT8MP_OK;
   if (!dY || !W || !X || !workspace) return INT8MP_ERR_INVALID_ARG;
   if (!aligned(dY, 16) || !aligned(X, 16) || !aligned(W, 16) || !aligned(workspace, 256) ||
-      (dX && !aligned(dX, 16)) || (dW && !aligned(dW, 16)))
+      (dX && !aligned(dX, 16)) || (dW && !aligned(dW, 16)) ||
+      (saved_absmax && !aligned(saved_absmax, 4)))
     return INT8MP_ERR_ALIGNMENT;
   if (ws_bytes < bwd_bytes(T, N, K)) return INT8MP_ERR_WORKSPACE;
   DeviceInfo dev;
@@ -276,10 +355,27 @@ int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, vo
   if (st != INT8MP_OK) return st;
   cudaStream_t s = as_stream(stream);
   Carver c{static_cast<char*>(workspace)};
-  const QOperand dyq = carve_operand(c, T, N);
-  const QOperand wqt = carve_operand(c, K, N);
-  const QOperand dyqt = carve_operand(c, N, T);
-  const QOperand xqt = carve_operand(c, K, T);
+  const BwdOperands o = carve_bwd(c, T, N, K);
+  const bool int8_dx = want_dx && cfg->int8_grad_in && N > 0;
+  const bool int8_dw = want_dw && cfg->int8_grad_w && T > 0;
+  // column absmax: dY's (grad weight) comes with its row pass when grad
+  // input runs in INT8; X's and W's are the forward's, or computed here
+  float* dy_absmax = o.absmax;
+  const float* x_absmax = saved_absmax ? saved_absmax : o.absmax + N;
+  const float* w_absmax = saved_absmax ? saved_absmax + K : o.absmax + N + K;
+  if ((int8_dx || int8_dw) &&
+      cudaMemsetAsync(o.absmax, 0, static_cast<size_t>(N + 2 * K) * 4, s) != cudaSuccess)
+    return INT8MP_ERR_CUDA;
+  if (!saved_absmax) {
+    cudaError_t e = cudaSuccess;
+    if (int8_dx) e = int8mp::launch_column_absmax(W, N, K, K, o.absmax + N + K, dev, s);
+    if (e == cudaSuccess && int8_dw) e = int8mp::launch_column_absmax(X, T, K, K, o.absmax + N, dev, s);
+    if (e != cudaSuccess) return INT8MP_ERR_CUDA;
+  }
+  if (int8_dw && !int8_dx &&
+      int8mp::launch_column_absmax(dY, T, N, N, dy_absmax, dev, s) != cudaSuccess)
+    return INT8MP_ERR_CUDA;
+
   if (want_dx && !cfg->int8_grad_in) {
     // BF16 pass: dX [T,K] = dY W, i.e. column-major dX^T [K,T] = W^T dY^T
     if (N == 0)
@@ -289,18 +385,20 @@ int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, vo
       st = from_cuda(int8mp::bf16_gemm_colmajor(W, dY, dX, K, T, N, false, false, K, N, K, s));
     if (st != INT8MP_OK) return st;
   } else if (want_dx) {
-    // grad input: contraction over N; dY by rows, W by columns (-> [K, N])
+    // grad input: contraction over N; dY by rows, W by columns; dY W is A @ B
     if (N > 0) {
       cudaError_t e = int8mp::launch_quantize_rows(dY, T, N, N, cfg->mode,
-                                                   sr_of(cfg, INT8MP_STREAM_GI_DY), dyq.q,
-                                                   INT8MP_CODES_F16, dyq.s, dev, s);
+                                                   sr_of(cfg, INT8MP_STREAM_GI_DY), o.dy_rows.q,
+                                                   INT8MP_CODES_F16, o.dy_rows.s,
+                                                   int8_dw ? dy_absmax : nullptr, dev, s);
       if (e == cudaSuccess)
-        e = int8mp::launch_quantize_cols(W, N, K, K, cfg->mode, sr_of(cfg, INT8MP_STREAM_GI_W),
-                                         wqt.q, INT8MP_CODES_F16, wqt.s, dev, s);
+        e = int8mp::launch_quantize_cols_from_absmax(W, N, K, K, w_absmax, cfg->mode,
+                                                     sr_of(cfg, INT8MP_STREAM_GI_W), o.w_cols.q,
+                                                     INT8MP_CODES_F16, o.w_cols.s, dev, s);
       if (e != cudaSuccess) return INT8MP_ERR_CUDA;
     }
-    st = run_mm(dyq.q, dyq.s, wqt.q, wqt.s, T, K, N, int8mp::GemmOut::kBf16Scaled, dX, K,
-                int8mp::GemmDebug{}, s);
+    st = run_mm(o.dy_rows.q, o.dy_rows.s, o.w_cols.q, o.w_cols.s, T, K, N, INT8MP_AxB,
+                int8mp::GemmOut::kBf16Scaled, dX, K, int8mp::GemmDebug{}, s);
     if (st != INT8MP_OK) return st;
   }
   if (want_dw && !cfg->int8_grad_w) {
@@ -311,20 +409,53 @@ int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, vo
     else
       st = from_cuda(int8mp::bf16_gemm_colmajor(X, dY, dW, K, N, T, false, true, K, N, K, s));
   } else if (want_dw) {
-    // grad weight: contraction over T; dY and X by columns (-> [N, T], [K, T])
+    // grad weight: contraction over T; dY and X by columns; dY^T X is A.T @ B
     if (T > 0) {
-      cudaError_t e = int8mp::launch_quantize_cols(dY, T, N, N, cfg->mode,
-                                                   sr_of(cfg, INT8MP_STREAM_GW_DY), dyqt.q,
-                                                   INT8MP_CODES_F16, dyqt.s, dev, s);
+      cudaError_t e = int8mp::launch_quantize_cols_from_absmax(
+          dY, T, N, N, dy_absmax, cfg->mode, sr_of(cfg, INT8MP_STREAM_GW_DY), o.dy_cols.q,
+          INT8MP_CODES_F16, o.dy_cols.s, dev, s);
       if (e == cudaSuccess)
-        e = int8mp::launch_quantize_cols(X, T, K, K, cfg->mode, sr_of(cfg, INT8MP_STREAM_GW_X),
-                                         xqt.q, INT8MP_CODES_F16, xqt.s, dev, s);
+        e = int8mp::launch_quantize_cols_from_absmax(X, T, K, K, x_absmax, cfg->mode,
+                                                     sr_of(cfg, INT8MP_STREAM_GW_X), o.x_cols.q,
+                                                     INT8MP_CODES_F16, o.x_cols.s, dev, s);
       if (e != cudaSuccess) return INT8MP_ERR_CUDA;
     }
-    st = run_mm(dyqt.q, dyqt.s, xqt.q, xqt.s, N, K, T, int8mp::GemmOut::kBf16Scaled, dW, K,
-                int8mp::GemmDebug{}, s);
+    st = run_mm(o.dy_cols.q, o.dy_cols.s, o.x_cols.q, o.x_cols.s, N, K, T, INT8MP_ATxB,
+                int8mp::GemmOut::kBf16Scaled, dW, K, int8mp::GemmDebug{}, s);
   }
   return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+int8mp_status int8mp_linear_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t N,
+                                int64_t K, const int8mp_linear_cfg* cfg, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  return linear_fwd_impl(X, W, Y, T, N, K, cfg, nullptr, workspace, ws_bytes, stream);
+}
+
+int8mp_status int8mp_linear_fwd_save(const void* X, const void* W, void* Y, int64_t T, int64_t N,
+                                     int64_t K, const int8mp_linear_cfg* cfg, float* absmax,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+  if (!absmax) return INT8MP_ERR_INVALID_ARG;
+  return linear_fwd_impl(X, W, Y, T, N, K, cfg, absmax, workspace, ws_bytes, stream);
+}
+
+int8mp_status int8mp_linear_bwd(const void* dY, const void* X, const void* W, void* dX,
+                                void* dW, int64_t T, int64_t N, int64_t K,
+                                const int8mp_linear_cfg* cfg, void* workspace, size_t ws_bytes,
+                                void* stream) {
+  return linear_bwd_impl(dY, X, W, dX, dW, T, N, K, cfg, nullptr, workspace, ws_bytes, stream);
+}
+
+int8mp_status int8mp_linear_bwd_saved(const void* dY, const void* X, const void* W, void* dX,
+                                      void* dW, int64_t T, int64_t N, int64_t K,
+                                      const int8mp_linear_cfg* cfg, const float* absmax,
+                                      void* workspace, size_t ws_bytes, void* stream) {
+  if (!absmax) return INT8MP_ERR_INVALID_ARG;
+  return linear_bwd_impl(dY, X, W, dX, dW, T, N, K, cfg, absmax, workspace, ws_bytes, stream);
 }
 
 int8mp_status int8mp_poll_device_status(void* stream) {
@@ -368,7 +499,7 @@ int8mp_status int8mp_debug_mm_s32_drop_first_load(const void* A, const void* B, 
   int8mp::GemmDebug dbg;
   dbg.drop_first_load = 1;
   dbg.wait_limit_ns = static_cast<uint64_t>(wait_limit_ms) * 1000000ull;
-  return run_mm(A, nullptr, B, nullptr, M, N, K, int8mp::GemmOut::kS32, out, ldo, dbg,
+  return run_mm(A, nullptr, B, nullptr, M, N, K, INT8MP_AxBT, int8mp::GemmOut::kS32, out, ldo, dbg,
                 as_stream(stream));
 }
 

@@ -37,15 +37,27 @@ bool encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataTyp
 
 // ---- quantize (quantize.cu) ------------------------------------------------
 // x bf16 [rows, cols] stride ld.  Row groups: q [rows, cols]; scale [rows].
+// colmax (optional, fp32 [cols]): each column's absmax is max-merged into it.
 cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                  int8mp_round mode, const SrArgs& sr, void* q,
-                                 int8mp_codes codes, float* scale, const DeviceInfo& dev,
-                                 cudaStream_t stream);
-// Column groups, codes written transposed: q [cols, rows]; scale [cols].
+                                 int8mp_codes codes, float* scale, float* colmax,
+                                 const DeviceInfo& dev, cudaStream_t stream);
+// colmax[c] = max(colmax[c], max_r |x[r,c]|) (fp32 [cols]), one pass.
+cudaError_t launch_column_absmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                 float* colmax, const DeviceInfo& dev, cudaStream_t stream);
+// Column groups whose absmax is given (fp32 [cols]): scale [cols] =
+// absmax / 127, codes q [rows, cols] (row stride cols).
+cudaError_t launch_quantize_cols_from_absmax(const void* x, int64_t rows, int64_t cols,
+                                             int64_t ld, const float* absmax, int8mp_round mode,
+                                             const SrArgs& sr, void* q, int8mp_codes codes,
+                                             float* scale, const DeviceInfo& dev,
+                                             cudaStream_t stream);
+// Column groups, scale [cols]; codes q [rows, cols] (row stride cols), or
+// transposed q [cols, rows] (row stride rows) when `transposed`.
 cudaError_t launch_quantize_cols(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                  int8mp_round mode, const SrArgs& sr, void* q,
-                                 int8mp_codes codes, float* scale, const DeviceInfo& dev,
-                                 cudaStream_t stream);
+                                 int8mp_codes codes, float* scale, bool transposed,
+                                 const DeviceInfo& dev, cudaStream_t stream);
 
 // ---- GEMM (gemm.cu) ---------------------------------------------------------
 enum class GemmOut { kBf16Scaled = 0, kS32 = 1 };
@@ -56,9 +68,11 @@ struct GemmDebug {
   uint64_t wait_limit_ns = kWaitLimitNs;
 };
 
-// A [M,K], B [N,K]: f16 containers of integer codes, K contiguous.
-cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const float* sB,
-                        int64_t M, int64_t N, int64_t K, GemmOut mode, void* out,
+// f16 containers of integer codes.  A is [M,K] (a_mn false, K contiguous)
+// or [K,M] (a_mn true, M contiguous); B is [N,K] or [K,N] likewise.  Every
+// combination but (a_mn, !b_mn) is served.
+cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B, bool b_mn,
+                        const float* sB, int64_t M, int64_t N, int64_t K, GemmOut mode, void* out,
                         int64_t ldo, const DeviceInfo& dev, const GemmDebug& dbg,
                         cudaStream_t stream);
 

@@ -16,6 +16,11 @@
 // warps convert it (exactly) to int32 and add it into per-thread int32
 // totals while the tensor core fills the other accumulator.
 //
+// Operands are K-major (contraction innermost: A [M,K], B [N,K]) or
+// MN-major (A stored [K,M], B stored [K,N]); an MN-major operand arrives in
+// 64-column TMA boxes and is described to the tensor core as such, so that
+// column-grouped codes need no transposition.
+//
 // Structure (one persistent CTA per SM, 320 threads):
 //   warp 0      TMA producer (one thread): 4-stage ring of 128x64 A and
 //               256x64 B f16 tiles, 128-byte swizzled, one mbarrier per stage
@@ -49,6 +54,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;  // two 128x256 fp32 accumulators
 constexpr int kBarrierBytes = 256;
+constexpr int kMnBlockBytes = 64 * kBK * 2;  // one 64 (M or N) x 64 (K) MN-major box
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes;
 
 struct GemmParams {
@@ -67,6 +73,43 @@ struct GemmParams {
 __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned int* status) {
   *abort = 1;
   atomicOr(status, 1u);
+}
+
+// TMA of one operand's k-block: kRows rows (M or N) x 64 k.  K-major: one
+// box of 64 k x kRows rows.  MN-major: kRows / 64 boxes of 64 (M or N) x 64
+// k, each a 8 KB block of 64 swizzled 128-byte rows, one per k.
+template <bool kMN, int kRows>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                             int kb, int mn0) {
+  if (kMN) {
+#pragma unroll
+    for (int j = 0; j < kRows / 64; ++j)
+      ptx::tma_load_2d(dst + j * kMnBlockBytes, map, bar, mn0 + 64 * j, kb * kBK);
+  } else {
+    ptx::tma_load_2d(dst, map, bar, kb * kBK, mn0);
+  }
+}
+template <bool kMN, int kRows>
+__device__ __forceinline__ void load_operand_pair(uint32_t dst, const CUtensorMap* map,
+                                                  uint32_t bar, int kb, int mn0) {
+  if (kMN) {
+#pragma unroll
+    for (int j = 0; j < kRows / 64; ++j)
+      ptx::tma_load_2d_pair(dst + j * kMnBlockBytes, map, bar, mn0 + 64 * j, kb * kBK);
+  } else {
+    ptx::tma_load_2d_pair(dst, map, bar, kb * kBK, mn0);
+  }
+}
+
+// Descriptor of an operand's stage tile and its advance per MMA (16 k):
+// 32 bytes along a K-major row, two 8-row groups (2048 bytes) MN-major.
+template <bool kMN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t addr) {
+  return kMN ? ptx::smem_desc_mnmajor_sw128(addr, kMnBlockBytes) : ptx::smem_desc_kmajor_sw128(addr);
+}
+template <bool kMN>
+__host__ __device__ constexpr uint64_t k_step() {
+  return kMN ? (16u * 128u) >> 4 : 32u >> 4;
 }
 
 // One thread's output: row `row`, columns col0 .. col0+127, from its int32
@@ -121,6 +164,7 @@ __device__ __forceinline__ void drain_chunk(uint32_t taddr, int32_t (&tot)[128])
   }
 }
 
+template <bool kAmn, bool kBmn>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_s8f16_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
@@ -188,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool drop = p.drop_first_load && tile == static_cast<int>(blockIdx.x) && kb == 0;
           if (!drop) {
             ptx::mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-            ptx::tma_load_2d(a_base + stage * kABytes, &tmA, full_bar(stage), kb * kBK, m0);
-            ptx::tma_load_2d(b_base + stage * kBBytes, &tmB, full_bar(stage), kb * kBK, n0);
+            load_operand<kAmn, kBM>(a_base + stage * kABytes, &tmA, full_bar(stage), kb, m0);
+            load_operand<kBmn, kBN>(b_base + stage * kBBytes, &tmB, full_bar(stage), kb, n0);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
@@ -209,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ----------------------------------------------------------- MMA
-      constexpr uint32_t idesc = ptx::idesc_f16_f32(kBM, kBN);
+      constexpr uint32_t idesc = ptx::idesc_f16_f32(kBM, kBN, kAmn, kBmn);
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -228,14 +272,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             ptx::tc_fence_after();
-            const uint64_t adesc = ptx::smem_desc_kmajor_sw128(a_base + stage * kABytes);
-            const uint64_t bdesc = ptx::smem_desc_kmajor_sw128(b_base + stage * kBBytes);
+            const uint64_t adesc = operand_desc<kAmn>(a_base + stage * kABytes);
+            const uint64_t bdesc = operand_desc<kBmn>(b_base + stage * kBBytes);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              // advance 16 f16 = 32 bytes along K inside the swizzled row
-              ptx::mma_f16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              ptx::mma_f16(d_tmem, adesc + k_step<kAmn>() * kk, bdesc + k_step<kBmn>() * kk, idesc,
                            (kb > kb0 || kk > 0) ? 1u : 0u);
-            }
             ptx::mma_commit(empty_bar(stage));
             if (++stage == kStages) {
               stage = 0;
@@ -315,6 +357,7 @@ constexpr int kPairBBytes = 128 * kBK * 2;
 constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + kBarrierBytes;
 
+template <bool kAmn, bool kBmn>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_s8f16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
@@ -390,8 +433,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               armed |= 1u << stage;
               armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
             }
-            ptx::tma_load_2d_pair(a_base + stage * kPairABytes, &tmA, fb, kb * kBK, m0);
-            ptx::tma_load_2d_pair(b_base + stage * kPairBBytes, &tmB, fb, kb * kBK, n0);
+            load_operand_pair<kAmn, 128>(a_base + stage * kPairABytes, &tmA, fb, kb, m0);
+            load_operand_pair<kBmn, 128>(b_base + stage * kPairBBytes, &tmB, fb, kb, n0);
           }
           if (++stage == kPairStages) {
             stage = 0;
@@ -408,7 +451,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && even) {
       // ----------------------------------------------------------- MMA
-      constexpr uint32_t idesc = ptx::idesc_f16_f32(256, 256);
+      constexpr uint32_t idesc = ptx::idesc_f16_f32(256, 256, kAmn, kBmn);
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
@@ -427,12 +470,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               break;
             }
             ptx::tc_fence_after();
-            const uint64_t adesc = ptx::smem_desc_kmajor_sw128(a_base + stage * kPairABytes);
-            const uint64_t bdesc = ptx::smem_desc_kmajor_sw128(b_base + stage * kPairBBytes);
+            const uint64_t adesc = operand_desc<kAmn>(a_base + stage * kPairABytes);
+            const uint64_t bdesc = operand_desc<kBmn>(b_base + stage * kPairBBytes);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-              ptx::mma_f16_pair(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                                (kb > kb0 || kk > 0) ? 1u : 0u);
+              ptx::mma_f16_pair(d_tmem, adesc + k_step<kAmn>() * kk, bdesc + k_step<kBmn>() * kk,
+                                idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
             ptx::mma_commit_pair(empty_bar(stage), 0x3);
             if (++stage == kPairStages) {
               stage = 0;
@@ -502,18 +545,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-// K-major f16 operand [rows, K]: box of 64 (K) x box_rows, 128-byte swizzle,
-// zero fill outside the tensor.
-bool make_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
-  return encode_tensor_map_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows, K, K, kBK,
-                              box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+// f16 operand map, 128-byte swizzle, zero fill outside the tensor.
+// K-major [mn, K] (row stride K): boxes of 64 k x box_mn rows.
+// MN-major [K, mn] (row stride mn): boxes of 64 (M or N) x 64 k.
+bool make_operand_map(CUtensorMap* map, const void* base, bool mn_major, int64_t mn, int64_t K,
+                      int box_mn) {
+  if (mn_major)
+    return encode_tensor_map_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, mn, mn, 64, kBK,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+  return encode_tensor_map_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, mn, K, K, kBK, box_mn,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <bool kAmn, bool kBmn>
+cudaError_t set_smem_attrs() {
+  cudaError_t err = cudaFuncSetAttribute(gemm_s8f16_kernel<kAmn, kBmn>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+  return err;
+}
+
+template <bool kAmn, bool kBmn>
+void launch_kernel(bool pair, int grid, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                   const GemmParams& p, cudaStream_t stream) {
+  if (pair)
+    gemm_s8f16_pair_kernel<kAmn, kBmn><<<grid, kThreads, kPairSmemBytes, stream>>>(mapA, mapB, p);
+  else
+    gemm_s8f16_kernel<kAmn, kBmn><<<grid, kThreads, kSmemBytes, stream>>>(mapA, mapB, p);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const float* sB,
-                        int64_t M, int64_t N, int64_t K, GemmOut mode, void* out, int64_t ldo,
-                        const DeviceInfo& dev, const GemmDebug& dbg, cudaStream_t stream) {
+cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B, bool b_mn,
+                        const float* sB, int64_t M, int64_t N, int64_t K, GemmOut mode, void* out,
+                        int64_t ldo, const DeviceInfo& dev, const GemmDebug& dbg,
+                        cudaStream_t stream) {
+  if (a_mn && !b_mn) return cudaErrorInvalidValue;  // no layout of the API needs it
   static std::mutex mu;
   static bool attr_set[64] = {};
   int device = 0;
@@ -523,11 +592,9 @@ cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const flo
     std::lock_guard<std::mutex> lock(mu);
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[device]) {
-      err = cudaFuncSetAttribute(gemm_s8f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
-      if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+      err = set_smem_attrs<false, false>();
+      if (err == cudaSuccess) err = set_smem_attrs<false, true>();
+      if (err == cudaSuccess) err = set_smem_attrs<true, true>();
       if (err != cudaSuccess) return err;
       attr_set[device] = true;
     }
@@ -538,7 +605,8 @@ cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const flo
   const int64_t pair_tiles = ((M + 255) / 256) * ((N + kBN - 1) / kBN);
   const bool pair = M > kBM && (pair_tiles >= dev.sms / 2 || K >= 8192) && !dbg.single_cta;
   CUtensorMap mapA, mapB;
-  if (!make_kmajor_map(&mapA, A, M, K, kBM) || !make_kmajor_map(&mapB, B, N, K, pair ? 128 : kBN))
+  if (!make_operand_map(&mapA, A, a_mn, M, K, kBM) ||
+      !make_operand_map(&mapB, B, b_mn, N, K, pair ? 128 : kBN))
     return cudaErrorInvalidValue;
   GemmParams p;
   p.sA = sA;
@@ -556,14 +624,14 @@ cudaError_t launch_gemm(const void* A, const float* sA, const void* B, const flo
   p.wait_limit_ns = dbg.wait_limit_ns;
   p.drop_first_load = dbg.drop_first_load;
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-  if (pair) {
-    const int64_t pairs_max = dev.sms / 2;
-    const int grid = static_cast<int>(2 * (tiles < pairs_max ? tiles : pairs_max));
-    gemm_s8f16_pair_kernel<<<grid, kThreads, kPairSmemBytes, stream>>>(mapA, mapB, p);
-  } else {
-    const int grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
-    gemm_s8f16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mapA, mapB, p);
-  }
+  const int64_t slots = pair ? dev.sms / 2 : dev.sms;
+  const int grid = static_cast<int>((pair ? 2 : 1) * (tiles < slots ? tiles : slots));
+  if (!a_mn && !b_mn)
+    launch_kernel<false, false>(pair, grid, mapA, mapB, p, stream);
+  else if (!a_mn)
+    launch_kernel<false, true>(pair, grid, mapA, mapB, p, stream);
+  else
+    launch_kernel<true, true>(pair, grid, mapA, mapB, p, stream);
   return cudaGetLastError();
 }
 

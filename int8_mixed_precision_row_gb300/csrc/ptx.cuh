@@ -263,12 +263,30 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand tile with 128-byte
+// swizzling: 128-byte rows hold 64 f16 values along M (or N) for one k, in
+// atoms of 8 rows (1024 bytes, one swizzle period).  Consecutive 8-row
+// groups along K are 1024 bytes apart (stride byte offset); consecutive
+// 64-element blocks along M/N are `mn_stride` bytes apart (leading byte
+// offset).  Same fixed fields as the K-major form.
+__device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16: f16 A and B, fp32 D,
-// both operands K-major, dense, M x N.
+// dense, M x N; a_mn / b_mn select MN-major operands.
 //   bits 4-5 D format (1 = f32); 7-9 A format (0 = f16); 10-12 B format;
-//   15/16 A/B major (0 = K); 17-22 N >> 3; 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+//   15/16 A/B major (0 = K, 1 = MN); 17-22 N >> 3; 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, bool a_mn = false,
+                                                     bool b_mn = false) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 }  // namespace ptx

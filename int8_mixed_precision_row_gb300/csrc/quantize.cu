@@ -15,10 +15,12 @@
 //   columns one group per column (the contraction axis is the leading one):
 //           pass 1 reduces column absmax over row blocks into the scale
 //           buffer (atomic max on the fp32 bit pattern, valid for values
-//           >= 0); pass 2 turns it into absmax / 127 in place; pass 3 has
-//           each warp stream 32x64 sub-tiles through its own two-slot ring
-//           of 2-D TMA loads, quantize them, and write the codes transposed
-//           [cols, rows] through its own staging tile.
+//           >= 0); pass 2 turns it into absmax / 127 in place; pass 3
+//           writes the codes either in the input's layout [rows, cols]
+//           (each thread streams one 8-column vector down its rows with the
+//           8 scales in registers) or transposed [cols, rows] (each warp
+//           streams 32x64 sub-tiles through its own two-slot ring of 2-D TMA
+//           loads and writes them through its own staging tile).
 //
 // Arithmetic per element (identical to the header of int8mp.h):
 //   v = x / s rounded as an IEEE division (div8_*: a reciprocal and two FMAs,
@@ -168,11 +170,27 @@ __device__ __forceinline__ void quantize_two(const uint4& a, const uint4& b, boo
   }
 }
 
-template <typename CodeT, bool SR>
+// Column absmax alongside the row groups (kColMax): each thread owns the same
+// vectors first + k*step, k < kColVecs, of every row it sees and keeps their
+// running |x| maxima as packed bf16 pairs (|x| of a bf16 is a bf16, and
+// non-negative bf16 bit patterns order as unsigned integers, so a per-halfword
+// unsigned max is the max).  At the end the teams of a block merge theirs in
+// shared memory and the block merges into colmax[] by atomic max on the fp32
+// bit pattern (the bf16 bits shifted up: the same value).
+constexpr int kColVecs = 8;
+
+__device__ __forceinline__ void colmax_acc(uint4& m, const uint4& v) {
+  m.x = __vmaxu2(m.x, v.x & 0x7FFF7FFFu);
+  m.y = __vmaxu2(m.y, v.y & 0x7FFF7FFFu);
+  m.z = __vmaxu2(m.z, v.z & 0x7FFF7FFFu);
+  m.w = __vmaxu2(m.w, v.w & 0x7FFF7FFFu);
+}
+
+template <typename CodeT, bool SR, bool kColMax>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, CodeT* __restrict__ q,
     float* __restrict__ scale, SrArgs sr, uint32_t slot_bytes, int T, unsigned int* status,
-    uint64_t limit_ns) {
+    uint64_t limit_ns, unsigned int* __restrict__ colmax) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t bars[kThreads / 32][2];
   __shared__ float red[kThreads / 32];
@@ -204,6 +222,10 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
       }
     }
   }
+  const int first = wt * 32 + lane, step = T * 32;  // this thread's vectors of a row
+  uint4 cm[kColMax ? kColVecs : 1];
+#pragma unroll
+  for (int k = 0; k < (kColMax ? kColVecs : 1); ++k) cm[k] = make_uint4(0u, 0u, 0u, 0u);
   int it = 0;
   for (int64_t r = g; r < rows; r += n, ++it) {
     const int b = it & 1;
@@ -225,9 +247,20 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
       pend_par = (pend_par & ~(1u << nb)) | (static_cast<uint32_t>(((it + 1) >> 1) & 1) << nb);
     }
     const uint4* rowv = reinterpret_cast<const uint4*>(slots + b * slot_bytes);
-    const int first = wt * 32 + lane, step = T * 32;
     float amax = 0.0f;
-    for (int v = first; v < nvec; v += step) amax = absmax8(amax, rowv[v]);
+    if (kColMax) {
+#pragma unroll
+      for (int k = 0; k < kColVecs; ++k) {
+        const int v = first + k * step;
+        if (v < nvec) {
+          const uint4 xv = rowv[v];
+          amax = absmax8(amax, xv);
+          colmax_acc(cm[k], xv);
+        }
+      }
+    } else {
+      for (int v = first; v < nvec; v += step) amax = absmax8(amax, rowv[v]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     if (T > 1) {
@@ -252,10 +285,38 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     }
   }
   // after a timeout: never leave a copy in flight into this block's memory
+  bool copies_done = true;
   if (leader) {
     for (int k = 0; k < 2; ++k)
       if (pending & (1u << k))
-        if (!ptx::mbar_wait_timeout(bar[k], (pend_par >> k) & 1u, limit_ns)) atomicOr(status, 1u);
+        if (!ptx::mbar_wait_timeout(bar[k], (pend_par >> k) & 1u, limit_ns)) {
+          atomicOr(status, 1u);
+          copies_done = false;
+        }
+  }
+  if (kColMax) {
+    // every team's maxima into its own first slot (cols bf16 values), then
+    // the block's maximum over teams, one atomic per column
+    __shared__ int all_done;
+    if (threadIdx.x == 0) all_done = 1;
+    __syncthreads();
+    if (leader && !copies_done) all_done = 0;
+    __syncthreads();
+    if (!all_done) return;  // a copy may still land in the slots: leave them alone
+    uint4* mine = reinterpret_cast<uint4*>(smem + static_cast<size_t>(team) * 2 * slot_bytes);
+#pragma unroll
+    for (int k = 0; k < kColVecs; ++k) {
+      const int v = first + k * step;
+      if (v < nvec) mine[v] = cm[k];
+    }
+    __syncthreads();
+    const uint16_t* all = reinterpret_cast<const uint16_t*>(smem);
+    const size_t team_stride = static_cast<size_t>(slot_bytes);  // in uint16: 2 slots of bytes / 2
+    for (int c = threadIdx.x; c < cols; c += kThreads) {
+      uint32_t mx = 0u;
+      for (int t = 0; t < teams; ++t) mx = max(mx, static_cast<uint32_t>(all[t * team_stride + c]));
+      if (mx != 0u) atomicMax(colmax + c, mx << 16);
+    }
   }
 }
 
@@ -350,6 +411,63 @@ __global__ void __launch_bounds__(kThreads) col_absmax_kernel(
 __global__ void col_scale_kernel(unsigned int* __restrict__ amax_bits, int64_t cols) {
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c < cols) amax_bits[c] = __float_as_uint(__fdiv_rn(__uint_as_float(amax_bits[c]), 127.0f));
+}
+
+// Pass 3, codes in the input's layout q [rows, cols]: lane = one 8-column
+// vector (16-byte loads and stores), warp = row phase, four rows in flight
+// per thread; the thread's eight column scales and their reciprocals stay in
+// registers for all of its rows.  kFromAbsmax: `in` holds the columns'
+// absmax (computed elsewhere, e.g. alongside a row quantization of x); the
+// kernel forms the scales, the blocks of the first row band store them, and
+// the codes keep their clamp (the absmax is the caller's claim).  Otherwise
+// `in` is the scale array itself.
+constexpr int kNatUnroll = 4;
+
+template <typename CodeT, bool SR, bool kFromAbsmax>
+__global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+    int64_t rows_per_block, const float* __restrict__ in, float* __restrict__ scale_out,
+    CodeT* __restrict__ q, SrArgs sr) {
+  using P = Pack8<CodeT>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t vi = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  if (vi >= (cols >> 3)) return;
+  const int64_t c = vi * 8;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_block;
+  const int64_t r1 = min(rows, r0 + rows_per_block);
+  float s[8], r[8];
+  bool all_fast = true, normal = !kFromAbsmax;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    s[j] = kFromAbsmax ? __fdiv_rn(__ldg(in + c + j), 127.0f) : __ldg(in + c + j);
+    all_fast = all_fast && scale_is_fast(s[j]);
+    if (!kFromAbsmax) normal = normal && scale_is_normal(s[j]);
+    r[j] = __frcp_rn(s[j]);
+  }
+  if (kFromAbsmax && blockIdx.y == 0 && warp == 0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) scale_out[c + j] = s[j];
+  }
+  const uint16_t* xc = x + c;
+  for (int64_t rr = r0 + warp; rr < r1; rr += kNatUnroll * 8) {
+    uint4 a[kNatUnroll];
+#pragma unroll
+    for (int u = 0; u < kNatUnroll; ++u) {
+      const int64_t row = rr + u * 8;
+      a[u] = row < r1 ? __ldg(reinterpret_cast<const uint4*>(xc + row * ld)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kNatUnroll; ++u) {
+      const int64_t row = rr + u * 8;
+      if (row < r1) {
+        float f[8], v[8], cd[8];
+        unpack8(a[u], f);
+        if (!div8_each_try(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
+        codes_of<SR>(v, sr, sr.offset + static_cast<uint64_t>(row * cols + c), normal, cd);
+        *reinterpret_cast<typename P::Vec*>(q + row * cols + c) = P::pack(cd);
+      }
+    }
+  }
 }
 
 // Pass 3: codes, one warp per 32-row x 64-column sub-tile at a time.  Each
@@ -580,72 +698,126 @@ cudaError_t allow_smem(Kernel k, bool* done) {
   return cudaSuccess;
 }
 
+// One wave of blocks of 32 8-column vectors x rows_per_block rows (a
+// multiple of `row_quantum`), for the passes that walk columns.
+struct ColGrid {
+  unsigned gx, gy;
+  int64_t rows_per_block;
+};
+ColGrid col_grid(int64_t rows, int64_t cols, int64_t blocks_target, int64_t row_quantum) {
+  const int64_t gx = ((cols >> 3) + 31) / 32;
+  int64_t gy = blocks_target / gx;
+  const int64_t max_gy = (rows + 63) / 64;
+  if (gy > max_gy) gy = max_gy;
+  if (gy < 1) gy = 1;
+  if (gy > 65535) gy = 65535;
+  int64_t rpb = (rows + gy - 1) / gy;
+  rpb = (rpb + row_quantum - 1) / row_quantum * row_quantum;
+  gy = (rows + rpb - 1) / rpb;
+  return ColGrid{static_cast<unsigned>(gx), static_cast<unsigned>(gy), rpb};
+}
+
+// column absmax merged into amax_bits (atomic max), pass 1 of the columns
+cudaError_t launch_col_absmax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                              unsigned int* amax_bits, int sms, cudaStream_t stream) {
+  static const int occ1 = blocks_per_sm(col_absmax_kernel, kThreads, 0);
+  const ColGrid g1 = col_grid(rows, cols, static_cast<int64_t>(sms) * occ1, 1);
+  col_absmax_kernel<<<dim3(g1.gx, g1.gy), kThreads, 0, stream>>>(x, rows, cols, ld,
+                                                                  g1.rows_per_block, amax_bits);
+  return cudaGetLastError();
+}
+
+// Row groups; with colmax != nullptr also max-merge each column's absmax
+// into colmax (in the same pass when every thread's share of a row fits
+// its registers, else by a separate column pass).
 template <typename CodeT, bool SR>
 cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
-                          float* scale, const SrArgs& sr, const DeviceInfo& dev,
+                          float* scale, float* colmax, const SrArgs& sr, const DeviceInfo& dev,
                           cudaStream_t stream) {
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   CodeT* qp = static_cast<CodeT*>(q);
+  unsigned int* cmx = reinterpret_cast<unsigned int*>(colmax);
+  const int sms = dev.sms > 0 ? dev.sms : 148;
   const uint32_t slot = static_cast<uint32_t>((cols * 2 + 127) / 128 * 128);
   if (2ull * slot > kMaxDynSmem) {
     quant_rows_long_kernel<CodeT, SR><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(
         xp, rows, cols, ld, qp, scale, sr);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, sms, stream);
+    return e;
   }
-  static bool attr[64] = {};
-  cudaError_t e = allow_smem(quant_rows_kernel<CodeT, SR>, attr);
-  if (e != cudaSuccess) return e;
   // 8 warps per block in teams of T: the smallest T whose slots (two per
   // team) fit in 72 KB, so that at least three blocks share an SM
   int T = 1;
   while (T < 8 && static_cast<size_t>(kThreads / 32 / T) * 2 * slot > 72u * 1024u) T <<= 1;
   const size_t smem = static_cast<size_t>(kThreads / 32 / T) * 2 * slot;
-  const int occ = blocks_per_sm(quant_rows_kernel<CodeT, SR>, kThreads, smem);
-  const int sms = dev.sms > 0 ? dev.sms : 148;
+  const bool fused = cmx && (cols >> 3) <= static_cast<int64_t>(kColVecs) * 32 * T;
   const int64_t teams = kThreads / 32 / T;
   const int64_t need = (rows + teams - 1) / teams;
+  cudaError_t e;
+  if (fused) {
+    static bool attr[64] = {};
+    e = allow_smem(quant_rows_kernel<CodeT, SR, true>, attr);
+    if (e != cudaSuccess) return e;
+    const int occ = blocks_per_sm(quant_rows_kernel<CodeT, SR, true>, kThreads, smem);
+    const int64_t cap = static_cast<int64_t>(sms) * occ;
+    const unsigned blocks = static_cast<unsigned>(need < cap ? need : cap);
+    quant_rows_kernel<CodeT, SR, true><<<blocks, kThreads, smem, stream>>>(
+        xp, rows, cols, ld, qp, scale, sr, slot, T, dev.status_word, kWaitLimitNs, cmx);
+    return cudaGetLastError();
+  }
+  static bool attr[64] = {};
+  e = allow_smem(quant_rows_kernel<CodeT, SR, false>, attr);
+  if (e != cudaSuccess) return e;
+  const int occ = blocks_per_sm(quant_rows_kernel<CodeT, SR, false>, kThreads, smem);
   const int64_t cap = static_cast<int64_t>(sms) * occ;
   const unsigned blocks = static_cast<unsigned>(need < cap ? need : cap);
-  quant_rows_kernel<CodeT, SR><<<blocks, kThreads, smem, stream>>>(
-      xp, rows, cols, ld, qp, scale, sr, slot, T, dev.status_word, kWaitLimitNs);
+  quant_rows_kernel<CodeT, SR, false><<<blocks, kThreads, smem, stream>>>(
+      xp, rows, cols, ld, qp, scale, sr, slot, T, dev.status_word, kWaitLimitNs, nullptr);
+  e = cudaGetLastError();
+  if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, sms, stream);
+  return e;
+}
+
+template <typename CodeT, bool SR, bool kFromAbsmax>
+cudaError_t launch_cols_nat(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                            const float* in, float* scale_out, CodeT* q, const SrArgs& sr, int sms,
+                            cudaStream_t stream) {
+  static const int occ = blocks_per_sm(quant_cols_nat_kernel<CodeT, SR, kFromAbsmax>, kThreads, 0);
+  const ColGrid g = col_grid(rows, cols, static_cast<int64_t>(sms) * occ, 8 * kNatUnroll);
+  quant_cols_nat_kernel<CodeT, SR, kFromAbsmax><<<dim3(g.gx, g.gy), kThreads, 0, stream>>>(
+      x, rows, cols, ld, g.rows_per_block, in, scale_out, q, sr);
   return cudaGetLastError();
 }
 
 template <typename CodeT, bool SR>
 cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
-                          float* scale, const SrArgs& sr, const DeviceInfo& dev,
+                          float* scale, bool transposed, const SrArgs& sr, const DeviceInfo& dev,
                           cudaStream_t stream) {
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   unsigned int* amax = reinterpret_cast<unsigned int*>(scale);
+  cudaError_t err = cudaMemsetAsync(amax, 0, static_cast<size_t>(cols) * sizeof(float), stream);
+  if (err != cudaSuccess) return err;
+  const int sms = dev.sms > 0 ? dev.sms : 148;
+  // pass 1: one wave of blocks
+  err = launch_col_absmax(xp, rows, cols, ld, amax, sms, stream);
+  if (err != cudaSuccess) return err;
+  col_scale_kernel<<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(amax, cols);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (!transposed) {
+    // pass 3 in the input's layout: one wave, whole 32-row steps per block
+    return launch_cols_nat<CodeT, SR, false>(xp, rows, cols, ld, scale, nullptr,
+                                             static_cast<CodeT*>(q), sr, sms, stream);
+  }
   CUtensorMap tmx;
   if (!encode_tensor_map_2d(&tmx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, cols, ld,
                             kCwCols, kCwRows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   static bool attr[64] = {};
-  cudaError_t err = allow_smem(quant_cols_kernel<CodeT, SR>, attr);
+  err = allow_smem(quant_cols_kernel<CodeT, SR>, attr);
   if (err != cudaSuccess) return err;
-  err = cudaMemsetAsync(amax, 0, static_cast<size_t>(cols) * sizeof(float), stream);
-  if (err != cudaSuccess) return err;
-  const int sms = dev.sms > 0 ? dev.sms : 148;
-  // pass 1: one wave of blocks
-  const int64_t nvec = cols >> 3;
-  const int64_t gx = (nvec + 31) / 32;
-  static const int occ1 = blocks_per_sm(col_absmax_kernel, kThreads, 0);
-  const int64_t target = static_cast<int64_t>(sms) * occ1;
-  int64_t gy = target / gx;
-  const int64_t max_gy = (rows + 63) / 64;
-  if (gy > max_gy) gy = max_gy;
-  if (gy < 1) gy = 1;
-  if (gy > 65535) gy = 65535;
-  const int64_t rpb = (rows + gy - 1) / gy;
-  col_absmax_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), kThreads, 0, stream>>>(
-      xp, rows, cols, ld, rpb, amax);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  col_scale_kernel<<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(amax, cols);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  // pass 3: persistent warps over 32x64 sub-tiles, column-block fastest
+  // pass 3 transposed: persistent warps over 32x64 sub-tiles, column-block fastest
   const int64_t col_tiles = (cols + kCwCols - 1) / kCwCols;
   const int64_t tiles = col_tiles * ((rows + kCwRows - 1) / kCwRows);
   const size_t smem = 1024 + (kThreads / 32) * col_warp_bytes<CodeT>();
@@ -676,26 +848,54 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
 
 cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                  int8mp_round mode, const SrArgs& sr, void* q,
-                                 int8mp_codes codes, float* scale, const DeviceInfo& dev,
-                                 cudaStream_t stream) {
+                                 int8mp_codes codes, float* scale, float* colmax,
+                                 const DeviceInfo& dev, cudaStream_t stream) {
   const bool s = mode == INT8MP_SR;
+  float* cm = colmax;
   if (codes == INT8MP_CODES_S8)
-    return s ? rows_dispatch<int8_t, true>(x, rows, cols, ld, q, scale, sr, dev, stream)
-             : rows_dispatch<int8_t, false>(x, rows, cols, ld, q, scale, sr, dev, stream);
-  return s ? rows_dispatch<__half, true>(x, rows, cols, ld, q, scale, sr, dev, stream)
-           : rows_dispatch<__half, false>(x, rows, cols, ld, q, scale, sr, dev, stream);
+    return s ? rows_dispatch<int8_t, true>(x, rows, cols, ld, q, scale, cm, sr, dev, stream)
+             : rows_dispatch<int8_t, false>(x, rows, cols, ld, q, scale, cm, sr, dev, stream);
+  return s ? rows_dispatch<__half, true>(x, rows, cols, ld, q, scale, cm, sr, dev, stream)
+           : rows_dispatch<__half, false>(x, rows, cols, ld, q, scale, cm, sr, dev, stream);
+}
+
+cudaError_t launch_column_absmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                 float* colmax, const DeviceInfo& dev, cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  return launch_col_absmax(static_cast<const uint16_t*>(x), rows, cols, ld,
+                           reinterpret_cast<unsigned int*>(colmax), dev.sms > 0 ? dev.sms : 148,
+                           stream);
+}
+
+cudaError_t launch_quantize_cols_from_absmax(const void* x, int64_t rows, int64_t cols,
+                                             int64_t ld, const float* absmax, int8mp_round mode,
+                                             const SrArgs& sr, void* q, int8mp_codes codes,
+                                             float* scale, const DeviceInfo& dev,
+                                             cudaStream_t stream) {
+  const uint16_t* xp = static_cast<const uint16_t*>(x);
+  const int sms = dev.sms > 0 ? dev.sms : 148;
+  const bool s = mode == INT8MP_SR;
+  if (codes == INT8MP_CODES_S8) {
+    int8_t* qp = static_cast<int8_t*>(q);
+    return s ? launch_cols_nat<int8_t, true, true>(xp, rows, cols, ld, absmax, scale, qp, sr, sms, stream)
+             : launch_cols_nat<int8_t, false, true>(xp, rows, cols, ld, absmax, scale, qp, sr, sms, stream);
+  }
+  __half* qp = static_cast<__half*>(q);
+  return s ? launch_cols_nat<__half, true, true>(xp, rows, cols, ld, absmax, scale, qp, sr, sms, stream)
+           : launch_cols_nat<__half, false, true>(xp, rows, cols, ld, absmax, scale, qp, sr, sms, stream);
 }
 
 cudaError_t launch_quantize_cols(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                  int8mp_round mode, const SrArgs& sr, void* q,
-                                 int8mp_codes codes, float* scale, const DeviceInfo& dev,
-                                 cudaStream_t stream) {
+                                 int8mp_codes codes, float* scale, bool transposed,
+                                 const DeviceInfo& dev, cudaStream_t stream) {
   const bool s = mode == INT8MP_SR;
+  const bool t = transposed;
   if (codes == INT8MP_CODES_S8)
-    return s ? cols_dispatch<int8_t, true>(x, rows, cols, ld, q, scale, sr, dev, stream)
-             : cols_dispatch<int8_t, false>(x, rows, cols, ld, q, scale, sr, dev, stream);
-  return s ? cols_dispatch<__half, true>(x, rows, cols, ld, q, scale, sr, dev, stream)
-           : cols_dispatch<__half, false>(x, rows, cols, ld, q, scale, sr, dev, stream);
+    return s ? cols_dispatch<int8_t, true>(x, rows, cols, ld, q, scale, t, sr, dev, stream)
+             : cols_dispatch<int8_t, false>(x, rows, cols, ld, q, scale, t, sr, dev, stream);
+  return s ? cols_dispatch<__half, true>(x, rows, cols, ld, q, scale, t, sr, dev, stream)
+           : cols_dispatch<__half, false>(x, rows, cols, ld, q, scale, t, sr, dev, stream);
 }
 
 }  // namespace int8mp

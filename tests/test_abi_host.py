@@ -51,7 +51,7 @@ def _q(lib, x, rows, cols, ld, axis, mode=0, codes=0, q=16, scale=16):
 
 
 def test_quantize_host_validation(lib):
-    assert _q(lib, 16, 8, 8, 8, axis=2) == m.INT8MP_ERR_INVALID_ARG
+    assert _q(lib, 16, 8, 8, 8, axis=3) == m.INT8MP_ERR_INVALID_ARG
     assert _q(lib, 16, 8, 8, 8, axis=0, mode=3) == m.INT8MP_ERR_INVALID_ARG
     assert _q(lib, 16, 8, 8, 8, axis=0, codes=5) == m.INT8MP_ERR_INVALID_ARG
     assert _q(lib, 16, 8, 16, 8, axis=0) == m.INT8MP_ERR_INVALID_ARG      # ld < cols
@@ -62,14 +62,37 @@ def test_quantize_host_validation(lib):
     assert _q(lib, 16, 12, 8, 8, axis=1) == m.INT8MP_ERR_ALIGNMENT        # axis 1 needs rows % 8
 
 
+def test_absmax_entry_points_host_validation(lib):
+    rc = lib.int8mp_quantize_rows_colmax(P(16), 8, 8, 8, 0, 0, 0, 0, P(16), 1, P(16), None, None)
+    assert rc == m.INT8MP_ERR_INVALID_ARG                                 # colmax missing
+    rc = lib.int8mp_quantize_rows_colmax(P(16), 8, 8, 8, 0, 0, 0, 0, P(16), 1, P(16), P(18), None)
+    assert rc == m.INT8MP_ERR_ALIGNMENT                                   # colmax misaligned
+    rc = lib.int8mp_quantize_cols_absmax(P(16), 8, 8, 8, None, 0, 0, 0, 0, P(16), 1, P(16), None)
+    assert rc == m.INT8MP_ERR_INVALID_ARG
+    rc = lib.int8mp_quantize_cols_absmax(P(16), 8, 12, 16, P(16), 0, 0, 0, 0, P(16), 1, P(16), None)
+    assert rc == m.INT8MP_ERR_ALIGNMENT                                   # cols % 8
+    assert lib.int8mp_quantize_cols_absmax(P(16), 0, 8, 8, None, 0, 0, 0, 0, None, 1, None,
+                                           None) == m.INT8MP_OK          # empty
+    cfg = m.linear_cfg()
+    ref = ctypes.byref(cfg)
+    assert lib.int8mp_linear_fwd_save(P(16), P(16), P(16), 32, 32, 32, ref, None, P(256), 1 << 20,
+                                      None) == m.INT8MP_ERR_INVALID_ARG
+    assert lib.int8mp_linear_bwd_saved(P(16), P(16), P(16), P(16), P(16), 32, 32, 32, ref, None,
+                                       P(256), 1 << 20, None) == m.INT8MP_ERR_INVALID_ARG
+    assert lib.int8mp_linear_bwd_saved(P(16), P(16), P(16), P(16), P(16), 32, 32, 32, ref, P(18),
+                                       P(256), 1 << 20, None) == m.INT8MP_ERR_ALIGNMENT
+
+
 def _mm(lib, M, N, K, layout=0, codes=1, A=16, B=16, out=16, ldo=None):
     return lib.int8mp_mm_s32(P(A), P(B), M, N, K, layout, codes, P(out), N if ldo is None else ldo,
                              None)
 
 
 def test_matmul_host_validation(lib):
-    assert _mm(lib, 8, 8, 16, layout=1) == m.INT8MP_ERR_INVALID_ARG       # tensor core needs A@B.T
-    assert _mm(lib, 8, 8, 16, codes=0) == m.INT8MP_ERR_INVALID_ARG        # and f16 containers
+    assert _mm(lib, 8, 8, 16, layout=3) == m.INT8MP_ERR_INVALID_ARG       # no such layout
+    assert _mm(lib, 8, 8, 16, codes=0) == m.INT8MP_ERR_INVALID_ARG        # tensor core: f16 containers
+    assert _mm(lib, 12, 8, 16, layout=2) == m.INT8MP_ERR_ALIGNMENT        # A.T@B: rows of A^T, M % 8
+    assert _mm(lib, 8, 12, 16, layout=1) == m.INT8MP_ERR_ALIGNMENT        # A@B: rows of B, N % 8
     assert _mm(lib, 8, 8, m.INT8MP_MAX_K + 1) == m.INT8MP_ERR_INVALID_ARG
     assert _mm(lib, 8, 8, 24) == m.INT8MP_ERR_ALIGNMENT                   # K % 16
     assert _mm(lib, 8, 12, 16) == m.INT8MP_ERR_ALIGNMENT                  # N % 8

@@ -93,21 +93,27 @@ def test_full_size_linear_sampled_rows(spec_name, name, mode):
 
 @pytest.mark.parametrize("layout", ["AxBT", "AxB", "ATxB"])
 def test_square_4096_sampled_rows(layout):
+    # as the benchmark runs it: operands stored K-first are quantized by
+    # columns with their codes left in place and multiplied in that layout
     S = 4096
     A, B = synth.square_inputs(S, layout)
-    a_axis = 1 if layout == "ATxB" else 0
-    b_axis = 0 if layout == "AxBT" else 1
-    qa, sa = m.int8mp_quantize_rowwise(A.to(DEV), axis=a_axis, codes=m.INT8MP_CODES_F16)
-    qb, sb = m.int8mp_quantize_rowwise(B.to(DEV), axis=b_axis, codes=m.INT8MP_CODES_F16)
-    out = m.int8mp_scaled_mm(qa, sa, qb, sb)
+    a_cols = layout == "ATxB"
+    b_cols = layout != "AxBT"
+    ax = lambda cols: m.INT8MP_GROUP_COLS if cols else m.INT8MP_GROUP_ROWS
+    lay = {"AxBT": m.INT8MP_AxBT, "AxB": m.INT8MP_AxB, "ATxB": m.INT8MP_ATxB}[layout]
+    qa, sa = m.int8mp_quantize_rowwise(A.to(DEV), axis=ax(a_cols), codes=m.INT8MP_CODES_F16)
+    qb, sb = m.int8mp_quantize_rowwise(B.to(DEV), axis=ax(b_cols), codes=m.INT8MP_CODES_F16)
+    out = m.int8mp_scaled_mm(qa, sa, qb, sb, layout=lay)
     torch.cuda.synchronize()
-    qar, sar = oracle.quantize(bf16_bits(A), axis=a_axis)
-    qbr, sbr = oracle.quantize(bf16_bits(B), axis=b_axis)
-    # the quantized operands themselves, in full
+    # the oracle returns K-major codes (column groups transposed)
+    qar, sar = oracle.quantize(bf16_bits(A), axis=1 if a_cols else 0)
+    qbr, sbr = oracle.quantize(bf16_bits(B), axis=1 if b_cols else 0)
+    # the quantized operands themselves, in full, in the stored layout
+    stored = lambda q, cols: np.ascontiguousarray(q.T) if cols else q
     np.testing.assert_array_equal(sa.cpu().numpy().view(np.int32), sar.view(np.int32))
-    np.testing.assert_array_equal(qa.cpu().float().to(torch.int8).numpy(), qar)
+    np.testing.assert_array_equal(qa.cpu().float().to(torch.int8).numpy(), stored(qar, a_cols))
     np.testing.assert_array_equal(sb.cpu().numpy().view(np.int32), sbr.view(np.int32))
-    np.testing.assert_array_equal(qb.cpu().float().to(torch.int8).numpy(), qbr)
+    np.testing.assert_array_equal(qb.cpu().float().to(torch.int8).numpy(), stored(qbr, b_cols))
     rows = _sample(S, 8, 3)
     ref = oracle.scaled_mm(qar[rows], sar[rows], qbr, sbr, len(rows), S, S)  # K-major codes
     _rows_equal(out, rows, ref, f"square 4096 {layout}")

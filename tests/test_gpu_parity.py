@@ -106,6 +106,76 @@ def test_quantize_cols_bit_exact(shape, mode, codes):
     np.testing.assert_array_equal(_codes_np(q), qr)
 
 
+COL_NAT_SHAPES = [(256, 512), (8, 8), (77, 136), (1032, 64), (520, 2048), (16, 4096),
+                  (3001, 264), (1, 5632)]
+
+
+@pytest.mark.parametrize("codes", [m.INT8MP_CODES_S8, m.INT8MP_CODES_F16])
+@pytest.mark.parametrize("mode", [m.INT8MP_RNE, m.INT8MP_SR])
+@pytest.mark.parametrize("shape", COL_NAT_SHAPES)
+def test_quantize_cols_in_input_layout_bit_exact(shape, mode, codes):
+    # column groups with the codes left in x's layout: the same numbers as
+    # the oracle's column quantization, which it returns transposed
+    rows, cols = shape
+    x = _edge_input(rows, cols, seed=5 * rows + cols)
+    seed, off, sid = 4242, 2**35 + 3, 4
+    q, s = m.int8mp_quantize_rowwise(_dev(x), axis=m.INT8MP_GROUP_COLS, mode=mode, seed=seed,
+                                     offset=off, stream_id=sid, codes=codes)
+    assert tuple(q.shape) == (rows, cols)
+    qr, sr = oracle.quantize(bf16_bits(x), axis=1, mode=mode, seed=seed, offset=off, stream_id=sid)
+    np.testing.assert_array_equal(_f32_bits(s), sr.view(np.int32))
+    np.testing.assert_array_equal(_codes_np(q), np.ascontiguousarray(qr.T))
+
+
+def _col_absmax_bits(x):
+    """Each column's absmax as fp32 bits: the plain definition, max |x|."""
+    return np.abs(bits_to_f32(bf16_bits(x))).max(axis=0).astype(np.float32).view(np.int32)
+
+
+# cols 2048 / 4096 / 5632 / 14336 take the fused pass; 24576 (more vectors
+# per thread than registers hold) and 53248 (the long-row kernel) fall back
+# to a separate column pass
+COLMAX_SHAPES = [(256, 512), (8, 8), (77, 136), (520, 2048), (300, 5632), (33, 4096),
+                 (40, 14336), (9, 24576), (3, 53248), (4099, 1024)]
+
+
+@pytest.mark.parametrize("mode", [m.INT8MP_RNE, m.INT8MP_SR])
+@pytest.mark.parametrize("shape", COLMAX_SHAPES)
+def test_rows_with_column_absmax_then_columns(shape, mode):
+    rows, cols = shape
+    x = _edge_input(rows, cols, seed=11 * rows + cols)
+    xd = _dev(x)
+    seed, off = 77, 5
+    colmax = torch.zeros(cols, dtype=torch.float32, device=DEV)
+    q, s = m.int8mp_quantize_rows_colmax(xd, colmax, mode=mode, seed=seed, offset=off, stream_id=2,
+                                         codes=m.INT8MP_CODES_F16)
+    qr, sr = oracle.quantize(bf16_bits(x), axis=0, mode=mode, seed=seed, offset=off, stream_id=2)
+    np.testing.assert_array_equal(_f32_bits(s), sr.view(np.int32))
+    np.testing.assert_array_equal(_codes_np(q), qr)
+    np.testing.assert_array_equal(_f32_bits(colmax), _col_absmax_bits(x))
+    # the column groups fed by that absmax: the oracle's column quantization
+    qc, sc = m.int8mp_quantize_cols_absmax(xd, colmax, mode=mode, seed=seed, offset=off,
+                                           stream_id=4, codes=m.INT8MP_CODES_F16)
+    qcr, scr = oracle.quantize(bf16_bits(x), axis=1, mode=mode, seed=seed, offset=off, stream_id=4)
+    np.testing.assert_array_equal(_f32_bits(sc), scr.view(np.int32))
+    np.testing.assert_array_equal(_codes_np(qc), np.ascontiguousarray(qcr.T))
+
+
+def test_column_absmax_accumulates_over_row_blocks():
+    x = _edge_input(640, 2048, seed=91)
+    xd = _dev(x)
+    colmax = torch.zeros(2048, dtype=torch.float32, device=DEV)
+    m.int8mp_quantize_rows_colmax(xd[:320], colmax, codes=m.INT8MP_CODES_S8)
+    m.int8mp_quantize_rows_colmax(xd[320:], colmax, codes=m.INT8MP_CODES_S8)
+    np.testing.assert_array_equal(_f32_bits(colmax), _col_absmax_bits(x))
+    # an initial value above every column's absmax survives (the input's
+    # largest entries are about 1e38: its row 5 is scaled by 1e36)
+    big = torch.finfo(torch.float32).max
+    colmax.fill_(big)
+    m.int8mp_quantize_rows_colmax(xd, colmax, codes=m.INT8MP_CODES_S8)
+    assert bool((colmax == big).all())
+
+
 def test_quantize_with_padded_leading_dimension():
     base = _edge_input(64, 160, seed=3)
     view = _dev(base)[:, :136]  # ld 160 > cols 136
@@ -116,6 +186,12 @@ def test_quantize_with_padded_leading_dimension():
     qr1, sr1 = oracle.quantize(bf16_bits(base[:, :136].contiguous()), axis=1)
     np.testing.assert_array_equal(_codes_np(q1), qr1)
     np.testing.assert_array_equal(_f32_bits(s1), sr1.view(np.int32))
+    q2, s2 = m.int8mp_quantize_rowwise(view, axis=m.INT8MP_GROUP_COLS, mode=m.INT8MP_SR, seed=8,
+                                       codes=m.INT8MP_CODES_F16)
+    qr2, sr2 = oracle.quantize(bf16_bits(base[:, :136].contiguous()), axis=1, mode=oracle.SR,
+                               seed=8)
+    np.testing.assert_array_equal(_codes_np(q2), np.ascontiguousarray(qr2.T))
+    np.testing.assert_array_equal(_f32_bits(s2), sr2.view(np.int32))
 
 
 def _rand_codes(M, K, seed, extreme=False):
@@ -154,6 +230,38 @@ def test_mm_s32_chunking_keeps_large_sums_exact(M):
     np.testing.assert_array_equal(acc, ref)
 
 
+# M-major / N-major operands: A stored [K,M] (A.T @ B), B stored [K,N] (A @ B
+# and A.T @ B).  Shapes reach the single-CTA kernel (M <= 128, or few tiles)
+# and the CTA-pair kernel (>= 76 pair tiles, or K >= 8192), ragged M and N.
+LAYOUT_MM_SHAPES = [(128, 256, 512), (200, 264, 144), (64, 776, 1040), (2560, 2048, 128),
+                    (256, 264, 8192), (1000, 520, 2096)]
+
+
+@pytest.mark.parametrize("layout", [m.INT8MP_AxB, m.INT8MP_ATxB])
+@pytest.mark.parametrize("shape", LAYOUT_MM_SHAPES)
+def test_mm_s32_mn_major_layouts_bit_exact(shape, layout):
+    M, N, K = shape
+    a = _rand_codes(M, K, 5) if layout == m.INT8MP_AxB else _rand_codes(K, M, 5)
+    b = _rand_codes(K, N, 6)
+    acc = m.int8mp_mm_s32(_dev(a.half()), _dev(b.half()), layout=layout)
+    ref = oracle.mm_s32(a.numpy(), b.numpy(), M, N, K, layout=layout)
+    np.testing.assert_array_equal(acc.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("layout", [m.INT8MP_AxB, m.INT8MP_ATxB])
+def test_mm_s32_mn_major_large_sums_exact(layout):
+    M, N, K = 256, 256, 8192
+    a = _rand_codes(M, K, 7, extreme=True)
+    b = _rand_codes(N, K, 8, extreme=True)
+    b[0] = a[0]
+    b[1] = -a[1]
+    a_st = a if layout == m.INT8MP_AxB else a.T.contiguous()
+    b_st = b.T.contiguous()
+    acc = m.int8mp_mm_s32(_dev(a_st.half()), _dev(b_st.half()), layout=layout).cpu().numpy()
+    assert acc[0, 0] == 127 * 127 * K and acc[1, 1] == -127 * 127 * K
+    np.testing.assert_array_equal(acc, oracle.mm_s32(a.numpy(), b.numpy(), M, N, K))
+
+
 @pytest.mark.parametrize("shape", [(256, 256, 512), (200, 264, 144), (384, 512, 2048)])
 def test_scaled_mm_bit_exact(shape):
     M, N, K = shape
@@ -189,6 +297,32 @@ def test_square_layouts_through_quantize_side_transpose(layout):
     assert_bf16_equal(out, ref, f"square {layout}")
 
 
+@pytest.mark.parametrize("layout", ["AxB", "ATxB"])
+@pytest.mark.parametrize("S", [256, 2560])
+def test_square_layouts_with_column_codes_in_place(layout, S):
+    # the K-first operand quantized by columns with its codes left in place,
+    # multiplied in the stored layout (no transposition anywhere)
+    A, B = synth.square_inputs(S, layout)
+    a_axis = m.INT8MP_GROUP_COLS if layout == "ATxB" else m.INT8MP_GROUP_ROWS
+    qa, sa = m.int8mp_quantize_rowwise(_dev(A), axis=a_axis, codes=m.INT8MP_CODES_F16)
+    qb, sb = m.int8mp_quantize_rowwise(_dev(B), axis=m.INT8MP_GROUP_COLS, codes=m.INT8MP_CODES_F16)
+    lay = {"AxB": m.INT8MP_AxB, "ATxB": m.INT8MP_ATxB}[layout]
+    out = m.int8mp_scaled_mm(qa, sa, qb, sb, layout=lay)
+    qar, sar = oracle.quantize(bf16_bits(A), axis=1 if layout == "ATxB" else 0)
+    qbr, sbr = oracle.quantize(bf16_bits(B), axis=1)
+    qa_st = qar if layout == "AxB" else np.ascontiguousarray(qar.T)
+    qb_st = np.ascontiguousarray(qbr.T)
+    if S == 256:
+        ref = oracle.scaled_mm(qa_st, sar, qb_st, sbr, S, S, S, layout=lay)
+        assert_bf16_equal(out, ref, f"square {layout}")
+    else:
+        # sampled output rows: each is exact on its own
+        rows = np.random.default_rng(S).choice(S, 8, replace=False)
+        acc = oracle.mm_s32(np.ascontiguousarray(qar[rows]), qbr, 8, S, S)
+        ref = oracle.rescale_bf16(acc, sar[rows], sbr)
+        assert_bf16_equal(out[torch.from_numpy(rows).to(DEV)], ref, f"square {layout} rows")
+
+
 LINEAR_SHAPES = [(256, 256, 512), (128, 96, 160), (48, 32, 1056), (1040, 64, 48)]
 
 
@@ -208,6 +342,37 @@ def test_linear_fwd_bwd_bit_exact(shape, mode):
     assert_bf16_equal(Y, Yr, "fwd")
     assert_bf16_equal(dX, dXr, "grad_input")
     assert_bf16_equal(dW, dWr, "grad_weight")
+
+
+@pytest.mark.parametrize("flags", [(1, 1, 1), (1, 0, 1), (1, 1, 0), (0, 1, 1)])
+@pytest.mark.parametrize("shape", [(256, 256, 512), (1040, 64, 48), (48, 5632, 2048)])
+def test_linear_with_saved_absmax_matches_plain_passes(shape, flags):
+    T, N, K = shape
+    X = synth.bf16_normal((T, K), 14, outlier_frac=0.005, outlier_scale=30.0)
+    W = synth.bf16_normal((N, K), 24, std=0.02)
+    dY = synth.bf16_normal((T, N), 34, std=1e-3)
+    f, gi, gw = flags
+    cfg = m.linear_cfg(mode=m.INT8MP_SR, seed=9, offset=3, int8_fwd=f, int8_grad_in=gi,
+                       int8_grad_w=gw)
+    Xd, Wd, dYd = _dev(X), _dev(W), _dev(dY)
+    absmax = torch.full((2 * K,), -1.0, dtype=torch.float32, device=DEV)  # overwritten
+    Y1 = m.int8mp_linear_fwd_save(Xd, Wd, absmax, cfg)
+    dX1, dW1 = m.int8mp_linear_bwd_saved(dYd, Xd, Wd, absmax, cfg)
+    Y0 = m.int8mp_linear_fwd(Xd, Wd, cfg)
+    dX0, dW0 = m.int8mp_linear_bwd(dYd, Xd, Wd, cfg)
+    assert m.int8mp_poll_device_status() == m.INT8MP_OK
+    zero = np.zeros(K, dtype=np.int32)
+    np.testing.assert_array_equal(_f32_bits(absmax[:K]), _col_absmax_bits(X) if gw else zero)
+    np.testing.assert_array_equal(_f32_bits(absmax[K:]), _col_absmax_bits(W) if gi else zero)
+    for a, b, what in ((Y1, Y0, "Y"), (dX1, dX0, "dX"), (dW1, dW0, "dW")):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), what
+    if f and gi and gw:
+        Yr = oracle.linear_fwd(bf16_bits(X), bf16_bits(W), mode=oracle.SR, seed=9, offset=3)
+        dXr, dWr = oracle.linear_bwd(bf16_bits(dY), bf16_bits(X), bf16_bits(W), mode=oracle.SR,
+                                     seed=9, offset=3)
+        assert_bf16_equal(Y1, Yr, "saved forward")
+        assert_bf16_equal(dX1, dXr, "saved grad input")
+        assert_bf16_equal(dW1, dWr, "saved grad weight")
 
 
 def test_single_forward_matmul_256x512():
