@@ -202,6 +202,8 @@ class LayerStep:
         # (by its grad-input row pass), per linear: [K | K | N]
         for l in self.linears:
             l["colmax"] = torch.empty(2 * l["K"] + l["N"], dtype=torch.float32, device=device)
+        # the matmuls' scratch for splitting their last wave of tiles
+        self.mm_ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
         self.flops = 6.0 * T * sum(l["N"] * l["K"] for l in self.linears)
         self.gemms_per_step = 3 * len(self.linears)
         # kernels of this library per step and linear: three row quantizations
@@ -252,15 +254,17 @@ class LayerStep:
             # forward: X and W along K (their rows); their column absmax on the way
             qx, sx = rec("quant_rows", lambda: self._q(X, 0, m.INT8MP_STREAM_FWD_X, self.qa, self.sa, seed, offset, cx))
             qw, sw = rec("quant_rows", lambda: self._q(W, 0, m.INT8MP_STREAM_FWD_W, self.qb, self.sb, seed, offset, cw))
-            rec("gemm", lambda: m.int8mp_scaled_mm(qx, sx, qw, sw, out=l["Y"]))
+            rec("gemm", lambda: m.int8mp_scaled_mm(qx, sx, qw, sw, out=l["Y"], workspace=self.mm_ws))
             # grad input: dY along N (rows), W along N (columns, codes [N, K]): A @ B
             qg, sg = rec("quant_rows", lambda: self._q(dY, 0, m.INT8MP_STREAM_GI_DY, self.qa, self.sa, seed, offset, cg))
             qwc, swc = rec("quant_cols", lambda: self._q(W, 2, m.INT8MP_STREAM_GI_W, self.qb, self.sb, seed, offset, cw))
-            rec("gemm", lambda: m.int8mp_scaled_mm(qg, sg, qwc, swc, layout=m.INT8MP_AxB, out=l["dX"]))
+            rec("gemm", lambda: m.int8mp_scaled_mm(qg, sg, qwc, swc, layout=m.INT8MP_AxB, out=l["dX"],
+                                                   workspace=self.mm_ws))
             # grad weight: dY and X along T (columns, codes [T, N], [T, K]): A.T @ B
             qgc, sgc = rec("quant_cols", lambda: self._q(dY, 2, m.INT8MP_STREAM_GW_DY, self.qa, self.sa, seed, offset, cg))
             qxc, sxc = rec("quant_cols", lambda: self._q(X, 2, m.INT8MP_STREAM_GW_X, self.qb, self.sb, seed, offset, cx))
-            rec("gemm", lambda: m.int8mp_scaled_mm(qgc, sgc, qxc, sxc, layout=m.INT8MP_ATxB, out=l["dW"]))
+            rec("gemm", lambda: m.int8mp_scaled_mm(qgc, sgc, qxc, sxc, layout=m.INT8MP_ATxB, out=l["dW"],
+                                                   workspace=self.mm_ws))
 
 
 def time_steps(step, steps, warmup, world, device):
@@ -383,6 +387,7 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
         sa = torch.empty(S, dtype=torch.float32, device=device)
         sb = torch.empty(S, dtype=torch.float32, device=device)
         Y = torch.empty((S, S), dtype=torch.bfloat16, device=device)
+        mm_ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
         for layout, (ax_a, ax_b, lay) in (("A@B.T", (0, 0, m.INT8MP_AxBT)), ("A@B", (0, 2, m.INT8MP_AxB)),
                                           ("A.T@B", (2, 2, m.INT8MP_ATxB))):
             tq, tm = [], []
@@ -393,7 +398,7 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
                 m.int8mp_quantize_rowwise(A, axis=ax_a, codes=m.INT8MP_CODES_F16, q=qa, scale=sa)
                 m.int8mp_quantize_rowwise(B, axis=ax_b, codes=m.INT8MP_CODES_F16, q=qb, scale=sb)
                 e[1].record()
-                m.int8mp_scaled_mm(qa, sa, qb, sb, layout=lay, out=Y)
+                m.int8mp_scaled_mm(qa, sa, qb, sb, layout=lay, out=Y, workspace=mm_ws)
                 e[2].record()
                 torch.cuda.synchronize()
                 if it >= 3:

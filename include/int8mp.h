@@ -204,6 +204,27 @@ int8mp_status int8mp_mm_s32(const void* A, const void* B, int64_t M, int64_t N, 
                             int64_t ldo, void* stream);
 
 /*
+ * int8mp_scaled_mm_ws / int8mp_mm_s32_ws -- the same matmuls with a
+ * caller-provided device workspace of at least int8mp_mm_workspace_size()
+ * bytes (256-byte aligned; no initialization needed).  With it, when the
+ * output tiles leave a partial last wave on the GPU's SM pairs, the GEMM
+ * splits the contraction of those last tiles into equal parts computed by
+ * the otherwise idle pairs; the parts are added as exact int32 totals, so
+ * the results are those of the plain calls bit for bit.  workspace may be NULL (the plain
+ * schedule); a non-NULL one smaller than int8mp_mm_workspace_size() returns
+ * INT8MP_ERR_WORKSPACE, a misaligned one INT8MP_ERR_ALIGNMENT.  One workspace
+ * must not be used by two calls that may run at the same time.
+ */
+size_t int8mp_mm_workspace_size(void);
+int8mp_status int8mp_scaled_mm_ws(const void* A, const float* sA, const void* B, const float* sB,
+                                  int64_t M, int64_t N, int64_t K, int8mp_layout layout,
+                                  int8mp_codes codes, void* out, int64_t ldo, void* workspace,
+                                  size_t ws_bytes, void* stream);
+int8mp_status int8mp_mm_s32_ws(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                               int8mp_layout layout, int8mp_codes codes, int32_t* out, int64_t ldo,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Per-pass configuration of a linear layer (the pages' per-matmul INT8
  * switches and stochastic-rounding switch; "Quantized model training"
  * README, INT8 mixed precision training table).  int8_* = 1 runs that pass
@@ -222,9 +243,12 @@ typedef struct {
   uint64_t offset;
 } int8mp_linear_cfg;
 
-/* Bytes of device workspace int8mp_linear_fwd / int8mp_linear_bwd need for
- * these sizes (codes and scales of the quantized operands, 256-byte aligned
- * sub-buffers).  Returns 0 for invalid sizes. */
+/* Bytes of device workspace int8mp_linear_fwd / int8mp_linear_bwd use for
+ * these sizes: the codes and scales of the quantized operands (256-byte
+ * aligned sub-buffers, required) followed by the matmul's last-wave scratch
+ * (int8mp_mm_workspace_size() bytes; optional: a workspace that ends before
+ * it gives the same results without splitting the last wave).  Returns 0
+ * for invalid sizes. */
 size_t int8mp_linear_workspace_size(int64_t T, int64_t N, int64_t K,
                                     const int8mp_linear_cfg* cfg);
 
@@ -232,8 +256,9 @@ size_t int8mp_linear_workspace_size(int64_t T, int64_t N, int64_t K,
  * int8mp_linear_fwd -- Y [T,N] = X [T,K] . W [N,K]^T: X and W quantized
  * along K (SR streams 0 and 1), scaled matmul, bf16 out.
  * Requirements: T >= 0, N >= 0, K >= 16; K % 16 == 0, N % 16 == 0,
- * T % 16 == 0; all pointers 16-byte aligned; workspace at least
- * int8mp_linear_workspace_size() bytes (INT8MP_ERR_WORKSPACE otherwise).
+ * T % 16 == 0; all pointers 16-byte aligned; workspace (256-byte aligned)
+ * of int8mp_linear_workspace_size() bytes, of which all but the trailing
+ * int8mp_mm_workspace_size() are required (INT8MP_ERR_WORKSPACE otherwise).
  */
 int8mp_status int8mp_linear_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t N,
                                 int64_t K, const int8mp_linear_cfg* cfg, void* workspace,

@@ -36,7 +36,8 @@ EXPORTED = (
     "int8mp_poll_device_status", "int8mp_status_string", "int8mp_version",
     "int8mp_debug_mm_s32_drop_first_load", "int8mp_linear_fwd_noalloc",
     "int8mp_debug_check_division", "int8mp_quantize_rows_colmax", "int8mp_quantize_cols_absmax",
-    "int8mp_linear_fwd_save", "int8mp_linear_bwd_saved",
+    "int8mp_linear_fwd_save", "int8mp_linear_bwd_saved", "int8mp_mm_workspace_size",
+    "int8mp_scaled_mm_ws", "int8mp_mm_s32_ws",
 )
 INT8MP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -104,7 +105,13 @@ def load(path=None):
                                          ctypes.POINTER(int8mp_linear_cfg), _P, _P, _SZ, _P]
     L.int8mp_linear_bwd_saved.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64,
                                           ctypes.POINTER(int8mp_linear_cfg), _P, _P, _SZ, _P]
-    for name in ("int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
+    L.int8mp_mm_workspace_size.argtypes = []
+    L.int8mp_mm_workspace_size.restype = _SZ
+    L.int8mp_scaled_mm_ws.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _I64, _P,
+                                      _SZ, _P]
+    L.int8mp_mm_s32_ws.argtypes = [_P, _P, _I64, _I64, _I64, _INT, _INT, _P, _I64, _P, _SZ, _P]
+    for name in ("int8mp_scaled_mm_ws", "int8mp_mm_s32_ws",
+                 "int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
                  "int8mp_linear_fwd", "int8mp_linear_bwd", "int8mp_poll_device_status",
                  "int8mp_version", "int8mp_debug_mm_s32_drop_first_load",
                  "int8mp_linear_fwd_noalloc", "int8mp_debug_check_division",
@@ -207,8 +214,21 @@ def int8mp_quantize_cols_absmax(x, colmax, mode=INT8MP_RNE, seed=0, offset=0, st
     return q, scale
 
 
+def int8mp_mm_workspace_size():
+    return int(load().int8mp_mm_workspace_size())
+
+
+def _mm_ws(workspace, device):
+    """workspace: None (plain schedule), True (allocate one) or a uint8 tensor."""
+    if workspace is None or workspace is False:
+        return None, 0
+    if workspace is True:
+        workspace = torch.empty(int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
 def int8mp_scaled_mm(A, sA, B, sB, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, out=None,
-                     stream=None):
+                     stream=None, workspace=None):
     """Codes (f16 containers) A, B stored per layout -- A@B.T: A [M,K], B [N,K];
     A@B: A [M,K], B [K,N]; A.T@B: A [K,M], B [K,N] -- sA [M], sB [N] -> bf16
     [M,N]."""
@@ -216,18 +236,32 @@ def int8mp_scaled_mm(A, sA, B, sB, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, o
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     ldo = out.stride(0) if M > 0 else N
-    _check(load().int8mp_scaled_mm(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), M, N, K, int(layout),
-                                   int(codes), _ptr(out), ldo, _stream(stream)), "int8mp_scaled_mm")
+    ws, nbytes = _mm_ws(workspace, A.device)
+    if ws is None:
+        _check(load().int8mp_scaled_mm(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), M, N, K, int(layout),
+                                       int(codes), _ptr(out), ldo, _stream(stream)),
+               "int8mp_scaled_mm")
+    else:
+        _check(load().int8mp_scaled_mm_ws(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), M, N, K,
+                                          int(layout), int(codes), _ptr(out), ldo, _ptr(ws), nbytes,
+                                          _stream(stream)), "int8mp_scaled_mm_ws")
     return out
 
 
-def int8mp_mm_s32(A, B, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, out=None, stream=None):
+def int8mp_mm_s32(A, B, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, out=None, stream=None,
+                  workspace=None):
     M, N, K = _mm_sizes(A, B, layout)
     if out is None:
         out = torch.empty((M, N), dtype=torch.int32, device=A.device)
     ldo = out.stride(0) if M > 0 else N
-    _check(load().int8mp_mm_s32(_ptr(A), _ptr(B), M, N, K, int(layout), int(codes), _ptr(out), ldo,
-                                _stream(stream)), "int8mp_mm_s32")
+    ws, nbytes = _mm_ws(workspace, A.device)
+    if ws is None:
+        _check(load().int8mp_mm_s32(_ptr(A), _ptr(B), M, N, K, int(layout), int(codes), _ptr(out),
+                                    ldo, _stream(stream)), "int8mp_mm_s32")
+    else:
+        _check(load().int8mp_mm_s32_ws(_ptr(A), _ptr(B), M, N, K, int(layout), int(codes),
+                                       _ptr(out), ldo, _ptr(ws), nbytes, _stream(stream)),
+               "int8mp_mm_s32_ws")
     return out
 
 

@@ -102,9 +102,19 @@ int8mp_status check_mm(const void* A, const void* B, int64_t M, int64_t N, int64
 
 // layout AxBT: both operands K-major; AxB: B MN-major ([K,N]); ATxB: both
 // MN-major (A [K,M], B [K,N]).
+// workspace of the *_ws matmuls: NULL (whole tiles), or at least
+// int8mp_mm_workspace_size() bytes, 256-byte aligned
+int8mp_status check_mm_workspace(const void* workspace, size_t ws_bytes) {
+  if (!workspace) return INT8MP_OK;
+  if (!aligned(workspace, 256)) return INT8MP_ERR_ALIGNMENT;
+  if (ws_bytes < int8mp::kSplitTailScratchBytes) return INT8MP_ERR_WORKSPACE;
+  return INT8MP_OK;
+}
+
 int8mp_status run_mm(const void* A, const float* sA, const void* B, const float* sB, int64_t M,
                      int64_t N, int64_t K, int8mp_layout layout, int8mp::GemmOut mode, void* out,
-                     int64_t ldo, const int8mp::GemmDebug& dbg, cudaStream_t stream) {
+                     int64_t ldo, void* scratch, const int8mp::GemmDebug& dbg,
+                     cudaStream_t stream) {
   if (M == 0 || N == 0) return INT8MP_OK;
   DeviceInfo dev;
   int8mp_status st = current_device(&dev);
@@ -115,8 +125,8 @@ int8mp_status run_mm(const void* A, const float* sA, const void* B, const float*
                                        static_cast<size_t>(N) * esize, static_cast<size_t>(M),
                                        stream));
   const bool a_mn = layout == INT8MP_ATxB, b_mn = layout != INT8MP_AxBT;
-  return from_cuda(
-      int8mp::launch_gemm(A, a_mn, sA, B, b_mn, sB, M, N, K, mode, out, ldo, dev, dbg, stream));
+  return from_cuda(int8mp::launch_gemm(A, a_mn, sA, B, b_mn, sB, M, N, K, mode, out, ldo, scratch,
+                                       dev, dbg, stream));
 }
 
 // ------------------------------------------------------------- workspace
@@ -173,6 +183,13 @@ size_t bwd_bytes(int64_t T, int64_t N, int64_t K) {
   Carver c{nullptr};
   carve_bwd(c, T, N, K);
   return c.used;
+}
+
+// The GEMM's last-wave scratch, when the workspace extends that far past the
+// `used` bytes the pass needs (else NULL: whole-tile schedule).
+void* gemm_scratch(void* workspace, size_t ws_bytes, size_t used) {
+  if (!workspace || ws_bytes < used + int8mp::kSplitTailScratchBytes) return nullptr;
+  return static_cast<char*>(workspace) + used;
 }
 
 int8mp_status check_linear(int64_t T, int64_t N, int64_t K, const int8mp_linear_cfg* cfg) {
@@ -246,32 +263,51 @@ int8mp_status int8mp_quantize_cols_absmax(const void* x, int64_t rows, int64_t c
                                                             as_stream(stream)));
 }
 
+size_t int8mp_mm_workspace_size(void) { return int8mp::kSplitTailScratchBytes; }
+
 int8mp_status int8mp_scaled_mm(const void* A, const float* sA, const void* B, const float* sB,
                                int64_t M, int64_t N, int64_t K, int8mp_layout layout,
                                int8mp_codes codes, void* out, int64_t ldo, void* stream) {
+  return int8mp_scaled_mm_ws(A, sA, B, sB, M, N, K, layout, codes, out, ldo, nullptr, 0, stream);
+}
+
+int8mp_status int8mp_scaled_mm_ws(const void* A, const float* sA, const void* B, const float* sB,
+                                  int64_t M, int64_t N, int64_t K, int8mp_layout layout,
+                                  int8mp_codes codes, void* out, int64_t ldo, void* workspace,
+                                  size_t ws_bytes, void* stream) {
   int8mp_status st = check_mm(A, B, M, N, K, layout, codes, out, ldo);
+  if (st != INT8MP_OK) return st;
+  st = check_mm_workspace(workspace, ws_bytes);
   if (st != INT8MP_OK) return st;
   if (M > 0 && N > 0 && K > 0) {
     if (!sA || !sB) return INT8MP_ERR_INVALID_ARG;
     if (!aligned(sA, 4) || !aligned(sB, 4)) return INT8MP_ERR_ALIGNMENT;
   }
   return run_mm(A, sA, B, sB, M, N, K, layout, int8mp::GemmOut::kBf16Scaled, out, ldo,
-                int8mp::GemmDebug{}, as_stream(stream));
+                workspace, int8mp::GemmDebug{}, as_stream(stream));
 }
 
 int8mp_status int8mp_mm_s32(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
                             int8mp_layout layout, int8mp_codes codes, int32_t* out, int64_t ldo,
                             void* stream) {
+  return int8mp_mm_s32_ws(A, B, M, N, K, layout, codes, out, ldo, nullptr, 0, stream);
+}
+
+int8mp_status int8mp_mm_s32_ws(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                               int8mp_layout layout, int8mp_codes codes, int32_t* out, int64_t ldo,
+                               void* workspace, size_t ws_bytes, void* stream) {
   int8mp_status st = check_mm(A, B, M, N, K, layout, codes, out, ldo);
   if (st != INT8MP_OK) return st;
+  st = check_mm_workspace(workspace, ws_bytes);
+  if (st != INT8MP_OK) return st;
   return run_mm(A, nullptr, B, nullptr, M, N, K, layout, int8mp::GemmOut::kS32, out, ldo,
-                int8mp::GemmDebug{}, as_stream(stream));
+                workspace, int8mp::GemmDebug{}, as_stream(stream));
 }
 
 size_t int8mp_linear_workspace_size(int64_t T, int64_t N, int64_t K, const int8mp_linear_cfg* cfg) {
   if (check_linear(T, N, K, cfg) != INT8MP_OK) return 0;
   const size_t f = fwd_bytes(T, N, K), b = bwd_bytes(T, N, K);
-  return f > b ? f : b;
+  return (f > b ? f : b) + int8mp::kSplitTailScratchBytes;
 }
 
 }  // extern "C"
@@ -330,7 +366,7 @@ int8mp_status linear_fwd_impl(const void* X, const void* W, void* Y, int64_t T, 
     if (e != cudaSuccess) return INT8MP_ERR_CUDA;
   }
   return run_mm(xq.q, xq.s, wq.q, wq.s, T, N, K, INT8MP_AxBT, int8mp::GemmOut::kBf16Scaled, Y, N,
-                int8mp::GemmDebug{}, s);
+                gemm_scratch(workspace, ws_bytes, fwd_bytes(T, N, K)), int8mp::GemmDebug{}, s);
 }
 
 // Backward pass.  saved_absmax (optional, fp32 [2K]): what the forward pass
@@ -356,6 +392,7 @@ int8mp_status linear_bwd_impl(const void* dY, const void* X, const void* W, void
   cudaStream_t s = as_stream(stream);
   Carver c{static_cast<char*>(workspace)};
   const BwdOperands o = carve_bwd(c, T, N, K);
+  void* scratch = gemm_scratch(workspace, ws_bytes, bwd_bytes(T, N, K));
   const bool int8_dx = want_dx && cfg->int8_grad_in && N > 0;
   const bool int8_dw = want_dw && cfg->int8_grad_w && T > 0;
   // column absmax: dY's (grad weight) comes with its row pass when grad
@@ -398,7 +435,7 @@ int8mp_status linear_bwd_impl(const void* dY, const void* X, const void* W, void
       if (e != cudaSuccess) return INT8MP_ERR_CUDA;
     }
     st = run_mm(o.dy_rows.q, o.dy_rows.s, o.w_cols.q, o.w_cols.s, T, K, N, INT8MP_AxB,
-                int8mp::GemmOut::kBf16Scaled, dX, K, int8mp::GemmDebug{}, s);
+                int8mp::GemmOut::kBf16Scaled, dX, K, scratch, int8mp::GemmDebug{}, s);
     if (st != INT8MP_OK) return st;
   }
   if (want_dw && !cfg->int8_grad_w) {
@@ -421,7 +458,7 @@ int8mp_status linear_bwd_impl(const void* dY, const void* X, const void* W, void
       if (e != cudaSuccess) return INT8MP_ERR_CUDA;
     }
     st = run_mm(o.dy_cols.q, o.dy_cols.s, o.x_cols.q, o.x_cols.s, N, K, T, INT8MP_ATxB,
-                int8mp::GemmOut::kBf16Scaled, dW, K, int8mp::GemmDebug{}, s);
+                int8mp::GemmOut::kBf16Scaled, dW, K, scratch, int8mp::GemmDebug{}, s);
   }
   return st;
 }
@@ -499,8 +536,8 @@ int8mp_status int8mp_debug_mm_s32_drop_first_load(const void* A, const void* B, 
   int8mp::GemmDebug dbg;
   dbg.drop_first_load = 1;
   dbg.wait_limit_ns = static_cast<uint64_t>(wait_limit_ms) * 1000000ull;
-  return run_mm(A, nullptr, B, nullptr, M, N, K, INT8MP_AxBT, int8mp::GemmOut::kS32, out, ldo, dbg,
-                as_stream(stream));
+  return run_mm(A, nullptr, B, nullptr, M, N, K, INT8MP_AxBT, int8mp::GemmOut::kS32, out, ldo,
+                nullptr, dbg, as_stream(stream));
 }
 
 }  // extern "C"

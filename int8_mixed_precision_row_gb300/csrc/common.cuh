@@ -65,15 +65,26 @@ enum class GemmOut { kBf16Scaled = 0, kS32 = 1 };
 struct GemmDebug {
   int drop_first_load = 0;        // test only: never issue the first TMA load
   int single_cta = 0;             // test only: use the single-CTA kernel for any M
+  int no_split_tail = 0;            // test only: no split last wave even with scratch
   uint64_t wait_limit_ns = kWaitLimitNs;
 };
 
+// Scratch of the CTA-pair GEMM's split last wave: a 256x256 int32 slot per
+// pair and 16 64-bit counters per split tile, for up to kSplitTailMaxPairs
+// pairs.  Needs no initialization; one scratch must not serve two GEMMs at
+// the same time.
+constexpr int kSplitTailMaxPairs = 80;
+constexpr size_t kSplitTailScratchBytes =
+    static_cast<size_t>(kSplitTailMaxPairs) * 256 * 256 * 4 + kSplitTailMaxPairs * 2 * 8 * 8;
+
 // f16 containers of integer codes.  A is [M,K] (a_mn false, K contiguous)
 // or [K,M] (a_mn true, M contiguous); B is [N,K] or [K,N] likewise.  Every
-// combination but (a_mn, !b_mn) is served.
+// combination but (a_mn, !b_mn) is served.  scratch: NULL, or
+// kSplitTailScratchBytes (16-byte aligned) that lets the CTA-pair kernel
+// split its last wave of tiles.
 cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B, bool b_mn,
                         const float* sB, int64_t M, int64_t N, int64_t K, GemmOut mode, void* out,
-                        int64_t ldo, const DeviceInfo& dev, const GemmDebug& dbg,
+                        int64_t ldo, void* scratch, const DeviceInfo& dev, const GemmDebug& dbg,
                         cudaStream_t stream);
 
 // ---- BF16 passes (blas.cu) --------------------------------------------------

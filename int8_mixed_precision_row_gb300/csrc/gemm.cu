@@ -36,6 +36,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "common.cuh"
@@ -68,6 +70,11 @@ struct GemmParams {
   unsigned int* status;
   uint64_t wait_limit_ns;
   int drop_first_load;
+  int32_t* partials;             // split tail: a 256 x 256 int32 slot per pair
+  unsigned long long* counters;  // split tail: 2 x 8 counters per tail tile
+  uint64_t epoch;                // split tail: tags this launch's counts (40 bits)
+  int dp_tiles;                  // tiles computed whole (all of them without a split tail)
+  int sk_tail, sk_split;         // split tail: its tiles, and the parts of each
 };
 
 __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned int* status) {
@@ -112,42 +119,39 @@ __host__ __device__ constexpr uint64_t k_step() {
   return kMN ? (16u * 128u) >> 4 : 32u >> 4;
 }
 
+// Eight outputs of row `row`, columns col .. col+7 (N % 8 == 0, so all or
+// none are inside), from their int32 totals.  bf16: (fp32(acc) * sA[row]) *
+// sB[col], round to nearest even; int32: the totals themselves.
+__device__ __forceinline__ void store_vec8(const GemmParams& p, int64_t row, int64_t col, float sa,
+                                           const int32_t* t) {
+  if (col >= p.N) return;
+  if (p.mode == 1) {
+    int4* o = reinterpret_cast<int4*>(static_cast<int32_t*>(p.out) + row * p.ldo + col);
+    o[0] = make_int4(t[0], t[1], t[2], t[3]);
+    o[1] = make_int4(t[4], t[5], t[6], t[7]);
+    return;
+  }
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float o0 = __fmul_rn(__fmul_rn(__int2float_rn(t[2 * e]), sa), __ldg(p.sB + col + 2 * e));
+    const float o1 =
+        __fmul_rn(__fmul_rn(__int2float_rn(t[2 * e + 1]), sa), __ldg(p.sB + col + 2 * e + 1));
+    const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
+    w[e] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.ldo + col) =
+      make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // One thread's output: row `row`, columns col0 .. col0+127, from its int32
-// totals.  bf16: (fp32(acc) * sA[row]) * sB[col], round to nearest even;
-// int32: the totals themselves.  Columns are 16-byte vectors (N % 8 == 0).
+// totals.
 __device__ __forceinline__ void store_rows(const GemmParams& p, int64_t row, int64_t col0,
                                            const int32_t (&tot)[128]) {
   if (row >= p.M) return;
-  if (p.mode == 1) {
-    int32_t* orow = static_cast<int32_t*>(p.out) + row * p.ldo;
+  const float sa = p.mode == 1 ? 0.0f : __ldg(p.sA + row);
 #pragma unroll
-    for (int v = 0; v < 32; ++v) {
-      const int64_t col = col0 + v * 4;
-      if (col < p.N)
-        *reinterpret_cast<int4*>(orow + col) =
-            make_int4(tot[4 * v], tot[4 * v + 1], tot[4 * v + 2], tot[4 * v + 3]);
-    }
-  } else {
-    const float sa = __ldg(p.sA + row);
-    uint16_t* orow = static_cast<uint16_t*>(p.out) + row * p.ldo;
-#pragma unroll
-    for (int v = 0; v < 16; ++v) {
-      const int64_t col = col0 + v * 8;
-      if (col < p.N) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float o0 = __fmul_rn(__fmul_rn(__int2float_rn(tot[v * 8 + 2 * e]), sa),
-                                     __ldg(p.sB + col + 2 * e));
-          const float o1 = __fmul_rn(__fmul_rn(__int2float_rn(tot[v * 8 + 2 * e + 1]), sa),
-                                     __ldg(p.sB + col + 2 * e + 1));
-          const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
-          w[e] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        *reinterpret_cast<uint4*>(orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-  }
+  for (int v = 0; v < 16; ++v) store_vec8(p, row, col0 + v * 8, sa, tot + v * 8);
 }
 
 // Drain one 128-column half of a chunk accumulator (this warp's 32 lanes)
@@ -155,12 +159,12 @@ __device__ __forceinline__ void store_rows(const GemmParams& p, int64_t row, int
 // integer below 2^24 in magnitude.
 __device__ __forceinline__ void drain_chunk(uint32_t taddr, int32_t (&tot)[128]) {
 #pragma unroll
-  for (int sub = 0; sub < 4; ++sub) {
-    uint32_t r[32];
-    ptx::tmem_ld_32cols(taddr + sub * 32, r);
+  for (int sub = 0; sub < 8; ++sub) {
+    uint32_t r[16];
+    ptx::tmem_ld_16cols(taddr + sub * 16, r);
     ptx::tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 32; ++i) tot[sub * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+    for (int i = 0; i < 16; ++i) tot[sub * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
   }
 }
 
@@ -351,11 +355,130 @@ __global__ void __launch_bounds__(kThreads, 1)
 // both CTAs' empty and accumulator-full barriers; the odd CTA's epilogue warps
 // arrive on the even CTA's accumulator-empty barrier.  K runs in exact
 // 1024-term chunks drained into int32 totals, as in the single-CTA kernel.
+//
+// Work split.  Data-parallel: pair p takes tiles p, p + P, ... (P pairs).
+// Stream-K (when the tiles do not fill the pairs evenly): the k-blocks of
+// all tiles, tile after tile, are cut into P equal contiguous ranges and pair
+// p takes range p, so a tile may be split between consecutive pairs.  A pair
+// that computed part of a tile stores its int32 totals for that part in its
+// own slot (two slots per pair: its first and its last fragment), then
+// counts itself in on the tile's counter; whichever contributor arrives last
+// adds the other contributors' totals to its own and writes the tile.  No
+// CTA waits for another: the last arrival finds every other part stored.
 constexpr int kPairStages = 6;
 constexpr int kPairABytes = 128 * kBK * 2;
 constexpr int kPairBBytes = 128 * kBK * 2;
 constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + kBarrierBytes;
+constexpr int kCasLimit = 4096;  // bound on the counter's compare-and-swap retries
+constexpr int kMaxSplit = 4;     // most parts a tile of the last wave is split into
+static_assert(static_cast<size_t>(kSplitTailMaxPairs) * 256 * 256 * 4 +
+                      kSplitTailMaxPairs * 2 * kEpiWarps * 8 <= kSplitTailScratchBytes,
+              "split-tail scratch layout");
+
+// The fragments (tile, k-blocks [kb0, kb1)) one pair computes, in order:
+// whole tiles pair, pair + P, ... below p.dp_tiles (P pairs), then, when
+// the last wave is split, unit `pair` of the tail: tile dp_tiles + pair / s,
+// k-part pair % s of s equal parts (pairs from tail * s on have no unit).
+struct FragIter {
+  int g;
+  bool tail_done;
+  __device__ FragIter(const GemmParams&, int pair) : g(pair), tail_done(false) {}
+  __device__ bool next(const GemmParams& p, int pair, int npairs, int& tile, int& kb0, int& kb1) {
+    if (g < p.dp_tiles) {
+      tile = g;
+      kb0 = 0;
+      kb1 = p.k_blocks;
+      g += npairs;
+      return true;
+    }
+    if (tail_done || pair >= p.sk_tail * p.sk_split) return false;
+    tail_done = true;
+    tile = p.dp_tiles + pair / p.sk_split;
+    const int j = pair % p.sk_split;
+    kb0 = j * p.k_blocks / p.sk_split;
+    kb1 = (j + 1) * p.k_blocks / p.sk_split;
+    return true;
+  }
+};
+
+// Counts one contributor in on a split tile's counter for this launch and
+// tells whether it was the last of n.  The counter holds the launch's epoch
+// in its high 40 bits and the count in the low 24; a word left by another
+// launch (or never written) carries another epoch and counts as 0, so the
+// counters need no clearing.  Returns -1 if the compare-and-swap kept failing.
+__device__ __forceinline__ int sk_arrive(unsigned long long* ctr, uint64_t epoch, int n) {
+  const unsigned long long tag = (epoch & 0xFFFFFFFFFFull) << 24;
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  for (int i = 0; i < kCasLimit; ++i) {
+    const unsigned long long cnt = (old & ~0xFFFFFFull) == tag ? (old & 0xFFFFFFull) : 0ull;
+    const unsigned long long seen = atomicCAS(ctr, old, tag | (cnt + 1ull));
+    if (seen == old) return static_cast<int>(cnt + 1ull) == n ? 1 : 0;
+    old = seen;
+  }
+  return -1;
+}
+
+// Epilogue of a tail unit (part of a split tile), per epilogue warp (32
+// tile rows x 128 columns) with its own counter.  A slot holds the pair's
+// 256 x 256 int32 totals warp-coalesced: vector v (columns 4v .. 4v+3 of the
+// lane's 128) of lane l of epilogue warp w of CTA r at int4 index
+// ((r * 8 + w) * 32 + v) * 32 + l, so each store or load instruction of a
+// warp moves 512 contiguous bytes.  The warp stores its totals, counts itself
+// in, and the last of the tile's s parts sums all s parts' totals (its own
+// read back) and stores the outputs.
+__device__ __forceinline__ const int4* sk_warp_slot(const GemmParams& p, int slot, int rank,
+                                                    int ewarp) {
+  return reinterpret_cast<const int4*>(p.partials + static_cast<size_t>(slot) * (256u * 256u)) +
+         (rank * kEpiWarps + ewarp) * 32 * 32 + (threadIdx.x & 31);
+}
+
+__device__ __forceinline__ void sk_store_part(const GemmParams& p, int pair, int rank, int ewarp,
+                                              const int32_t (&tot)[128]) {
+  int4* dst = const_cast<int4*>(sk_warp_slot(p, pair, rank, ewarp));
+#pragma unroll
+  for (int v = 0; v < 32; ++v)
+    __stcg(dst + v * 32, make_int4(tot[4 * v], tot[4 * v + 1], tot[4 * v + 2], tot[4 * v + 3]));
+  __threadfence();
+  __syncwarp();
+}
+
+__device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int ewarp, int tile,
+                                            int64_t row, int64_t col0, volatile int* abort) {
+  const int t = tile - p.dp_tiles;  // tail tile: parts come from pairs t*s .. t*s+s-1
+  int r = 0;
+  if ((threadIdx.x & 31) == 0)
+    r = sk_arrive(p.counters + (2 * t + rank) * kEpiWarps + ewarp, p.epoch, p.sk_split);
+  r = __shfl_sync(0xFFFFFFFFu, r, 0);
+  if (r < 0) {
+    if ((threadIdx.x & 31) == 0) raise_abort(abort, p.status);
+    return;
+  }
+  if (r == 0 || row >= p.M) return;
+  __threadfence();
+  const float sa = p.mode == 1 ? 0.0f : __ldg(p.sA + row);
+  // 32 columns at a time: each part's 8 vectors are loaded together
+  for (int h = 0; h < 4; ++h) {
+    int32_t acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0;
+    for (int j = 0; j < p.sk_split; ++j) {
+      const int4* src = sk_warp_slot(p, t * p.sk_split + j, rank, ewarp) + h * 8 * 32;
+      int4 x[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = __ldcg(src + i * 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        acc[4 * i] += x[i].x;
+        acc[4 * i + 1] += x[i].y;
+        acc[4 * i + 2] += x[i].z;
+        acc[4 * i + 3] += x[i].w;
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < 4; ++v) store_vec8(p, row, col0 + h * 32 + v * 8, sa, acc + v * 8);
+  }
+}
 
 template <bool kAmn, bool kBmn>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -407,7 +530,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int num_tiles = p.m_tiles * p.n_tiles;  // 256 x 256 tiles
   const uint64_t limit = p.wait_limit_ns;
 
   if (warp == 0) {
@@ -415,17 +537,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------ producer
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0u, armed_par = 0u;  // even CTA: stages whose full barrier it armed
-      bool ok = true;
-      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+      bool ok = true, first_load = true;
+      FragIter it(p, pair);
+      int tile, kb0, kb1;
+      while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
         const int m0 = (tile / p.n_tiles) * 256 + static_cast<int>(rank) * 128;
         const int n0 = (tile % p.n_tiles) * 256 + static_cast<int>(rank) * 128;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort, limit)) {
             ok = false;
             break;
           }
           armed &= ~(1u << stage);
-          const bool drop = p.drop_first_load && even && tile == pair && kb == 0;
+          const bool drop = p.drop_first_load && even && first_load;
+          first_load = false;
           if (!drop) {
             const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);
             if (even) {
@@ -454,8 +579,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = ptx::idesc_f16_f32(256, 256, kAmn, kBmn);
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true;
-      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-        for (int kb0 = 0; kb0 < p.k_blocks && ok; kb0 += kChunkBlocks) {
+      FragIter it(p, pair);
+      int tile, kb0, kb1;
+      while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
+        for (int kc = kb0; kc < kb1 && ok; kc += kChunkBlocks) {
           const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
           if (!ptx::mbar_wait_bounded(tempty_bar(buf), aph ^ 1u, abort, limit)) {
             ok = false;
@@ -463,8 +590,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * kBN;
-          const int kb_end = min(kb0 + kChunkBlocks, p.k_blocks);
-          for (int kb = kb0; kb < kb_end; ++kb) {
+          const int kc_end = min(kc + kChunkBlocks, kb1);
+          for (int kb = kc; kb < kc_end; ++kb) {
             if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort, limit)) {
               ok = false;
               break;
@@ -475,7 +602,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
               ptx::mma_f16_pair(d_tmem, adesc + k_step<kAmn>() * kk, bdesc + k_step<kBmn>() * kk,
-                                idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                                idesc, (kb > kc || kk > 0) ? 1u : 0u);
             ptx::mma_commit_pair(empty_bar(stage), 0x3);
             if (++stage == kPairStages) {
               stage = 0;
@@ -497,13 +624,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;
     uint32_t chunk = 0;
     bool ok = true;
-    for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+    FragIter it(p, pair);
+    int tile, kb0, kb1;
+    while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
       const int m0 = (tile / p.n_tiles) * 256 + static_cast<int>(rank) * 128;
       const int n0 = (tile % p.n_tiles) * 256;
       int32_t tot[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) tot[i] = 0;
-      for (int kb0 = 0; kb0 < p.k_blocks; kb0 += kChunkBlocks) {
+      for (int kc = kb0; kc < kb1; kc += kChunkBlocks) {
         const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
         int got = 1;
         if (lane == 0) got = ptx::mbar_wait_bounded(tfull_bar(buf), aph, abort, limit) ? 1 : 0;
@@ -522,8 +651,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++chunk;
       }
       if (!ok) break;
-      store_rows(p, static_cast<int64_t>(m0) + quad * 32 + lane,
-                 static_cast<int64_t>(n0) + half * 128, tot);
+      const int64_t row = static_cast<int64_t>(m0) + quad * 32 + lane;
+      const int64_t col0 = static_cast<int64_t>(n0) + half * 128;
+      if (kb0 == 0 && kb1 == p.k_blocks) {
+        store_rows(p, row, col0, tot);
+      } else {
+        sk_store_part(p, pair, static_cast<int>(rank), warp - 2, tot);
+        sk_complete(p, static_cast<int>(rank), warp - 2, tile, row, col0, abort);
+      }
     }
     if (!ok && lane == 0) raise_abort(abort, p.status);
   }
@@ -567,6 +702,20 @@ cudaError_t set_smem_attrs() {
   return err;
 }
 
+// Launch epochs for the split-tail counters: 40 bits, never 0, distinct for
+// 2^40 launches of the process.
+uint64_t next_epoch() {
+  static std::atomic<uint64_t> ctr{0};
+  static const uint64_t base = [] {
+    uint64_t x = static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count());
+    x ^= reinterpret_cast<uintptr_t>(&ctr);
+    x *= 0x9E3779B97F4A7C15ull;
+    return x >> 24;
+  }();
+  uint64_t e = (base + ctr.fetch_add(1)) & 0xFFFFFFFFFFull;
+  return e == 0 ? 1 : e;
+}
+
 template <bool kAmn, bool kBmn>
 void launch_kernel(bool pair, int grid, const CUtensorMap& mapA, const CUtensorMap& mapB,
                    const GemmParams& p, cudaStream_t stream) {
@@ -580,7 +729,7 @@ void launch_kernel(bool pair, int grid, const CUtensorMap& mapA, const CUtensorM
 
 cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B, bool b_mn,
                         const float* sB, int64_t M, int64_t N, int64_t K, GemmOut mode, void* out,
-                        int64_t ldo, const DeviceInfo& dev, const GemmDebug& dbg,
+                        int64_t ldo, void* scratch, const DeviceInfo& dev, const GemmDebug& dbg,
                         cudaStream_t stream) {
   if (a_mn && !b_mn) return cudaErrorInvalidValue;  // no layout of the API needs it
   static std::mutex mu;
@@ -623,9 +772,38 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   p.status = dev.status_word;
   p.wait_limit_ns = dbg.wait_limit_ns;
   p.drop_first_load = dbg.drop_first_load;
+  p.dp_tiles = static_cast<int>(p.m_tiles) * p.n_tiles;
+  p.sk_tail = 0;
+  p.sk_split = 1;
+  p.partials = nullptr;
+  p.counters = nullptr;
+  p.epoch = 0;
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   const int64_t slots = pair ? dev.sms / 2 : dev.sms;
-  const int grid = static_cast<int>((pair ? 2 : 1) * (tiles < slots ? tiles : slots));
+  int grid = static_cast<int>((pair ? 2 : 1) * (tiles < slots ? tiles : slots));
+  if (pair && scratch && !dbg.no_split_tail) {
+    // the R tiles of a partial last wave split into s = min(P / R, 4)
+    // k-parts each (P pairs): the wave then takes 1/s of a tile's time
+    // instead of a whole one
+    const int64_t npairs = slots < kSplitTailMaxPairs ? slots : kSplitTailMaxPairs;
+    const int64_t tail = tiles % npairs;
+    int64_t split = tail > 0 ? npairs / tail : 0;
+    if (split > kMaxSplit) split = kMaxSplit;  // the last part reads all parts back
+    if (split > p.k_blocks) split = p.k_blocks;
+    // worth it when the wave shrinks by at least 32 k-blocks of MMA time,
+    // about what storing and summing the parts costs (~10 us on GB300)
+    const bool worth = split >= 2 && (split - 1) * p.k_blocks >= 32 * split;
+    if (tail > 0 && worth) {
+      p.dp_tiles = static_cast<int>(tiles - tail);
+      p.sk_tail = static_cast<int>(tail);
+      p.sk_split = static_cast<int>(split);
+      p.partials = static_cast<int32_t*>(scratch);
+      p.counters = reinterpret_cast<unsigned long long*>(static_cast<char*>(scratch) +
+                                                         kSplitTailMaxPairs * 256 * 256 * 4);
+      p.epoch = next_epoch();
+      grid = static_cast<int>(2 * npairs);
+    }
+  }
   if (!a_mn && !b_mn)
     launch_kernel<false, false>(pair, grid, mapA, mapB, p, stream);
   else if (!a_mn)

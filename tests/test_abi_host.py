@@ -101,6 +101,20 @@ def test_matmul_host_validation(lib):
     assert _mm(lib, 0, 8, 16, A=0, B=0, out=0) == m.INT8MP_OK             # empty
 
 
+def test_matmul_workspace_host_validation(lib):
+    need = m.int8mp_mm_workspace_size()
+    assert need >= 76 * 256 * 256 * 4                                     # an int32 tile per SM pair
+    f = lib.int8mp_mm_s32_ws
+    assert f(P(16), P(16), 8, 8, 16, 0, 1, P(16), 8, P(128), need, None) == m.INT8MP_ERR_ALIGNMENT
+    assert f(P(16), P(16), 8, 8, 16, 0, 1, P(256), 8, P(256), need - 1, None) == \
+        m.INT8MP_ERR_WORKSPACE
+    g = lib.int8mp_scaled_mm_ws
+    assert g(P(16), P(16), P(16), P(16), 8, 8, 16, 0, 1, P(16), 8, P(256), 16, None) == \
+        m.INT8MP_ERR_WORKSPACE
+    assert g(P(16), P(16), P(16), P(16), 8, 8, 16, 0, 0, P(16), 8, P(256), need, None) == \
+        m.INT8MP_ERR_INVALID_ARG                                          # codes must be f16
+
+
 def test_linear_host_validation(lib):
     cfg = m.linear_cfg()
     ref = ctypes.byref(cfg)
@@ -115,7 +129,7 @@ def test_linear_host_validation(lib):
     assert lib.int8mp_linear_fwd_noalloc(P(16), P(16), P(16), 32, 32, 32, ctypes.byref(bf16_fwd),
                                          None) == m.INT8MP_ERR_INVALID_ARG
     need = m.int8mp_linear_workspace_size(32, 48, 64, cfg)
-    assert need >= 2 * (32 * 64 + 48 * 64) and need % 256 == 0
+    assert need >= 2 * (32 * 64 + 48 * 64) + m.int8mp_mm_workspace_size() and need % 256 == 0
     assert m.int8mp_linear_workspace_size(32, 48, 24, cfg) == 0
 
 

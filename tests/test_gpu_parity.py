@@ -262,6 +262,67 @@ def test_mm_s32_mn_major_large_sums_exact(layout):
     np.testing.assert_array_equal(acc, oracle.mm_s32(a.numpy(), b.numpy(), M, N, K))
 
 
+# Split last wave: with a workspace, the CTA-pair kernel splits the R tiles
+# of a partial last wave into s = min(pairs / R, 4) k-parts each, added as
+# int32 totals: one tile of K = 8192, 80 tiles (4 left over: 4 parts of 16
+# to 33 k-blocks), 90 tiles (14 left, 4 parts), 12 tiles (4 parts); 64
+# tiles on 76 pairs are left whole.
+SPLIT_TAIL_SHAPES = [(256, 256, 8192, m.INT8MP_AxBT), (2048, 2048, 8192, m.INT8MP_AxBT),
+                  (2560, 2048, 4096, m.INT8MP_AxBT), (2312, 2056, 8192, m.INT8MP_AxB),
+                  (2312, 1800, 8256, m.INT8MP_ATxB), (768, 776, 16384, m.INT8MP_ATxB)]
+
+
+def _stored(codes, layout, which, M, N, K, seed):
+    """Random codes for operand `which` stored as `layout` wants."""
+    if which == "A":
+        return _rand_codes(K, M, seed) if layout == m.INT8MP_ATxB else _rand_codes(M, K, seed)
+    return _rand_codes(N, K, seed) if layout == m.INT8MP_AxBT else _rand_codes(K, N, seed)
+
+
+@pytest.mark.parametrize("shape", SPLIT_TAIL_SHAPES)
+def test_mm_s32_split_tail_bit_exact(shape):
+    M, N, K, layout = shape
+    a = _stored(None, layout, "A", M, N, K, 21)
+    b = _stored(None, layout, "B", M, N, K, 22)
+    ad, bd = _dev(a.half()), _dev(b.half())
+    ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=DEV)
+    acc = m.int8mp_mm_s32(ad, bd, layout=layout, workspace=ws)
+    acc2 = m.int8mp_mm_s32(ad, bd, layout=layout, workspace=ws)  # the scratch is reusable as is
+    plain = m.int8mp_mm_s32(ad, bd, layout=layout)
+    assert m.int8mp_poll_device_status() == m.INT8MP_OK
+    assert torch.equal(acc, acc2) and torch.equal(acc, plain)
+    ref = oracle.mm_s32(a.numpy(), b.numpy(), M, N, K, layout=layout)
+    np.testing.assert_array_equal(acc.cpu().numpy(), ref)
+
+
+def test_mm_s32_split_tail_extreme_sums():
+    # +-127 everywhere with K = 16384, 4 tiles split 4 ways: every part and
+    # the total stay exact
+    M, N, K = 512, 512, 16384
+    a = _rand_codes(M, K, 23, extreme=True)
+    b = _rand_codes(N, K, 24, extreme=True)
+    b[0] = a[0]
+    b[300] = -a[300]
+    acc = m.int8mp_mm_s32(_dev(a.half()), _dev(b.half()), workspace=True).cpu().numpy()
+    assert acc[0, 0] == 127 * 127 * K and acc[300, 300] == -127 * 127 * K
+    np.testing.assert_array_equal(acc, oracle.mm_s32(a.numpy(), b.numpy(), M, N, K))
+
+
+def test_scaled_mm_split_tail_bit_exact():
+    M, N, K = 2048, 2312, 4096
+    A = synth.bf16_normal((M, K), 31, outlier_frac=0.01, outlier_scale=20.0)
+    B = synth.bf16_normal((N, K), 32, outlier_frac=0.01, outlier_scale=20.0)
+    qa, sa = m.int8mp_quantize_rowwise(_dev(A), axis=0, codes=m.INT8MP_CODES_F16)
+    qb, sb = m.int8mp_quantize_rowwise(_dev(B), axis=0, codes=m.INT8MP_CODES_F16)
+    out = m.int8mp_scaled_mm(qa, sa, qb, sb, workspace=True)
+    plain = m.int8mp_scaled_mm(qa, sa, qb, sb)
+    assert torch.equal(out.view(torch.int16), plain.view(torch.int16))
+    qar, sar = oracle.quantize(bf16_bits(A), axis=0)
+    qbr, sbr = oracle.quantize(bf16_bits(B), axis=0)
+    ref = oracle.scaled_mm(qar, sar, qbr, sbr, M, N, K)
+    assert_bf16_equal(out, ref, "scaled_mm split tail")
+
+
 @pytest.mark.parametrize("shape", [(256, 256, 512), (200, 264, 144), (384, 512, 2048)])
 def test_scaled_mm_bit_exact(shape):
     M, N, K = shape
