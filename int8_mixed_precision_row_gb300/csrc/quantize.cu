@@ -186,13 +186,15 @@ __device__ __forceinline__ void colmax_acc(uint4& m, const uint4& v) {
   m.w = __vmaxu2(m.w, v.w & 0x7FFF7FFFu);
 }
 
+constexpr int kMaxSlots = 4;
+
 template <typename CodeT, bool SR, bool kColMax>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, CodeT* __restrict__ q,
-    float* __restrict__ scale, SrArgs sr, uint32_t slot_bytes, int T, unsigned int* status,
+    float* __restrict__ scale, SrArgs sr, uint32_t slot_bytes, int T, int S, unsigned int* status,
     uint64_t limit_ns, unsigned int* __restrict__ colmax) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t bars[kThreads / 32][2];
+  __shared__ uint64_t bars[kThreads / 32][kMaxSlots];
   __shared__ float red[kThreads / 32];
   __shared__ int got_row[kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -201,23 +203,22 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
   const bool leader = wt == 0 && lane == 0;
   const uint32_t row_bytes = static_cast<uint32_t>(cols) * 2u;
   const int nvec = static_cast<int>(cols >> 3);
-  const uint8_t* slots = smem + static_cast<size_t>(team) * 2 * slot_bytes;
+  const uint8_t* slots = smem + static_cast<size_t>(team) * S * slot_bytes;
   const uint32_t slot_addr = ptx::smem_addr(slots);
-  const uint32_t bar[2] = {ptx::smem_addr(&bars[team][0]), ptx::smem_addr(&bars[team][1])};
+  const uint32_t bar0 = ptx::smem_addr(&bars[team][0]);  // slot k's barrier: bar0 + 8k
   const int64_t g = static_cast<int64_t>(blockIdx.x) * teams + team;
   const int64_t n = static_cast<int64_t>(gridDim.x) * teams;
   using P = Pack8<CodeT>;
 
   uint32_t pending = 0u, pend_par = 0u;  // leader: copies in flight per slot, their parity
   if (leader) {
-    ptx::mbar_init(bar[0], 1);
-    ptx::mbar_init(bar[1], 1);
+    for (int k = 0; k < S; ++k) ptx::mbar_init(bar0 + 8u * k, 1);
     ptx::fence_mbar_init();
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < S; ++k) {
       const int64_t r = g + k * n;
       if (r < rows) {
-        ptx::mbar_arrive_expect_tx(bar[k], row_bytes);
-        ptx::bulk_load(slot_addr + k * slot_bytes, x + r * ld, row_bytes, bar[k]);
+        ptx::mbar_arrive_expect_tx(bar0 + 8u * k, row_bytes);
+        ptx::bulk_load(slot_addr + k * slot_bytes, x + r * ld, row_bytes, bar0 + 8u * k);
         pending |= 1u << k;
       }
     }
@@ -226,27 +227,34 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
   uint4 cm[kColMax ? kColVecs : 1];
 #pragma unroll
   for (int k = 0; k < (kColMax ? kColVecs : 1); ++k) cm[k] = make_uint4(0u, 0u, 0u, 0u);
-  int it = 0;
+  // row it of the team sits in slot it % S; its wait parity is (it / S) & 1
+  int it = 0, b = 0;
+  uint32_t phase = 0u;
   for (int64_t r = g; r < rows; r += n, ++it) {
-    const int b = it & 1;
     if (leader) {
-      const bool ok = ptx::mbar_wait_timeout(bar[b], (it >> 1) & 1, limit_ns);
+      const bool ok = ptx::mbar_wait_timeout(bar0 + 8u * b, phase, limit_ns);
       got_row[team] = ok ? 1 : 0;
       if (ok) pending &= ~(1u << b);
       else atomicOr(status, 1u);
     }
     team_sync(team, T);  // the row has landed; every warp has left row it-1
     if (!got_row[team]) break;
-    if (leader && it >= 1 && r + n < rows) {
-      // slot (it+1)&1 held row it-1, which every warp of the team has left
-      const int nb = (it + 1) & 1;
+    if (leader && it >= 1 && r + (S - 1) * n < rows) {
+      // row it+S-1 goes to the slot of row it-1, which every warp has left
+      const int nb = b == 0 ? S - 1 : b - 1;
+      const int j = it + S - 1;
       ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive_expect_tx(bar[nb], row_bytes);
-      ptx::bulk_load(slot_addr + nb * slot_bytes, x + (r + n) * ld, row_bytes, bar[nb]);
+      ptx::mbar_arrive_expect_tx(bar0 + 8u * nb, row_bytes);
+      ptx::bulk_load(slot_addr + nb * slot_bytes, x + (r + (S - 1) * n) * ld, row_bytes,
+                     bar0 + 8u * nb);
       pending |= 1u << nb;
-      pend_par = (pend_par & ~(1u << nb)) | (static_cast<uint32_t>(((it + 1) >> 1) & 1) << nb);
+      pend_par = (pend_par & ~(1u << nb)) | (static_cast<uint32_t>((j / S) & 1) << nb);
     }
     const uint4* rowv = reinterpret_cast<const uint4*>(slots + b * slot_bytes);
+    if (++b == S) {
+      b = 0;
+      phase ^= 1u;
+    }
     float amax = 0.0f;
     if (kColMax) {
 #pragma unroll
@@ -287,9 +295,9 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
   // after a timeout: never leave a copy in flight into this block's memory
   bool copies_done = true;
   if (leader) {
-    for (int k = 0; k < 2; ++k)
+    for (int k = 0; k < S; ++k)
       if (pending & (1u << k))
-        if (!ptx::mbar_wait_timeout(bar[k], (pend_par >> k) & 1u, limit_ns)) {
+        if (!ptx::mbar_wait_timeout(bar0 + 8u * k, (pend_par >> k) & 1u, limit_ns)) {
           atomicOr(status, 1u);
           copies_done = false;
         }
@@ -303,7 +311,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     if (leader && !copies_done) all_done = 0;
     __syncthreads();
     if (!all_done) return;  // a copy may still land in the slots: leave them alone
-    uint4* mine = reinterpret_cast<uint4*>(smem + static_cast<size_t>(team) * 2 * slot_bytes);
+    uint4* mine = reinterpret_cast<uint4*>(smem + static_cast<size_t>(team) * S * slot_bytes);
 #pragma unroll
     for (int k = 0; k < kColVecs; ++k) {
       const int v = first + k * step;
@@ -311,7 +319,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     }
     __syncthreads();
     const uint16_t* all = reinterpret_cast<const uint16_t*>(smem);
-    const size_t team_stride = static_cast<size_t>(slot_bytes);  // in uint16: 2 slots of bytes / 2
+    const size_t team_stride = static_cast<size_t>(S) * slot_bytes / 2;  // in uint16
     for (int c = threadIdx.x; c < cols; c += kThreads) {
       uint32_t mx = 0u;
       for (int t = 0; t < teams; ++t) mx = max(mx, static_cast<uint32_t>(all[t * team_stride + c]));
@@ -746,13 +754,30 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
     if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, sms, stream);
     return e;
   }
-  // 8 warps per block in teams of T: the smallest T whose slots (two per
-  // team) fit in 72 KB, so that at least three blocks share an SM
+  // 8 warps per block in teams of T, each team with a ring of S row slots
+  // (S - 1 rows in flight while it works on one).  Shared memory per block:
+  // 72 KB, so that three blocks share an SM, or 108 KB for the variant that
+  // also keeps column maxima (its registers allow two blocks per SM).  T is
+  // the smallest whose two slots per team fit (and, for the column maxima,
+  // whose threads' share of a row fits their registers); S fills the rest.
+  const int warps = kThreads / 32;
+  const size_t budget = cmx ? 108u * 1024u : 72u * 1024u;
   int T = 1;
-  while (T < 8 && static_cast<size_t>(kThreads / 32 / T) * 2 * slot > 72u * 1024u) T <<= 1;
-  const size_t smem = static_cast<size_t>(kThreads / 32 / T) * 2 * slot;
-  const bool fused = cmx && (cols >> 3) <= static_cast<int64_t>(kColVecs) * 32 * T;
-  const int64_t teams = kThreads / 32 / T;
+  while (T < 8 && (static_cast<size_t>(warps / T) * 2 * slot > budget ||
+                   (cmx && (cols >> 3) > static_cast<int64_t>(kColVecs) * 32 * T)))
+    T <<= 1;
+  const bool fused = cmx && (cols >> 3) <= static_cast<int64_t>(kColVecs) * 32 * T &&
+                     static_cast<size_t>(warps / T) * 2 * slot <= budget;
+  if (cmx && !fused) {  // the plain ring and a separate column pass
+    T = 1;
+    while (T < 8 && static_cast<size_t>(warps / T) * 2 * slot > 72u * 1024u) T <<= 1;
+  }
+  const size_t team_bytes = static_cast<size_t>(warps / T) * slot;
+  int S = static_cast<int>((fused ? budget : 72u * 1024u) / team_bytes);
+  if (S > kMaxSlots) S = kMaxSlots;
+  if (S < 2) S = 2;
+  const size_t smem = team_bytes * S;
+  const int64_t teams = warps / T;
   const int64_t need = (rows + teams - 1) / teams;
   cudaError_t e;
   if (fused) {
@@ -763,7 +788,7 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
     const int64_t cap = static_cast<int64_t>(sms) * occ;
     const unsigned blocks = static_cast<unsigned>(need < cap ? need : cap);
     quant_rows_kernel<CodeT, SR, true><<<blocks, kThreads, smem, stream>>>(
-        xp, rows, cols, ld, qp, scale, sr, slot, T, dev.status_word, kWaitLimitNs, cmx);
+        xp, rows, cols, ld, qp, scale, sr, slot, T, S, dev.status_word, kWaitLimitNs, cmx);
     return cudaGetLastError();
   }
   static bool attr[64] = {};
@@ -773,7 +798,7 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   const int64_t cap = static_cast<int64_t>(sms) * occ;
   const unsigned blocks = static_cast<unsigned>(need < cap ? need : cap);
   quant_rows_kernel<CodeT, SR, false><<<blocks, kThreads, smem, stream>>>(
-      xp, rows, cols, ld, qp, scale, sr, slot, T, dev.status_word, kWaitLimitNs, nullptr);
+      xp, rows, cols, ld, qp, scale, sr, slot, T, S, dev.status_word, kWaitLimitNs, nullptr);
   e = cudaGetLastError();
   if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, sms, stream);
   return e;
