@@ -205,6 +205,8 @@ class LayerStep:
         # the matmuls' scratch for splitting their last wave of tiles
         self.mm_ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
         self.flops = 6.0 * T * sum(l["N"] * l["K"] for l in self.linears)
+        # GEMM operands read once (f16 codes) and bf16 outputs written, per step
+        self.gemm_bytes = 6.0 * sum(T * l["K"] + T * l["N"] + l["N"] * l["K"] for l in self.linears)
         self.gemms_per_step = 3 * len(self.linears)
         # kernels of this library per step and linear: three row quantizations
         # (each also recording column absmax), three column quantizations
@@ -465,6 +467,27 @@ def pass_switch_table(spec, device, steps=5, warmup=2):
 
 
 # -------------------------------------------------------------------- main
+# DRAM traffic of the dominant kernel (gemm_s8f16_pair_kernel), per launch,
+# averaged over the 21 launches of one step of this workload:
+# dram__bytes_read.sum + dram__bytes_write.sum from one ncu launch list of
+# `python bench.py --steps 2 --warmup 3 --profile-steps` (one pass per
+# launch), valid for the GEMM sources whose digest is given (reported as null
+# once they change).
+GEMM_TRAFFIC = {"bytes_per_launch": 424975492, "sources_sha256_16": "1ace9ae47c77db10"}
+GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "common.cuh")
+
+
+def gemm_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "int8_mixed_precision_row_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != GEMM_TRAFFIC["sources_sha256_16"]:
+        return None
+    return GEMM_TRAFFIC["bytes_per_launch"]
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -551,7 +574,10 @@ def main():
         "roofline": {"bound": "tensor",
                      "kernel": "gemm_s8f16_pair_kernel (CTA-pair tcgen05 kind::f16, exact int32)",
                      "achieved": round(gemm_tflops, 1), "peak": bf16_sust, "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / bf16_sust, 3), "traffic": None,
+                     "frac": round(gemm_tflops / bf16_sust, 3),
+                     "traffic": gemm_traffic() if step.T == spec["T"] and not only else None,
+                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
+                     "algorithmic_bytes": round(step.gemm_bytes / step.gemms_per_step),
                      "peak_source": f"{peak_src} dense bf16 sustained (f16 runs at the bf16 rate); "
                                     f"burst {bf16_burst} TFLOP/s -> frac "
                                     f"{round(gemm_tflops / bf16_burst, 3)}",
