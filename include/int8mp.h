@@ -76,7 +76,8 @@ typedef enum {
 
 /* Storage of INT8 codes.  INT8MP_CODES_S8: one int8_t per code.
  * INT8MP_CODES_F16: one IEEE binary16 per code holding the same integer
- * exactly; this is the container the tensor-core GEMM reads directly. */
+ * exactly (a zero code may be stored as -0); this is the container the
+ * tensor-core GEMM reads directly. */
 typedef enum { INT8MP_CODES_S8 = 0, INT8MP_CODES_F16 = 1 } int8mp_codes;
 
 /* Stochastic-rounding stream ids used by the linear entry points, one per

@@ -57,6 +57,17 @@ int8mp_status current_device(DeviceInfo* info) {
   return st.status;
 }
 
+// The device's info with the SM count of `stream`'s partition: kernels
+// launched on a green-context stream see only that context's SMs, and the
+// persistent grids are sized for them.
+int8mp_status current_device(DeviceInfo* info, cudaStream_t stream) {
+  const int8mp_status st = current_device(info);
+  if (st != INT8MP_OK) return st;
+  const int part = int8mp::stream_sm_count(stream);
+  if (part > 0 && part < info->sms) info->sms = part;
+  return INT8MP_OK;
+}
+
 inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
@@ -117,7 +128,7 @@ int8mp_status run_mm(const void* A, const float* sA, const void* B, const float*
                      cudaStream_t stream) {
   if (M == 0 || N == 0) return INT8MP_OK;
   DeviceInfo dev;
-  int8mp_status st = current_device(&dev);
+  int8mp_status st = current_device(&dev, stream);
   if (st != INT8MP_OK) return st;
   const size_t esize = mode == int8mp::GemmOut::kS32 ? 4 : 2;
   if (K == 0)  // empty contraction: every accumulator is 0, and so is 0 * sA * sB
@@ -219,7 +230,7 @@ int8mp_status int8mp_quantize_rowwise(const void* x, int64_t rows, int64_t cols,
   int8mp_status st = check_quantize(x, rows, cols, ld, axis, mode, q, codes, scale);
   if (st != INT8MP_OK || rows == 0 || cols == 0) return st;
   DeviceInfo dev;
-  st = current_device(&dev);
+  st = current_device(&dev, as_stream(stream));
   if (st != INT8MP_OK) return st;
   const int8mp::SrArgs sr{seed, offset, stream_id};
   cudaError_t e = axis == 0
@@ -239,7 +250,7 @@ int8mp_status int8mp_quantize_rows_colmax(const void* x, int64_t rows, int64_t c
   if (!colmax) return INT8MP_ERR_INVALID_ARG;
   if (!aligned(colmax, 4)) return INT8MP_ERR_ALIGNMENT;
   DeviceInfo dev;
-  st = current_device(&dev);
+  st = current_device(&dev, as_stream(stream));
   if (st != INT8MP_OK) return st;
   const int8mp::SrArgs sr{seed, offset, stream_id};
   return from_cuda(int8mp::launch_quantize_rows(x, rows, cols, ld, mode, sr, q, codes, scale,
@@ -255,7 +266,7 @@ int8mp_status int8mp_quantize_cols_absmax(const void* x, int64_t rows, int64_t c
   if (!colmax) return INT8MP_ERR_INVALID_ARG;
   if (!aligned(colmax, 4)) return INT8MP_ERR_ALIGNMENT;
   DeviceInfo dev;
-  st = current_device(&dev);
+  st = current_device(&dev, as_stream(stream));
   if (st != INT8MP_OK) return st;
   const int8mp::SrArgs sr{seed, offset, stream_id};
   return from_cuda(int8mp::launch_quantize_cols_from_absmax(x, rows, cols, ld, colmax, mode, sr,
@@ -335,7 +346,7 @@ int8mp_status linear_fwd_impl(const void* X, const void* W, void* Y, int64_t T, 
     return INT8MP_ERR_ALIGNMENT;
   if (ws_bytes < fwd_bytes(T, N, K)) return INT8MP_ERR_WORKSPACE;
   DeviceInfo dev;
-  st = current_device(&dev);
+  st = current_device(&dev, as_stream(stream));
   if (st != INT8MP_OK) return st;
   cudaStream_t s = as_stream(stream);
   if (save_absmax && K > 0 &&
@@ -387,7 +398,7 @@ int8mp_status linear_bwd_impl(const void* dY, const void* X, const void* W, void
     return INT8MP_ERR_ALIGNMENT;
   if (ws_bytes < bwd_bytes(T, N, K)) return INT8MP_ERR_WORKSPACE;
   DeviceInfo dev;
-  st = current_device(&dev);
+  st = current_device(&dev, as_stream(stream));
   if (st != INT8MP_OK) return st;
   cudaStream_t s = as_stream(stream);
   Carver c{static_cast<char*>(workspace)};

@@ -28,6 +28,11 @@ struct SrArgs {
 // %globaltimer.  Long enough that no healthy wait reaches it.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// ---- driver entry points (tma.cu) ------------------------------------------
+// SMs of the green context (SM partition) `stream` belongs to; 0 if it
+// belongs to none (then the device's count applies).
+int stream_sm_count(cudaStream_t stream);
+
 // ---- TMA tensor maps (tma.cu) -----------------------------------------------
 // Row-major [rows, cols] matrix of `esize`-byte elements, row stride ld
 // elements; boxes of box_rows x box_cols; zero fill outside the matrix.

@@ -34,6 +34,7 @@
 #include <cuda_fp16.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "divide.cuh"
@@ -47,6 +48,21 @@ constexpr int kThreads = 256;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// |v| of eight bf16 values, bit patterns still packed two per word
+__device__ __forceinline__ uint4 abs_bits8(const uint4& v) {
+  return make_uint4(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
+}
+// Running max of |bf16| kept as a packed pair: non-negative bf16 bit
+// patterns order as unsigned integers, so a per-halfword unsigned max is the
+// max (one instruction per two values).
+__device__ __forceinline__ uint32_t absmax8_bits(uint32_t m2, const uint4& a) {
+  return __vmaxu2(m2, __vmaxu2(__vmaxu2(a.x, a.y), __vmaxu2(a.z, a.w)));
+}
+// the float value of the larger half of a packed pair (bf16 bits shifted up)
+__device__ __forceinline__ float unpack_max(uint32_t m2) {
+  return __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+}
 
 // max(m, |v_0|, ..., |v_7|) as a tree: a dependency depth of 4, not 8
 __device__ __forceinline__ float absmax8(float m, const uint4& v) {
@@ -64,21 +80,20 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
-// Code from an exact quotient v: an exact float in [-127, 127], never -0.
+// Code from an exact quotient v: an exact float in [-127, 127] (a zero code
+// may come out as -0; both containers hold the integer 0 for it).
 __device__ __forceinline__ float code_rne(float v) {
-  return __fadd_rn(fminf(fmaxf(rintf(v), -127.0f), 127.0f), 0.0f);
+  return fminf(fmaxf(rintf(v), -127.0f), 127.0f);
 }
 // Same when the group scale is a normal number s = RN(absmax / 127): then
 // s >= (absmax / 127)(1 - 2^-24), so |v| <= 127 (1 + 2^-23) < 127.5 and
 // rounding cannot leave [-127, 127]; the clamp is dropped.
-__device__ __forceinline__ float code_rne_normal_scale(float v) {
-  return __fadd_rn(rintf(v), 0.0f);
-}
+__device__ __forceinline__ float code_rne_normal_scale(float v) { return rintf(v); }
 __device__ __forceinline__ float code_sr(float v, uint32_t word) {
   const float f = floorf(v);
   const float fr = __fsub_rn(v, f);
   const float q = (sr_uniform(word) < fr) ? __fadd_rn(f, 1.0f) : f;
-  return __fadd_rn(fminf(fmaxf(q, -127.0f), 127.0f), 0.0f);
+  return fminf(fmaxf(q, -127.0f), 127.0f);
 }
 
 // Eight codes from eight quotients (elements n0 .. n0+7 of the SR stream).
@@ -99,6 +114,20 @@ __device__ __forceinline__ void codes_of(const float (&v)[8], const SrArgs& sr, 
     for (int i = 0; i < 8; ++i) c[i] = code_rne(v[i]);
   }
 }
+
+// eight f16 codes (one uint4) clamped to [-127, 127]
+__device__ __forceinline__ uint4 clamp_half8(uint4 v) {
+  const __half2 lo = __float2half2_rn(-127.0f), hi = __float2half2_rn(127.0f);
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+    h = __hmin2(__hmax2(h, lo), hi);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ uint2 clamp_half8(uint2 v) { return v; }  // int8 codes: clamped before
 
 template <typename CodeT>
 struct Pack8;
@@ -179,11 +208,11 @@ __device__ __forceinline__ void quantize_two(const uint4& a, const uint4& b, boo
 // bit pattern (the bf16 bits shifted up: the same value).
 constexpr int kColVecs = 8;
 
-__device__ __forceinline__ void colmax_acc(uint4& m, const uint4& v) {
-  m.x = __vmaxu2(m.x, v.x & 0x7FFF7FFFu);
-  m.y = __vmaxu2(m.y, v.y & 0x7FFF7FFFu);
-  m.z = __vmaxu2(m.z, v.z & 0x7FFF7FFFu);
-  m.w = __vmaxu2(m.w, v.w & 0x7FFF7FFFu);
+__device__ __forceinline__ void colmax_acc(uint4& m, const uint4& a) {  // a = abs_bits8(v)
+  m.x = __vmaxu2(m.x, a.x);
+  m.y = __vmaxu2(m.y, a.y);
+  m.z = __vmaxu2(m.z, a.z);
+  m.w = __vmaxu2(m.w, a.w);
 }
 
 constexpr int kMaxSlots = 4;
@@ -255,20 +284,21 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
       b = 0;
       phase ^= 1u;
     }
-    float amax = 0.0f;
+    uint32_t am2 = 0u;  // packed pair of |x| maxima
     if (kColMax) {
 #pragma unroll
       for (int k = 0; k < kColVecs; ++k) {
         const int v = first + k * step;
         if (v < nvec) {
-          const uint4 xv = rowv[v];
-          amax = absmax8(amax, xv);
-          colmax_acc(cm[k], xv);
+          const uint4 a = abs_bits8(rowv[v]);
+          am2 = absmax8_bits(am2, a);
+          colmax_acc(cm[k], a);
         }
       }
     } else {
-      for (int v = first; v < nvec; v += step) amax = absmax8(amax, rowv[v]);
+      for (int v = first; v < nvec; v += step) am2 = absmax8_bits(am2, abs_bits8(rowv[v]));
     }
+    float amax = unpack_max(am2);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     if (T > 1) {
@@ -443,13 +473,17 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
   const int64_t c = vi * 8;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_block;
   const int64_t r1 = min(rows, r0 + rows_per_block);
+  // f16 codes from a given absmax keep their clamp as a packed half2 min/max
+  // after rounding (a caller's absmax below the true one would otherwise let
+  // a code leave [-127, 127]); int8 codes from it clamp before packing
+  constexpr bool kHalfClamp = kFromAbsmax && !SR && std::is_same<CodeT, __half>::value;
   float s[8], r[8];
-  bool all_fast = true, normal = !kFromAbsmax;
+  bool all_fast = true, normal = !kFromAbsmax || kHalfClamp;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     s[j] = kFromAbsmax ? __fdiv_rn(__ldg(in + c + j), 127.0f) : __ldg(in + c + j);
     all_fast = all_fast && scale_is_fast(s[j]);
-    if (!kFromAbsmax) normal = normal && scale_is_normal(s[j]);
+    normal = normal && scale_is_normal(s[j]);
     r[j] = __frcp_rn(s[j]);
   }
   if (kFromAbsmax && blockIdx.y == 0 && warp == 0) {
@@ -472,7 +506,9 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
         unpack8(a[u], f);
         if (!div8_each_try(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
         codes_of<SR>(v, sr, sr.offset + static_cast<uint64_t>(row * cols + c), normal, cd);
-        *reinterpret_cast<typename P::Vec*>(q + row * cols + c) = P::pack(cd);
+        typename P::Vec out = P::pack(cd);
+        if (kHalfClamp) out = clamp_half8(out);
+        *reinterpret_cast<typename P::Vec*>(q + row * cols + c) = out;
       }
     }
   }
