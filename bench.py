@@ -503,17 +503,27 @@ def pass_switch_table(spec, device, steps=5, warmup=2):
 # `python bench.py --steps 2 --warmup 3 --profile-steps` (one pass per
 # launch), valid for the GEMM sources whose digest is given (reported as null
 # once they change).
-GEMM_TRAFFIC = {"bytes_per_launch": 424846455, "sources_sha256_16": "d22a84d5b1375e0b"}
+GEMM_TRAFFIC = {"bytes_per_launch": 424846455, "sources_sha256_16": "6ccba3d5829bb24c"}
 GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "common.cuh")
 
 
-def gemm_traffic():
+def gemm_sources_digest():
+    """sha256 (16 hex digits) of the GEMM sources with // comments, blank
+    lines and indentation removed: only a change of the code counts."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in GEMM_SOURCES:
-        with open(os.path.join(ROOT, "int8_mixed_precision_row_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    if h.hexdigest()[:16] != GEMM_TRAFFIC["sources_sha256_16"]:
+        with open(os.path.join(ROOT, "int8_mixed_precision_row_gb300", "csrc", f)) as fh:
+            for line in fh:
+                code = re.sub(r"//.*$", "", line).strip()
+                if code:
+                    h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
+def gemm_traffic():
+    if gemm_sources_digest() != GEMM_TRAFFIC["sources_sha256_16"]:
         return None
     return GEMM_TRAFFIC["bytes_per_launch"]
 

@@ -356,15 +356,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // arrive on the even CTA's accumulator-empty barrier.  K runs in exact
 // 1024-term chunks drained into int32 totals, as in the single-CTA kernel.
 //
-// Work split.  Data-parallel: pair p takes tiles p, p + P, ... (P pairs).
-// Stream-K (when the tiles do not fill the pairs evenly): the k-blocks of
-// all tiles, tile after tile, are cut into P equal contiguous ranges and pair
-// p takes range p, so a tile may be split between consecutive pairs.  A pair
-// that computed part of a tile stores its int32 totals for that part in its
-// own slot (two slots per pair: its first and its last fragment), then
-// counts itself in on the tile's counter; whichever contributor arrives last
-// adds the other contributors' totals to its own and writes the tile.  No
-// CTA waits for another: the last arrival finds every other part stored.
+// Work split.  Pair p takes tiles p, p + P, ... (P pairs), so that the pairs
+// of a wave work on neighbouring tiles at the same k and share their A and B
+// k-slices in L2.  When the tiles leave a partial last wave of R < P tiles
+// and a scratch is given, those R tiles are instead split into s equal
+// k-parts (s = min(P / R, 4)) computed by otherwise idle pairs, still in step
+// with one another.  Each part stores its int32 totals in the pair's slot and
+// counts itself in on the tile's counters; whichever part arrives last sums
+// the s parts and writes the tile.  No CTA waits for another: the last
+// arrival finds every other part stored.
 constexpr int kPairStages = 6;
 constexpr int kPairABytes = 128 * kBK * 2;
 constexpr int kPairBBytes = 128 * kBK * 2;

@@ -8,19 +8,20 @@
 //
 // Two groupings, both HBM-bound and both fed by TMA:
 //   rows    one group per row of x [rows, cols] (the contraction axis is
-//           contiguous).  Each warp streams whole rows into a double-buffered
-//           shared-memory slot with a bulk copy (cp.async.bulk), reduces the
-//           absmax from shared memory, and writes the codes; the copy of the
-//           row after next is issued as soon as a slot is free.
+//           contiguous).  Teams of warps stream whole rows into a ring of
+//           2-4 shared-memory slots with bulk copies (cp.async.bulk), reduce
+//           the absmax from shared memory and write the codes; a slot is
+//           refilled as soon as every warp of the team has left it.  One
+//           variant also keeps each column's absmax on the way (for the
+//           column groups of the same matrix).
 //   columns one group per column (the contraction axis is the leading one):
-//           pass 1 reduces column absmax over row blocks into the scale
-//           buffer (atomic max on the fp32 bit pattern, valid for values
-//           >= 0); pass 2 turns it into absmax / 127 in place; pass 3
-//           writes the codes either in the input's layout [rows, cols]
-//           (each thread streams one 8-column vector down its rows with the
-//           8 scales in registers) or transposed [cols, rows] (each warp
-//           streams 32x64 sub-tiles through its own two-slot ring of 2-D TMA
-//           loads and writes them through its own staging tile).
+//           the column absmax comes from that row pass, or from a pass of
+//           its own (atomic max on the fp32 bit pattern, valid for values
+//           >= 0); the codes are written either in the input's layout
+//           [rows, cols] (each thread streams one 8-column vector down its
+//           rows with the 8 scales in registers) or transposed [cols, rows]
+//           (each warp streams 32x64 sub-tiles through its own two-slot ring
+//           of 2-D TMA loads and writes them through its own staging tile).
 //
 // Arithmetic per element (identical to the header of int8mp.h):
 //   v = x / s rounded as an IEEE division (div8_*: a reciprocal and two FMAs,
@@ -158,13 +159,13 @@ struct Pack8<__half> {
 
 // ------------------------------------------------------------ row groups
 // The block's warps form teams of T warps (T = 1, 2, 4 or 8).  Each team owns
-// two row slots of `slot_bytes` in dynamic shared memory and walks the rows
+// a ring of S row slots of `slot_bytes` in dynamic shared memory and walks the rows
 // g, g + n, ... (g = its global team index, n = teams in the grid).  The
 // team's first lane issues the bulk copies, waits for them and publishes the
 // outcome; each warp of the team reduces and quantizes a strided share of the
 // row's 16-byte vectors, and the partial absmax values meet in shared memory.
-// The copy of the next row starts as soon as every warp of the team has left
-// the previous one.
+// The copy of row it + S - 1 starts as soon as every warp of the team has
+// left row it - 1.
 __device__ __forceinline__ void team_sync(int team, int T) {
   if (T == 1) {
     __syncwarp();
