@@ -62,7 +62,9 @@ typedef enum {
   INT8MP_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103         */
   INT8MP_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed    */
   INT8MP_ERR_TIMEOUT = 5,            /* a bounded device-side wait ran out   */
-  INT8MP_ERR_WORKSPACE = 6           /* workspace too small                  */
+  INT8MP_ERR_WORKSPACE = 6,          /* workspace too small                  */
+  INT8MP_ERR_BOUNDS = 7              /* a checked build caught an index out  */
+                                     /* of its buffer (see below)            */
 } int8mp_status;
 
 typedef enum { INT8MP_RNE = 0, INT8MP_SR = 1 } int8mp_round;
@@ -332,8 +334,11 @@ int8mp_status int8mp_linear_fwd_noalloc(const void* X, const void* W, void* Y, i
 
 /* Synchronizes `stream`, then returns and clears the device status word of
  * the current device: INT8MP_ERR_TIMEOUT if a bounded device wait ran out
- * since the last poll, INT8MP_ERR_CUDA if the stream reports an error,
- * INT8MP_OK otherwise. */
+ * since the last poll, INT8MP_ERR_BOUNDS if a bounds check of a checked
+ * build failed (a library compiled with -DINT8MP_CHECK checks every global
+ * index its kernels compute against its buffer and skips the access instead
+ * of making it; the ordinary build has no checks), INT8MP_ERR_CUDA if the
+ * stream reports an error, INT8MP_OK otherwise. */
 int8mp_status int8mp_poll_device_status(void* stream);
 
 /* Static, NUL-terminated description of a status code. */

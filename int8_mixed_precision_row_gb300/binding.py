@@ -20,6 +20,7 @@ INT8MP_ERR_UNSUPPORTED_DEVICE = 3
 INT8MP_ERR_CUDA = 4
 INT8MP_ERR_TIMEOUT = 5
 INT8MP_ERR_WORKSPACE = 6
+INT8MP_ERR_BOUNDS = 7
 
 INT8MP_RNE, INT8MP_SR = 0, 1
 INT8MP_AxBT, INT8MP_AxB, INT8MP_ATxB = 0, 1, 2
@@ -67,6 +68,26 @@ _P, _I64, _U64, _U32, _INT, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uin
 
 def library_path():
     return _build.LIB
+
+
+class use_library:
+    """Context manager: route the binding's calls to another build of the
+    library (e.g. the bounds-checked one from build.build(check=True)) while
+    inside, then back."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self.saved = _lib
+        _lib = None
+        return load(self.path)
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
 
 
 def load(path=None):

@@ -15,7 +15,8 @@ namespace {
 
 using int8mp::DeviceInfo;
 
-// Bit 0 set by any kernel whose bounded wait ran out.
+// Bit 0 set by any kernel whose bounded wait ran out; bit 1 by a failed
+// bounds check (checked builds only).
 __device__ unsigned int g_status_word;
 
 constexpr int kMaxDevices = 64;
@@ -517,7 +518,7 @@ int8mp_status int8mp_poll_device_status(void* stream) {
     return INT8MP_ERR_CUDA;
   if (word != 0) {
     if (cudaMemset(dev.status_word, 0, sizeof word) != cudaSuccess) return INT8MP_ERR_CUDA;
-    return INT8MP_ERR_TIMEOUT;
+    return (word & 1u) ? INT8MP_ERR_TIMEOUT : INT8MP_ERR_BOUNDS;
   }
   return INT8MP_OK;
 }
@@ -531,6 +532,7 @@ const char* int8mp_status_string(int8mp_status status) {
     case INT8MP_ERR_CUDA: return "CUDA runtime or launch error";
     case INT8MP_ERR_TIMEOUT: return "a bounded device-side wait ran out";
     case INT8MP_ERR_WORKSPACE: return "workspace too small";
+    case INT8MP_ERR_BOUNDS: return "a bounds check of a checked build failed";
   }
   return "unknown status";
 }

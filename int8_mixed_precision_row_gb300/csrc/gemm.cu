@@ -40,6 +40,7 @@
 #include <chrono>
 #include <mutex>
 
+#include "check.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -125,6 +126,7 @@ __host__ __device__ constexpr uint64_t k_step() {
 __device__ __forceinline__ void store_vec8(const GemmParams& p, int64_t row, int64_t col, float sa,
                                            const int32_t* t) {
   if (col >= p.N) return;
+  if (!in_bounds(row < p.M && col + 8 <= p.ldo, p.status)) return;
   if (p.mode == 1) {
     int4* o = reinterpret_cast<int4*>(static_cast<int32_t*>(p.out) + row * p.ldo + col);
     o[0] = make_int4(t[0], t[1], t[2], t[3]);
@@ -435,6 +437,7 @@ __device__ __forceinline__ const int4* sk_warp_slot(const GemmParams& p, int slo
 
 __device__ __forceinline__ void sk_store_part(const GemmParams& p, int pair, int rank, int ewarp,
                                               const int32_t (&tot)[128]) {
+  if (!in_bounds(pair < kSplitTailMaxPairs, p.status)) return;
   int4* dst = const_cast<int4*>(sk_warp_slot(p, pair, rank, ewarp));
 #pragma unroll
   for (int v = 0; v < 32; ++v)
@@ -446,6 +449,10 @@ __device__ __forceinline__ void sk_store_part(const GemmParams& p, int pair, int
 __device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int ewarp, int tile,
                                             int64_t row, int64_t col0, volatile int* abort) {
   const int t = tile - p.dp_tiles;  // tail tile: parts come from pairs t*s .. t*s+s-1
+  if (!in_bounds(t >= 0 && t * p.sk_split + p.sk_split <= kSplitTailMaxPairs &&
+                     (2 * t + rank) * kEpiWarps + ewarp < 2 * kSplitTailMaxPairs * kEpiWarps,
+                 p.status))
+    return;
   int r = 0;
   if ((threadIdx.x & 31) == 0)
     r = sk_arrive(p.counters + (2 * t + rank) * kEpiWarps + ewarp, p.epoch, p.sk_split);

@@ -37,6 +37,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "check.cuh"
 #include "common.cuh"
 #include "divide.cuh"
 #include "philox.cuh"
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     ptx::fence_mbar_init();
     for (int k = 0; k < S; ++k) {
       const int64_t r = g + k * n;
-      if (r < rows) {
+      if (r < rows && in_bounds(r >= 0 && (k + 1) * slot_bytes <= S * slot_bytes, status)) {
         ptx::mbar_arrive_expect_tx(bar0 + 8u * k, row_bytes);
         ptx::bulk_load(slot_addr + k * slot_bytes, x + r * ld, row_bytes, bar0 + 8u * k);
         pending |= 1u << k;
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     }
     team_sync(team, T);  // the row has landed; every warp has left row it-1
     if (!got_row[team]) break;
-    if (leader && it >= 1 && r + (S - 1) * n < rows) {
+    if (leader && it >= 1 && r + (S - 1) * n < rows && in_bounds(r >= 0, status)) {
       // row it+S-1 goes to the slot of row it-1, which every warp has left
       const int nb = b == 0 ? S - 1 : b - 1;
       const int j = it + S - 1;
@@ -290,14 +291,16 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
 #pragma unroll
       for (int k = 0; k < kColVecs; ++k) {
         const int v = first + k * step;
-        if (v < nvec) {
+        if (v < nvec && in_bounds((v + 1) * 16u <= slot_bytes, status)) {
           const uint4 a = abs_bits8(rowv[v]);
           am2 = absmax8_bits(am2, a);
           colmax_acc(cm[k], a);
         }
       }
     } else {
-      for (int v = first; v < nvec; v += step) am2 = absmax8_bits(am2, abs_bits8(rowv[v]));
+      for (int v = first; v < nvec; v += step)
+        if (in_bounds((v + 1) * 16u <= slot_bytes, status))
+          am2 = absmax8_bits(am2, abs_bits8(rowv[v]));
     }
     float amax = unpack_max(am2);
 #pragma unroll
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
       for (int w = 1; w < T; ++w) amax = fmaxf(amax, red[team * T + w]);
     }
     const float s = __fdiv_rn(amax, 127.0f);
-    if (leader) scale[r] = s;
+    if (leader && in_bounds(r < rows, status)) scale[r] = s;
     const ScaleDiv d = make_scale_div(s);
     const bool normal = scale_is_normal(s);
     typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + r * cols);
@@ -317,6 +320,9 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     for (int v = first; v < nvec; v += 2 * step) {
       const int v2 = v + step;
       const bool has2 = v2 < nvec;
+      if (!in_bounds(r < rows && (has2 ? v2 : v) < nvec &&
+                         ((has2 ? v2 : v) + 1) * 16u <= slot_bytes, status))
+        continue;
       const uint4 a = rowv[v];
       const uint4 bb = has2 ? rowv[v2] : make_uint4(0u, 0u, 0u, 0u);
       quantize_two<CodeT, SR>(a, bb, has2, d, normal, sr, nrow + 8u * v, nrow + 8u * v2,
@@ -346,14 +352,16 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
 #pragma unroll
     for (int k = 0; k < kColVecs; ++k) {
       const int v = first + k * step;
-      if (v < nvec) mine[v] = cm[k];
+      if (v < nvec && in_bounds((v + 1) * 16u <= S * slot_bytes, status)) mine[v] = cm[k];
     }
     __syncthreads();
     const uint16_t* all = reinterpret_cast<const uint16_t*>(smem);
     const size_t team_stride = static_cast<size_t>(S) * slot_bytes / 2;  // in uint16
     for (int c = threadIdx.x; c < cols; c += kThreads) {
       uint32_t mx = 0u;
-      for (int t = 0; t < teams; ++t) mx = max(mx, static_cast<uint32_t>(all[t * team_stride + c]));
+      for (int t = 0; t < teams; ++t)
+        if (in_bounds(t * team_stride + c < teams * team_stride, status))
+          mx = max(mx, static_cast<uint32_t>(all[t * team_stride + c]));
       if (mx != 0u) atomicMax(colmax + c, mx << 16);
     }
   }
@@ -364,11 +372,11 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
 template <typename CodeT, bool SR>
 __global__ void __launch_bounds__(kThreads) quant_rows_long_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, CodeT* __restrict__ q,
-    float* __restrict__ scale, SrArgs sr) {
+    float* __restrict__ scale, SrArgs sr, unsigned int* status) {
   __shared__ float red[kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = blockIdx.x;
-  if (row >= rows) return;
+  if (row >= rows || !in_bounds(cols <= ld, status)) return;
   const int64_t nvec = cols >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * ld);
   float amax = 0.0f;
@@ -399,7 +407,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_long_kernel(
 // rows in flight per thread.
 __global__ void __launch_bounds__(kThreads) col_absmax_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-    int64_t rows_per_block, unsigned int* __restrict__ amax_bits) {
+    int64_t rows_per_block, unsigned int* __restrict__ amax_bits, unsigned int* status) {
   __shared__ float red[kThreads / 32][32][9];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nvec = cols >> 3;
@@ -409,7 +417,7 @@ __global__ void __launch_bounds__(kThreads) col_absmax_kernel(
   float m[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) m[i] = 0.0f;
-  if (vi < nvec) {
+  if (vi < nvec && in_bounds(vi * 8 + 8 <= cols && r1 <= rows, status)) {
     const uint16_t* base = x + vi * 8;
     int64_t r = r0 + warp;
     constexpr int U = 8;
@@ -466,11 +474,11 @@ template <typename CodeT, bool SR, bool kFromAbsmax>
 __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
     int64_t rows_per_block, const float* __restrict__ in, float* __restrict__ scale_out,
-    CodeT* __restrict__ q, SrArgs sr) {
+    CodeT* __restrict__ q, SrArgs sr, unsigned int* status) {
   using P = Pack8<CodeT>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t vi = static_cast<int64_t>(blockIdx.x) * 32 + lane;
-  if (vi >= (cols >> 3)) return;
+  if (vi >= (cols >> 3) || !in_bounds(vi * 8 + 8 <= cols && cols <= ld, status)) return;
   const int64_t c = vi * 8;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * rows_per_block;
   const int64_t r1 = min(rows, r0 + rows_per_block);
@@ -497,7 +505,9 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
 #pragma unroll
     for (int u = 0; u < kNatUnroll; ++u) {
       const int64_t row = rr + u * 8;
-      a[u] = row < r1 ? __ldg(reinterpret_cast<const uint4*>(xc + row * ld)) : make_uint4(0u, 0u, 0u, 0u);
+      a[u] = row < r1 && in_bounds(row < rows, status)
+                 ? __ldg(reinterpret_cast<const uint4*>(xc + row * ld))
+                 : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < kNatUnroll; ++u) {
@@ -509,7 +519,8 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
         codes_of<SR>(v, sr, sr.offset + static_cast<uint64_t>(row * cols + c), normal, cd);
         typename P::Vec out = P::pack(cd);
         if (kHalfClamp) out = clamp_half8(out);
-        *reinterpret_cast<typename P::Vec*>(q + row * cols + c) = out;
+        if (in_bounds(row < rows, status))
+          *reinterpret_cast<typename P::Vec*>(q + row * cols + c) = out;
       }
     }
   }
@@ -702,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 2) quant_cols_kernel(
     for (int k = 0; k < 8; ++k) {
       const int rho = k * 8 + (lane >> 2), slot = lane & 3;
       const int64_t cc = c0 + rho, rr = r0 + slot * 8;
-      if (cc < cols && rr < rows)
+      if (cc < cols && rr < rows && in_bounds(rr + 8 <= rows, status))
         *reinterpret_cast<Vec*>(q + cc * rows + rr) = out[SG::row(rho)][SG::slot(rho, slot)];
     }
     __syncwarp();  // the staging tile may be rewritten
@@ -764,11 +775,12 @@ ColGrid col_grid(int64_t rows, int64_t cols, int64_t blocks_target, int64_t row_
 
 // column absmax merged into amax_bits (atomic max), pass 1 of the columns
 cudaError_t launch_col_absmax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
-                              unsigned int* amax_bits, int sms, cudaStream_t stream) {
+                              unsigned int* amax_bits, const DeviceInfo& dev, cudaStream_t stream) {
   static const int occ1 = blocks_per_sm(col_absmax_kernel, kThreads, 0);
+  const int sms = dev.sms > 0 ? dev.sms : 148;
   const ColGrid g1 = col_grid(rows, cols, static_cast<int64_t>(sms) * occ1, 1);
-  col_absmax_kernel<<<dim3(g1.gx, g1.gy), kThreads, 0, stream>>>(x, rows, cols, ld,
-                                                                  g1.rows_per_block, amax_bits);
+  col_absmax_kernel<<<dim3(g1.gx, g1.gy), kThreads, 0, stream>>>(
+      x, rows, cols, ld, g1.rows_per_block, amax_bits, dev.status_word);
   return cudaGetLastError();
 }
 
@@ -786,9 +798,9 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   const uint32_t slot = static_cast<uint32_t>((cols * 2 + 127) / 128 * 128);
   if (2ull * slot > kMaxDynSmem) {
     quant_rows_long_kernel<CodeT, SR><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(
-        xp, rows, cols, ld, qp, scale, sr);
+        xp, rows, cols, ld, qp, scale, sr, dev.status_word);
     cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, sms, stream);
+    if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, dev, stream);
     return e;
   }
   // 8 warps per block in teams of T, each team with a ring of S row slots
@@ -837,18 +849,19 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   quant_rows_kernel<CodeT, SR, false><<<blocks, kThreads, smem, stream>>>(
       xp, rows, cols, ld, qp, scale, sr, slot, T, S, dev.status_word, kWaitLimitNs, nullptr);
   e = cudaGetLastError();
-  if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, sms, stream);
+  if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, dev, stream);
   return e;
 }
 
 template <typename CodeT, bool SR, bool kFromAbsmax>
 cudaError_t launch_cols_nat(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
-                            const float* in, float* scale_out, CodeT* q, const SrArgs& sr, int sms,
-                            cudaStream_t stream) {
+                            const float* in, float* scale_out, CodeT* q, const SrArgs& sr,
+                            const DeviceInfo& dev, cudaStream_t stream) {
   static const int occ = blocks_per_sm(quant_cols_nat_kernel<CodeT, SR, kFromAbsmax>, kThreads, 0);
+  const int sms = dev.sms > 0 ? dev.sms : 148;
   const ColGrid g = col_grid(rows, cols, static_cast<int64_t>(sms) * occ, 8 * kNatUnroll);
   quant_cols_nat_kernel<CodeT, SR, kFromAbsmax><<<dim3(g.gx, g.gy), kThreads, 0, stream>>>(
-      x, rows, cols, ld, g.rows_per_block, in, scale_out, q, sr);
+      x, rows, cols, ld, g.rows_per_block, in, scale_out, q, sr, dev.status_word);
   return cudaGetLastError();
 }
 
@@ -862,7 +875,7 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   if (err != cudaSuccess) return err;
   const int sms = dev.sms > 0 ? dev.sms : 148;
   // pass 1: one wave of blocks
-  err = launch_col_absmax(xp, rows, cols, ld, amax, sms, stream);
+  err = launch_col_absmax(xp, rows, cols, ld, amax, dev, stream);
   if (err != cudaSuccess) return err;
   col_scale_kernel<<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(amax, cols);
   err = cudaGetLastError();
@@ -870,7 +883,7 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   if (!transposed) {
     // pass 3 in the input's layout: one wave, whole 32-row steps per block
     return launch_cols_nat<CodeT, SR, false>(xp, rows, cols, ld, scale, nullptr,
-                                             static_cast<CodeT*>(q), sr, sms, stream);
+                                             static_cast<CodeT*>(q), sr, dev, stream);
   }
   CUtensorMap tmx;
   if (!encode_tensor_map_2d(&tmx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, cols, ld,
@@ -925,8 +938,7 @@ cudaError_t launch_column_absmax(const void* x, int64_t rows, int64_t cols, int6
                                  float* colmax, const DeviceInfo& dev, cudaStream_t stream) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   return launch_col_absmax(static_cast<const uint16_t*>(x), rows, cols, ld,
-                           reinterpret_cast<unsigned int*>(colmax), dev.sms > 0 ? dev.sms : 148,
-                           stream);
+                           reinterpret_cast<unsigned int*>(colmax), dev, stream);
 }
 
 cudaError_t launch_quantize_cols_from_absmax(const void* x, int64_t rows, int64_t cols,
@@ -935,16 +947,15 @@ cudaError_t launch_quantize_cols_from_absmax(const void* x, int64_t rows, int64_
                                              float* scale, const DeviceInfo& dev,
                                              cudaStream_t stream) {
   const uint16_t* xp = static_cast<const uint16_t*>(x);
-  const int sms = dev.sms > 0 ? dev.sms : 148;
   const bool s = mode == INT8MP_SR;
   if (codes == INT8MP_CODES_S8) {
     int8_t* qp = static_cast<int8_t*>(q);
-    return s ? launch_cols_nat<int8_t, true, true>(xp, rows, cols, ld, absmax, scale, qp, sr, sms, stream)
-             : launch_cols_nat<int8_t, false, true>(xp, rows, cols, ld, absmax, scale, qp, sr, sms, stream);
+    return s ? launch_cols_nat<int8_t, true, true>(xp, rows, cols, ld, absmax, scale, qp, sr, dev, stream)
+             : launch_cols_nat<int8_t, false, true>(xp, rows, cols, ld, absmax, scale, qp, sr, dev, stream);
   }
   __half* qp = static_cast<__half*>(q);
-  return s ? launch_cols_nat<__half, true, true>(xp, rows, cols, ld, absmax, scale, qp, sr, sms, stream)
-           : launch_cols_nat<__half, false, true>(xp, rows, cols, ld, absmax, scale, qp, sr, sms, stream);
+  return s ? launch_cols_nat<__half, true, true>(xp, rows, cols, ld, absmax, scale, qp, sr, dev, stream)
+           : launch_cols_nat<__half, false, true>(xp, rows, cols, ld, absmax, scale, qp, sr, dev, stream);
 }
 
 cudaError_t launch_quantize_cols(const void* x, int64_t rows, int64_t cols, int64_t ld,

@@ -37,9 +37,17 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     assert m.int8mp_version() >= 100
-    for st in range(7):
+    for st in range(8):
         assert m.int8mp_status_string(st) != "unknown status"
     assert m.int8mp_status_string(99) == "unknown status"
+
+
+def test_checked_build_compiles_and_exports_everything():
+    path = mbuild.build(check=True)
+    assert path != mbuild.LIB and os.path.exists(path)
+    lib = ctypes.CDLL(path)
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
 
 
 P = ctypes.c_void_p

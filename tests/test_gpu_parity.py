@@ -161,6 +161,40 @@ def test_rows_with_column_absmax_then_columns(shape, mode):
     np.testing.assert_array_equal(_codes_np(qc), np.ascontiguousarray(qcr.T))
 
 
+@pytest.mark.parametrize("mode", [m.INT8MP_RNE, m.INT8MP_SR])
+def test_columns_from_absmax_int8_codes(mode):
+    rows, cols = 1000, 2056
+    x = _edge_input(rows, cols, seed=17)
+    xd = _dev(x)
+    colmax = torch.zeros(cols, dtype=torch.float32, device=DEV)
+    m.int8mp_quantize_rows_colmax(xd, colmax, codes=m.INT8MP_CODES_S8)
+    q, s = m.int8mp_quantize_cols_absmax(xd, colmax, mode=mode, seed=5, offset=9, stream_id=4,
+                                         codes=m.INT8MP_CODES_S8)
+    qr, sr = oracle.quantize(bf16_bits(x), axis=1, mode=mode, seed=5, offset=9, stream_id=4)
+    np.testing.assert_array_equal(_f32_bits(s), sr.view(np.int32))
+    np.testing.assert_array_equal(_codes_np(q), np.ascontiguousarray(qr.T))
+
+
+@pytest.mark.parametrize("codes", [m.INT8MP_CODES_S8, m.INT8MP_CODES_F16])
+def test_columns_from_a_too_small_absmax_are_clamped(codes):
+    # a caller's absmax below the true one: scale = claim / 127 and every
+    # code still lies in [-127, 127], equal to the clamped nearest-even code
+    rows, cols = 256, 512
+    x = synth.bf16_normal((rows, cols), 18)
+    xd = _dev(x)
+    true_max = xd.float().abs().amax(dim=0)
+    claim = (true_max * 0.5).contiguous()
+    q, s = m.int8mp_quantize_cols_absmax(xd, claim, codes=codes)
+    codes_np = _codes_np(q).astype(np.int64)
+    assert np.abs(codes_np).max() == 127
+    sc = (claim.cpu().double() / 127).float().double().numpy()      # fp32 scale, as stored
+    np.testing.assert_array_equal(_f32_bits(s), (claim.cpu() / 127).numpy().view(np.int32))
+    v = bits_to_f32(bf16_bits(x)).astype(np.float64) / sc[None, :]
+    far = np.abs(np.abs(v) - np.floor(np.abs(v)) - 0.5) > 1e-3    # away from ties
+    expect = np.clip(np.rint(v), -127, 127)
+    np.testing.assert_array_equal(codes_np[far], expect[far])
+
+
 def test_column_absmax_accumulates_over_row_blocks():
     x = _edge_input(640, 2048, seed=91)
     xd = _dev(x)
@@ -382,6 +416,27 @@ def test_square_layouts_with_column_codes_in_place(layout, S):
         acc = oracle.mm_s32(np.ascontiguousarray(qar[rows]), qbr, 8, S, S)
         ref = oracle.rescale_bf16(acc, sar[rows], sbr)
         assert_bf16_equal(out[torch.from_numpy(rows).to(DEV)], ref, f"square {layout} rows")
+
+
+@pytest.mark.parametrize("layout", ["AxBT", "AxB", "ATxB"])
+@pytest.mark.parametrize("S", [1024, 2048])
+def test_square_sweep_sizes(layout, S):
+    # the square quant+scaled-mm configuration at 1024 and 2048 (4096 is in
+    # the full-size tests), run as the benchmark runs it: K-first operands
+    # quantized by columns in place, the matmul in the stored layout, with
+    # the split-last-wave workspace
+    A, B = synth.square_inputs(S, layout)
+    a_cols, b_cols = layout == "ATxB", layout != "AxBT"
+    ax = lambda cols: m.INT8MP_GROUP_COLS if cols else m.INT8MP_GROUP_ROWS
+    lay = {"AxBT": m.INT8MP_AxBT, "AxB": m.INT8MP_AxB, "ATxB": m.INT8MP_ATxB}[layout]
+    qa, sa = m.int8mp_quantize_rowwise(_dev(A), axis=ax(a_cols), codes=m.INT8MP_CODES_F16)
+    qb, sb = m.int8mp_quantize_rowwise(_dev(B), axis=ax(b_cols), codes=m.INT8MP_CODES_F16)
+    out = m.int8mp_scaled_mm(qa, sa, qb, sb, layout=lay, workspace=True)
+    qar, sar = oracle.quantize(bf16_bits(A), axis=1 if a_cols else 0)
+    qbr, sbr = oracle.quantize(bf16_bits(B), axis=1 if b_cols else 0)
+    rows = np.random.default_rng(S + len(layout)).choice(S, 16, replace=False)
+    ref = oracle.scaled_mm(np.ascontiguousarray(qar[rows]), sar[rows], qbr, sbr, len(rows), S, S)
+    assert_bf16_equal(out[torch.from_numpy(rows).to(DEV)], ref, f"square {S} {layout}")
 
 
 LINEAR_SHAPES = [(256, 256, 512), (128, 96, 160), (48, 32, 1056), (1040, 64, 48)]
