@@ -408,14 +408,21 @@ struct FragIter {
 // tells whether it was the last of n.  The counter holds the launch's epoch
 // in its high 40 bits and the count in the low 24; a word left by another
 // launch (or never written) carries another epoch and counts as 0, so the
-// counters need no clearing.  Returns -1 if the compare-and-swap kept failing.
+// counters need no clearing before a launch.  The last arrival clears the
+// word (0 is no launch's tag), so that a launch replayed with the same epoch
+// -- a captured CUDA graph -- starts from 0 too.  Returns -1 if the
+// compare-and-swap kept failing.
 __device__ __forceinline__ int sk_arrive(unsigned long long* ctr, uint64_t epoch, int n) {
   const unsigned long long tag = (epoch & 0xFFFFFFFFFFull) << 24;
   unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
   for (int i = 0; i < kCasLimit; ++i) {
     const unsigned long long cnt = (old & ~0xFFFFFFull) == tag ? (old & 0xFFFFFFull) : 0ull;
     const unsigned long long seen = atomicCAS(ctr, old, tag | (cnt + 1ull));
-    if (seen == old) return static_cast<int>(cnt + 1ull) == n ? 1 : 0;
+    if (seen == old) {
+      if (static_cast<int>(cnt + 1ull) != n) return 0;
+      atomicExch(ctr, 0ull);  // every part has arrived: nothing else touches it
+      return 1;
+    }
     old = seen;
   }
   return -1;

@@ -357,6 +357,49 @@ def test_scaled_mm_split_tail_bit_exact():
     assert_bf16_equal(out, ref, "scaled_mm split tail")
 
 
+def test_split_tail_gemm_replays_in_a_cuda_graph():
+    # a captured launch keeps its counter epoch; the last part of each split
+    # tile clears its counter, so every replay finalizes every tile
+    M, N, K = 2048, 2312, 4096            # 80 tiles: 4 split 4 ways on 76 SM pairs
+    g = torch.Generator().manual_seed(40)
+    a = torch.empty((M, K), dtype=torch.float16, device=DEV)
+    b = torch.empty((N, K), dtype=torch.float16, device=DEV)
+    sa = torch.rand(M, generator=g).to(DEV)
+    sb = torch.rand(N, generator=g).to(DEV)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=DEV)
+
+    def refill():
+        a.copy_(_rand_codes(M, K, int(torch.randint(0, 1 << 30, (1,), generator=g))).half())
+        b.copy_(_rand_codes(N, K, int(torch.randint(0, 1 << 30, (1,), generator=g))).half())
+
+    refill()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # first calls outside the capture
+        m.int8mp_scaled_mm(a, sa, b, sb, out=out, workspace=ws)
+        m.int8mp_mm_s32(a, b, out=acc, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        m.int8mp_scaled_mm(a, sa, b, sb, out=out, workspace=ws)
+        m.int8mp_mm_s32(a, b, out=acc, workspace=ws)
+    for _ in range(3):
+        refill()
+        graph.replay()
+        ref_out = m.int8mp_scaled_mm(a, sa, b, sb)
+        ref_acc = m.int8mp_mm_s32(a, b)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(acc, ref_acc)
+    assert m.int8mp_poll_device_status() == m.INT8MP_OK
+    rows = np.array([0, 1000, 2047])
+    ref = oracle.mm_s32(a.cpu().to(torch.int8).numpy()[rows], b.cpu().to(torch.int8).numpy(),
+                        len(rows), N, K)
+    np.testing.assert_array_equal(acc.cpu().numpy()[rows], ref)
+
+
 @pytest.mark.parametrize("shape", [(256, 256, 512), (200, 264, 144), (384, 512, 2048)])
 def test_scaled_mm_bit_exact(shape):
     M, N, K = shape
