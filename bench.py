@@ -270,25 +270,34 @@ class LayerStep:
 
 
 def time_steps(step, steps, warmup, world, device):
+    """`steps` steps timed end to end with nothing but the workload between
+    the two events; then, for the per-kernel breakdown, up to 20 more steps
+    with CUDA events around every call (their per-kind sums are scaled to
+    `steps` steps)."""
     import torch
     for _ in range(warmup):
         step.run()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    timers = {}
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record()
     for _ in range(steps):
-        step.run(timers=timers)
+        step.run()
     end.record()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     elapsed_ms = start.elapsed_time(end)
-    per_kind = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in timers.items()}
-    counts = {k: len(v) for k, v in timers.items()}
+    timers = {}
+    n_inst = max(1, min(steps, 20))
+    for _ in range(n_inst):
+        step.run(timers=timers)
+    torch.cuda.synchronize()
+    scale = steps / n_inst
+    per_kind = {k: scale * sum(a.elapsed_time(b) for a, b in v) for k, v in timers.items()}
+    counts = {k: round(scale * len(v)) for k, v in timers.items()}
     return elapsed_ms, per_kind, counts
 
 
@@ -628,7 +637,9 @@ def main():
             "quant_rows_ms_per_step": round(per_kind.get("quant_rows", 0.0) / args.steps, 3),
             "quant_cols_ms_per_step": round(per_kind.get("quant_cols", 0.0) / args.steps, 3),
             "quant_gbs_f16codes": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1) if quant_ms else None,
-            "hbm_peak_gbs": hbm},
+            "hbm_peak_gbs": hbm,
+            "timing": "value: the timed steps with no per-kernel events; this breakdown: up "
+                      "to 20 further steps with CUDA events around every call, scaled"},
         "gpu_launches": step.kernels_per_step * args.steps,
         "clocks": clk.summary(),
     }

@@ -28,6 +28,27 @@ struct SrArgs {
 // %globaltimer.  Long enough that no healthy wait reaches it.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// ---- launches ----------------------------------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialization: its launch and set-up overlap the end of the kernel before
+// it in the stream, and it waits (griddepcontrol.wait) before touching
+// global memory, so stream order still holds for every byte.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- driver entry points (tma.cu) ------------------------------------------
 // SMs of the green context (SM partition) `stream` belongs to; 0 if it
 // belongs to none (then the device's count applies).

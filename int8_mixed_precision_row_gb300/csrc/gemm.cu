@@ -216,6 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
 
   const int num_tiles = p.m_tiles * p.n_tiles;
   const uint64_t limit = p.wait_limit_ns;
@@ -542,6 +544,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::cluster_sync();  // both CTAs' barriers exist before any remote use
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
 
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const uint64_t limit = p.wait_limit_ns;
@@ -731,12 +735,13 @@ uint64_t next_epoch() {
 }
 
 template <bool kAmn, bool kBmn>
-void launch_kernel(bool pair, int grid, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                   const GemmParams& p, cudaStream_t stream) {
+cudaError_t launch_kernel(bool pair, int grid, const CUtensorMap& mapA, const CUtensorMap& mapB,
+                          const GemmParams& p, cudaStream_t stream) {
   if (pair)
-    gemm_s8f16_pair_kernel<kAmn, kBmn><<<grid, kThreads, kPairSmemBytes, stream>>>(mapA, mapB, p);
-  else
-    gemm_s8f16_kernel<kAmn, kBmn><<<grid, kThreads, kSmemBytes, stream>>>(mapA, mapB, p);
+    return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn>, dim3(grid), dim3(kThreads),
+                             kPairSmemBytes, stream, mapA, mapB, p);
+  return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn>, dim3(grid), dim3(kThreads), kSmemBytes,
+                           stream, mapA, mapB, p);
 }
 
 }  // namespace
@@ -818,13 +823,9 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
       grid = static_cast<int>(2 * npairs);
     }
   }
-  if (!a_mn && !b_mn)
-    launch_kernel<false, false>(pair, grid, mapA, mapB, p, stream);
-  else if (!a_mn)
-    launch_kernel<false, true>(pair, grid, mapA, mapB, p, stream);
-  else
-    launch_kernel<true, true>(pair, grid, mapA, mapB, p, stream);
-  return cudaGetLastError();
+  if (!a_mn && !b_mn) return launch_kernel<false, false>(pair, grid, mapA, mapB, p, stream);
+  if (!a_mn) return launch_kernel<false, true>(pair, grid, mapA, mapB, p, stream);
+  return launch_kernel<true, true>(pair, grid, mapA, mapB, p, stream);
 }
 
 }  // namespace int8mp

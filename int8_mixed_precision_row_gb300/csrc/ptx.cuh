@@ -77,6 +77,20 @@ __device__ __forceinline__ bool mbar_wait_timeout(uint32_t bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is still finishing.  It calls
+// grid_dependency_wait() before its first global-memory access (read or
+// write), which returns once the preceding grid has completed and its writes
+// are visible; without such a predecessor it returns at once.
+// allow_dependents() lets the next kernel of the stream start launching.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -240,6 +240,8 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
   const int64_t g = static_cast<int64_t>(blockIdx.x) * teams + team;
   const int64_t n = static_cast<int64_t>(gridDim.x) * teams;
   using P = Pack8<CodeT>;
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
 
   uint32_t pending = 0u, pend_par = 0u;  // leader: copies in flight per slot, their parity
   if (leader) {
@@ -374,6 +376,8 @@ __global__ void __launch_bounds__(kThreads) quant_rows_long_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, CodeT* __restrict__ q,
     float* __restrict__ scale, SrArgs sr, unsigned int* status) {
   __shared__ float red[kThreads / 32];
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = blockIdx.x;
   if (row >= rows || !in_bounds(cols <= ld, status)) return;
@@ -409,6 +413,9 @@ __global__ void __launch_bounds__(kThreads) col_absmax_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
     int64_t rows_per_block, unsigned int* __restrict__ amax_bits, unsigned int* status) {
   __shared__ float red[kThreads / 32][32][9];
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nvec = cols >> 3;
   const int64_t vi = static_cast<int64_t>(blockIdx.x) * 32 + lane;
@@ -456,6 +463,8 @@ __global__ void __launch_bounds__(kThreads) col_absmax_kernel(
 
 // Pass 2: scale = absmax / 127, in place, before any code is computed.
 __global__ void col_scale_kernel(unsigned int* __restrict__ amax_bits, int64_t cols) {
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c < cols) amax_bits[c] = __float_as_uint(__fdiv_rn(__uint_as_float(amax_bits[c]), 127.0f));
 }
@@ -476,6 +485,8 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
     int64_t rows_per_block, const float* __restrict__ in, float* __restrict__ scale_out,
     CodeT* __restrict__ q, SrArgs sr, unsigned int* status) {
   using P = Pack8<CodeT>;
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t vi = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   if (vi >= (cols >> 3) || !in_bounds(vi * 8 + 8 <= cols && cols <= ld, status)) return;
@@ -594,6 +605,9 @@ __global__ void __launch_bounds__(kThreads, 2) quant_cols_kernel(
     SrArgs sr, unsigned int* status, uint64_t limit_ns) {
   using CP = ColPack<CodeT>;
   using Vec = typename CP::Vec;
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
+
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t bars[kThreads / 32][2];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -779,9 +793,8 @@ cudaError_t launch_col_absmax(const uint16_t* x, int64_t rows, int64_t cols, int
   static const int occ1 = blocks_per_sm(col_absmax_kernel, kThreads, 0);
   const int sms = dev.sms > 0 ? dev.sms : 148;
   const ColGrid g1 = col_grid(rows, cols, static_cast<int64_t>(sms) * occ1, 1);
-  col_absmax_kernel<<<dim3(g1.gx, g1.gy), kThreads, 0, stream>>>(
-      x, rows, cols, ld, g1.rows_per_block, amax_bits, dev.status_word);
-  return cudaGetLastError();
+  return launch_overlapped(col_absmax_kernel, dim3(g1.gx, g1.gy), dim3(kThreads), 0, stream, x,
+                           rows, cols, ld, g1.rows_per_block, amax_bits, dev.status_word);
 }
 
 // Row groups; with colmax != nullptr also max-merge each column's absmax
@@ -797,9 +810,9 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   const int sms = dev.sms > 0 ? dev.sms : 148;
   const uint32_t slot = static_cast<uint32_t>((cols * 2 + 127) / 128 * 128);
   if (2ull * slot > kMaxDynSmem) {
-    quant_rows_long_kernel<CodeT, SR><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(
-        xp, rows, cols, ld, qp, scale, sr, dev.status_word);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_overlapped(quant_rows_long_kernel<CodeT, SR>,
+                                      dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0, stream,
+                                      xp, rows, cols, ld, qp, scale, sr, dev.status_word);
     if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, dev, stream);
     return e;
   }
@@ -836,9 +849,9 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
     const int occ = blocks_per_sm(quant_rows_kernel<CodeT, SR, true>, kThreads, smem);
     const int64_t cap = static_cast<int64_t>(sms) * occ;
     const unsigned blocks = static_cast<unsigned>(need < cap ? need : cap);
-    quant_rows_kernel<CodeT, SR, true><<<blocks, kThreads, smem, stream>>>(
-        xp, rows, cols, ld, qp, scale, sr, slot, T, S, dev.status_word, kWaitLimitNs, cmx);
-    return cudaGetLastError();
+    return launch_overlapped(quant_rows_kernel<CodeT, SR, true>, dim3(blocks), dim3(kThreads), smem,
+                             stream, xp, rows, cols, ld, qp, scale, sr, slot, T, S,
+                             dev.status_word, kWaitLimitNs, cmx);
   }
   static bool attr[64] = {};
   e = allow_smem(quant_rows_kernel<CodeT, SR, false>, attr);
@@ -846,9 +859,9 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   const int occ = blocks_per_sm(quant_rows_kernel<CodeT, SR, false>, kThreads, smem);
   const int64_t cap = static_cast<int64_t>(sms) * occ;
   const unsigned blocks = static_cast<unsigned>(need < cap ? need : cap);
-  quant_rows_kernel<CodeT, SR, false><<<blocks, kThreads, smem, stream>>>(
-      xp, rows, cols, ld, qp, scale, sr, slot, T, S, dev.status_word, kWaitLimitNs, nullptr);
-  e = cudaGetLastError();
+  e = launch_overlapped(quant_rows_kernel<CodeT, SR, false>, dim3(blocks), dim3(kThreads), smem,
+                        stream, xp, rows, cols, ld, qp, scale, sr, slot, T, S, dev.status_word,
+                        kWaitLimitNs, nullptr);
   if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, dev, stream);
   return e;
 }
@@ -860,9 +873,9 @@ cudaError_t launch_cols_nat(const uint16_t* x, int64_t rows, int64_t cols, int64
   static const int occ = blocks_per_sm(quant_cols_nat_kernel<CodeT, SR, kFromAbsmax>, kThreads, 0);
   const int sms = dev.sms > 0 ? dev.sms : 148;
   const ColGrid g = col_grid(rows, cols, static_cast<int64_t>(sms) * occ, 8 * kNatUnroll);
-  quant_cols_nat_kernel<CodeT, SR, kFromAbsmax><<<dim3(g.gx, g.gy), kThreads, 0, stream>>>(
-      x, rows, cols, ld, g.rows_per_block, in, scale_out, q, sr, dev.status_word);
-  return cudaGetLastError();
+  return launch_overlapped(quant_cols_nat_kernel<CodeT, SR, kFromAbsmax>, dim3(g.gx, g.gy),
+                           dim3(kThreads), 0, stream, x, rows, cols, ld, g.rows_per_block, in,
+                           scale_out, q, sr, dev.status_word);
 }
 
 template <typename CodeT, bool SR>
@@ -877,8 +890,8 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   // pass 1: one wave of blocks
   err = launch_col_absmax(xp, rows, cols, ld, amax, dev, stream);
   if (err != cudaSuccess) return err;
-  col_scale_kernel<<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(amax, cols);
-  err = cudaGetLastError();
+  err = launch_overlapped(col_scale_kernel, dim3(static_cast<unsigned>((cols + 255) / 256)),
+                          dim3(256), 0, stream, amax, cols);
   if (err != cudaSuccess) return err;
   if (!transposed) {
     // pass 3 in the input's layout: one wave, whole 32-row steps per block
@@ -913,10 +926,10 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
       if ((b * wpb) % col_tiles == 0) blocks = b;
     }
   }
-  quant_cols_kernel<CodeT, SR><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(
-      tmx, rows, cols, scale, static_cast<CodeT*>(q), col_tiles, tiles, sr, dev.status_word,
-      kWaitLimitNs);
-  return cudaGetLastError();
+  return launch_overlapped(quant_cols_kernel<CodeT, SR>, dim3(static_cast<unsigned>(blocks)),
+                           dim3(kThreads), smem, stream, tmx, rows, cols, scale,
+                           static_cast<CodeT*>(q), col_tiles, tiles, sr, dev.status_word,
+                           kWaitLimitNs);
 }
 
 }  // namespace
