@@ -199,9 +199,14 @@ class LayerStep:
         self.sa = torch.empty(max(T, nmax, kmax), dtype=torch.float32, device=device)
         self.sb = torch.empty(max(T, nmax, kmax), dtype=torch.float32, device=device)
         # column absmax of X, W (recorded by their forward row passes) and dY
-        # (by its grad-input row pass), per linear: [K | K | N]
-        for l in self.linears:
-            l["colmax"] = torch.empty(2 * l["K"] + l["N"], dtype=torch.float32, device=device)
+        # (by its grad-input row pass), per linear [K | K | N], all linears in
+        # one buffer cleared once per step
+        sizes = [2 * l["K"] + l["N"] for l in self.linears]
+        self.colmax_all = torch.empty(sum(sizes), dtype=torch.float32, device=device)
+        at = 0
+        for l, n in zip(self.linears, sizes):
+            l["colmax"] = self.colmax_all[at:at + n]
+            at += n
         # the matmuls' scratch for splitting their last wave of tiles
         self.mm_ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
         self.flops = 6.0 * T * sum(l["N"] * l["K"] for l in self.linears)
@@ -247,12 +252,12 @@ class LayerStep:
             b.record()
             timers.setdefault(kind, []).append((a, b))
             return r
+        self.colmax_all.zero_()
         for l in self.linears:
             X, W, dY = l["X"], l["W"], l["dY"]
             K = l["K"]
             cm = l["colmax"]
             cx, cw, cg = cm[:K], cm[K:2 * K], cm[2 * K:]
-            cm.zero_()
             # forward: X and W along K (their rows); their column absmax on the way
             qx, sx = rec("quant_rows", lambda: self._q(X, 0, m.INT8MP_STREAM_FWD_X, self.qa, self.sa, seed, offset, cx))
             qw, sw = rec("quant_rows", lambda: self._q(W, 0, m.INT8MP_STREAM_FWD_W, self.qb, self.sb, seed, offset, cw))

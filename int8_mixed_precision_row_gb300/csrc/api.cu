@@ -350,8 +350,7 @@ int8mp_status linear_fwd_impl(const void* X, const void* W, void* Y, int64_t T, 
   st = current_device(&dev, as_stream(stream));
   if (st != INT8MP_OK) return st;
   cudaStream_t s = as_stream(stream);
-  if (save_absmax && K > 0 &&
-      cudaMemsetAsync(save_absmax, 0, static_cast<size_t>(2 * K) * 4, s) != cudaSuccess)
+  if (save_absmax && K > 0 && int8mp::launch_zero_words(save_absmax, 2 * K, dev, s) != cudaSuccess)
     return INT8MP_ERR_CUDA;
   float* x_absmax = save_absmax && K > 0 && cfg->int8_grad_w ? save_absmax : nullptr;
   float* w_absmax = save_absmax && K > 0 && cfg->int8_grad_in ? save_absmax + K : nullptr;
@@ -412,8 +411,7 @@ int8mp_status linear_bwd_impl(const void* dY, const void* X, const void* W, void
   float* dy_absmax = o.absmax;
   const float* x_absmax = saved_absmax ? saved_absmax : o.absmax + N;
   const float* w_absmax = saved_absmax ? saved_absmax + K : o.absmax + N + K;
-  if ((int8_dx || int8_dw) &&
-      cudaMemsetAsync(o.absmax, 0, static_cast<size_t>(N + 2 * K) * 4, s) != cudaSuccess)
+  if ((int8_dx || int8_dw) && int8mp::launch_zero_words(o.absmax, N + 2 * K, dev, s) != cudaSuccess)
     return INT8MP_ERR_CUDA;
   if (!saved_absmax) {
     cudaError_t e = cudaSuccess;

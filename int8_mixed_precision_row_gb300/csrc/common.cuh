@@ -68,6 +68,8 @@ cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int6
                                  int8mp_round mode, const SrArgs& sr, void* q,
                                  int8mp_codes codes, float* scale, float* colmax,
                                  const DeviceInfo& dev, cudaStream_t stream);
+// n 32-bit words at p set to 0 (a kernel: keeps dependent launches going).
+cudaError_t launch_zero_words(void* p, int64_t n, const DeviceInfo& dev, cudaStream_t stream);
 // colmax[c] = max(colmax[c], max_r |x[r,c]|) (fp32 [cols]), one pass.
 cudaError_t launch_column_absmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                  float* colmax, const DeviceInfo& dev, cudaStream_t stream);

@@ -461,6 +461,16 @@ __global__ void __launch_bounds__(kThreads) col_absmax_kernel(
   }
 }
 
+// Zeroes n 32-bit words (absmax buffers before an atomic-max merge); a kernel
+// rather than a memset so that it keeps the stream's dependent launches.
+__global__ void zero_words_kernel(unsigned int* __restrict__ p, int64_t n) {
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    p[i] = 0u;
+}
+
 // Pass 2: scale = absmax / 127, in place, before any code is computed.
 __global__ void col_scale_kernel(unsigned int* __restrict__ amax_bits, int64_t cols) {
   ptx::grid_dependency_wait();  // the previous kernel in the stream is done
@@ -884,7 +894,7 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
                           cudaStream_t stream) {
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   unsigned int* amax = reinterpret_cast<unsigned int*>(scale);
-  cudaError_t err = cudaMemsetAsync(amax, 0, static_cast<size_t>(cols) * sizeof(float), stream);
+  cudaError_t err = launch_zero_words(amax, cols, dev, stream);
   if (err != cudaSuccess) return err;
   const int sms = dev.sms > 0 ? dev.sms : 148;
   // pass 1: one wave of blocks
@@ -945,6 +955,15 @@ cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int6
              : rows_dispatch<int8_t, false>(x, rows, cols, ld, q, scale, cm, sr, dev, stream);
   return s ? rows_dispatch<__half, true>(x, rows, cols, ld, q, scale, cm, sr, dev, stream)
            : rows_dispatch<__half, false>(x, rows, cols, ld, q, scale, cm, sr, dev, stream);
+}
+
+cudaError_t launch_zero_words(void* p, int64_t n, const DeviceInfo& dev, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const int sms = dev.sms > 0 ? dev.sms : 148;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4 * sms) blocks = 4 * sms;
+  return launch_overlapped(zero_words_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                           stream, static_cast<unsigned int*>(p), n);
 }
 
 cudaError_t launch_column_absmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
