@@ -36,6 +36,9 @@ int8mp_status int8mp_debug_mm_s32_drop_first_load(const void* A, const void* B, 
  * pairs) and compares the codes the two quotients give: the nearest-even code
  * bit for bit, and for stochastic rounding floor(v) and the number of draws
  * u = k 2^-24 below v - floor(v), which fix the code for every u.
+ * The fast rule has two forms, scalar (column quantizers) and packed two
+ * lanes per instruction (row quantizers); a pair whose two fast quotients
+ * differ counts as a mismatch too.
  * results[0] = pairs whose codes differ, [1] = pairs checked, [2] = pairs on
  * the fast path, [3] = pairs whose quotients differ in any bit (informative:
  * tiny x only).  first_bad[0..1] = bf16 bits (absmax, x) of one pair whose

@@ -27,8 +27,10 @@ __device__ __forceinline__ void sr_signature(float v, float& f, float& below) {
 
 // One block per positive finite bf16 absmax (bit patterns 0x0001..0x7F7F);
 // its threads sweep every bf16 x with |x| <= absmax (magnitude bits <= the
-// absmax bits, both signs) and compare the codes from div_scale with the
-// codes from IEEE division.
+// absmax bits, both signs) and compare the codes from the fast division with
+// the codes from IEEE division; a pair also counts as a mismatch if the
+// packed two-lane form (row quantizers) and the scalar form (column
+// quantizers) give different quotients.
 __global__ void __launch_bounds__(256) check_division_kernel() {
   const uint32_t a = blockIdx.x + 1u;
   const float amax = __uint_as_float(a << 16);
@@ -36,17 +38,24 @@ __global__ void __launch_bounds__(256) check_division_kernel() {
   const int8mp::ScaleDiv d = int8mp::make_scale_div(s);
   unsigned long long bad = 0, pairs = 0, qdiff = 0;
   for (uint32_t m = threadIdx.x; m <= a; m += blockDim.x) {
+    const float xp = __uint_as_float(m << 16), xn = __uint_as_float((0x8000u | m) << 16);
+    const float2 fast = int8mp::div2_fast(make_float2(xp, xn), make_float2(d.s, d.s),
+                                          make_float2(d.r, d.r));
     for (uint32_t sign = 0; sign < 2; ++sign) {
       const uint32_t xb = (sign << 15) | m;
-      const float x = __uint_as_float(xb << 16);
-      const float got = int8mp::div_scale(x, d);
+      const float x = sign ? xn : xp;
+      // both fast forms: the packed lane must equal the scalar result
+      const float lane = sign ? fast.y : fast.x;
+      const float got = d.fast ? int8mp::div_fast(x, d.s, d.r) : __fdiv_rn(x, d.s);
+      const bool forms_agree = !d.fast || __float_as_uint(lane) == __float_as_uint(got);
       const float ref = __fdiv_rn(x, s);
       ++pairs;
       if (!(got == ref)) ++qdiff;
       float fg, bg, fr, br;
       sr_signature(got, fg, bg);
       sr_signature(ref, fr, br);
-      const bool same = __float_as_uint(rne_code_of(got)) == __float_as_uint(rne_code_of(ref)) &&
+      const bool same = forms_agree &&
+                        __float_as_uint(rne_code_of(got)) == __float_as_uint(rne_code_of(ref)) &&
                         fg == fr && bg == br;
       if (!same) {
         ++bad;

@@ -1,5 +1,5 @@
 // divide.cuh -- x / s for a fixed per-group scale s, in three fused
-// operations, for the quantizers' codes.
+// operations (two lanes per instruction), for the quantizers' codes.
 //
 // Method: Markstein's correction (P. W. Markstein, "Computation of elementary
 // functions on the IBM RISC System/6000 processor", IBM J. Res. Develop.
@@ -39,27 +39,40 @@ __device__ __forceinline__ ScaleDiv make_scale_div(float s) {
   return d;
 }
 
+// The fast form for two quotients at once, with the packed two-lane fp32
+// instructions of sm_100+ (FMUL2 / FFMA2): each lane is rounded exactly as
+// its scalar counterpart, so every quotient equals the scalar three-operation
+// result.  The division certificate runs both forms over every bf16 pair and
+// requires them to agree.
+__device__ __forceinline__ float2 div2_fast(float2 x, float2 s, float2 r) {
+  const float2 q0 = __fmul2_rn(x, r);
+  const float2 rem = __ffma2_rn(make_float2(-q0.x, -q0.y), s, x);
+  return __ffma2_rn(rem, r, q0);
+}
+
+// Fast quotients of eight elements of one group; returns d.fast (otherwise
+// redo them with div8_ieee).
+__device__ __forceinline__ bool div8_try(const float (&x)[8], const ScaleDiv& d, float (&v)[8]) {
+  const float2 s2 = make_float2(d.s, d.s), r2 = make_float2(d.r, d.r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 q = div2_fast(make_float2(x[2 * i], x[2 * i + 1]), s2, r2);
+    v[2 * i] = q.x;
+    v[2 * i + 1] = q.y;
+  }
+  return d.fast;
+}
+
+// The same three operations for one quotient.
 __device__ __forceinline__ float div_fast(float x, float s, float r) {
   const float q0 = __fmul_rn(x, r);
   const float rem = __fmaf_rn(-q0, s, x);
   return __fmaf_rn(rem, r, q0);
 }
 
-// x / s for s > 0 as the quantizers compute it
-__device__ __forceinline__ float div_scale(float x, const ScaleDiv& d) {
-  return d.fast ? div_fast(x, d.s, d.r) : __fdiv_rn(x, d.s);
-}
-
-// Fast quotients of eight elements of one group; returns d.fast (otherwise
-// redo them with div8_ieee).
-__device__ __forceinline__ bool div8_try(const float (&x)[8], const ScaleDiv& d, float (&v)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = div_fast(x[i], d.s, d.r);
-  return d.fast;
-}
-
 // Same for eight elements of eight groups (scales s[i], reciprocals r[i]);
-// all_fast: every s[i] is in the fast range.
+// all_fast: every s[i] is in the fast range.  Scalar: pairing eight
+// different scales into two-lane operands costs more than it saves.
 __device__ __forceinline__ bool div8_each_try(const float (&x)[8], const float (&s)[8],
                                               const float (&r)[8], bool all_fast,
                                               float (&v)[8]) {
