@@ -91,6 +91,15 @@ __device__ __forceinline__ float code_rne(float v) {
 // s >= (absmax / 127)(1 - 2^-24), so |v| <= 127 (1 + 2^-23) < 127.5 and
 // rounding cannot leave [-127, 127]; the clamp is dropped.
 __device__ __forceinline__ float code_rne_normal_scale(float v) { return rintf(v); }
+// Two such codes with two packed fp32 adds: for |v| < 2^22, v + 1.5 * 2^23
+// lies in [2^23, 2^24), where the spacing of floats is 1, so the nearest-even
+// rounding of the sum is 1.5 * 2^23 plus the nearest-even integer to v (the
+// constant is even), and subtracting the constant back is exact.
+__device__ __forceinline__ float2 code_rne_normal_scale2(float2 v) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  const float2 t = __fadd2_rn(v, make_float2(kMagic, kMagic));
+  return __fadd2_rn(t, make_float2(-kMagic, -kMagic));
+}
 __device__ __forceinline__ float code_sr(float v, uint32_t word) {
   const float f = floorf(v);
   const float fr = __fsub_rn(v, f);
@@ -110,7 +119,11 @@ __device__ __forceinline__ void codes_of(const float (&v)[8], const SrArgs& sr, 
     for (int i = 0; i < 8; ++i) c[i] = code_sr(v[i], w[i]);
   } else if (normal_scales) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = code_rne_normal_scale(v[i]);
+    for (int i = 0; i < 4; ++i) {
+      const float2 q = code_rne_normal_scale2(make_float2(v[2 * i], v[2 * i + 1]));
+      c[2 * i] = q.x;
+      c[2 * i + 1] = q.y;
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) c[i] = code_rne(v[i]);
