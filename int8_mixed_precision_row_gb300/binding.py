@@ -190,6 +190,13 @@ def int8mp_quantize_rowwise(x, axis=0, mode=INT8MP_RNE, seed=0, offset=0, stream
     return q, scale
 
 
+def _check_out(out, M, N, dtype):
+    """The matmul writes rows of N elements at stride out.stride(0)."""
+    if out.shape != (M, N) or out.dtype != dtype or (N > 1 and out.stride(1) != 1):
+        raise ValueError(f"out must be {dtype} [{M}, {N}] with contiguous rows, got "
+                         f"{out.dtype} {tuple(out.shape)} strides {out.stride()}")
+
+
 def _mm_sizes(A, B, layout):
     if layout == INT8MP_AxBT:
         return A.shape[0], B.shape[0], A.shape[1]
@@ -256,6 +263,7 @@ def int8mp_scaled_mm(A, sA, B, sB, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, o
     M, N, K = _mm_sizes(A, B, layout)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _check_out(out, M, N, torch.bfloat16)
     ldo = out.stride(0) if M > 0 else N
     ws, nbytes = _mm_ws(workspace, A.device)
     if ws is None:
@@ -274,6 +282,7 @@ def int8mp_mm_s32(A, B, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, out=None, st
     M, N, K = _mm_sizes(A, B, layout)
     if out is None:
         out = torch.empty((M, N), dtype=torch.int32, device=A.device)
+    _check_out(out, M, N, torch.int32)
     ldo = out.stride(0) if M > 0 else N
     ws, nbytes = _mm_ws(workspace, A.device)
     if ws is None:

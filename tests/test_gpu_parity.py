@@ -414,6 +414,44 @@ def test_scaled_mm_bit_exact(shape):
     assert_bf16_equal(out, ref, "scaled_mm")
 
 
+@pytest.mark.parametrize("s32", [False, True])
+def test_pair_gemm_writes_only_its_strided_output(s32):
+    # CTA-pair kernel (99 pair tiles), ragged M and N: the tile stores must
+    # land at row stride ldo and column offset 8 of a larger buffer, clip at
+    # row M and column N, and leave every other element as it was; sB at a
+    # 4-byte (not 16-byte) aligned address
+    M, N, K, ldo = 2600, 2056, 144, 2088
+    a, b = _rand_codes(M, K, 41), _rand_codes(N, K, 42)
+    ad, bd = _dev(a.half()), _dev(b.half())
+    g = torch.Generator().manual_seed(43)
+    sa = torch.rand(M, generator=g) + 0.5
+    sb_store = torch.rand(N + 1, generator=g) + 0.5
+    dtype = torch.int32 if s32 else torch.bfloat16
+    big = torch.full((M + 3, ldo), -7, dtype=torch.int32).to(dtype).to(DEV)
+    sentinel = big.clone()
+    view = big[1:M + 1, 8:8 + N]
+    if s32:
+        m.int8mp_mm_s32(ad, bd, out=view)
+    else:
+        m.int8mp_scaled_mm(ad, _dev(sa), bd, _dev(sb_store)[1:], out=view)
+    assert m.int8mp_poll_device_status() == m.INT8MP_OK
+    outside = torch.ones(big.shape, dtype=torch.bool)
+    outside[1:M + 1, 8:8 + N] = False
+    assert torch.equal(big.cpu()[outside], sentinel.cpu()[outside])
+    if s32:
+        np.testing.assert_array_equal(view.cpu().numpy(), oracle.mm_s32(a.numpy(), b.numpy(), M, N, K))
+    else:
+        ref = oracle.scaled_mm(a.numpy(), sa.numpy(), b.numpy(), sb_store[1:].numpy(), M, N, K)
+        assert_bf16_equal(view, ref, "scaled_mm into a strided output")
+
+
+def test_matmul_rejects_an_output_with_strided_columns():
+    a = _dev(_rand_codes(256, 64, 44).half())
+    out = torch.empty((256, 512), dtype=torch.int32, device=DEV)[:, ::2]
+    with pytest.raises(ValueError):
+        m.int8mp_mm_s32(a, a, out=out)
+
+
 @pytest.mark.parametrize("layout", ["AxBT", "AxB", "ATxB"])
 def test_square_layouts_through_quantize_side_transpose(layout):
     # A @ B: B [K,N] quantized along K = its columns (axis 1 writes [N,K]);
