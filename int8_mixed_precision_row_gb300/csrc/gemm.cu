@@ -28,7 +28,9 @@
 //               128x256x16 per stage, commit frees the stage; commit after
 //               each K-chunk hands the accumulator to the epilogue
 //   warps 2-9   epilogue: warp w reads TMEM lanes 32*(w%4).. and one half
-//               (128 columns) of the tile, keeps 128 int32 totals per thread
+//               (128 columns) of the tile, keeps 128 int32 totals per thread,
+//               and writes the finished tile through a 4 KB shared-memory
+//               staging buffer with TMA tensor stores
 // Every mbarrier wait is bounded (wall clock); a wait that runs out raises
 // the CTA abort flag and the device status word, every role winds down,
 // outstanding copies and MMAs are waited for (bounded), TMEM is freed.
@@ -58,7 +60,11 @@ constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;  // two 128x256 fp32 accumulators
 constexpr int kBarrierBytes = 256;
 constexpr int kMnBlockBytes = 64 * kBK * 2;  // one 64 (M or N) x 64 (K) MN-major box
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes;
+// each epilogue warp stages its outputs in 4 KB: one 32-row x 128-byte box
+constexpr int kStoreBoxBytes = 32 * 128;
+constexpr int kStagingBytes = kEpiWarps * kStoreBoxBytes;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kBarrierBytes;
+static_assert(kSmemBytes <= 227 * 1024, "single-CTA kernel shared memory");
 
 struct GemmParams {
   const float* sA;
@@ -146,16 +152,6 @@ __device__ __forceinline__ void store_vec8(const GemmParams& p, int64_t row, int
       make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// One thread's output: row `row`, columns col0 .. col0+127, from its int32
-// totals.
-__device__ __forceinline__ void store_rows(const GemmParams& p, int64_t row, int64_t col0,
-                                           const int32_t (&tot)[128]) {
-  if (row >= p.M) return;
-  const float sa = p.mode == 1 ? 0.0f : __ldg(p.sA + row);
-#pragma unroll
-  for (int v = 0; v < 16; ++v) store_vec8(p, row, col0 + v * 8, sa, tot + v * 8);
-}
-
 // Drain one 128-column half of a chunk accumulator (this warp's 32 lanes)
 // from tensor memory into the int32 totals; every fp32 value is an exact
 // integer below 2^24 in magnitude.
@@ -170,17 +166,98 @@ __device__ __forceinline__ void drain_chunk(uint32_t taddr, int32_t (&tot)[128])
   }
 }
 
+// Output of one epilogue warp's part of a whole tile (rows row0 ..
+// row0+31, columns col0 .. col0+127) by TMA tensor stores, one 128-byte-wide
+// box at a time (64 bf16 or 32 int32 columns x 32 rows).  Lane l converts
+// row row0 + l and writes it into the warp's 4 KB staging buffer in the
+// 128-byte swizzled layout of the store map -- 16-byte chunk c of row r at
+// r * 128 + (c ^ (r % 8)) * 16 -- so each group of eight lanes covers all 32
+// banks.  The store clips rows and columns outside the output; a box that
+// starts at or past column N is not stored.  Before the buffer is rewritten,
+// lane 0 waits until the previous store has read it.
+__device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtensorMap* map,
+                                               uint32_t buf, int64_t row0, int64_t col0,
+                                               const int32_t (&tot)[128]) {
+  if (row0 >= p.M) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = row0 + lane;
+  const uint32_t dst = buf + static_cast<uint32_t>(lane) * 128u;
+  const uint32_t sw = static_cast<uint32_t>(lane & 7);
+  auto publish = [&](int64_t c0) {
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(map, buf, static_cast<int32_t>(c0), static_cast<int32_t>(row0));
+      ptx::bulk_commit_group();
+    }
+  };
+  auto reuse = [&]() {
+    if (lane == 0) ptx::bulk_wait_group_read0();
+    __syncwarp();
+  };
+  if (p.mode == 1) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t c0 = col0 + 32 * j;
+      if (c0 >= p.N) break;
+      reuse();
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int32_t* t = tot + 32 * j + 4 * c;
+        ptx::st_shared_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), t[0], t[1], t[2], t[3]);
+      }
+      publish(c0);
+    }
+    return;
+  }
+  const float sa = row < p.M ? __ldg(p.sA + row) : 0.0f;
+  const bool sb_vec4 = (reinterpret_cast<uintptr_t>(p.sB) & 15u) == 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int64_t c0 = col0 + 64 * j;
+    if (c0 >= p.N) break;
+    reuse();
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int64_t col = c0 + 8 * c;
+      float sb[8];
+      if (col + 8 <= p.N && sb_vec4) {
+        const float4 lo = __ldg(reinterpret_cast<const float4*>(p.sB + col));
+        const float4 hi = __ldg(reinterpret_cast<const float4*>(p.sB + col) + 1);
+        sb[0] = lo.x, sb[1] = lo.y, sb[2] = lo.z, sb[3] = lo.w;
+        sb[4] = hi.x, sb[5] = hi.y, sb[6] = hi.z, sb[7] = hi.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sb[e] = col + 8 <= p.N ? __ldg(p.sB + col + e) : 0.0f;
+      }
+      const int32_t* t = tot + 64 * j + 8 * c;
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float o0 = __fmul_rn(__fmul_rn(__int2float_rn(t[2 * e]), sa), sb[2 * e]);
+        const float o1 = __fmul_rn(__fmul_rn(__int2float_rn(t[2 * e + 1]), sa), sb[2 * e + 1]);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
+        w[e] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      ptx::st_shared_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+    }
+    publish(c0);
+  }
+}
+
 template <bool kAmn, bool kBmn>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_s8f16_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = ptx::smem_addr(smem);
   const uint32_t a_base = sbase;
   const uint32_t b_base = sbase + kStages * kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  const uint32_t staging = sbase + kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kStagingBytes);
   const uint32_t bar0 = ptx::smem_addr(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
@@ -207,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+    ptx::tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
@@ -333,10 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++chunk;
       }
       if (!ok) break;
-      store_rows(p, static_cast<int64_t>(m0) + quad * 32 + lane,
-                 static_cast<int64_t>(n0) + half * 128, tot);
+      store_tile_tma(p, &tmO, staging + (warp - 2) * kStoreBoxBytes,
+                     static_cast<int64_t>(m0) + quad * 32, static_cast<int64_t>(n0) + half * 128,
+                     tot);
     }
     if (!ok && lane == 0) raise_abort(abort, p.status);
+    if (lane == 0) ptx::bulk_wait_group0();  // the tile stores are complete
   }
 
   // ------------------------------------------------------------ teardown
@@ -373,11 +453,8 @@ constexpr int kPairStages = 6;
 constexpr int kPairABytes = 128 * kBK * 2;
 constexpr int kPairBBytes = 128 * kBK * 2;
 constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
-// each epilogue warp stages its outputs in 4 KB: one 32-row x 128-byte box
-constexpr int kStoreBoxBytes = 32 * 128;
-constexpr int kPairStagingBytes = kEpiWarps * kStoreBoxBytes;
 constexpr int kPairSmemBytes =
-    1024 + kPairStages * kPairStageBytes + kPairStagingBytes + kBarrierBytes;
+    1024 + kPairStages * kPairStageBytes + kStagingBytes + kBarrierBytes;
 static_assert(kPairSmemBytes <= 227 * 1024, "pair kernel shared memory");
 constexpr int kCasLimit = 4096;  // bound on the counter's compare-and-swap retries
 constexpr int kMaxSplit = 4;     // most parts a tile of the last wave is split into
@@ -501,85 +578,6 @@ __device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int e
   }
 }
 
-// Output of one epilogue warp's part of a whole tile (rows row0 ..
-// row0+31, columns col0 .. col0+127) by TMA tensor stores, one 128-byte-wide
-// box at a time (64 bf16 or 32 int32 columns x 32 rows).  Lane l converts
-// row row0 + l and writes it into the warp's 4 KB staging buffer in the
-// 128-byte swizzled layout of the store map -- 16-byte chunk c of row r at
-// r * 128 + (c ^ (r % 8)) * 16 -- so each group of eight lanes covers all 32
-// banks.  The store clips rows and columns outside the output; a box that
-// starts at or past column N is not stored.  Before the buffer is rewritten,
-// lane 0 waits until the previous store has read it.
-__device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtensorMap* map,
-                                               uint32_t buf, int64_t row0, int64_t col0,
-                                               const int32_t (&tot)[128]) {
-  if (row0 >= p.M) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t row = row0 + lane;
-  const uint32_t dst = buf + static_cast<uint32_t>(lane) * 128u;
-  const uint32_t sw = static_cast<uint32_t>(lane & 7);
-  auto publish = [&](int64_t c0) {
-    ptx::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      ptx::tma_store_2d(map, buf, static_cast<int32_t>(c0), static_cast<int32_t>(row0));
-      ptx::bulk_commit_group();
-    }
-  };
-  auto reuse = [&]() {
-    if (lane == 0) ptx::bulk_wait_group_read0();
-    __syncwarp();
-  };
-  if (p.mode == 1) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t c0 = col0 + 32 * j;
-      if (c0 >= p.N) break;
-      reuse();
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int32_t* t = tot + 32 * j + 4 * c;
-        ptx::st_shared_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), t[0], t[1], t[2], t[3]);
-      }
-      publish(c0);
-    }
-    return;
-  }
-  const float sa = row < p.M ? __ldg(p.sA + row) : 0.0f;
-  const bool sb_vec4 = (reinterpret_cast<uintptr_t>(p.sB) & 15u) == 0;
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int64_t c0 = col0 + 64 * j;
-    if (c0 >= p.N) break;
-    reuse();
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int64_t col = c0 + 8 * c;
-      float sb[8];
-      if (col + 8 <= p.N && sb_vec4) {
-        const float4 lo = __ldg(reinterpret_cast<const float4*>(p.sB + col));
-        const float4 hi = __ldg(reinterpret_cast<const float4*>(p.sB + col) + 1);
-        sb[0] = lo.x, sb[1] = lo.y, sb[2] = lo.z, sb[3] = lo.w;
-        sb[4] = hi.x, sb[5] = hi.y, sb[6] = hi.z, sb[7] = hi.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sb[e] = col + 8 <= p.N ? __ldg(p.sB + col + e) : 0.0f;
-      }
-      const int32_t* t = tot + 64 * j + 8 * c;
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float o0 = __fmul_rn(__fmul_rn(__int2float_rn(t[2 * e]), sa), sb[2 * e]);
-        const float o1 = __fmul_rn(__fmul_rn(__int2float_rn(t[2 * e + 1]), sa), sb[2 * e + 1]);
-        const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
-        w[e] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      ptx::st_shared_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), w[0], w[1], w[2], w[3]);
-    }
-    publish(c0);
-  }
-}
-
 template <bool kAmn, bool kBmn>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_s8f16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -593,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t b_base = sbase + kPairStages * kPairABytes;
   const uint32_t staging = sbase + kPairStages * kPairStageBytes;
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes + kPairStagingBytes);
+      reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes + kStagingBytes);
   const uint32_t bar0 = ptx::smem_addr(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kPairStages + s); };
@@ -840,7 +838,7 @@ cudaError_t launch_kernel(bool pair, int grid, const CUtensorMap& mapA, const CU
     return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn>, dim3(grid), dim3(kThreads),
                              kPairSmemBytes, stream, mapA, mapB, mapO, p);
   return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn>, dim3(grid), dim3(kThreads), kSmemBytes,
-                           stream, mapA, mapB, p);
+                           stream, mapA, mapB, mapO, p);
 }
 
 }  // namespace
@@ -874,7 +872,7 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   CUtensorMap mapA, mapB, mapO;
   if (!make_operand_map(&mapA, A, a_mn, M, K, kBM) ||
       !make_operand_map(&mapB, B, b_mn, N, K, pair ? 128 : kBN) ||
-      (pair && !make_output_map(&mapO, out, mode == GemmOut::kS32, M, N, ldo)))
+      !make_output_map(&mapO, out, mode == GemmOut::kS32, M, N, ldo))
     return cudaErrorInvalidValue;
   GemmParams p;
   p.sA = sA;
