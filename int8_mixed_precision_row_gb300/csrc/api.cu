@@ -217,7 +217,7 @@ int8mp_status check_linear(int64_t T, int64_t N, int64_t K, const int8mp_linear_
 }
 
 int8mp::SrArgs sr_of(const int8mp_linear_cfg* cfg, uint32_t stream_id) {
-  return int8mp::SrArgs{cfg->seed, cfg->offset, stream_id};
+  return int8mp::make_sr(cfg->seed, cfg->offset, stream_id);
 }
 
 }  // namespace
@@ -233,7 +233,7 @@ int8mp_status int8mp_quantize_rowwise(const void* x, int64_t rows, int64_t cols,
   DeviceInfo dev;
   st = current_device(&dev, as_stream(stream));
   if (st != INT8MP_OK) return st;
-  const int8mp::SrArgs sr{seed, offset, stream_id};
+  const int8mp::SrArgs sr = int8mp::make_sr(seed, offset, stream_id);
   cudaError_t e = axis == 0
                       ? int8mp::launch_quantize_rows(x, rows, cols, ld, mode, sr, q, codes, scale,
                                                      nullptr, dev, as_stream(stream))
@@ -253,7 +253,7 @@ int8mp_status int8mp_quantize_rows_colmax(const void* x, int64_t rows, int64_t c
   DeviceInfo dev;
   st = current_device(&dev, as_stream(stream));
   if (st != INT8MP_OK) return st;
-  const int8mp::SrArgs sr{seed, offset, stream_id};
+  const int8mp::SrArgs sr = int8mp::make_sr(seed, offset, stream_id);
   return from_cuda(int8mp::launch_quantize_rows(x, rows, cols, ld, mode, sr, q, codes, scale,
                                                 colmax, dev, as_stream(stream)));
 }
@@ -269,7 +269,7 @@ int8mp_status int8mp_quantize_cols_absmax(const void* x, int64_t rows, int64_t c
   DeviceInfo dev;
   st = current_device(&dev, as_stream(stream));
   if (st != INT8MP_OK) return st;
-  const int8mp::SrArgs sr{seed, offset, stream_id};
+  const int8mp::SrArgs sr = int8mp::make_sr(seed, offset, stream_id);
   return from_cuda(int8mp::launch_quantize_cols_from_absmax(x, rows, cols, ld, colmax, mode, sr,
                                                             q, codes, scale, dev,
                                                             as_stream(stream)));

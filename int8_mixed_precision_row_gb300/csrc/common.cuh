@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "../../include/int8mp.h"
+#include "philox.cuh"
 
 namespace int8mp {
 
@@ -17,12 +18,18 @@ struct DeviceInfo {
   unsigned int* status_word = nullptr;  // device address of the status word
 };
 
-// Stochastic-rounding parameters (header of int8mp.h gives the mapping).
+// Stochastic-rounding parameters (header of int8mp.h gives the mapping),
+// with the Philox round keys of the seed computed once on the host.
 struct SrArgs {
   uint64_t seed;
   uint64_t offset;
   uint32_t stream_id;
+  PhiloxKeys keys;
 };
+
+inline SrArgs make_sr(uint64_t seed, uint64_t offset, uint32_t stream_id) {
+  return SrArgs{seed, offset, stream_id, philox_keys(seed, stream_id)};
+}
 
 // Wait limit for every bounded device-side wait, in nanoseconds of
 // %globaltimer.  Long enough that no healthy wait reaches it.

@@ -5,53 +5,80 @@
 // multiplies counter words 0 and 2 by two fixed odd constants (32x32 -> 64),
 // mixes the high halves with the other two words and the round key, and the
 // key advances by a Weyl sequence between rounds.
+//
+// The key is the same for every element of a launch, so the host computes
+// the ten round keys once (PhiloxKeys) and the kernels read them from their
+// parameters: each round is then two multiplies of each kind and two
+// three-input XORs.  Counter word 2 is the launch's stream id and word 3 is
+// 0, so round 0's second product is a launch constant too.
 #pragma once
 
 #include <stdint.h>
 
 namespace int8mp {
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
-  constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
-  constexpr uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
+constexpr uint32_t kPhiloxMulA = 0xD2511F53u, kPhiloxMulB = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxWeylA = 0x9E3779B9u, kPhiloxWeylB = 0xBB67AE85u;
+
+struct PhiloxKeys {
+  uint32_t k[20];      // round r uses key words k[2r], k[2r + 1]
+  uint32_t z_hi, z_lo; // round 0: kPhiloxMulB * stream id, high and low words
+};
+
+// Host side: the round keys of key (lo32(seed), hi32(seed)) and the round-0
+// product for counter word 2 = stream_id.
+inline PhiloxKeys philox_keys(uint64_t seed, uint32_t stream_id) {
+  PhiloxKeys p;
+  uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    p.k[2 * r] = k0;
+    p.k[2 * r + 1] = k1;
+    k0 += kPhiloxWeylA;
+    k1 += kPhiloxWeylB;
+  }
+  const uint64_t z = static_cast<uint64_t>(kPhiloxMulB) * stream_id;
+  p.z_hi = static_cast<uint32_t>(z >> 32);
+  p.z_lo = static_cast<uint32_t>(z);
+  return p;
+}
+
+// The four words of Philox4x32-10 at counter (c0, c1, stream id, 0).
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, const PhiloxKeys& pk) {
+  // round 0: word 2 * B is the launch constant (z_hi, z_lo), word 3 is 0
+  uint4 c = make_uint4(pk.z_hi ^ c1 ^ pk.k[0], pk.z_lo, __umulhi(kPhiloxMulA, c0) ^ pk.k[1],
+                       kPhiloxMulA * c0);
 #pragma unroll
-  for (int round = 0; round < 10; ++round) {
-    if (round != 0) {
-      k.x += kWeylA;
-      k.y += kWeylB;
-    }
-    const uint32_t hiA = __umulhi(kMulA, c.x), loA = kMulA * c.x;
-    const uint32_t hiB = __umulhi(kMulB, c.z), loB = kMulB * c.z;
-    c = make_uint4(hiB ^ c.y ^ k.x, loB, hiA ^ c.w ^ k.y, loA);
+  for (int round = 1; round < 10; ++round) {
+    const uint32_t hiA = __umulhi(kPhiloxMulA, c.x), loA = kPhiloxMulA * c.x;
+    const uint32_t hiB = __umulhi(kPhiloxMulB, c.z), loB = kPhiloxMulB * c.z;
+    c = make_uint4(hiB ^ c.y ^ pk.k[2 * round], loB, hiA ^ c.w ^ pk.k[2 * round + 1], loA);
   }
   return c;
 }
 
-// The eight random words for logical elements n0 .. n0+7, n0 = offset + e0.
-// Word for element n is word (n & 3) of philox at counter block n >> 2.
-__device__ __forceinline__ void philox_words8(uint64_t seed, uint64_t n0, uint32_t stream_id,
+// The eight random words for logical elements n0 .. n0+7.  Word for element
+// n is word (n & 3) of philox at counter block n >> 2.  When n0 is a
+// multiple of 4 (the usual case: every group and vector starts there) the
+// eight words are two whole blocks.
+__device__ __forceinline__ void philox_words8(const PhiloxKeys& pk, uint64_t n0,
                                               uint32_t (&w)[8]) {
-  const uint2 key = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
   const uint64_t blk = n0 >> 2;
-  const uint32_t shift = (uint32_t)(n0 & 3u);
-  uint32_t all[12];
-#pragma unroll
-  for (int b = 0; b < 3; ++b) {
-    if (b < 2 || shift != 0) {
-      const uint64_t cb = blk + (uint64_t)b;
-      const uint4 r = philox4x32_10(make_uint4((uint32_t)cb, (uint32_t)(cb >> 32), stream_id, 0u), key);
-      all[4 * b + 0] = r.x;
-      all[4 * b + 1] = r.y;
-      all[4 * b + 2] = r.z;
-      all[4 * b + 3] = r.w;
-    } else {
-      all[4 * b + 0] = all[4 * b + 1] = all[4 * b + 2] = all[4 * b + 3] = 0u;
-    }
+  const uint32_t shift = static_cast<uint32_t>(n0 & 3u);
+  const uint4 r0 = philox4x32_10(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), pk);
+  const uint4 r1 =
+      philox4x32_10(static_cast<uint32_t>(blk + 1), static_cast<uint32_t>((blk + 1) >> 32), pk);
+  if (shift == 0) {
+    w[0] = r0.x, w[1] = r0.y, w[2] = r0.z, w[3] = r0.w;
+    w[4] = r1.x, w[5] = r1.y, w[6] = r1.z, w[7] = r1.w;
+    return;
   }
+  const uint4 r2 =
+      philox4x32_10(static_cast<uint32_t>(blk + 2), static_cast<uint32_t>((blk + 2) >> 32), pk);
+  const uint32_t all[12] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w, r2.x, r2.y, r2.z, r2.w};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t a0 = all[i], a1 = all[i + 1], a2 = all[i + 2], a3 = all[i + 3];
-    w[i] = shift == 0 ? a0 : shift == 1 ? a1 : shift == 2 ? a2 : a3;
+    const uint32_t a1 = all[i + 1], a2 = all[i + 2], a3 = all[i + 3];
+    w[i] = shift == 1 ? a1 : shift == 2 ? a2 : a3;
   }
 }
 

@@ -114,7 +114,7 @@ __device__ __forceinline__ void codes_of(const float (&v)[8], const SrArgs& sr, 
                                          bool normal_scales, float (&c)[8]) {
   if (SR) {
     uint32_t w[8];
-    philox_words8(sr.seed, n0, sr.stream_id, w);
+    philox_words8(sr.keys, n0, w);
 #pragma unroll
     for (int i = 0; i < 8; ++i) c[i] = code_sr(v[i], w[i]);
   } else if (normal_scales) {
