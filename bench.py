@@ -419,7 +419,9 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
     """Square quant+scaled-mm in the three layouts: quantize A and B along K
     (by columns, codes left in place, for the operands stored K-first), then
     the matmul in the stored layout.  L2 flushed between iterations (256 MB
-    write)."""
+    write).  The iterations are queued back to back and the events read after
+    one synchronize at the end, so that the host's launch overhead does not
+    leave the device idle inside the timed intervals."""
     import torch
     import int8_mixed_precision_row_gb300 as m
     from int8_mixed_precision_row_gb300 import synth
@@ -436,7 +438,8 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
         mm_ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
         for layout, (ax_a, ax_b, lay) in (("A@B.T", (0, 0, m.INT8MP_AxBT)), ("A@B", (0, 2, m.INT8MP_AxB)),
                                           ("A.T@B", (2, 2, m.INT8MP_ATxB))):
-            tq, tm = [], []
+            events = []
+            torch.cuda.synchronize()
             for it in range(iters + 3):
                 flush.fill_(it & 0xFF)
                 e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -446,10 +449,11 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
                 e[1].record()
                 m.int8mp_scaled_mm(qa, sa, qb, sb, layout=lay, out=Y, workspace=mm_ws)
                 e[2].record()
-                torch.cuda.synchronize()
                 if it >= 3:
-                    tq.append(e[0].elapsed_time(e[1]))
-                    tm.append(e[1].elapsed_time(e[2]))
+                    events.append(e)
+            torch.cuda.synchronize()
+            tq = [e[0].elapsed_time(e[1]) for e in events]
+            tm = [e[1].elapsed_time(e[2]) for e in events]
             q_ms, mm_ms = statistics.median(tq), statistics.median(tm)
             ops = 2.0 * S ** 3
             out[f"{S}:{layout}"] = {
