@@ -418,14 +418,17 @@ def cpu_baseline(spec):
 def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
     """Square quant+scaled-mm in the three layouts: quantize A and B along K
     (by columns, codes left in place, for the operands stored K-first), then
-    the matmul in the stored layout.  L2 flushed between iterations (256 MB
-    write).  The iterations are queued back to back and the events read after
-    one synchronize at the end, so that the host's launch overhead does not
-    leave the device idle inside the timed intervals."""
+    the matmul in the stored layout.  L2 flushed between iterations: a 256 MB
+    write, then a read of another 256 MB buffer, so that the flush's dirty
+    lines are written back before the timed kernels start (they would
+    otherwise pay for them).  The iterations are queued back to back and the
+    events read after one synchronize at the end, so that the host's launch
+    overhead does not leave the device idle inside the timed intervals."""
     import torch
     import int8_mixed_precision_row_gb300 as m
     from int8_mixed_precision_row_gb300 import synth
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    clean = torch.zeros(64 << 20, dtype=torch.float32, device=device)  # 256 MB, read
     out = {}
     for S in sizes:
         A, B = synth.square_inputs(S, "AxBT")
@@ -442,6 +445,7 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
             torch.cuda.synchronize()
             for it in range(iters + 3):
                 flush.fill_(it & 0xFF)
+                clean.max()
                 e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
                 e[0].record()
                 m.int8mp_quantize_rowwise(A, axis=ax_a, codes=m.INT8MP_CODES_F16, q=qa, scale=sa)
@@ -521,8 +525,8 @@ def pass_switch_table(spec, device, steps=5, warmup=2):
 # `python bench.py --steps 2 --warmup 3 --profile-steps` (one pass per
 # launch), valid for the GEMM sources whose digest is given (reported as null
 # once they change).
-GEMM_TRAFFIC = {"bytes_per_launch": 429371092, "sources_sha256_16": "14351cc8e230fde9"}
-GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "common.cuh")
+GEMM_TRAFFIC = {"bytes_per_launch": 429371092, "sources_sha256_16": "4d8d2848f9ef7299"}
+GEMM_SOURCES = ("gemm.cu", "ptx.cuh")
 
 
 def gemm_sources_digest():

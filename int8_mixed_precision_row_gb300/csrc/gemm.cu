@@ -166,18 +166,47 @@ __device__ __forceinline__ void drain_chunk(uint32_t taddr, int32_t (&tot)[128])
   }
 }
 
+// Scales of an epilogue warp's part of a tile (rows row0 .. row0+31,
+// columns col0 .. col0+127) for launches whose CTAs have at most two tiles
+// each (kRegScales), where the store's own scale loads -- a DRAM round trip
+// per 64 columns -- would add straight to the kernel's time: loaded when the
+// tile starts, so that their latency hides behind its MMAs.  Lane l holds
+// its row's scale and the column scales col0 + 32 q + l in sb[q].  Outside
+// the output they are 0; int32 outputs need none.  Launches with more tiles
+// per CTA hide the store's latency behind the next tile's MMAs instead and
+// load nothing here.
+struct TileScales {
+  float sa;
+  float sb[4];
+};
+template <bool kRegScales>
+__device__ __forceinline__ TileScales load_tile_scales(const GemmParams& p, int64_t row0,
+                                                       int64_t col0) {
+  TileScales t{0.0f, {0.0f, 0.0f, 0.0f, 0.0f}};
+  if (!kRegScales || p.mode == 1) return t;
+  const int lane = threadIdx.x & 31;
+  if (row0 + lane < p.M) t.sa = __ldg(p.sA + row0 + lane);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (col0 + 32 * q + lane < p.N) t.sb[q] = __ldg(p.sB + col0 + 32 * q + lane);
+  return t;
+}
+
 // Output of one epilogue warp's part of a whole tile (rows row0 ..
 // row0+31, columns col0 .. col0+127) by TMA tensor stores, one 128-byte-wide
 // box at a time (64 bf16 or 32 int32 columns x 32 rows).  Lane l converts
 // row row0 + l and writes it into the warp's 4 KB staging buffer in the
 // 128-byte swizzled layout of the store map -- 16-byte chunk c of row r at
 // r * 128 + (c ^ (r % 8)) * 16 -- so each group of eight lanes covers all 32
-// banks.  The store clips rows and columns outside the output; a box that
-// starts at or past column N is not stored.  Before the buffer is rewritten,
-// lane 0 waits until the previous store has read it.
+// banks.  The scales come from ts (kRegScales: the column scales by shuffles
+// from the lanes holding them) or from global memory.  The store clips rows
+// and columns outside the output; a box that starts at or past column N is
+// not stored.  Before the buffer is rewritten, lane 0 waits until the
+// previous store has read it.
+template <bool kRegScales>
 __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtensorMap* map,
                                                uint32_t buf, int64_t row0, int64_t col0,
-                                               const int32_t (&tot)[128]) {
+                                               const TileScales& ts, const int32_t (&tot)[128]) {
   if (row0 >= p.M) return;
   const int lane = threadIdx.x & 31;
   const int64_t row = row0 + lane;
@@ -210,7 +239,7 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
     }
     return;
   }
-  const float sa = row < p.M ? __ldg(p.sA + row) : 0.0f;
+  const float sa = kRegScales ? ts.sa : row < p.M ? __ldg(p.sA + row) : 0.0f;
   const bool sb_vec4 = (reinterpret_cast<uintptr_t>(p.sB) & 15u) == 0;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
@@ -221,7 +250,13 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
     for (int c = 0; c < 8; ++c) {
       const int64_t col = c0 + 8 * c;
       float sb[8];
-      if (col + 8 <= p.N && sb_vec4) {
+      if (kRegScales) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int k = 64 * j + 8 * c + e;  // column col0 + k
+          sb[e] = __shfl_sync(0xFFFFFFFFu, ts.sb[k >> 5], k & 31);
+        }
+      } else if (col + 8 <= p.N && sb_vec4) {
         const float4 lo = __ldg(reinterpret_cast<const float4*>(p.sB + col));
         const float4 hi = __ldg(reinterpret_cast<const float4*>(p.sB + col) + 1);
         sb[0] = lo.x, sb[1] = lo.y, sb[2] = lo.z, sb[3] = lo.w;
@@ -245,7 +280,7 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
   }
 }
 
-template <bool kAmn, bool kBmn>
+template <bool kAmn, bool kBmn, bool kRegScales>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_s8f16_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
@@ -389,6 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       const int m0 = (tile / p.n_tiles) * kBM;
       const int n0 = (tile % p.n_tiles) * kBN;
+      const TileScales ts = load_tile_scales<kRegScales>(
+          p, static_cast<int64_t>(m0) + quad * 32, static_cast<int64_t>(n0) + half * 128);
       int32_t tot[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) tot[i] = 0;
@@ -411,9 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++chunk;
       }
       if (!ok) break;
-      store_tile_tma(p, &tmO, staging + (warp - 2) * kStoreBoxBytes,
-                     static_cast<int64_t>(m0) + quad * 32, static_cast<int64_t>(n0) + half * 128,
-                     tot);
+      store_tile_tma<kRegScales>(p, &tmO, staging + (warp - 2) * kStoreBoxBytes,
+                                 static_cast<int64_t>(m0) + quad * 32,
+                                 static_cast<int64_t>(n0) + half * 128, ts, tot);
     }
     if (!ok && lane == 0) raise_abort(abort, p.status);
     if (lane == 0) ptx::bulk_wait_group0();  // the tile stores are complete
@@ -578,7 +615,7 @@ __device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int e
   }
 }
 
-template <bool kAmn, bool kBmn>
+template <bool kAmn, bool kBmn, bool kRegScales>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_s8f16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -733,6 +770,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
       const int m0 = (tile / p.n_tiles) * 256 + static_cast<int>(rank) * 128;
       const int n0 = (tile % p.n_tiles) * 256;
+      const bool whole = kb0 == 0 && kb1 == p.k_blocks;
+      TileScales ts{0.0f, {0.0f, 0.0f, 0.0f, 0.0f}};
+      if (whole)
+        ts = load_tile_scales<kRegScales>(p, static_cast<int64_t>(m0) + quad * 32,
+                                          static_cast<int64_t>(n0) + half * 128);
       int32_t tot[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) tot[i] = 0;
@@ -757,8 +799,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const int64_t row = static_cast<int64_t>(m0) + quad * 32 + lane;
       const int64_t col0 = static_cast<int64_t>(n0) + half * 128;
-      if (kb0 == 0 && kb1 == p.k_blocks) {
-        store_tile_tma(p, &tmO, staging + (warp - 2) * kStoreBoxBytes, row - lane, col0, tot);
+      if (whole) {
+        store_tile_tma<kRegScales>(p, &tmO, staging + (warp - 2) * kStoreBoxBytes, row - lane,
+                                   col0, ts, tot);
       } else {
         sk_store_part(p, pair, static_cast<int>(rank), warp - 2, tot);
         sk_complete(p, static_cast<int>(rank), warp - 2, tile, row, col0, abort);
@@ -797,12 +840,12 @@ bool make_operand_map(CUtensorMap* map, const void* base, bool mn_major, int64_t
                               CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <bool kAmn, bool kBmn>
+template <bool kAmn, bool kBmn, bool kRegScales>
 cudaError_t set_smem_attrs() {
-  cudaError_t err = cudaFuncSetAttribute(gemm_s8f16_kernel<kAmn, kBmn>,
+  cudaError_t err = cudaFuncSetAttribute(gemm_s8f16_kernel<kAmn, kBmn, kRegScales>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn>,
+    err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
   return err;
 }
@@ -831,14 +874,22 @@ bool make_output_map(CUtensorMap* map, void* out, bool s32, int64_t M, int64_t N
                               CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <bool kAmn, bool kBmn>
+template <bool kAmn, bool kBmn, bool kRegScales>
 cudaError_t launch_kernel(bool pair, int grid, const CUtensorMap& mapA, const CUtensorMap& mapB,
                           const CUtensorMap& mapO, const GemmParams& p, cudaStream_t stream) {
   if (pair)
-    return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn>, dim3(grid), dim3(kThreads),
-                             kPairSmemBytes, stream, mapA, mapB, mapO, p);
-  return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn>, dim3(grid), dim3(kThreads), kSmemBytes,
-                           stream, mapA, mapB, mapO, p);
+    return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales>, dim3(grid),
+                             dim3(kThreads), kPairSmemBytes, stream, mapA, mapB, mapO, p);
+  return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn, kRegScales>, dim3(grid), dim3(kThreads),
+                           kSmemBytes, stream, mapA, mapB, mapO, p);
+}
+
+template <bool kAmn, bool kBmn>
+cudaError_t launch_layout(bool pair, bool reg_scales, int grid, const CUtensorMap& mapA,
+                          const CUtensorMap& mapB, const CUtensorMap& mapO, const GemmParams& p,
+                          cudaStream_t stream) {
+  return reg_scales ? launch_kernel<kAmn, kBmn, true>(pair, grid, mapA, mapB, mapO, p, stream)
+                    : launch_kernel<kAmn, kBmn, false>(pair, grid, mapA, mapB, mapO, p, stream);
 }
 
 }  // namespace
@@ -857,9 +908,12 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
     std::lock_guard<std::mutex> lock(mu);
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[device]) {
-      err = set_smem_attrs<false, false>();
-      if (err == cudaSuccess) err = set_smem_attrs<false, true>();
-      if (err == cudaSuccess) err = set_smem_attrs<true, true>();
+      err = set_smem_attrs<false, false, false>();
+      if (err == cudaSuccess) err = set_smem_attrs<false, true, false>();
+      if (err == cudaSuccess) err = set_smem_attrs<true, true, false>();
+      if (err == cudaSuccess) err = set_smem_attrs<false, false, true>();
+      if (err == cudaSuccess) err = set_smem_attrs<false, true, true>();
+      if (err == cudaSuccess) err = set_smem_attrs<true, true, true>();
       if (err != cudaSuccess) return err;
       attr_set[device] = true;
     }
@@ -921,9 +975,13 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
       grid = static_cast<int>(2 * npairs);
     }
   }
-  if (!a_mn && !b_mn) return launch_kernel<false, false>(pair, grid, mapA, mapB, mapO, p, stream);
-  if (!a_mn) return launch_kernel<false, true>(pair, grid, mapA, mapB, mapO, p, stream);
-  return launch_kernel<true, true>(pair, grid, mapA, mapB, mapO, p, stream);
+  // at most two tiles per CTA (pair): the scales are loaded when a tile starts
+  const int units = grid / (pair ? 2 : 1);
+  const bool reg_scales = static_cast<int64_t>(p.dp_tiles) <= 2 * units;
+  if (!a_mn && !b_mn)
+    return launch_layout<false, false>(pair, reg_scales, grid, mapA, mapB, mapO, p, stream);
+  if (!a_mn) return launch_layout<false, true>(pair, reg_scales, grid, mapA, mapB, mapO, p, stream);
+  return launch_layout<true, true>(pair, reg_scales, grid, mapA, mapB, mapO, p, stream);
 }
 
 }  // namespace int8mp

@@ -87,11 +87,10 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 __device__ __forceinline__ float code_rne(float v) {
   return fminf(fmaxf(rintf(v), -127.0f), 127.0f);
 }
-// Same when the group scale is a normal number s = RN(absmax / 127): then
+// When the group scale is a normal number s = RN(absmax / 127),
 // s >= (absmax / 127)(1 - 2^-24), so |v| <= 127 (1 + 2^-23) < 127.5 and
-// rounding cannot leave [-127, 127]; the clamp is dropped.
-__device__ __forceinline__ float code_rne_normal_scale(float v) { return rintf(v); }
-// Two such codes with two packed fp32 adds: for |v| < 2^22, v + 1.5 * 2^23
+// rounding cannot leave [-127, 127]: the clamp is dropped, and two codes
+// take two packed fp32 adds: for |v| < 2^22, v + 1.5 * 2^23
 // lies in [2^23, 2^24), where the spacing of floats is 1, so the nearest-even
 // rounding of the sum is 1.5 * 2^23 plus the nearest-even integer to v (the
 // constant is even), and subtracting the constant back is exact.
@@ -100,23 +99,28 @@ __device__ __forceinline__ float2 code_rne_normal_scale2(float2 v) {
   const float2 t = __fadd2_rn(v, make_float2(kMagic, kMagic));
   return __fadd2_rn(t, make_float2(-kMagic, -kMagic));
 }
+// kClamp false: the caller clamps afterwards (f16 codes, as packed half2
+// min/max: every unclamped code is an integer or +-inf after the f16
+// conversion, which is monotonic, so clamping after it gives the same codes).
+template <bool kClamp>
 __device__ __forceinline__ float code_sr(float v, uint32_t word) {
   const float f = floorf(v);
   const float fr = __fsub_rn(v, f);
   const float q = (sr_uniform(word) < fr) ? __fadd_rn(f, 1.0f) : f;
-  return fminf(fmaxf(q, -127.0f), 127.0f);
+  return kClamp ? fminf(fmaxf(q, -127.0f), 127.0f) : q;
 }
 
 // Eight codes from eight quotients (elements n0 .. n0+7 of the SR stream).
 // normal_scales: every element's group scale is at least 2^-126.
-template <bool SR>
+// kSrClamp false: stochastic codes are left unclamped for a later half2 clamp.
+template <bool SR, bool kSrClamp = true>
 __device__ __forceinline__ void codes_of(const float (&v)[8], const SrArgs& sr, uint64_t n0,
                                          bool normal_scales, float (&c)[8]) {
   if (SR) {
     uint32_t w[8];
     philox_words8(sr.keys, n0, w);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = code_sr(v[i], w[i]);
+    for (int i = 0; i < 8; ++i) c[i] = code_sr<kSrClamp>(v[i], w[i]);
   } else if (normal_scales) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -206,11 +210,15 @@ __device__ __forceinline__ void quantize_two(const uint4& a, const uint4& b, boo
     div8_ieee(fa, d.s, va);
     div8_ieee(fb, d.s, vb);
   }
-  codes_of<SR>(va, sr, na, normal, c);
+  // f16 stochastic codes: clamped as packed half2 after the conversion
+  constexpr bool kHalfClamp = SR && std::is_same<CodeT, __half>::value;
+  codes_of<SR, !kHalfClamp>(va, sr, na, normal, c);
   *qa = Pack8<CodeT>::pack(c);
+  if (kHalfClamp) *qa = clamp_half8(*qa);
   if (has_b) {
-    codes_of<SR>(vb, sr, nb, normal, c);
+    codes_of<SR, !kHalfClamp>(vb, sr, nb, normal, c);
     *qb = Pack8<CodeT>::pack(c);
+    if (kHalfClamp) *qb = clamp_half8(*qb);
   }
 }
 
@@ -518,8 +526,9 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
   const int64_t r1 = min(rows, r0 + rows_per_block);
   // f16 codes from a given absmax keep their clamp as a packed half2 min/max
   // after rounding (a caller's absmax below the true one would otherwise let
-  // a code leave [-127, 127]); int8 codes from it clamp before packing
-  constexpr bool kHalfClamp = kFromAbsmax && !SR && std::is_same<CodeT, __half>::value;
+  // a code leave [-127, 127]), and so do f16 stochastic codes; int8 codes
+  // clamp before packing
+  constexpr bool kHalfClamp = (kFromAbsmax || SR) && std::is_same<CodeT, __half>::value;
   float s[8], r[8];
   bool all_fast = true, normal = !kFromAbsmax || kHalfClamp;
 #pragma unroll
@@ -550,7 +559,8 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
         float f[8], v[8], cd[8];
         unpack8(a[u], f);
         if (!div8_each_try(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
-        codes_of<SR>(v, sr, sr.offset + static_cast<uint64_t>(row * cols + c), normal, cd);
+        codes_of<SR, !kHalfClamp>(v, sr, sr.offset + static_cast<uint64_t>(row * cols + c),
+                                  normal, cd);
         typename P::Vec out = P::pack(cd);
         if (kHalfClamp) out = clamp_half8(out);
         if (in_bounds(row < rows, status))
