@@ -213,10 +213,11 @@ class LayerStep:
         # GEMM operands read once (f16 codes) and bf16 outputs written, per step
         self.gemm_bytes = 6.0 * sum(T * l["K"] + T * l["N"] + l["N"] * l["K"] for l in self.linears)
         self.gemms_per_step = 3 * len(self.linears)
-        # kernels of this library per step and linear: three row quantizations
-        # (each also recording column absmax), three column quantizations
-        # (codes from that absmax), three GEMMs
-        self.kernels_per_step = len(self.linears) * (3 + 3 + 3)
+        # kernels of this library per step and linear: two row-quantization
+        # launches (X and W together, then dY; each also recording column
+        # absmax), three column quantizations (codes from that absmax), three
+        # GEMMs
+        self.kernels_per_step = len(self.linears) * (2 + 3 + 3)
         # algorithmic quantize bytes: bf16 read once, code (f16 container) and scale written
         self.quant_elems = sum(2 * (T * l["K"] + l["N"] * l["K"] + T * l["N"]) for l in self.linears)
 
@@ -235,6 +236,16 @@ class LayerStep:
             s = sbuf[:cols]
             m.int8mp_quantize_cols_absmax(x, colmax, scale=s, **kw)
         return q, s
+
+    def _q_rows2(self, X, W, cx, cw, seed, offset):
+        """X and W by rows in one launch, each recording its column absmax."""
+        m = self.m
+        (T, K), N = X.shape, W.shape[0]
+        return m.int8mp_quantize_rows_batch(
+            [X, W], mode=self.mode, seed=seed, offsets=[offset, offset],
+            stream_ids=[m.INT8MP_STREAM_FWD_X, m.INT8MP_STREAM_FWD_W], codes=m.INT8MP_CODES_F16,
+            qs=[self.qa[:T * K].view(T, K), self.qb[:N * K].view(N, K)],
+            scales=[self.sa[:T], self.sb[:N]], colmaxes=[cx, cw])
 
     def run(self, timers=None, seed=0, offset=0):
         """One step.  timers: optional dict of kernel class -> list of
@@ -258,9 +269,9 @@ class LayerStep:
             K = l["K"]
             cm = l["colmax"]
             cx, cw, cg = cm[:K], cm[K:2 * K], cm[2 * K:]
-            # forward: X and W along K (their rows); their column absmax on the way
-            qx, sx = rec("quant_rows", lambda: self._q(X, 0, m.INT8MP_STREAM_FWD_X, self.qa, self.sa, seed, offset, cx))
-            qw, sw = rec("quant_rows", lambda: self._q(W, 0, m.INT8MP_STREAM_FWD_W, self.qb, self.sb, seed, offset, cw))
+            # forward: X and W along K (their rows, one launch); their column
+            # absmax on the way
+            (qx, sx), (qw, sw) = rec("quant_rows", lambda: self._q_rows2(X, W, cx, cw, seed, offset))
             rec("gemm", lambda: m.int8mp_scaled_mm(qx, sx, qw, sw, out=l["Y"], workspace=self.mm_ws))
             # grad input: dY along N (rows), W along N (columns, codes [N, K]): A @ B
             qg, sg = rec("quant_rows", lambda: self._q(dY, 0, m.INT8MP_STREAM_GI_DY, self.qa, self.sa, seed, offset, cg))
@@ -448,8 +459,14 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
                 clean.max()
                 e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
                 e[0].record()
-                m.int8mp_quantize_rowwise(A, axis=ax_a, codes=m.INT8MP_CODES_F16, q=qa, scale=sa)
-                m.int8mp_quantize_rowwise(B, axis=ax_b, codes=m.INT8MP_CODES_F16, q=qb, scale=sb)
+                if ax_a == 0 and ax_b == 0:  # both by rows: one launch
+                    m.int8mp_quantize_rows_batch([A, B], codes=m.INT8MP_CODES_F16, qs=[qa, qb],
+                                                 scales=[sa, sb])
+                else:
+                    m.int8mp_quantize_rowwise(A, axis=ax_a, codes=m.INT8MP_CODES_F16, q=qa,
+                                              scale=sa)
+                    m.int8mp_quantize_rowwise(B, axis=ax_b, codes=m.INT8MP_CODES_F16, q=qb,
+                                              scale=sb)
                 e[1].record()
                 m.int8mp_scaled_mm(qa, sa, qb, sb, layout=lay, out=Y, workspace=mm_ws)
                 e[2].record()

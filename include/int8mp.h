@@ -157,6 +157,44 @@ int8mp_status int8mp_quantize_rows_colmax(const void* x, int64_t rows, int64_t c
                                           float* scale, float* colmax, void* stream);
 
 /*
+ * int8mp_quantize_rows_batch -- row groups (INT8MP_GROUP_ROWS) of up to two
+ * matrices with the same row length in one launch, e.g. the activations and
+ * the weight of a linear layer's forward pass.  The codes, scales and column
+ * maxima are those of one int8mp_quantize_rows_colmax call per job (colmax
+ * given) or one int8mp_quantize_rowwise call with INT8MP_GROUP_ROWS per job
+ * (colmax NULL), with the mode, seed and codes given here and each job's own
+ * offset and stream_id.
+ *   jobs    njobs job descriptions (host memory, read during the call):
+ *             x       bf16 [rows, cols], row stride ld elements
+ *             rows, ld
+ *             offset, stream_id   the job's place in the stochastic-rounding
+ *                                 stream (as for int8mp_quantize_rowwise)
+ *             q       codes [rows, cols] (container per `codes`)
+ *             scale   fp32 [rows]
+ *             colmax  fp32 [cols] column absmax, merged by atomic max, or
+ *                     NULL -- the same for every job
+ *   njobs   1 .. INT8MP_MAX_ROWS_JOBS.
+ * Requirements: every job those of int8mp_quantize_rowwise with
+ * INT8MP_GROUP_ROWS, and of int8mp_quantize_rows_colmax when colmax is
+ * given; a job with rows == 0 is skipped.  jobs NULL, njobs out of range, or
+ * colmax given for some jobs only: INT8MP_ERR_INVALID_ARG.
+ */
+#define INT8MP_MAX_ROWS_JOBS 2
+typedef struct {
+  const void* x;
+  int64_t rows;
+  int64_t ld;
+  uint64_t offset;
+  uint32_t stream_id;
+  void* q;
+  float* scale;
+  float* colmax;
+} int8mp_rows_job;
+int8mp_status int8mp_quantize_rows_batch(const int8mp_rows_job* jobs, int njobs, int64_t cols,
+                                         int8mp_round mode, uint64_t seed, int8mp_codes codes,
+                                         void* stream);
+
+/*
  * int8mp_quantize_cols_absmax -- column groups with the codes in the input's
  * layout (as INT8MP_GROUP_COLS), given each column's absmax (fp32 [cols],
  * e.g. from int8mp_quantize_rows_colmax over the same x): scale[c] =

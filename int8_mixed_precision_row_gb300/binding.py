@@ -29,6 +29,7 @@ INT8MP_CODES_S8, INT8MP_CODES_F16 = 0, 1
 (INT8MP_STREAM_FWD_X, INT8MP_STREAM_FWD_W, INT8MP_STREAM_GI_DY, INT8MP_STREAM_GI_W,
  INT8MP_STREAM_GW_DY, INT8MP_STREAM_GW_X) = range(6)
 INT8MP_MAX_K = 133143
+INT8MP_MAX_ROWS_JOBS = 2
 
 # every symbol the public headers declare
 EXPORTED = (
@@ -38,7 +39,7 @@ EXPORTED = (
     "int8mp_debug_mm_s32_drop_first_load", "int8mp_linear_fwd_noalloc",
     "int8mp_debug_check_division", "int8mp_quantize_rows_colmax", "int8mp_quantize_cols_absmax",
     "int8mp_linear_fwd_save", "int8mp_linear_bwd_saved", "int8mp_mm_workspace_size",
-    "int8mp_scaled_mm_ws", "int8mp_mm_s32_ws",
+    "int8mp_scaled_mm_ws", "int8mp_mm_s32_ws", "int8mp_quantize_rows_batch",
 )
 INT8MP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -47,6 +48,12 @@ class Int8mpError(RuntimeError):
     def __init__(self, status, what):
         self.status = status
         super().__init__(f"{what}: {int8mp_status_string(status)} (status {status})")
+
+
+class int8mp_rows_job(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("ld", ctypes.c_int64),
+                ("offset", ctypes.c_uint64), ("stream_id", ctypes.c_uint32),
+                ("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("colmax", ctypes.c_void_p)]
 
 
 class int8mp_linear_cfg(ctypes.Structure):
@@ -126,6 +133,8 @@ def load(path=None):
                                          ctypes.POINTER(int8mp_linear_cfg), _P, _P, _SZ, _P]
     L.int8mp_linear_bwd_saved.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64,
                                           ctypes.POINTER(int8mp_linear_cfg), _P, _P, _SZ, _P]
+    L.int8mp_quantize_rows_batch.argtypes = [ctypes.POINTER(int8mp_rows_job), _INT, _I64, _INT, _U64,
+                                             _INT, _P]
     L.int8mp_mm_workspace_size.argtypes = []
     L.int8mp_mm_workspace_size.restype = _SZ
     L.int8mp_scaled_mm_ws.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _I64, _P,
@@ -222,6 +231,38 @@ def int8mp_quantize_rows_colmax(x, colmax, mode=INT8MP_RNE, seed=0, offset=0, st
                                               _ptr(scale), _ptr(colmax), _stream(stream)),
            "int8mp_quantize_rows_colmax")
     return q, scale
+
+
+def int8mp_quantize_rows_batch(xs, mode=INT8MP_RNE, seed=0, offsets=None, stream_ids=None,
+                               codes=INT8MP_CODES_S8, qs=None, scales=None, colmaxes=None,
+                               stream=None):
+    """Row groups of up to two bf16 matrices with the same number of columns
+    in one launch; as one int8mp_quantize_rows_colmax call per matrix when
+    colmaxes is given, else as int8mp_quantize_rowwise(axis=0).  Returns the
+    list of (codes, scale) pairs."""
+    n = len(xs)
+    cols = xs[0].shape[1]
+    offsets = offsets or [0] * n
+    stream_ids = stream_ids or [0] * n
+    qs = qs or [None] * n
+    scales = scales or [None] * n
+    colmaxes = colmaxes or [None] * n
+    arr = (int8mp_rows_job * max(n, 1))()
+    out = []
+    for i, x in enumerate(xs):
+        assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda and x.shape[1] == cols
+        rows = x.shape[0]
+        q = qs[i] if qs[i] is not None else torch.empty((rows, cols), dtype=_code_dtype(codes),
+                                                        device=x.device)
+        sc = scales[i] if scales[i] is not None else torch.empty((rows,), dtype=torch.float32,
+                                                                 device=x.device)
+        arr[i] = int8mp_rows_job(x.data_ptr(), rows, x.stride(0) if rows > 0 else cols,
+                                 int(offsets[i]), int(stream_ids[i]), q.data_ptr(), sc.data_ptr(),
+                                 colmaxes[i].data_ptr() if colmaxes[i] is not None else None)
+        out.append((q, sc))
+    _check(load().int8mp_quantize_rows_batch(arr, n, cols, int(mode), int(seed), int(codes),
+                                             _stream(stream)), "int8mp_quantize_rows_batch")
+    return out
 
 
 def int8mp_quantize_cols_absmax(x, colmax, mode=INT8MP_RNE, seed=0, offset=0, stream_id=0,

@@ -258,6 +258,31 @@ int8mp_status int8mp_quantize_rows_colmax(const void* x, int64_t rows, int64_t c
                                                 colmax, dev, as_stream(stream)));
 }
 
+int8mp_status int8mp_quantize_rows_batch(const int8mp_rows_job* jobs, int njobs, int64_t cols,
+                                         int8mp_round mode, uint64_t seed, int8mp_codes codes,
+                                         void* stream) {
+  if (!jobs || njobs < 1 || njobs > INT8MP_MAX_ROWS_JOBS) return INT8MP_ERR_INVALID_ARG;
+  int8mp::RowsJob run[INT8MP_MAX_ROWS_JOBS];
+  int nrun = 0;
+  const bool cm = jobs[0].colmax != nullptr;
+  for (int i = 0; i < njobs; ++i) {
+    const int8mp_rows_job& j = jobs[i];
+    int8mp_status st = check_quantize(j.x, j.rows, cols, j.ld, 0, mode, j.q, codes, j.scale);
+    if (st != INT8MP_OK) return st;
+    if ((j.colmax != nullptr) != cm) return INT8MP_ERR_INVALID_ARG;
+    if (cm && !aligned(j.colmax, 4)) return INT8MP_ERR_ALIGNMENT;
+    if (j.rows > 0 && cols > 0)
+      run[nrun++] = int8mp::RowsJob{j.x, j.rows, j.ld, j.q, j.scale, j.colmax, j.offset,
+                                    j.stream_id};
+  }
+  if (nrun == 0) return INT8MP_OK;
+  DeviceInfo dev;
+  int8mp_status st = current_device(&dev, as_stream(stream));
+  if (st != INT8MP_OK) return st;
+  return from_cuda(int8mp::launch_quantize_rows_jobs(run, nrun, cols, mode, seed, codes, dev,
+                                                     as_stream(stream)));
+}
+
 int8mp_status int8mp_quantize_cols_absmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                           const float* colmax, int8mp_round mode, uint64_t seed,
                                           uint64_t offset, uint32_t stream_id, void* q,
@@ -369,11 +394,23 @@ int8mp_status linear_fwd_impl(const void* X, const void* W, void* Y, int64_t T, 
   const QOperand xq = carve_operand(c, T, K);
   const QOperand wq = carve_operand(c, N, K);
   if (K > 0) {
-    cudaError_t e = int8mp::launch_quantize_rows(X, T, K, K, cfg->mode, sr_of(cfg, INT8MP_STREAM_FWD_X),
-                                                 xq.q, INT8MP_CODES_F16, xq.s, x_absmax, dev, s);
-    if (e == cudaSuccess)
-      e = int8mp::launch_quantize_rows(W, N, K, K, cfg->mode, sr_of(cfg, INT8MP_STREAM_FWD_W), wq.q,
-                                       INT8MP_CODES_F16, wq.s, w_absmax, dev, s);
+    // X and W by rows: one launch when both keep their column maxima or
+    // neither does, else one each
+    int8mp::RowsJob jobs[2];
+    int n = 0;
+    if (T > 0)
+      jobs[n++] = int8mp::RowsJob{X, T, K, xq.q, xq.s, x_absmax, cfg->offset, INT8MP_STREAM_FWD_X};
+    if (N > 0)
+      jobs[n++] = int8mp::RowsJob{W, N, K, wq.q, wq.s, w_absmax, cfg->offset, INT8MP_STREAM_FWD_W};
+    cudaError_t e = cudaSuccess;
+    if (n == 2 && (x_absmax != nullptr) == (w_absmax != nullptr)) {
+      e = int8mp::launch_quantize_rows_jobs(jobs, 2, K, cfg->mode, cfg->seed, INT8MP_CODES_F16,
+                                            dev, s);
+    } else {
+      for (int i = 0; i < n && e == cudaSuccess; ++i)
+        e = int8mp::launch_quantize_rows_jobs(jobs + i, 1, K, cfg->mode, cfg->seed,
+                                              INT8MP_CODES_F16, dev, s);
+    }
     if (e != cudaSuccess) return INT8MP_ERR_CUDA;
   }
   return run_mm(xq.q, xq.s, wq.q, wq.s, T, N, K, INT8MP_AxBT, int8mp::GemmOut::kBf16Scaled, Y, N,

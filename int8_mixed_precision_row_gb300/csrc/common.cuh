@@ -19,17 +19,34 @@ struct DeviceInfo {
 };
 
 // Stochastic-rounding parameters (header of int8mp.h gives the mapping),
-// with the Philox round keys of the seed computed once on the host.
+// with the Philox round keys of the seed and the stream's round-0 product
+// computed once on the host.
 struct SrArgs {
   uint64_t seed;
   uint64_t offset;
   uint32_t stream_id;
   PhiloxKeys keys;
+  PhiloxStream stream;
 };
 
 inline SrArgs make_sr(uint64_t seed, uint64_t offset, uint32_t stream_id) {
-  return SrArgs{seed, offset, stream_id, philox_keys(seed, stream_id)};
+  return SrArgs{seed, offset, stream_id, philox_keys(seed), philox_stream(stream_id)};
 }
+
+// One matrix of a row-quantization launch (launch_quantize_rows_jobs):
+// x [rows, cols] bf16 at row stride ld, codes q [rows, cols], scales
+// [rows], column absmax colmax [cols] (updated) or null; offset and
+// stream_id place its elements in the stochastic-rounding stream.
+struct RowsJob {
+  const void* x;
+  int64_t rows, ld;
+  void* q;
+  float* scale;
+  float* colmax;
+  uint64_t offset;
+  uint32_t stream_id;
+};
+constexpr int kMaxRowsJobs = 2;
 
 // Wait limit for every bounded device-side wait, in nanoseconds of
 // %globaltimer.  Long enough that no healthy wait reaches it.
@@ -71,6 +88,12 @@ bool encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataTyp
 // ---- quantize (quantize.cu) ------------------------------------------------
 // x bf16 [rows, cols] stride ld.  Row groups: q [rows, cols]; scale [rows].
 // colmax (optional, fp32 [cols]): each column's absmax is max-merged into it.
+// One launch for up to kMaxRowsJobs matrices with the same row length (two
+// when their rows fit shared memory, one per matrix otherwise); every job
+// has a colmax or none has.
+cudaError_t launch_quantize_rows_jobs(const RowsJob* jobs, int njobs, int64_t cols,
+                                      int8mp_round mode, uint64_t seed, int8mp_codes codes,
+                                      const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                  int8mp_round mode, const SrArgs& sr, void* q,
                                  int8mp_codes codes, float* scale, float* colmax,

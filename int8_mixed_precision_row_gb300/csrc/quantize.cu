@@ -114,11 +114,12 @@ __device__ __forceinline__ float code_sr(float v, uint32_t word) {
 // normal_scales: every element's group scale is at least 2^-126.
 // kSrClamp false: stochastic codes are left unclamped for a later half2 clamp.
 template <bool SR, bool kSrClamp = true>
-__device__ __forceinline__ void codes_of(const float (&v)[8], const SrArgs& sr, uint64_t n0,
-                                         bool normal_scales, float (&c)[8]) {
+__device__ __forceinline__ void codes_of(const float (&v)[8], const PhiloxKeys& keys,
+                                         PhiloxStream st, uint64_t n0, bool normal_scales,
+                                         float (&c)[8]) {
   if (SR) {
     uint32_t w[8];
-    philox_words8(sr.keys, n0, w);
+    philox_words8(keys, st, n0, w);
 #pragma unroll
     for (int i = 0; i < 8; ++i) c[i] = code_sr<kSrClamp>(v[i], w[i]);
   } else if (normal_scales) {
@@ -197,7 +198,8 @@ __device__ __forceinline__ void team_sync(int team, int T) {
 // element outside the fast form's range), then the rounding.
 template <typename CodeT, bool SR>
 __device__ __forceinline__ void quantize_two(const uint4& a, const uint4& b, bool has_b,
-                                             const ScaleDiv& d, bool normal, const SrArgs& sr,
+                                             const ScaleDiv& d, bool normal,
+                                             const PhiloxKeys& keys, PhiloxStream st,
                                              uint64_t na, uint64_t nb,
                                              typename Pack8<CodeT>::Vec* qa,
                                              typename Pack8<CodeT>::Vec* qb) {
@@ -212,11 +214,11 @@ __device__ __forceinline__ void quantize_two(const uint4& a, const uint4& b, boo
   }
   // f16 stochastic codes: clamped as packed half2 after the conversion
   constexpr bool kHalfClamp = SR && std::is_same<CodeT, __half>::value;
-  codes_of<SR, !kHalfClamp>(va, sr, na, normal, c);
+  codes_of<SR, !kHalfClamp>(va, keys, st, na, normal, c);
   *qa = Pack8<CodeT>::pack(c);
   if (kHalfClamp) *qa = clamp_half8(*qa);
   if (has_b) {
-    codes_of<SR, !kHalfClamp>(vb, sr, nb, normal, c);
+    codes_of<SR, !kHalfClamp>(vb, keys, st, nb, normal, c);
     *qb = Pack8<CodeT>::pack(c);
     if (kHalfClamp) *qb = clamp_half8(*qb);
   }
@@ -240,15 +242,41 @@ __device__ __forceinline__ void colmax_acc(uint4& m, const uint4& a) {  // a = a
 
 constexpr int kMaxSlots = 4;
 
+// A second matrix of the same row length, quantized by blocks split ..
+// gridDim.x - 1 of the same launch (split = gridDim.x: none).
+struct RowsJob2 {
+  const uint16_t* x;
+  int64_t rows, ld;
+  void* q;
+  float* scale;
+  unsigned int* colmax;
+  uint64_t offset;
+  PhiloxStream stream;
+  int split;
+};
+
 template <typename CodeT, bool SR, bool kColMax>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
-    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, CodeT* __restrict__ q,
-    float* __restrict__ scale, SrArgs sr, uint32_t slot_bytes, int T, int S, unsigned int* status,
-    uint64_t limit_ns, unsigned int* __restrict__ colmax) {
+    const uint16_t* __restrict__ x1, int64_t rows1, int64_t cols, int64_t ld1,
+    CodeT* __restrict__ q1, float* __restrict__ scale1, SrArgs sr, uint32_t slot_bytes, int T,
+    int S, unsigned int* status, uint64_t limit_ns, unsigned int* __restrict__ colmax1,
+    RowsJob2 job2) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t bars[kThreads / 32][kMaxSlots];
   __shared__ float red[kThreads / 32];
   __shared__ int got_row[kThreads / 32];
+  // this block's matrix: the first one, or job2 from block job2.split on
+  const bool second = static_cast<int>(blockIdx.x) >= job2.split;
+  const uint16_t* __restrict__ x = second ? job2.x : x1;
+  const int64_t rows = second ? job2.rows : rows1;
+  const int64_t ld = second ? job2.ld : ld1;
+  CodeT* __restrict__ q = second ? static_cast<CodeT*>(job2.q) : q1;
+  float* __restrict__ scale = second ? job2.scale : scale1;
+  unsigned int* __restrict__ colmax = second ? job2.colmax : colmax1;
+  const uint64_t sr_offset = second ? job2.offset : sr.offset;
+  const PhiloxStream sr_stream = second ? job2.stream : sr.stream;
+  const int64_t block = second ? blockIdx.x - job2.split : blockIdx.x;
+  const int64_t blocks = second ? gridDim.x - job2.split : job2.split;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int team = warp / T, wt = warp % T;
   const int teams = (blockDim.x >> 5) / T;
@@ -258,8 +286,8 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
   const uint8_t* slots = smem + static_cast<size_t>(team) * S * slot_bytes;
   const uint32_t slot_addr = ptx::smem_addr(slots);
   const uint32_t bar0 = ptx::smem_addr(&bars[team][0]);  // slot k's barrier: bar0 + 8k
-  const int64_t g = static_cast<int64_t>(blockIdx.x) * teams + team;
-  const int64_t n = static_cast<int64_t>(gridDim.x) * teams;
+  const int64_t g = block * teams + team;
+  const int64_t n = blocks * teams;
   using P = Pack8<CodeT>;
   ptx::grid_dependency_wait();  // the previous kernel in the stream is done
   ptx::allow_dependents();
@@ -339,7 +367,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     const ScaleDiv d = make_scale_div(s);
     const bool normal = scale_is_normal(s);
     typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + r * cols);
-    const uint64_t nrow = sr.offset + static_cast<uint64_t>(r * cols);
+    const uint64_t nrow = sr_offset + static_cast<uint64_t>(r * cols);
     for (int v = first; v < nvec; v += 2 * step) {
       const int v2 = v + step;
       const bool has2 = v2 < nvec;
@@ -348,8 +376,8 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
         continue;
       const uint4 a = rowv[v];
       const uint4 bb = has2 ? rowv[v2] : make_uint4(0u, 0u, 0u, 0u);
-      quantize_two<CodeT, SR>(a, bb, has2, d, normal, sr, nrow + 8u * v, nrow + 8u * v2,
-                              qr + v, qr + (has2 ? v2 : v));
+      quantize_two<CodeT, SR>(a, bb, has2, d, normal, sr.keys, sr_stream, nrow + 8u * v,
+                              nrow + 8u * v2, qr + v, qr + (has2 ? v2 : v));
     }
   }
   // after a timeout: never leave a copy in flight into this block's memory
@@ -420,8 +448,8 @@ __global__ void __launch_bounds__(kThreads) quant_rows_long_kernel(
   typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + row * cols);
   for (int64_t vi = threadIdx.x; vi < nvec; vi += kThreads) {
     const uint64_t n0 = sr.offset + static_cast<uint64_t>(row * cols + vi * 8);
-    quantize_two<CodeT, SR>(__ldg(xr + vi), make_uint4(0u, 0u, 0u, 0u), false, d, normal, sr,
-                            n0, n0, qr + vi, qr + vi);
+    quantize_two<CodeT, SR>(__ldg(xr + vi), make_uint4(0u, 0u, 0u, 0u), false, d, normal, sr.keys,
+                            sr.stream, n0, n0, qr + vi, qr + vi);
   }
 }
 
@@ -559,8 +587,8 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
         float f[8], v[8], cd[8];
         unpack8(a[u], f);
         if (!div8_each_try(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
-        codes_of<SR, !kHalfClamp>(v, sr, sr.offset + static_cast<uint64_t>(row * cols + c),
-                                  normal, cd);
+        codes_of<SR, !kHalfClamp>(v, sr.keys, sr.stream,
+                                  sr.offset + static_cast<uint64_t>(row * cols + c), normal, cd);
         typename P::Vec out = P::pack(cd);
         if (kHalfClamp) out = clamp_half8(out);
         if (in_bounds(row < rows, status))
@@ -730,8 +758,8 @@ __global__ void __launch_bounds__(kThreads, 2) quant_cols_kernel(
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int i = 4 * h + 2 * p + e;
-            codes_of<SR>(quo[2 * p + e], sr, sr.offset + static_cast<uint64_t>((rb + i) * cols + c),
-                         normal, cd[e]);
+            codes_of<SR>(quo[2 * p + e], sr.keys, sr.stream,
+                         sr.offset + static_cast<uint64_t>((rb + i) * cols + c), normal, cd[e]);
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j) CP::put2(colv[j], 2 * h + p, cd[0][j], cd[1][j]);
@@ -834,20 +862,36 @@ cudaError_t launch_col_absmax(const uint16_t* x, int64_t rows, int64_t cols, int
 // into colmax (in the same pass when every thread's share of a row fits
 // its registers, else by a separate column pass).
 template <typename CodeT, bool SR>
-cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
-                          float* scale, float* colmax, const SrArgs& sr, const DeviceInfo& dev,
-                          cudaStream_t stream) {
-  const uint16_t* xp = static_cast<const uint16_t*>(x);
-  CodeT* qp = static_cast<CodeT*>(q);
-  unsigned int* cmx = reinterpret_cast<unsigned int*>(colmax);
+cudaError_t rows_dispatch(const RowsJob* jobs, int njobs, int64_t cols, const SrArgs& base,
+                          const DeviceInfo& dev, cudaStream_t stream) {
+  const bool cm = jobs[0].colmax != nullptr;
   const int sms = dev.sms > 0 ? dev.sms : 148;
   const uint32_t slot = static_cast<uint32_t>((cols * 2 + 127) / 128 * 128);
+  // the stochastic-rounding parameters of job j: the seed's keys, its own
+  // offset and stream
+  auto sr_of = [&](const RowsJob& j) {
+    SrArgs s = base;
+    s.offset = j.offset;
+    s.stream_id = j.stream_id;
+    s.stream = philox_stream(j.stream_id);
+    return s;
+  };
+  auto col_pass = [&](const RowsJob& j) {
+    return launch_col_absmax(static_cast<const uint16_t*>(j.x), j.rows, cols, j.ld,
+                             reinterpret_cast<unsigned int*>(j.colmax), dev, stream);
+  };
   if (2ull * slot > kMaxDynSmem) {
-    cudaError_t e = launch_overlapped(quant_rows_long_kernel<CodeT, SR>,
-                                      dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0, stream,
-                                      xp, rows, cols, ld, qp, scale, sr, dev.status_word);
-    if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, dev, stream);
-    return e;
+    for (int i = 0; i < njobs; ++i) {
+      const RowsJob& j = jobs[i];
+      cudaError_t e = launch_overlapped(quant_rows_long_kernel<CodeT, SR>,
+                                        dim3(static_cast<unsigned>(j.rows)), dim3(kThreads), 0,
+                                        stream, static_cast<const uint16_t*>(j.x), j.rows, cols,
+                                        j.ld, static_cast<CodeT*>(j.q), j.scale, sr_of(j),
+                                        dev.status_word);
+      if (e == cudaSuccess && cm) e = col_pass(j);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
   }
   // 8 warps per block in teams of T, each team with a ring of S row slots
   // (S - 1 rows in flight while it works on one).  Shared memory per block:
@@ -856,14 +900,14 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   // the smallest whose two slots per team fit (and, for the column maxima,
   // whose threads' share of a row fits their registers); S fills the rest.
   const int warps = kThreads / 32;
-  const size_t budget = cmx ? 108u * 1024u : 72u * 1024u;
+  const size_t budget = cm ? 108u * 1024u : 72u * 1024u;
   int T = 1;
   while (T < 8 && (static_cast<size_t>(warps / T) * 2 * slot > budget ||
-                   (cmx && (cols >> 3) > static_cast<int64_t>(kColVecs) * 32 * T)))
+                   (cm && (cols >> 3) > static_cast<int64_t>(kColVecs) * 32 * T)))
     T <<= 1;
-  const bool fused = cmx && (cols >> 3) <= static_cast<int64_t>(kColVecs) * 32 * T &&
+  const bool fused = cm && (cols >> 3) <= static_cast<int64_t>(kColVecs) * 32 * T &&
                      static_cast<size_t>(warps / T) * 2 * slot <= budget;
-  if (cmx && !fused) {  // the plain ring and a separate column pass
+  if (cm && !fused) {  // the plain ring and a separate column pass
     T = 1;
     while (T < 8 && static_cast<size_t>(warps / T) * 2 * slot > 72u * 1024u) T <<= 1;
   }
@@ -873,29 +917,44 @@ cudaError_t rows_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
   if (S < 2) S = 2;
   const size_t smem = team_bytes * S;
   const int64_t teams = warps / T;
-  const int64_t need = (rows + teams - 1) / teams;
-  cudaError_t e;
-  if (fused) {
-    static bool attr[64] = {};
-    e = allow_smem(quant_rows_kernel<CodeT, SR, true>, attr);
-    if (e != cudaSuccess) return e;
-    const int occ = blocks_per_sm(quant_rows_kernel<CodeT, SR, true>, kThreads, smem);
-    const int64_t cap = static_cast<int64_t>(sms) * occ;
-    const unsigned blocks = static_cast<unsigned>(need < cap ? need : cap);
-    return launch_overlapped(quant_rows_kernel<CodeT, SR, true>, dim3(blocks), dim3(kThreads), smem,
-                             stream, xp, rows, cols, ld, qp, scale, sr, slot, T, S,
-                             dev.status_word, kWaitLimitNs, cmx);
-  }
-  static bool attr[64] = {};
-  e = allow_smem(quant_rows_kernel<CodeT, SR, false>, attr);
+  auto need = [&](const RowsJob& j) { return (j.rows + teams - 1) / teams; };
+  auto kernel = fused ? quant_rows_kernel<CodeT, SR, true> : quant_rows_kernel<CodeT, SR, false>;
+  static bool attr_fused[64] = {}, attr_plain[64] = {};
+  cudaError_t e = allow_smem(kernel, fused ? attr_fused : attr_plain);
   if (e != cudaSuccess) return e;
-  const int occ = blocks_per_sm(quant_rows_kernel<CodeT, SR, false>, kThreads, smem);
+  const int occ = blocks_per_sm(kernel, kThreads, smem);
   const int64_t cap = static_cast<int64_t>(sms) * occ;
-  const unsigned blocks = static_cast<unsigned>(need < cap ? need : cap);
-  e = launch_overlapped(quant_rows_kernel<CodeT, SR, false>, dim3(blocks), dim3(kThreads), smem,
-                        stream, xp, rows, cols, ld, qp, scale, sr, slot, T, S, dev.status_word,
-                        kWaitLimitNs, nullptr);
-  if (e == cudaSuccess && cmx) e = launch_col_absmax(xp, rows, cols, ld, cmx, dev, stream);
+  // blocks [0, split) take job 0 and [split, blocks) job 1, in proportion
+  // to their rows when the two need more than one wave of blocks
+  int64_t split, blocks;
+  if (njobs == 1) {
+    split = blocks = need(jobs[0]) < cap ? need(jobs[0]) : cap;
+  } else if (need(jobs[0]) + need(jobs[1]) <= cap) {
+    split = need(jobs[0]);
+    blocks = split + need(jobs[1]);
+  } else {
+    blocks = cap;
+    const double share = static_cast<double>(jobs[0].rows) / (jobs[0].rows + jobs[1].rows);
+    split = static_cast<int64_t>(share * cap + 0.5);
+    if (split < 1) split = 1;
+    if (split > cap - 1) split = cap - 1;
+  }
+  const RowsJob& j0 = jobs[0];
+  RowsJob2 j2{nullptr, 0, 0, nullptr, nullptr, nullptr, 0, PhiloxStream{0u, 0u},
+              static_cast<int>(split)};
+  if (njobs > 1) {
+    const RowsJob& j1 = jobs[1];
+    j2 = RowsJob2{static_cast<const uint16_t*>(j1.x), j1.rows, j1.ld, j1.q, j1.scale,
+                  fused ? reinterpret_cast<unsigned int*>(j1.colmax) : nullptr, j1.offset,
+                  philox_stream(j1.stream_id), static_cast<int>(split)};
+  }
+  e = launch_overlapped(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem, stream,
+                        static_cast<const uint16_t*>(j0.x), j0.rows, cols, j0.ld,
+                        static_cast<CodeT*>(j0.q), j0.scale, sr_of(j0), slot, T, S,
+                        dev.status_word, kWaitLimitNs,
+                        fused ? reinterpret_cast<unsigned int*>(j0.colmax) : nullptr, j2);
+  if (e != cudaSuccess || !cm || fused) return e;
+  for (int i = 0; i < njobs && e == cudaSuccess; ++i) e = col_pass(jobs[i]);
   return e;
 }
 
@@ -967,17 +1026,32 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
 
 }  // namespace
 
+namespace {
+cudaError_t rows_jobs(const RowsJob* jobs, int njobs, int64_t cols, int8mp_round mode,
+                      const SrArgs& base, int8mp_codes codes, const DeviceInfo& dev,
+                      cudaStream_t stream) {
+  const bool s = mode == INT8MP_SR;
+  if (codes == INT8MP_CODES_S8)
+    return s ? rows_dispatch<int8_t, true>(jobs, njobs, cols, base, dev, stream)
+             : rows_dispatch<int8_t, false>(jobs, njobs, cols, base, dev, stream);
+  return s ? rows_dispatch<__half, true>(jobs, njobs, cols, base, dev, stream)
+           : rows_dispatch<__half, false>(jobs, njobs, cols, base, dev, stream);
+}
+}  // namespace
+
 cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                  int8mp_round mode, const SrArgs& sr, void* q,
                                  int8mp_codes codes, float* scale, float* colmax,
                                  const DeviceInfo& dev, cudaStream_t stream) {
-  const bool s = mode == INT8MP_SR;
-  float* cm = colmax;
-  if (codes == INT8MP_CODES_S8)
-    return s ? rows_dispatch<int8_t, true>(x, rows, cols, ld, q, scale, cm, sr, dev, stream)
-             : rows_dispatch<int8_t, false>(x, rows, cols, ld, q, scale, cm, sr, dev, stream);
-  return s ? rows_dispatch<__half, true>(x, rows, cols, ld, q, scale, cm, sr, dev, stream)
-           : rows_dispatch<__half, false>(x, rows, cols, ld, q, scale, cm, sr, dev, stream);
+  const RowsJob job{x, rows, ld, q, scale, colmax, sr.offset, sr.stream_id};
+  return rows_jobs(&job, 1, cols, mode, sr, codes, dev, stream);
+}
+
+cudaError_t launch_quantize_rows_jobs(const RowsJob* jobs, int njobs, int64_t cols,
+                                      int8mp_round mode, uint64_t seed, int8mp_codes codes,
+                                      const DeviceInfo& dev, cudaStream_t stream) {
+  if (njobs < 1 || njobs > kMaxRowsJobs) return cudaErrorInvalidValue;
+  return rows_jobs(jobs, njobs, cols, mode, make_sr(seed, 0, 0), codes, dev, stream);
 }
 
 cudaError_t launch_zero_words(void* p, int64_t n, const DeviceInfo& dev, cudaStream_t stream) {

@@ -1,9 +1,10 @@
 """The bounds-checked build (-DINT8MP_CHECK): every global index the kernels
 compute is checked against its buffer before the access.  Run the paths of
 the library through it -- row and column quantization in every variant, the
-column maxima, the GEMM in three layouts with and without the split last
-wave, the linear layer -- on ragged sizes: no check may fail, and every
-result must equal the ordinary build's bit for bit."""
+column maxima, two matrices' rows in one launch, the GEMM in three layouts
+with and without the split last wave, the linear layer -- on ragged sizes: no
+check may fail, and every result must equal the ordinary build's bit for
+bit."""
 import pytest
 import torch
 
@@ -36,6 +37,14 @@ def _codes_and_gemms():
                 cm = torch.zeros(cols, dtype=torch.float32, device=DEV)
                 out += list(m.int8mp_quantize_rows_colmax(x, cm, **kw)) + [cm]
                 out += list(m.int8mp_quantize_cols_absmax(x, cm, **kw))
+                x2 = synth.bf16_normal((rows // 2 + 1, cols), rows + 7).to(DEV)
+                cms = [torch.zeros(cols, dtype=torch.float32, device=DEV) for _ in range(2)]
+                bkw = dict(mode=mode, seed=3, offsets=[5, 9], stream_ids=[0, 1], codes=codes)
+                for pair in m.int8mp_quantize_rows_batch([x, x2], **bkw):
+                    out += list(pair)
+                for pair in m.int8mp_quantize_rows_batch([x, x2], colmaxes=cms, **bkw):
+                    out += list(pair)
+                out += cms
     g = torch.Generator().manual_seed(9)
     for M, N, K, lay in ((200, 264, 144, m.INT8MP_AxBT), (2560, 2048, 4096, m.INT8MP_AxB),
                          (2312, 1800, 8256, m.INT8MP_ATxB), (1000, 776, 2096, m.INT8MP_AxB)):

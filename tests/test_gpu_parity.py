@@ -161,6 +161,35 @@ def test_rows_with_column_absmax_then_columns(shape, mode):
     np.testing.assert_array_equal(_codes_np(qc), np.ascontiguousarray(qcr.T))
 
 
+# Two matrices with the same row length in one launch (int8mp_quantize_rows_batch):
+# ragged rows, a split of the launch's blocks that is not proportional
+# (3 and 300 rows), rows longer than a team's share (5632 columns)
+ROWS_BATCH_SHAPES = [((1040, 2048), (264, 2048)), ((77, 136), (9, 136)), ((3, 5632), (300, 5632)),
+                     ((16384, 1024), (1024, 1024))]
+
+
+@pytest.mark.parametrize("with_colmax", [False, True])
+@pytest.mark.parametrize("codes", [m.INT8MP_CODES_S8, m.INT8MP_CODES_F16])
+@pytest.mark.parametrize("mode", [m.INT8MP_RNE, m.INT8MP_SR])
+@pytest.mark.parametrize("shapes", ROWS_BATCH_SHAPES)
+def test_rows_batch_matches_the_oracle_per_matrix(shapes, mode, codes, with_colmax):
+    (r0, cols), (r1, _) = shapes
+    xs = [_edge_input(r0, cols, seed=r0 + 3), _edge_input(r1, cols, seed=r1 + 5)]
+    offs, sids, seed = [5, (1 << 33) + 4], [m.INT8MP_STREAM_FWD_X, m.INT8MP_STREAM_FWD_W], 19
+    cms = [torch.zeros(cols, dtype=torch.float32, device=DEV) for _ in xs] if with_colmax else None
+    got = m.int8mp_quantize_rows_batch([_dev(x) for x in xs], mode=mode, seed=seed, offsets=offs,
+                                       stream_ids=sids, codes=codes, colmaxes=cms)
+    assert m.int8mp_poll_device_status() == m.INT8MP_OK
+    for i, x in enumerate(xs):
+        q, sc = got[i]
+        qr, sr = oracle.quantize(bf16_bits(x), axis=0, mode=mode, seed=seed, offset=offs[i],
+                                 stream_id=sids[i])
+        np.testing.assert_array_equal(_f32_bits(sc), sr.view(np.int32), err_msg=str(i))
+        np.testing.assert_array_equal(_codes_np(q), qr, err_msg=str(i))
+        if with_colmax:
+            np.testing.assert_array_equal(_f32_bits(cms[i]), _col_absmax_bits(x), err_msg=str(i))
+
+
 @pytest.mark.parametrize("mode", [m.INT8MP_RNE, m.INT8MP_SR])
 def test_columns_from_absmax_int8_codes(mode):
     rows, cols = 1000, 2056
@@ -415,12 +444,15 @@ def test_scaled_mm_bit_exact(shape):
 
 
 @pytest.mark.parametrize("s32", [False, True])
-def test_pair_gemm_writes_only_its_strided_output(s32):
-    # CTA-pair kernel (99 pair tiles), ragged M and N: the tile stores must
-    # land at row stride ldo and column offset 8 of a larger buffer, clip at
-    # row M and column N, and leave every other element as it was; sB at a
-    # 4-byte (not 16-byte) aligned address
-    M, N, K, ldo = 2600, 2056, 144, 2088
+@pytest.mark.parametrize("M", [2600, 8200])
+def test_pair_gemm_writes_only_its_strided_output(s32, M):
+    # CTA-pair kernel, ragged M and N: the tile stores must land at row
+    # stride ldo and column offset 8 of a larger buffer, clip at row M and
+    # column N, and leave every other element as it was; sB at a 4-byte (not
+    # 16-byte) aligned address.  M = 2600: 99 tiles, at most two per SM pair
+    # (scales loaded when a tile starts); M = 8200: 297 tiles (scales loaded
+    # by the store, scalar loads for the misaligned sB)
+    N, K, ldo = 2056, 144, 2088
     a, b = _rand_codes(M, K, 41), _rand_codes(N, K, 42)
     ad, bd = _dev(a.half()), _dev(b.half())
     g = torch.Generator().manual_seed(43)
@@ -438,11 +470,14 @@ def test_pair_gemm_writes_only_its_strided_output(s32):
     outside = torch.ones(big.shape, dtype=torch.bool)
     outside[1:M + 1, 8:8 + N] = False
     assert torch.equal(big.cpu()[outside], sentinel.cpu()[outside])
+    rows = np.r_[0:40, M // 2 - 7:M // 2 + 9, M - 40:M]  # first, middle and ragged last tiles
+    got = view.cpu()[torch.from_numpy(rows)]
+    an = a.numpy()[rows]
     if s32:
-        np.testing.assert_array_equal(view.cpu().numpy(), oracle.mm_s32(a.numpy(), b.numpy(), M, N, K))
+        np.testing.assert_array_equal(got.numpy(), oracle.mm_s32(an, b.numpy(), len(rows), N, K))
     else:
-        ref = oracle.scaled_mm(a.numpy(), sa.numpy(), b.numpy(), sb_store[1:].numpy(), M, N, K)
-        assert_bf16_equal(view, ref, "scaled_mm into a strided output")
+        ref = oracle.scaled_mm(an, sa.numpy()[rows], b.numpy(), sb_store[1:].numpy(), len(rows), N, K)
+        assert_bf16_equal(got, ref, "scaled_mm into a strided output")
 
 
 def test_matmul_rejects_an_output_with_strided_columns():
