@@ -87,6 +87,36 @@ __device__ __forceinline__ void philox_words8(const PhiloxKeys& pk, PhiloxStream
   }
 }
 
+// The words of two groups of eight elements at na and nb, both multiples of
+// 4: four whole blocks, computed round by round so that the four
+// independent chains of multiplies overlap each other's latency.
+__device__ __forceinline__ void philox_words8x2(const PhiloxKeys& pk, PhiloxStream st,
+                                                uint64_t na, uint64_t nb, uint32_t (&wa)[8],
+                                                uint32_t (&wb)[8]) {
+  const uint64_t blk[4] = {na >> 2, (na >> 2) + 1, nb >> 2, (nb >> 2) + 1};
+  uint4 c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c0 = static_cast<uint32_t>(blk[i]), c1 = static_cast<uint32_t>(blk[i] >> 32);
+    c[i] = make_uint4(st.z_hi ^ c1 ^ pk.k[0], st.z_lo, __umulhi(kPhiloxMulA, c0) ^ pk.k[1],
+                      kPhiloxMulA * c0);
+  }
+#pragma unroll
+  for (int round = 1; round < 10; ++round) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t hiA = __umulhi(kPhiloxMulA, c[i].x), loA = kPhiloxMulA * c[i].x;
+      const uint32_t hiB = __umulhi(kPhiloxMulB, c[i].z), loB = kPhiloxMulB * c[i].z;
+      c[i] = make_uint4(hiB ^ c[i].y ^ pk.k[2 * round], loB, hiA ^ c[i].w ^ pk.k[2 * round + 1],
+                        loA);
+    }
+  }
+  wa[0] = c[0].x, wa[1] = c[0].y, wa[2] = c[0].z, wa[3] = c[0].w;
+  wa[4] = c[1].x, wa[5] = c[1].y, wa[6] = c[1].z, wa[7] = c[1].w;
+  wb[0] = c[2].x, wb[1] = c[2].y, wb[2] = c[2].z, wb[3] = c[2].w;
+  wb[4] = c[3].x, wb[5] = c[3].y, wb[6] = c[3].z, wb[7] = c[3].w;
+}
+
 // u in [0, 1) carrying the word's top 24 bits (exact in fp32).
 __device__ __forceinline__ float sr_uniform(uint32_t word) {
   return __uint2float_rn(word >> 8) * 0x1p-24f;

@@ -113,6 +113,14 @@ __device__ __forceinline__ float code_sr(float v, uint32_t word) {
 // Eight codes from eight quotients (elements n0 .. n0+7 of the SR stream).
 // normal_scales: every element's group scale is at least 2^-126.
 // kSrClamp false: stochastic codes are left unclamped for a later half2 clamp.
+// Eight stochastic codes from eight quotients and their random words.
+template <bool kSrClamp>
+__device__ __forceinline__ void codes_sr8(const float (&v)[8], const uint32_t (&w)[8],
+                                          float (&c)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c[i] = code_sr<kSrClamp>(v[i], w[i]);
+}
+
 template <bool SR, bool kSrClamp = true>
 __device__ __forceinline__ void codes_of(const float (&v)[8], const PhiloxKeys& keys,
                                          PhiloxStream st, uint64_t n0, bool normal_scales,
@@ -214,6 +222,18 @@ __device__ __forceinline__ void quantize_two(const uint4& a, const uint4& b, boo
   }
   // f16 stochastic codes: clamped as packed half2 after the conversion
   constexpr bool kHalfClamp = SR && std::is_same<CodeT, __half>::value;
+  if (SR && has_b && ((na | nb) & 3u) == 0) {
+    // both groups start a Philox block: their four blocks side by side
+    uint32_t wa[8], wb[8];
+    philox_words8x2(keys, st, na, nb, wa, wb);
+    codes_sr8<!kHalfClamp>(va, wa, c);
+    *qa = Pack8<CodeT>::pack(c);
+    if (kHalfClamp) *qa = clamp_half8(*qa);
+    codes_sr8<!kHalfClamp>(vb, wb, c);
+    *qb = Pack8<CodeT>::pack(c);
+    if (kHalfClamp) *qb = clamp_half8(*qb);
+    return;
+  }
   codes_of<SR, !kHalfClamp>(va, keys, st, na, normal, c);
   *qa = Pack8<CodeT>::pack(c);
   if (kHalfClamp) *qa = clamp_half8(*qa);
@@ -537,6 +557,7 @@ __global__ void col_scale_kernel(unsigned int* __restrict__ amax_bits, int64_t c
 // the codes keep their clamp (the absmax is the caller's claim).  Otherwise
 // `in` is the scale array itself.
 constexpr int kNatUnroll = 4;
+static_assert(kNatUnroll % 2 == 0, "stochastic codes go two rows at a time");
 
 template <typename CodeT, bool SR, bool kFromAbsmax>
 __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
@@ -580,19 +601,43 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
                  ? __ldg(reinterpret_cast<const uint4*>(xc + row * ld))
                  : make_uint4(0u, 0u, 0u, 0u);
     }
+    auto put = [&](int64_t row, const float (&cd)[8]) {
+      typename P::Vec out = P::pack(cd);
+      if (kHalfClamp) out = clamp_half8(out);
+      if (in_bounds(row < rows, status))
+        *reinterpret_cast<typename P::Vec*>(q + row * cols + c) = out;
+    };
 #pragma unroll
-    for (int u = 0; u < kNatUnroll; ++u) {
-      const int64_t row = rr + u * 8;
-      if (row < r1) {
-        float f[8], v[8], cd[8];
-        unpack8(a[u], f);
-        if (!div8_each_try(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
-        codes_of<SR, !kHalfClamp>(v, sr.keys, sr.stream,
-                                  sr.offset + static_cast<uint64_t>(row * cols + c), normal, cd);
-        typename P::Vec out = P::pack(cd);
-        if (kHalfClamp) out = clamp_half8(out);
-        if (in_bounds(row < rows, status))
-          *reinterpret_cast<typename P::Vec*>(q + row * cols + c) = out;
+    for (int u = 0; u < kNatUnroll; u += 2) {
+      const int64_t row_a = rr + u * 8, row_b = row_a + 8;
+      const uint64_t n_a = sr.offset + static_cast<uint64_t>(row_a * cols + c);
+      const uint64_t n_b = sr.offset + static_cast<uint64_t>(row_b * cols + c);
+      if (SR && row_b < r1 && ((n_a | n_b) & 3u) == 0) {
+        // stochastic codes of two rows: their four Philox blocks side by side
+        float f_a[8], f_b[8], v_a[8], v_b[8], cd[8];
+        unpack8(a[u], f_a);
+        unpack8(a[u + 1], f_b);
+        if (!div8_each_try(f_a, s, r, all_fast, v_a)) div8_each_ieee(f_a, s, v_a);
+        if (!div8_each_try(f_b, s, r, all_fast, v_b)) div8_each_ieee(f_b, s, v_b);
+        uint32_t w_a[8], w_b[8];
+        philox_words8x2(sr.keys, sr.stream, n_a, n_b, w_a, w_b);
+        codes_sr8<!kHalfClamp>(v_a, w_a, cd);
+        put(row_a, cd);
+        codes_sr8<!kHalfClamp>(v_b, w_b, cd);
+        put(row_b, cd);
+        continue;
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int64_t row = row_a + 8 * e;
+        if (row < r1) {
+          float f[8], v[8], cd[8];
+          unpack8(a[u + e], f);
+          if (!div8_each_try(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
+          codes_of<SR, !kHalfClamp>(v, sr.keys, sr.stream,
+                                    sr.offset + static_cast<uint64_t>(row * cols + c), normal, cd);
+          put(row, cd);
+        }
       }
     }
   }
