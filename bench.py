@@ -52,6 +52,8 @@ def parse_args():
                     help="profiling cases only: tokens per step instead of 16x2048")
     ap.add_argument("--linears", default=None,
                     help="profiling cases only: comma-separated subset of q,k,v,o,gate,up,down")
+    ap.add_argument("--rounding", choices=["rne", "sr"], default="rne",
+                    help="profiling cases only: round to nearest even or stochastically")
     return ap.parse_args()
 
 
@@ -625,9 +627,11 @@ def main():
     init_dist(world, "nccl")
     spec = synth.LLAMA2_1B
     only = set(args.linears.split(",")) if args.linears else None
-    if (args.tokens or only) and not args.profile_steps:
-        raise SystemExit("--tokens/--linears select profiling cases and need --profile-steps")
-    step = LayerStep(spec, m.INT8MP_RNE, device, T=args.tokens, only=only)
+    if (args.tokens or only or args.rounding != "rne") and not args.profile_steps:
+        raise SystemExit("--tokens/--linears/--rounding select profiling cases and need "
+                         "--profile-steps")
+    mode = m.INT8MP_SR if args.rounding == "sr" else m.INT8MP_RNE
+    step = LayerStep(spec, mode, device, T=args.tokens, only=only)
     with ClockSampler(local) as clk:
         elapsed_ms, per_kind, counts = time_steps(step, args.steps, args.warmup, world, device)
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)
@@ -647,7 +651,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens": step.T, "hidden": spec["hidden"],
-                   "intermediate": spec["inter"], "linears": len(step.linears), "rounding": "RNE",
+                   "intermediate": spec["inter"], "linears": len(step.linears),
+                   "rounding": "SR" if mode == m.INT8MP_SR else "RNE",
                    "l2": "inputs larger than L2 (about 5 GB touched per step, L2 129 MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor",
