@@ -148,23 +148,42 @@ def test_fuzz_matmul(case):
 
 @pytest.mark.parametrize("case", range(CASES // 2))
 def test_fuzz_linear(case):
+    # random per-pass switches (a pass at 0 runs in BF16) and, for every
+    # other case, the forward pass that saves X's and W's column absmax and
+    # the backward pass that takes them
+    from test_gpu_parity import _bf16_pass_close
     g = _rng(200 + case)
     T = 16 * int(g.integers(1, 80))
     N = 16 * int(g.integers(1, 80))
     K = 16 * int(g.integers(1, 80))
     mode = int(g.integers(0, 2))
     seed, off = int(g.integers(0, 1 << 40)), int(g.integers(0, 1 << 30))
+    f, gi, gw = (1, 1, 1) if case % 3 == 0 else tuple(int(v) for v in g.integers(0, 2, size=3))
+    saved = case % 2 == 1
     X = _input(T, K, 300 + case)
     W = synth.bf16_normal((N, K), 400 + case, std=0.02)
     dY = synth.bf16_normal((T, N), 500 + case, std=1e-3)
-    cfg = m.linear_cfg(mode=mode, seed=seed, offset=off)
+    cfg = m.linear_cfg(mode=mode, seed=seed, offset=off, int8_fwd=f, int8_grad_in=gi,
+                       int8_grad_w=gw)
     Xd, Wd, dYd = X.to(DEV), W.to(DEV), dY.to(DEV)
-    Y = m.int8mp_linear_fwd(Xd, Wd, cfg)
-    dX, dW = m.int8mp_linear_bwd(dYd, Xd, Wd, cfg)
+    if saved:
+        absmax = torch.empty(2 * K, dtype=torch.float32, device=DEV)
+        Y = m.int8mp_linear_fwd_save(Xd, Wd, absmax, cfg)
+        dX, dW = m.int8mp_linear_bwd_saved(dYd, Xd, Wd, absmax, cfg)
+    else:
+        Y = m.int8mp_linear_fwd(Xd, Wd, cfg)
+        dX, dW = m.int8mp_linear_bwd(dYd, Xd, Wd, cfg)
     assert m.int8mp_poll_device_status() == m.INT8MP_OK
-    Yr = oracle.linear_fwd(bf16_bits(X), bf16_bits(W), mode=mode, seed=seed, offset=off)
-    dXr, dWr = oracle.linear_bwd(bf16_bits(dY), bf16_bits(X), bf16_bits(W), mode=mode, seed=seed,
-                                 offset=off)
-    np.testing.assert_array_equal(bf16_bits(Y.cpu()), Yr)
-    np.testing.assert_array_equal(bf16_bits(dX.cpu()), dXr)
-    np.testing.assert_array_equal(bf16_bits(dW.cpu()), dWr)
+    kw = dict(mode=mode, seed=seed, offset=off)
+    Yr = oracle.linear_fwd_cfg(bf16_bits(X), bf16_bits(W), int8_fwd=f, **kw)
+    dXr, dWr = oracle.linear_bwd_cfg(bf16_bits(dY), bf16_bits(X), bf16_bits(W), int8_grad_in=gi,
+                                     int8_grad_w=gw, **kw)
+    xf, wf, gf = X.float(), W.float(), dY.float()
+    for got, ref, int8, a, b, what in ((Y, Yr, f, xf, wf, "forward"),
+                                       (dX, dXr, gi, gf, wf.T.contiguous(), "grad input"),
+                                       (dW, dWr, gw, gf.T.contiguous(), xf.T.contiguous(),
+                                        "grad weight")):
+        if int8:
+            np.testing.assert_array_equal(bf16_bits(got.cpu()), ref, err_msg=what)
+        else:
+            _bf16_pass_close(got, ref, a, b, what)
