@@ -325,6 +325,24 @@ def test_mm_s32_mn_major_large_sums_exact(layout):
     np.testing.assert_array_equal(acc, oracle.mm_s32(a.numpy(), b.numpy(), M, N, K))
 
 
+@pytest.mark.parametrize("layout", [m.INT8MP_AxBT, m.INT8MP_ATxB])
+def test_mm_s32_at_the_int32_limit_of_k(layout):
+    # K = 133,136, the largest multiple of 16 within the API's bound: with
+    # every code +-127, sums reach 127^2 K = 2,147,350,544, 133,104 below
+    # 2^31; 131 exact fp32 chunks per output, on the CTA-pair kernel
+    M, N, K = 256, 256, 133136
+    assert K <= m.INT8MP_MAX_K < K + 16
+    a = _rand_codes(M, K, 61, extreme=True)
+    b = _rand_codes(N, K, 62, extreme=True)
+    b[0] = a[0]
+    b[1] = -a[1]
+    a_st = a if layout == m.INT8MP_AxBT else a.T.contiguous()
+    b_st = b if layout == m.INT8MP_AxBT else b.T.contiguous()
+    acc = m.int8mp_mm_s32(_dev(a_st.half()), _dev(b_st.half()), layout=layout).cpu().numpy()
+    assert acc[0, 0] == 127 * 127 * K and acc[1, 1] == -127 * 127 * K
+    np.testing.assert_array_equal(acc, oracle.mm_s32(a.numpy(), b.numpy(), M, N, K))
+
+
 # Split last wave: with a workspace, the CTA-pair kernel splits the R tiles
 # of a partial last wave into s = min(pairs / R, 4) k-parts each, added as
 # int32 totals: one tile of K = 8192, 80 tiles (4 left over: 4 parts of 16
