@@ -447,6 +447,51 @@ def test_split_tail_gemm_replays_in_a_cuda_graph():
     np.testing.assert_array_equal(acc.cpu().numpy()[rows], ref)
 
 
+def test_linear_layer_replays_in_a_cuda_graph():
+    # forward with saved absmax and backward, captured once and replayed on
+    # fresh inputs: the absmax zeroing, the dependent launches and the split
+    # last wave (80 tiles of grad input) must give the eager calls' results
+    # (which the other tests hold to the oracle) bit for bit each time
+    T, N, K = 2560, 2048, 2048
+    cfg = m.linear_cfg(mode=m.INT8MP_SR, seed=5, offset=3)
+    X = torch.empty((T, K), dtype=torch.bfloat16, device=DEV)
+    W = torch.empty((N, K), dtype=torch.bfloat16, device=DEV)
+    dY = torch.empty((T, N), dtype=torch.bfloat16, device=DEV)
+    Y = torch.empty((T, N), dtype=torch.bfloat16, device=DEV)
+    dX = torch.empty((T, K), dtype=torch.bfloat16, device=DEV)
+    dW = torch.empty((N, K), dtype=torch.bfloat16, device=DEV)
+    absmax = torch.empty(2 * K, dtype=torch.float32, device=DEV)
+    ws = torch.empty(m.int8mp_linear_workspace_size(T, N, K, cfg), dtype=torch.uint8, device=DEV)
+
+    def step():
+        m.int8mp_linear_fwd_save(X, W, absmax, cfg, Y=Y, workspace=ws)
+        m.int8mp_linear_bwd_saved(dY, X, W, absmax, cfg, dX=dX, dW=dW, workspace=ws)
+
+    def refill(i):
+        X.copy_(synth.bf16_normal((T, K), 70 + i))
+        W.copy_(synth.bf16_normal((N, K), 80 + i, std=0.02))
+        dY.copy_(synth.bf16_normal((T, N), 90 + i, std=1e-3))
+
+    refill(0)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for i in range(1, 4):
+        refill(i)
+        graph.replay()
+        got = [t.clone() for t in (Y, dX, dW)]
+        step()
+        torch.cuda.synchronize()
+        for g_, e_ in zip(got, (Y, dX, dW)):
+            assert torch.equal(g_.view(torch.int16), e_.view(torch.int16)), i
+    assert m.int8mp_poll_device_status() == m.INT8MP_OK
+
+
 @pytest.mark.parametrize("shape", [(256, 256, 512), (200, 264, 144), (384, 512, 2048)])
 def test_scaled_mm_bit_exact(shape):
     M, N, K = shape
