@@ -82,7 +82,22 @@ struct GemmParams {
   uint64_t epoch;                // split tail: tags this launch's counts (40 bits)
   int dp_tiles;                  // tiles computed whole (all of them without a split tail)
   int sk_tail, sk_split;         // split tail: its tiles, and the parts of each
+  int m_fastest;                 // tile order: 1 = consecutive tiles down a column of tiles
 };
+
+// Row and column block of a tile.  Consecutive tiles (the CTAs of one wave)
+// share a row block (and its A k-slices) -- or, with m_fastest, a column
+// block: each wave then streams all of A's k-slices instead of all of B's,
+// which re-reads less from DRAM when A is the smaller operand (M < N).
+__device__ __forceinline__ void tile_mn(const GemmParams& p, int tile, int& mb, int& nb) {
+  if (p.m_fastest) {
+    mb = tile % p.m_tiles;
+    nb = tile / p.m_tiles;
+  } else {
+    mb = tile / p.n_tiles;
+    nb = tile % p.n_tiles;
+  }
+}
 
 __device__ __forceinline__ void raise_abort(volatile int* abort, unsigned int* status) {
   *abort = 1;
@@ -342,8 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t armed = 0u, armed_par = 0u;  // per-stage outstanding copy + its parity
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile / p.n_tiles) * kBM;
-        const int n0 = (tile % p.n_tiles) * kBN;
+        int mb, nb;
+        tile_mn(p, tile, mb, nb);
+        const int m0 = mb * kBM;
+        const int n0 = nb * kBN;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort, limit)) {
             ok = false;
@@ -422,8 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t chunk = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      const int m0 = (tile / p.n_tiles) * kBM;
-      const int n0 = (tile % p.n_tiles) * kBN;
+      int mb, nb;
+      tile_mn(p, tile, mb, nb);
+      const int m0 = mb * kBM;
+      const int n0 = nb * kBN;
       const TileScales ts = load_tile_scales<kRegScales>(
           p, static_cast<int64_t>(m0) + quad * 32, static_cast<int64_t>(n0) + half * 128);
       int32_t tot[128];
@@ -682,8 +701,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       FragIter it(p, pair);
       int tile, kb0, kb1;
       while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
-        const int m0 = (tile / p.n_tiles) * 256 + static_cast<int>(rank) * 128;
-        const int n0 = (tile % p.n_tiles) * 256 + static_cast<int>(rank) * 128;
+        int mb, nb;
+        tile_mn(p, tile, mb, nb);
+        const int m0 = mb * 256 + static_cast<int>(rank) * 128;
+        const int n0 = nb * 256 + static_cast<int>(rank) * 128;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort, limit)) {
             ok = false;
@@ -768,8 +789,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     FragIter it(p, pair);
     int tile, kb0, kb1;
     while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
-      const int m0 = (tile / p.n_tiles) * 256 + static_cast<int>(rank) * 128;
-      const int n0 = (tile % p.n_tiles) * 256;
+      int mb, nb;
+      tile_mn(p, tile, mb, nb);
+      const int m0 = mb * 256 + static_cast<int>(rank) * 128;
+      const int n0 = nb * 256;
       const bool whole = kb0 == 0 && kb1 == p.k_blocks;
       TileScales ts{0.0f, {0.0f, 0.0f, 0.0f, 0.0f}};
       if (whole)
@@ -938,6 +961,7 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   p.K = static_cast<int>(K);
   p.m_tiles = static_cast<int>((M + (pair ? 255 : kBM - 1)) / (pair ? 256 : kBM));
   p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
+  p.m_fastest = M < N ? 1 : 0;
   p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
   p.mode = mode == GemmOut::kS32 ? 1 : 0;
   p.status = dev.status_word;
