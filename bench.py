@@ -420,11 +420,38 @@ def oracle_layer_sample(spec, T_sample, mode=0, nthreads=None):
     return time.perf_counter() - t0, nthreads
 
 
+def oracle_small_single_core():
+    """Milliseconds the oracle takes on one core for the two small problems:
+    the 256x512 single forward matmul (quantize X and W by rows, scaled mm)
+    and the 1024^3 square A @ B.T (same steps)."""
+    import numpy as np
+    import torch
+    import oracle
+    from int8_mixed_precision_row_gb300 import synth
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    def one(A, B):
+        a, b = bits(A), bits(B)
+        t0 = time.perf_counter()
+        qa, sa = oracle.quantize(a, axis=0)
+        qb, sb = oracle.quantize(b, axis=0)
+        oracle.scaled_mm(qa, sa, qb, sb, a.shape[0], b.shape[0], a.shape[1], nthreads=1)
+        return round((time.perf_counter() - t0) * 1e3, 1)
+    oracle.lib()
+    X, W = synth.single_matmul_inputs()
+    A, B = synth.square_inputs(1024, "AxBT")
+    return {"single_matmul_256x256x512_ms": one(X, W), "square_1024_AxBT_ms": one(A, B),
+            "cores": 1}
+
+
 def cpu_baseline(spec):
     secs, cores = oracle_layer_sample(spec, ORACLE_SAMPLE_TOKENS)
     return {"value": ORACLE_SAMPLE_TOKENS / secs, "unit": "tok/s", "cores": cores, "kind": "oracle",
             "sample": f"first {ORACLE_SAMPLE_TOKENS} tokens of the same layer inputs, all 7 linears "
-                      f"fwd+grad_in+grad_w, RNE ({secs:.1f} s)"}
+                      f"fwd+grad_in+grad_w, RNE ({secs:.1f} s)",
+            "small_problems_single_core": oracle_small_single_core()}
 
 
 # ------------------------------------------------------------------ extras
