@@ -174,6 +174,10 @@ int8mp_status int8mp_quantize_rows_colmax(const void* x, int64_t rows, int64_t c
  *             colmax  fp32 [cols] column absmax, merged by atomic max, or
  *                     NULL -- the same for every job
  *   njobs   1 .. INT8MP_MAX_ROWS_JOBS.
+ *   cols    the row length of every job.
+ *   mode, seed, codes, stream   as for int8mp_quantize_rowwise, shared by
+ *           all jobs; the caller owns every buffer and initializes colmax
+ *           as for int8mp_quantize_rows_colmax.
  * Requirements: every job those of int8mp_quantize_rowwise with
  * INT8MP_GROUP_ROWS, and of int8mp_quantize_rows_colmax when colmax is
  * given; a job with rows == 0 is skipped.  jobs NULL, njobs out of range, or
