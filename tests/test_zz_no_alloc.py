@@ -35,7 +35,11 @@ def _inputs(T, N, K, seed):
 
 def test_noalloc_forward_matches_workspace_forward_on_two_calls_in_a_row():
     cases = [((256, 256, 512), m.linear_cfg()),                                   # first call on the device
-             ((1040, 64, 1056), m.linear_cfg(mode=m.INT8MP_SR, seed=11, offset=5))]  # second: other sizes, SR
+             ((1040, 64, 1056), m.linear_cfg(mode=m.INT8MP_SR, seed=11, offset=5)),  # second: other sizes, SR
+             # a long contraction: the CTA-pair matmul, whose last wave the
+             # workspace forward splits but the scratch array must not
+             ((384, 256, 8192), m.linear_cfg()),
+             ((256, 256, 512), m.linear_cfg(mode=m.INT8MP_SR, seed=3))]
     for (T, N, K), cfg in cases:
         X, W = _inputs(T, N, K, seed=T + K)
         ref = m.int8mp_linear_fwd(X, W, cfg)
