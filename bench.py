@@ -514,6 +514,68 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
     return out
 
 
+def single_matmul_latency(device, iters=200):
+    """The 256x512 single forward matmul (X and W quantized by rows in one
+    launch, then the scaled matmul): median device time per call, from
+    events around each call, inputs resident."""
+    import torch
+    import int8_mixed_precision_row_gb300 as m
+    from int8_mixed_precision_row_gb300 import synth
+    X, W = synth.single_matmul_inputs()
+    X, W = X.to(device), W.to(device)
+    qx = torch.empty((256, 512), dtype=torch.float16, device=device)
+    qw = torch.empty((256, 512), dtype=torch.float16, device=device)
+    sx = torch.empty(256, dtype=torch.float32, device=device)
+    sw = torch.empty(256, dtype=torch.float32, device=device)
+    Y = torch.empty((256, 256), dtype=torch.bfloat16, device=device)
+    ev = []
+    for it in range(iters + 10):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record()
+        m.int8mp_quantize_rows_batch([X, W], codes=m.INT8MP_CODES_F16, qs=[qx, qw], scales=[sx, sw])
+        m.int8mp_scaled_mm(qx, sx, qw, sw, out=Y)
+        e[1].record()
+        if it >= 10:
+            ev.append(e)
+    torch.cuda.synchronize()
+    us = statistics.median([a.elapsed_time(b) for a, b in ev]) * 1e3
+    return {"us_per_call": round(us, 2), "tops": round(2.0 * 256 * 256 * 512 / (us * 1e-6) / 1e12, 2),
+            "launches_per_call": 2}
+
+
+def decoder_module_tok_s(spec, device, steps=5, warmup=2):
+    """The decoder layer's seven linears as Int8MixedPrecisionDecoderLinears
+    (SwiGLU between gate/up and down, glue in fp32 torch ops), forward and
+    backward through torch.autograd on T tokens."""
+    import torch
+    import int8_mixed_precision_row_gb300 as m
+    from int8_mixed_precision_row_gb300 import synth
+    T = spec["T"]
+    layer = m.Int8MixedPrecisionDecoderLinears(spec["hidden"], spec["inter"], device=device)
+    x = synth.bf16_normal((T, spec["hidden"]), 10).to(device).requires_grad_(True)
+    dy = synth.bf16_normal((T, spec["hidden"]), 30, std=1e-3).to(device)
+
+    def one():
+        layer.zero_grad(set_to_none=True)
+        x.grad = None
+        layer(x).backward(dy)
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    del layer, x, dy
+    torch.cuda.empty_cache()
+    return {"tok_s": round(T / (ms * 1e-3), 1), "ms_per_step": round(ms, 3),
+            "glue": "fp32 torch elementwise (stand-in attention a = v + q*k, SwiGLU, residuals)"}
+
+
 def layer_tok_s(spec, mode, device, steps=5, warmup=2):
     import torch
     step = LayerStep(spec, mode, device)
@@ -672,6 +734,7 @@ def main():
     gemm_tflops = step.flops * args.steps / (gemm_ms * 1e-3) / 1e12
     quant_ms = per_kind.get("quant_rows", 0.0) + per_kind.get("quant_cols", 0.0)
     quant_bytes = step.quant_elems * 4 * args.steps  # bf16 read + f16 code written per element
+    quant_bytes_alg = step.quant_elems * 3 * args.steps  # bf16 read + one int8 code: the minimum
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 3),
@@ -684,14 +747,14 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor",
                      "kernel": "gemm_s8f16_pair_kernel (CTA-pair tcgen05 kind::f16, exact int32)",
-                     "achieved": round(gemm_tflops, 1), "peak": bf16_sust, "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / bf16_sust, 3),
+                     "achieved": round(gemm_tflops, 1), "peak": bf16_burst, "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / bf16_burst, 3),
                      "traffic": gemm_traffic() if step.T == spec["T"] and not only else None,
                      "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
                      "algorithmic_bytes": round(step.gemm_bytes / step.gemms_per_step),
-                     "peak_source": f"{peak_src} dense bf16 sustained (f16 runs at the bf16 rate); "
-                                    f"burst {bf16_burst} TFLOP/s -> frac "
-                                    f"{round(gemm_tflops / bf16_burst, 3)}",
+                     "peak_source": f"{peak_src} dense bf16 burst (f16 runs at the bf16 rate; "
+                                    f"sm_103a has no faster INT8 MMA); sustained {bf16_sust} "
+                                    f"TFLOP/s -> frac {round(gemm_tflops / bf16_sust, 3)}",
                      "launches_timed": gemm_launches,
                      "avg_launch_ms": round(gemm_ms / gemm_launches, 4)},
         "kernels": {
@@ -699,6 +762,15 @@ def main():
             "quant_rows_ms_per_step": round(per_kind.get("quant_rows", 0.0) / args.steps, 3),
             "quant_cols_ms_per_step": round(per_kind.get("quant_cols", 0.0) / args.steps, 3),
             "quant_gbs_f16codes": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1) if quant_ms else None,
+            "quant_frac_of_hbm_f16codes": round(quant_bytes / (quant_ms * 1e-3) / 1e9 / hbm, 3)
+            if quant_ms else None,
+            "quant_gbs_algorithmic_3B": round(quant_bytes_alg / (quant_ms * 1e-3) / 1e9, 1)
+            if quant_ms else None,
+            "quant_frac_of_hbm_algorithmic_3B": round(quant_bytes_alg / (quant_ms * 1e-3) / 1e9 / hbm, 3)
+            if quant_ms else None,
+            "quant_bytes_note": "f16codes: bytes moved (bf16 read + f16 code container written, 4 B "
+                                "per element); algorithmic_3B: bf16 read + int8 code, 3 B per "
+                                "element",
             "hbm_peak_gbs": hbm,
             "timing": "value: the timed steps with no per-kernel events; this breakdown: up "
                       "to 20 further steps with CUDA events around every call, scaled"},
@@ -717,7 +789,9 @@ def main():
     torch.cuda.empty_cache()
     if rank == 0 and not args.profile_steps and not args.no_extra:
         line["extra"] = {
+            "single_forward_matmul_256x256x512": single_matmul_latency(device),
             "square_quant_scaled_mm": square_sweep(device),
+            "llama2-1b_decoder_module_autograd": decoder_module_tok_s(synth.LLAMA2_1B, device),
             "llama2-1b_stochastic_rounding": layer_tok_s(synth.LLAMA2_1B, m.INT8MP_SR, device),
             "llama3-8b_T16384": layer_tok_s(synth.LLAMA3_8B, m.INT8MP_RNE, device),
             "llama2-1b_pass_switches (forward/grad-input/grad-weight)":

@@ -274,10 +274,13 @@ int8mp_status int8mp_mm_s32_ws(const void* A, const void* B, int64_t M, int64_t 
  * switches and stochastic-rounding switch; "Quantized model training"
  * README, INT8 mixed precision training table).  int8_* = 1 runs that pass
  * in INT8 as described above; 0 runs it in BF16: the plain product of the
- * bf16 operands with fp32 accumulation and a bf16 result, computed by
- * cuBLASLt (a library GEMM; cuBLASLt keeps a per-device handle, created on
- * first use).  Other values return INT8MP_ERR_INVALID_ARG.  mode, seed and
- * offset apply to the INT8 passes.
+ * bf16 operands, accumulated in fp32 by the same tcgen05 kernels (bf16
+ * operand format, one accumulator over the whole contraction; a split last
+ * wave adds its fp32 parts in a fixed order) and rounded once to bf16
+ * (nearest even).  The fp32 summation order is the tensor core's, so a BF16
+ * pass matches the plain product within fp32 accumulation error, not bit for
+ * bit.  Other values return INT8MP_ERR_INVALID_ARG.  mode, seed and offset
+ * apply to the INT8 passes.
  */
 typedef struct {
   int int8_fwd;
@@ -359,8 +362,7 @@ int8mp_status int8mp_linear_bwd_saved(const void* dY, const void* X, const void*
  * round256(4*N) bytes above the maximum, return INT8MP_ERR_WORKSPACE before
  * anything is launched.  Nothing is allocated by the call.
  *
- * The forward pass must be the INT8 one (cfg->int8_fwd = 1; the BF16 pass runs
- * in a library GEMM that may allocate, so it returns INT8MP_ERR_INVALID_ARG).
+ * cfg->int8_fwd may be 0 (the BF16 forward pass needs no workspace).
  * The first call on a device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress); make that first call before
  * any stream capture.  All calls on a device share the array and it keeps the

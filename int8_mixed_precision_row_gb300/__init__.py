@@ -8,3 +8,4 @@ from .binding import *  # noqa: F401,F403
 from .binding import (EXPORTED, Int8mpError, int8mp_linear_cfg, linear_cfg, load,  # noqa: F401
                       library_path)
 from .autograd import Int8MixedPrecisionLinear, Int8MixedPrecisionLinearFunction  # noqa: F401,E402
+from .decoder import Int8MixedPrecisionDecoderLinears  # noqa: F401,E402

@@ -296,11 +296,23 @@ def _mm_ws(workspace, device):
     return workspace, workspace.numel() * workspace.element_size()
 
 
-def int8mp_scaled_mm(A, sA, B, sB, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, out=None,
+def _mm_codes(A, B, codes):
+    """The code container: given, or that of the operands' dtype (int8 ->
+    INT8MP_CODES_S8, float16 -> INT8MP_CODES_F16)."""
+    if codes is None:
+        codes = INT8MP_CODES_S8 if A.dtype == torch.int8 else INT8MP_CODES_F16
+    want = _code_dtype(codes)
+    if A.dtype != want or B.dtype != want:
+        raise ValueError(f"codes {codes} need {want} operands, got {A.dtype} and {B.dtype}")
+    return codes
+
+
+def int8mp_scaled_mm(A, sA, B, sB, layout=INT8MP_AxBT, codes=None, out=None,
                      stream=None, workspace=None):
-    """Codes (f16 containers) A, B stored per layout -- A@B.T: A [M,K], B [N,K];
-    A@B: A [M,K], B [K,N]; A.T@B: A [K,M], B [K,N] -- sA [M], sB [N] -> bf16
-    [M,N]."""
+    """Codes A, B (int8, or f16 containers) stored per layout -- A@B.T: A
+    [M,K], B [N,K]; A@B: A [M,K], B [K,N]; A.T@B: A [K,M], B [K,N] -- sA [M],
+    sB [N] -> bf16 [M,N]."""
+    codes = _mm_codes(A, B, codes)
     M, N, K = _mm_sizes(A, B, layout)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
@@ -318,8 +330,10 @@ def int8mp_scaled_mm(A, sA, B, sB, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, o
     return out
 
 
-def int8mp_mm_s32(A, B, layout=INT8MP_AxBT, codes=INT8MP_CODES_F16, out=None, stream=None,
+def int8mp_mm_s32(A, B, layout=INT8MP_AxBT, codes=None, out=None, stream=None,
                   workspace=None):
+    """The exact int32 product of codes A, B (int8 or f16 containers)."""
+    codes = _mm_codes(A, B, codes)
     M, N, K = _mm_sizes(A, B, layout)
     if out is None:
         out = torch.empty((M, N), dtype=torch.int32, device=A.device)

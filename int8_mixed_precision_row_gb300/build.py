@@ -24,7 +24,7 @@ LIB = os.path.join(OUT_DIR, "libint8mp.so")
 CHECK_DIR = os.path.join(HERE, "_build_check")
 CHECK_LIB = os.path.join(CHECK_DIR, "libint8mp.so")
 
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "tma.cu", "blas.cu", "noalloc.cu", "debug.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "tma.cu", "noalloc.cu", "debug.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "philox.cuh", "divide.cuh", "check.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
@@ -68,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, check: bool = False) -> st
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose, out_dir, extra), SOURCES))
     tmp = lib + f".tmp{os.getpid()}"
-    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-lcublasLt"]
+    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -102,12 +102,14 @@ int8mp_status check_mm(const void* A, const void* B, int64_t M, int64_t N, int64
   if (codes != INT8MP_CODES_S8 && codes != INT8MP_CODES_F16) return INT8MP_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || K > INT8MP_MAX_K || ldo < N) return INT8MP_ERR_INVALID_ARG;
   if (M > INT32_MAX || N > INT32_MAX) return INT8MP_ERR_INVALID_ARG;
-  // the tensor-core path reads f16 containers
-  if (codes != INT8MP_CODES_F16) return INT8MP_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return INT8MP_OK;
   if (!out || (K > 0 && (!A || !B))) return INT8MP_ERR_INVALID_ARG;
   if (K % 16 || N % 8 || ldo % 8 || !aligned(out, 16)) return INT8MP_ERR_ALIGNMENT;
   if (layout == INT8MP_ATxB && M % 8) return INT8MP_ERR_ALIGNMENT;  // rows of A^T are M long
+  // int8 rows of a [K, M] or [K, N] operand are 16-byte multiples (TMA strides)
+  if (codes == INT8MP_CODES_S8 && ((layout != INT8MP_AxBT && N % 16) ||
+                                   (layout == INT8MP_ATxB && M % 16)))
+    return INT8MP_ERR_ALIGNMENT;
   if (K > 0 && (!aligned(A, 16) || !aligned(B, 16))) return INT8MP_ERR_ALIGNMENT;
   return INT8MP_OK;
 }
@@ -126,7 +128,7 @@ int8mp_status check_mm_workspace(const void* workspace, size_t ws_bytes) {
 int8mp_status run_mm(const void* A, const float* sA, const void* B, const float* sB, int64_t M,
                      int64_t N, int64_t K, int8mp_layout layout, int8mp::GemmOut mode, void* out,
                      int64_t ldo, void* scratch, const int8mp::GemmDebug& dbg,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, bool s8 = false) {
   if (M == 0 || N == 0) return INT8MP_OK;
   DeviceInfo dev;
   int8mp_status st = current_device(&dev, stream);
@@ -137,8 +139,8 @@ int8mp_status run_mm(const void* A, const float* sA, const void* B, const float*
                                        static_cast<size_t>(N) * esize, static_cast<size_t>(M),
                                        stream));
   const bool a_mn = layout == INT8MP_ATxB, b_mn = layout != INT8MP_AxBT;
-  return from_cuda(int8mp::launch_gemm(A, a_mn, sA, B, b_mn, sB, M, N, K, mode, out, ldo, scratch,
-                                       dev, dbg, stream));
+  return from_cuda(int8mp::launch_gemm(A, a_mn, sA, B, b_mn, sB, M, N, K, s8, mode, out, ldo,
+                                       scratch, dev, dbg, stream));
 }
 
 // ------------------------------------------------------------- workspace
@@ -321,7 +323,7 @@ int8mp_status int8mp_scaled_mm_ws(const void* A, const float* sA, const void* B,
     if (!aligned(sA, 4) || !aligned(sB, 4)) return INT8MP_ERR_ALIGNMENT;
   }
   return run_mm(A, sA, B, sB, M, N, K, layout, int8mp::GemmOut::kBf16Scaled, out, ldo,
-                workspace, int8mp::GemmDebug{}, as_stream(stream));
+                workspace, int8mp::GemmDebug{}, as_stream(stream), codes == INT8MP_CODES_S8);
 }
 
 int8mp_status int8mp_mm_s32(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
@@ -338,7 +340,7 @@ int8mp_status int8mp_mm_s32_ws(const void* A, const void* B, int64_t M, int64_t 
   st = check_mm_workspace(workspace, ws_bytes);
   if (st != INT8MP_OK) return st;
   return run_mm(A, nullptr, B, nullptr, M, N, K, layout, int8mp::GemmOut::kS32, out, ldo,
-                workspace, int8mp::GemmDebug{}, as_stream(stream));
+                workspace, int8mp::GemmDebug{}, as_stream(stream), codes == INT8MP_CODES_S8);
 }
 
 size_t int8mp_linear_workspace_size(int64_t T, int64_t N, int64_t K, const int8mp_linear_cfg* cfg) {
@@ -384,11 +386,9 @@ int8mp_status linear_fwd_impl(const void* X, const void* W, void* Y, int64_t T, 
     if (x_absmax) e = int8mp::launch_column_absmax(X, T, K, K, x_absmax, dev, s);
     if (e == cudaSuccess && w_absmax) e = int8mp::launch_column_absmax(W, N, K, K, w_absmax, dev, s);
     if (e != cudaSuccess) return INT8MP_ERR_CUDA;
-    // BF16 pass: Y [T,N] = X W^T, i.e. column-major Y^T [N,T] = W X^T
-    if (K == 0)
-      return from_cuda(cudaMemset2DAsync(Y, static_cast<size_t>(N) * 2, 0,
-                                         static_cast<size_t>(N) * 2, static_cast<size_t>(T), s));
-    return from_cuda(int8mp::bf16_gemm_colmajor(W, X, Y, N, T, K, true, false, K, K, N, s));
+    // BF16 pass: Y [T,N] = X W^T (A @ B.T), bf16 operands, fp32 accumulation
+    return run_mm(X, nullptr, W, nullptr, T, N, K, INT8MP_AxBT, int8mp::GemmOut::kBf16Plain, Y, N,
+                  gemm_scratch(workspace, ws_bytes, fwd_bytes(T, N, K)), int8mp::GemmDebug{}, s);
   }
   Carver c{static_cast<char*>(workspace)};
   const QOperand xq = carve_operand(c, T, K);
@@ -461,12 +461,9 @@ int8mp_status linear_bwd_impl(const void* dY, const void* X, const void* W, void
     return INT8MP_ERR_CUDA;
 
   if (want_dx && !cfg->int8_grad_in) {
-    // BF16 pass: dX [T,K] = dY W, i.e. column-major dX^T [K,T] = W^T dY^T
-    if (N == 0)
-      st = from_cuda(cudaMemset2DAsync(dX, static_cast<size_t>(K) * 2, 0,
-                                       static_cast<size_t>(K) * 2, static_cast<size_t>(T), s));
-    else
-      st = from_cuda(int8mp::bf16_gemm_colmajor(W, dY, dX, K, T, N, false, false, K, N, K, s));
+    // BF16 pass: dX [T,K] = dY W (A @ B, W read N-major)
+    st = run_mm(dY, nullptr, W, nullptr, T, K, N, INT8MP_AxB, int8mp::GemmOut::kBf16Plain, dX, K,
+                scratch, int8mp::GemmDebug{}, s);
     if (st != INT8MP_OK) return st;
   } else if (want_dx) {
     // grad input: contraction over N; dY by rows, W by columns; dY W is A @ B
@@ -486,12 +483,9 @@ int8mp_status linear_bwd_impl(const void* dY, const void* X, const void* W, void
     if (st != INT8MP_OK) return st;
   }
   if (want_dw && !cfg->int8_grad_w) {
-    // BF16 pass: dW [N,K] = dY^T X, i.e. column-major dW^T [K,N] = X^T dY
-    if (T == 0)
-      st = from_cuda(cudaMemset2DAsync(dW, static_cast<size_t>(K) * 2, 0,
-                                       static_cast<size_t>(K) * 2, static_cast<size_t>(N), s));
-    else
-      st = from_cuda(int8mp::bf16_gemm_colmajor(X, dY, dW, K, N, T, false, true, K, N, K, s));
+    // BF16 pass: dW [N,K] = dY^T X (A.T @ B, both read T-major)
+    st = run_mm(dY, nullptr, X, nullptr, N, K, T, INT8MP_ATxB, int8mp::GemmOut::kBf16Plain, dW, K,
+                scratch, int8mp::GemmDebug{}, s);
   } else if (want_dw) {
     // grad weight: contraction over T; dY and X by columns; dY^T X is A.T @ B
     if (T > 0) {

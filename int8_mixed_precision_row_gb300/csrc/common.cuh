@@ -118,7 +118,10 @@ cudaError_t launch_quantize_cols(const void* x, int64_t rows, int64_t cols, int6
                                  const DeviceInfo& dev, cudaStream_t stream);
 
 // ---- GEMM (gemm.cu) ---------------------------------------------------------
-enum class GemmOut { kBf16Scaled = 0, kS32 = 1 };
+// kBf16Scaled: integer codes in f16 containers, out = bf16((acc * sA) * sB);
+// kS32: the same codes, out = the int32 accumulator; kBf16Plain: bf16
+// operands, out = bf16_RNE of their fp32-accumulated product (sA, sB unused).
+enum class GemmOut { kBf16Scaled = 0, kS32 = 1, kBf16Plain = 2 };
 
 struct GemmDebug {
   int drop_first_load = 0;        // test only: never issue the first TMA load
@@ -135,20 +138,15 @@ constexpr int kSplitTailMaxPairs = 80;
 constexpr size_t kSplitTailScratchBytes =
     static_cast<size_t>(kSplitTailMaxPairs) * 256 * 256 * 4 + kSplitTailMaxPairs * 2 * 8 * 8;
 
-// f16 containers of integer codes.  A is [M,K] (a_mn false, K contiguous)
-// or [K,M] (a_mn true, M contiguous); B is [N,K] or [K,N] likewise.  Every
-// combination but (a_mn, !b_mn) is served.  scratch: NULL, or
-// kSplitTailScratchBytes (16-byte aligned) that lets the CTA-pair kernel
+// Integer codes in f16 containers, or as int8 (s8: widened to f16 inside the
+// CTA-pair kernel), or bf16 values for kBf16Plain.  A is [M,K] (a_mn false,
+// K contiguous) or [K,M] (a_mn true, M contiguous); B is [N,K] or [K,N]
+// likewise.  Every combination but (a_mn, !b_mn) is served.  scratch: NULL,
+// or kSplitTailScratchBytes (16-byte aligned) that lets the CTA-pair kernel
 // split its last wave of tiles.
 cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B, bool b_mn,
-                        const float* sB, int64_t M, int64_t N, int64_t K, GemmOut mode, void* out,
-                        int64_t ldo, void* scratch, const DeviceInfo& dev, const GemmDebug& dbg,
-                        cudaStream_t stream);
-
-// ---- BF16 passes (blas.cu) --------------------------------------------------
-// Column-major C [m, n] = op(A) op(B), bf16 in and out, fp32 accumulation.
-cudaError_t bf16_gemm_colmajor(const void* A, const void* B, void* C, int64_t m, int64_t n,
-                               int64_t k, bool transa, bool transb, int64_t lda, int64_t ldb,
-                               int64_t ldc, cudaStream_t stream);
+                        const float* sB, int64_t M, int64_t N, int64_t K, bool s8, GemmOut mode,
+                        void* out, int64_t ldo, void* scratch, const DeviceInfo& dev,
+                        const GemmDebug& dbg, cudaStream_t stream);
 
 }  // namespace int8mp

@@ -5,6 +5,9 @@
 // torchao 0.7": the product is scaled back to BF16):
 //   acc[i,j] = sum_k qA[i,k] * qB[j,k]                 (exact int32)
 //   out[i,j] = bf16_RNE((fp32_RN(acc) * sA[i]) * sB[j])  or acc itself.
+// The same kernels also run the BF16 passes of the training table's mixed
+// rows (a matmul left in BF16): bf16 operands, one fp32 accumulation over
+// the whole contraction in tensor memory, out = bf16_RNE(acc).
 //
 // How: sm_103a has no INT8 tcgen05 MMA, so the codes arrive as f16 values
 // (exact for |q| <= 127) and the contraction runs on tcgen05.mma.kind::f16
@@ -73,7 +76,9 @@ struct GemmParams {
   int64_t ldo;
   int M, N, K;
   int m_tiles, n_tiles, k_blocks;
-  int mode;  // 0: bf16 scaled, 1: int32 accumulators
+  int mode;  // 0: bf16 scaled, 1: int32 accumulators, 2: plain bf16 (fp32 accumulator)
+  uint32_t ab_format;   // operand-format bits of the instruction descriptor (bf16 or f16)
+  int chunk_blocks;     // k-blocks per accumulator hand-off (exact chunks, or all of K)
   unsigned int* status;
   uint64_t wait_limit_ns;
   int drop_first_load;
@@ -155,6 +160,17 @@ __device__ __forceinline__ void store_vec8(const GemmParams& p, int64_t row, int
     return;
   }
   uint32_t w[4];
+  if (p.mode == 2) {  // t holds fp32 bit patterns
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 h =
+          __floats2bfloat162_rn(__int_as_float(t[2 * e]), __int_as_float(t[2 * e + 1]));
+      w[e] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.ldo + col) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+    return;
+  }
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float o0 = __fmul_rn(__fmul_rn(__int2float_rn(t[2 * e]), sa), __ldg(p.sB + col + 2 * e));
@@ -169,8 +185,20 @@ __device__ __forceinline__ void store_vec8(const GemmParams& p, int64_t row, int
 
 // Drain one 128-column half of a chunk accumulator (this warp's 32 lanes)
 // from tensor memory into the int32 totals; every fp32 value is an exact
-// integer below 2^24 in magnitude.
-__device__ __forceinline__ void drain_chunk(uint32_t taddr, int32_t (&tot)[128]) {
+// integer below 2^24 in magnitude.  Plain bf16 launches (one chunk per tile)
+// keep the fp32 bit patterns themselves.
+__device__ __forceinline__ void drain_chunk(uint32_t taddr, int32_t (&tot)[128], bool plain) {
+  if (plain) {
+#pragma unroll
+    for (int sub = 0; sub < 8; ++sub) {
+      uint32_t r[16];
+      ptx::tmem_ld_16cols(taddr + sub * 16, r);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) tot[sub * 16 + i] = static_cast<int32_t>(r[i]);
+    }
+    return;
+  }
 #pragma unroll
   for (int sub = 0; sub < 8; ++sub) {
     uint32_t r[16];
@@ -198,7 +226,7 @@ template <bool kRegScales>
 __device__ __forceinline__ TileScales load_tile_scales(const GemmParams& p, int64_t row0,
                                                        int64_t col0) {
   TileScales t{0.0f, {0.0f, 0.0f, 0.0f, 0.0f}};
-  if (!kRegScales || p.mode == 1) return t;
+  if (!kRegScales || p.mode != 0) return t;
   const int lane = threadIdx.x & 31;
   if (row0 + lane < p.M) t.sa = __ldg(p.sA + row0 + lane);
 #pragma unroll
@@ -249,6 +277,28 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
       for (int c = 0; c < 8; ++c) {
         const int32_t* t = tot + 32 * j + 4 * c;
         ptx::st_shared_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), t[0], t[1], t[2], t[3]);
+      }
+      publish(c0);
+    }
+    return;
+  }
+  if (p.mode == 2) {  // plain bf16: tot holds fp32 bit patterns
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int64_t c0 = col0 + 64 * j;
+      if (c0 >= p.N) break;
+      reuse();
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int32_t* t = tot + 64 * j + 8 * c;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 h =
+              __floats2bfloat162_rn(__int_as_float(t[2 * e]), __int_as_float(t[2 * e + 1]));
+          w[e] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        ptx::st_shared_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), w[0], w[1], w[2], w[3]);
       }
       publish(c0);
     }
@@ -391,11 +441,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ----------------------------------------------------------- MMA
-      constexpr uint32_t idesc = ptx::idesc_f16_f32(kBM, kBN, kAmn, kBmn);
+      const uint32_t idesc = ptx::idesc_f16_f32(kBM, kBN, kAmn, kBmn) | p.ab_format;
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        for (int kb0 = 0; kb0 < p.k_blocks && ok; kb0 += kChunkBlocks) {
+        for (int kb0 = 0; kb0 < p.k_blocks && ok; kb0 += p.chunk_blocks) {
           const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
           if (!ptx::mbar_wait_bounded(tempty_bar(buf), aph ^ 1u, abort, limit)) {
             ok = false;
@@ -403,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * kBN;
-          const int kb_end = min(kb0 + kChunkBlocks, p.k_blocks);
+          const int kb_end = min(kb0 + p.chunk_blocks, p.k_blocks);
           for (int kb = kb0; kb < kb_end; ++kb) {
             if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort, limit)) {
               ok = false;
@@ -448,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t tot[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) tot[i] = 0;
-      for (int kb0 = 0; kb0 < p.k_blocks; kb0 += kChunkBlocks) {
+      for (int kb0 = 0; kb0 < p.k_blocks; kb0 += p.chunk_blocks) {
         const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
         int got = 1;
         if (lane == 0) got = ptx::mbar_wait_bounded(tfull_bar(buf), aph, abort, limit) ? 1 : 0;
@@ -460,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kBN +
                                static_cast<uint32_t>(half * 128);
-        drain_chunk(taddr, tot);
+        drain_chunk(taddr, tot, p.mode == 2);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
@@ -512,11 +562,89 @@ constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairSmemBytes =
     1024 + kPairStages * kPairStageBytes + kStagingBytes + kBarrierBytes;
 static_assert(kPairSmemBytes <= 227 * 1024, "pair kernel shared memory");
+// int8 operands (kS8): TMA brings each CTA's int8 k-block (128 x 64 codes of
+// A and of B, 16 KB) into a ring of its own, and two converter warps widen it
+// into the f16 stage the tensor core reads -- fewer f16 stages, more raw ones
+// (the raw ring covers the DRAM latency, the f16 ring only decouples the
+// converters from the MMA).
+constexpr int kS8Stages = 3;
+constexpr int kRawStages = 6;
+constexpr int kRawOperandBytes = 128 * kBK;  // 128 rows x 64 k, one byte each
+constexpr int kRawStageBytes = 2 * kRawOperandBytes;
+constexpr int kConvWarps = 2;
+constexpr int kS8Threads = kThreads + kConvWarps * 32;
+constexpr int kS8SmemBytes = 1024 + kS8Stages * kPairStageBytes + kRawStages * kRawStageBytes +
+                             kStagingBytes + kBarrierBytes;
+static_assert(kS8SmemBytes <= 227 * 1024, "int8-operand pair kernel shared memory");
+static_assert((2 * kS8Stages + 5 + 2 * kRawStages) * 8 + 12 <= kBarrierBytes, "barrier area");
 constexpr int kCasLimit = 4096;  // bound on the counter's compare-and-swap retries
 constexpr int kMaxSplit = 4;     // most parts a tile of the last wave is split into
 static_assert(static_cast<size_t>(kSplitTailMaxPairs) * 256 * 256 * 4 +
                       kSplitTailMaxPairs * 2 * kEpiWarps * 8 <= kSplitTailScratchBytes,
               "split-tail scratch layout");
+
+// TMA of one operand's int8 k-block (128 rows of M or N x 64 k) into the
+// CTA's raw ring, unswizzled: K-major [128][64] (a 64-byte row per M/N),
+// MN-major [64][128] (a 128-byte row per k).  Completion on this CTA's own
+// barrier.
+template <bool kMN>
+__device__ __forceinline__ void load_raw(uint32_t dst, const CUtensorMap* map, uint32_t bar, int kb,
+                                         int mn0) {
+  if (kMN)
+    ptx::tma_load_2d(dst, map, bar, mn0, kb * kBK);
+  else
+    ptx::tma_load_2d(dst, map, bar, kb * kBK, mn0);
+}
+
+// Four int8 codes (one word) as two f16x2 words holding the same integers:
+// the biased byte u = q + 128 becomes the f16 0x6400 | u = 1024 + u, and
+// subtracting 1152 leaves q exactly (every value involved is an integer
+// below 2048, exact in f16).
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+// Widen one operand's raw int8 k-block (8 KB at `raw`) into its f16 stage
+// tile at `dst`, in the 128-byte swizzled layout a TMA load would have
+// written: K-major, row m (128 bytes: 64 k) at m * 128; MN-major, 64-wide
+// block b, row k at b * 8192 + k * 128; 16-byte chunk c of row r at
+// (c ^ (r % 8)) * 16.  Converter thread ct (of 64) takes 16-byte raw chunks
+// ct, ct + 64, ...; each becomes 32 bytes (two chunks) of one f16 row.
+// Bank conflicts: eight consecutive raw chunks (a quarter warp) are 128
+// contiguous bytes.  K-major, they fill two f16 rows with different
+// swizzles, so the first (and the second) stores of the quarter warp land in
+// complementary chunk sets.  MN-major, they are one k of both 64-wide blocks
+// (same swizzle): the threads of block 1 store their second chunk first.
+template <bool kMN>
+__device__ __forceinline__ void widen_tile(uint32_t raw, uint32_t dst, int ct) {
+  const int swap = kMN ? (ct >> 2) & 1 : 0;  // the same for every chunk of this thread
+#pragma unroll 4
+  for (int i = 0; i < kRawOperandBytes / 16 / (kConvWarps * 32); ++i) {
+    const int c = ct + kConvWarps * 32 * i;
+    const int row = kMN ? ((c >> 2) & 1) * 64 + (c >> 3) : c >> 2;
+    const int chunk = (c & 3) * 2;  // first of the row's two 16-byte chunks
+    uint4 v = ptx::ld_shared_v4(raw + static_cast<uint32_t>(c) * 16u);
+    if (swap) {
+      const uint32_t x = v.x, y = v.y;
+      v.x = v.z, v.y = v.w, v.z = x, v.w = y;
+    }
+    uint32_t h[8];
+    widen4(v.x, h[0], h[1]);
+    widen4(v.y, h[2], h[3]);
+    widen4(v.z, h[4], h[5]);
+    widen4(v.w, h[6], h[7]);
+    const uint32_t rowaddr = dst + static_cast<uint32_t>(row) * 128u;
+    const uint32_t sw = static_cast<uint32_t>(row & 7);
+    const uint32_t c0 = static_cast<uint32_t>(chunk + swap), c1 = static_cast<uint32_t>(chunk + 1 - swap);
+    ptx::st_shared_v4(rowaddr + ((c0 ^ sw) << 4), h[0], h[1], h[2], h[3]);
+    ptx::st_shared_v4(rowaddr + ((c1 ^ sw) << 4), h[4], h[5], h[6], h[7]);
+  }
+}
 
 // The fragments (tile, k-blocks [kb0, kb1)) one pair computes, in order:
 // whole tiles pair, pair + P, ... below p.dp_tiles (P pairs), then, when
@@ -593,6 +721,11 @@ __device__ __forceinline__ void sk_store_part(const GemmParams& p, int pair, int
   __syncwarp();
 }
 
+// fp32 sum of two fp32 bit patterns, as a bit pattern
+__device__ __forceinline__ int32_t fadd_bits(int32_t a, int32_t b) {
+  return __float_as_int(__fadd_rn(__int_as_float(a), __int_as_float(b)));
+}
+
 __device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int ewarp, int tile,
                                             int64_t row, int64_t col0, volatile int* abort) {
   const int t = tile - p.dp_tiles;  // tail tile: parts come from pairs t*s .. t*s+s-1
@@ -610,7 +743,7 @@ __device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int e
   }
   if (r == 0 || row >= p.M) return;
   __threadfence();
-  const float sa = p.mode == 1 ? 0.0f : __ldg(p.sA + row);
+  const float sa = p.mode != 0 ? 0.0f : __ldg(p.sA + row);
   // 32 columns at a time: each part's 8 vectors are loaded together
   for (int h = 0; h < 4; ++h) {
     int32_t acc[32];
@@ -621,12 +754,22 @@ __device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int e
       int4 x[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) x[i] = __ldcg(src + i * 32);
+      if (p.mode == 2) {  // fp32 partial sums, added in part order
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        acc[4 * i] += x[i].x;
-        acc[4 * i + 1] += x[i].y;
-        acc[4 * i + 2] += x[i].z;
-        acc[4 * i + 3] += x[i].w;
+        for (int i = 0; i < 8; ++i) {
+          acc[4 * i] = fadd_bits(acc[4 * i], x[i].x);
+          acc[4 * i + 1] = fadd_bits(acc[4 * i + 1], x[i].y);
+          acc[4 * i + 2] = fadd_bits(acc[4 * i + 2], x[i].z);
+          acc[4 * i + 3] = fadd_bits(acc[4 * i + 3], x[i].w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[4 * i] += x[i].x;
+          acc[4 * i + 1] += x[i].y;
+          acc[4 * i + 2] += x[i].z;
+          acc[4 * i + 3] += x[i].w;
+        }
       }
     }
 #pragma unroll
@@ -634,27 +777,39 @@ __device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int e
   }
 }
 
-template <bool kAmn, bool kBmn, bool kRegScales>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// kS8: the operands are int8 codes (INT8MP_CODES_S8).  Each CTA's producer
+// brings its int8 k-blocks into a raw ring (its own barriers); converter
+// warps 10-11 of both CTAs widen them into the f16 stages and arrive on the
+// even CTA's full barrier (release at cluster scope, after a proxy fence so
+// that the tensor core sees the stores), which the MMA thread waits on at
+// cluster scope.  Everything else is the f16 kernel.
+template <bool kAmn, bool kBmn, bool kRegScales, bool kS8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : kThreads, 1)
     gemm_s8f16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
+  constexpr int kStagesHere = kS8 ? kS8Stages : kPairStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = ptx::smem_addr(smem);
   const uint32_t a_base = sbase;
-  const uint32_t b_base = sbase + kPairStages * kPairABytes;
-  const uint32_t staging = sbase + kPairStages * kPairStageBytes;
-  uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes + kStagingBytes);
+  const uint32_t b_base = sbase + kStagesHere * kPairABytes;
+  const uint32_t rawring = sbase + kStagesHere * kPairStageBytes;  // kS8 only
+  constexpr int kRawBytesHere = kS8 ? kRawStages * kRawStageBytes : 0;
+  const uint32_t staging = sbase + kStagesHere * kPairStageBytes + kRawBytesHere;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStagesHere * kPairStageBytes +
+                                               kRawBytesHere + kStagingBytes);
   const uint32_t bar0 = ptx::smem_addr(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kPairStages + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kPairStages + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kPairStages + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kPairStages + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStagesHere + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStagesHere + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStagesHere + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStagesHere + 4);
+  auto rfull_bar = [&](int s) { return bar0 + 8u * (2 * kStagesHere + 5 + s); };
+  auto rempty_bar = [&](int s) { return bar0 + 8u * (2 * kStagesHere + 5 + kRawStages + s); };
+  constexpr int kBarsHere = 2 * kStagesHere + 5 + (kS8 ? 2 * kRawStages : 0);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarsHere);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
@@ -662,8 +817,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = ptx::cluster_ctarank();
   const bool even = rank == 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPairStages; ++s) {
-      ptx::mbar_init(full_bar(s), 1);
+    for (int s = 0; s < kStagesHere; ++s) {
+      // int8 operands: both CTAs' converter warps arrive; f16: the TMA bytes
+      ptx::mbar_init(full_bar(s), kS8 ? 2 * kConvWarps : 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -671,6 +827,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(tempty_bar(b), 2 * kEpiWarps);
     }
     ptx::mbar_init(drain_bar, 1);
+    if constexpr (kS8) {
+      for (int s = 0; s < kRawStages; ++s) {
+        ptx::mbar_init(rfull_bar(s), 1);
+        ptx::mbar_init(rempty_bar(s), kConvWarps);
+      }
+    }
     *abort = 0;
     *never = 0;
     ptx::fence_mbar_init();
@@ -692,7 +854,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const uint64_t limit = p.wait_limit_ns;
 
-  if (warp == 0) {
+  if (warp == 0 && kS8) {
+    if (lane == 0) {
+      // ------------------------------------------ producer (int8 operands)
+      // each CTA fills its own raw ring with its 128 rows of A and of B
+      uint32_t stage = 0, phase = 0;
+      uint32_t armed = 0u, armed_par = 0u;  // raw stages with a copy in flight
+      bool ok = true;
+      FragIter it(p, pair);
+      int tile, kb0, kb1;
+      while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
+        int mb, nb;
+        tile_mn(p, tile, mb, nb);
+        const int m0 = mb * 256 + static_cast<int>(rank) * 128;
+        const int n0 = nb * 256 + static_cast<int>(rank) * 128;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!ptx::mbar_wait_bounded(rempty_bar(stage), phase ^ 1u, abort, limit)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = rawring + stage * kRawStageBytes;
+          ptx::mbar_arrive_expect_tx(rfull_bar(stage), kRawStageBytes);
+          load_raw<kAmn>(dst, &tmA, rfull_bar(stage), kb, m0);
+          load_raw<kBmn>(dst + kRawOperandBytes, &tmB, rfull_bar(stage), kb, n0);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kRawStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) raise_abort(abort, p.status);
+      // never leave a copy in flight into shared memory of an exiting CTA:
+      // wait for the last copy into every raw stage (the earlier ones were
+      // consumed before the stage was refilled)
+      for (int s = 0; s < kRawStages; ++s)
+        if (armed & (1u << s))
+          if (!ptx::mbar_wait_bounded(rfull_bar(s), (armed_par >> s) & 1u, never, limit))
+            raise_abort(abort, p.status);
+    }
+  } else if (kS8 && warp >= 2 + kEpiWarps) {
+    // ------------------------------------------- converters (int8 operands)
+    const int ct = threadIdx.x - (2 + kEpiWarps) * 32;
+    uint32_t rstage = 0, rphase = 0, stage = 0, phase = 0;
+    bool ok = true;
+    FragIter it(p, pair);
+    int tile, kb0, kb1;
+    while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
+      for (int kb = kb0; kb < kb1; ++kb) {
+        // every lane waits (each then reads the copied bytes itself); the
+        // waits are bounded, so all lanes reach the vote and leave together
+        bool got = ptx::mbar_wait_bounded(rfull_bar(rstage), rphase, abort, limit);
+        got = got && ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort, limit);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          ok = false;
+          break;
+        }
+        const uint32_t raw = rawring + rstage * kRawStageBytes;
+        widen_tile<kAmn>(raw, a_base + stage * kPairABytes, ct);
+        widen_tile<kBmn>(raw + kRawOperandBytes, b_base + stage * kPairBBytes, ct);
+        ptx::fence_proxy_async_smem();  // the tensor core reads these stores
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(rempty_bar(rstage));
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(full_bar(stage), 0));
+        }
+        if (++rstage == kRawStages) {
+          rstage = 0;
+          rphase ^= 1u;
+        }
+        if (++stage == kStagesHere) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) raise_abort(abort, p.status);
+  } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ producer
       uint32_t stage = 0, phase = 0;
@@ -723,14 +962,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             load_operand_pair<kAmn, 128>(a_base + stage * kPairABytes, &tmA, fb, kb, m0);
             load_operand_pair<kBmn, 128>(b_base + stage * kPairBBytes, &tmB, fb, kb, n0);
           }
-          if (++stage == kPairStages) {
+          if (++stage == kStagesHere) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (!ok) raise_abort(abort, p.status);
-      for (int s = 0; s < kPairStages; ++s)
+      for (int s = 0; s < kStagesHere; ++s)
         if (armed & (1u << s))
           if (!ptx::mbar_wait_bounded(full_bar(s), (armed_par >> s) & 1u, never, limit))
             raise_abort(abort, p.status);
@@ -738,13 +977,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && even) {
       // ----------------------------------------------------------- MMA
-      constexpr uint32_t idesc = ptx::idesc_f16_f32(256, 256, kAmn, kBmn);
+      const uint32_t idesc = ptx::idesc_f16_f32(256, 256, kAmn, kBmn) | p.ab_format;
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true;
       FragIter it(p, pair);
       int tile, kb0, kb1;
       while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
-        for (int kc = kb0; kc < kb1 && ok; kc += kChunkBlocks) {
+        for (int kc = kb0; kc < kb1 && ok; kc += p.chunk_blocks) {
           const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
           if (!ptx::mbar_wait_bounded(tempty_bar(buf), aph ^ 1u, abort, limit)) {
             ok = false;
@@ -752,9 +991,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * kBN;
-          const int kc_end = min(kc + kChunkBlocks, kb1);
+          const int kc_end = min(kc + p.chunk_blocks, kb1);
           for (int kb = kc; kb < kc_end; ++kb) {
-            if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort, limit)) {
+            const bool got = kS8 ? ptx::mbar_wait_bounded_cluster(full_bar(stage), phase, abort, limit)
+                                 : ptx::mbar_wait_bounded(full_bar(stage), phase, abort, limit);
+            if (!got) {
               ok = false;
               break;
             }
@@ -766,7 +1007,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ptx::mma_f16_pair(d_tmem, adesc + k_step<kAmn>() * kk, bdesc + k_step<kBmn>() * kk,
                                 idesc, (kb > kc || kk > 0) ? 1u : 0u);
             ptx::mma_commit_pair(empty_bar(stage), 0x3);
-            if (++stage == kPairStages) {
+            if (++stage == kStagesHere) {
               stage = 0;
               phase ^= 1u;
             }
@@ -801,7 +1042,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int32_t tot[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) tot[i] = 0;
-      for (int kc = kb0; kc < kb1; kc += kChunkBlocks) {
+      for (int kc = kb0; kc < kb1; kc += p.chunk_blocks) {
         const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
         int got = 1;
         if (lane == 0) got = ptx::mbar_wait_bounded(tfull_bar(buf), aph, abort, limit) ? 1 : 0;
@@ -813,7 +1054,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kBN +
                                static_cast<uint32_t>(half * 128);
-        drain_chunk(taddr, tot);
+        drain_chunk(taddr, tot, p.mode == 2);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(buf), 0));
@@ -851,16 +1092,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-// f16 operand map, 128-byte swizzle, zero fill outside the tensor.
+// Operand map of 16-bit elements (f16 code containers, or bf16 for the plain
+// passes), 128-byte swizzle, zero fill outside the tensor.
 // K-major [mn, K] (row stride K): boxes of 64 k x box_mn rows.
 // MN-major [K, mn] (row stride mn): boxes of 64 (M or N) x 64 k.
 bool make_operand_map(CUtensorMap* map, const void* base, bool mn_major, int64_t mn, int64_t K,
-                      int box_mn) {
+                      int box_mn, bool bf16) {
+  const CUtensorMapDataType t =
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (mn_major)
-    return encode_tensor_map_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, mn, mn, 64, kBK,
-                                CU_TENSOR_MAP_SWIZZLE_128B);
-  return encode_tensor_map_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, mn, K, K, kBK, box_mn,
-                              CU_TENSOR_MAP_SWIZZLE_128B);
+    return encode_tensor_map_2d(map, base, t, 2, K, mn, mn, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
+  return encode_tensor_map_2d(map, base, t, 2, mn, K, K, kBK, box_mn, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Operand-format field of the kind::f16 instruction descriptor (bits 7-9 for
+// A, 10-12 for B): 0 = f16, 1 = bf16.
+constexpr uint32_t kFormatBf16 = (1u << 7) | (1u << 10);
+
+// Operand map of int8 codes for the int8-operand pair kernel, no swizzle:
+// K-major [mn, K]: boxes of 64 k x 128 rows; MN-major [K, mn]: boxes of 128
+// (M or N) x 64 k.
+bool make_raw_map(CUtensorMap* map, const void* base, bool mn_major, int64_t mn, int64_t K) {
+  if (mn_major)
+    return encode_tensor_map_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, mn, mn, 128, kBK,
+                                CU_TENSOR_MAP_SWIZZLE_NONE);
+  return encode_tensor_map_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, mn, K, K, kBK, 128,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <bool kAmn, bool kBmn, bool kRegScales>
@@ -868,8 +1125,11 @@ cudaError_t set_smem_attrs() {
   cudaError_t err = cudaFuncSetAttribute(gemm_s8f16_kernel<kAmn, kBmn, kRegScales>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales>,
+    err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kS8SmemBytes);
   return err;
 }
 
@@ -898,30 +1158,36 @@ bool make_output_map(CUtensorMap* map, void* out, bool s32, int64_t M, int64_t N
 }
 
 template <bool kAmn, bool kBmn, bool kRegScales>
-cudaError_t launch_kernel(bool pair, int grid, const CUtensorMap& mapA, const CUtensorMap& mapB,
-                          const CUtensorMap& mapO, const GemmParams& p, cudaStream_t stream) {
+cudaError_t launch_kernel(bool pair, bool s8, int grid, const CUtensorMap& mapA,
+                          const CUtensorMap& mapB, const CUtensorMap& mapO, const GemmParams& p,
+                          cudaStream_t stream) {
+  if (s8)
+    return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, true>, dim3(grid),
+                             dim3(kS8Threads), kS8SmemBytes, stream, mapA, mapB, mapO, p);
   if (pair)
-    return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales>, dim3(grid),
+    return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, false>, dim3(grid),
                              dim3(kThreads), kPairSmemBytes, stream, mapA, mapB, mapO, p);
   return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn, kRegScales>, dim3(grid), dim3(kThreads),
                            kSmemBytes, stream, mapA, mapB, mapO, p);
 }
 
 template <bool kAmn, bool kBmn>
-cudaError_t launch_layout(bool pair, bool reg_scales, int grid, const CUtensorMap& mapA,
+cudaError_t launch_layout(bool pair, bool s8, bool reg_scales, int grid, const CUtensorMap& mapA,
                           const CUtensorMap& mapB, const CUtensorMap& mapO, const GemmParams& p,
                           cudaStream_t stream) {
-  return reg_scales ? launch_kernel<kAmn, kBmn, true>(pair, grid, mapA, mapB, mapO, p, stream)
-                    : launch_kernel<kAmn, kBmn, false>(pair, grid, mapA, mapB, mapO, p, stream);
+  return reg_scales
+             ? launch_kernel<kAmn, kBmn, true>(pair, s8, grid, mapA, mapB, mapO, p, stream)
+             : launch_kernel<kAmn, kBmn, false>(pair, s8, grid, mapA, mapB, mapO, p, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B, bool b_mn,
-                        const float* sB, int64_t M, int64_t N, int64_t K, GemmOut mode, void* out,
-                        int64_t ldo, void* scratch, const DeviceInfo& dev, const GemmDebug& dbg,
-                        cudaStream_t stream) {
+                        const float* sB, int64_t M, int64_t N, int64_t K, bool s8, GemmOut mode,
+                        void* out, int64_t ldo, void* scratch, const DeviceInfo& dev,
+                        const GemmDebug& dbg, cudaStream_t stream) {
   if (a_mn && !b_mn) return cudaErrorInvalidValue;  // no layout of the API needs it
+  if (s8 && mode == GemmOut::kBf16Plain) return cudaErrorInvalidValue;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int device = 0;
@@ -944,12 +1210,17 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   // CTA pairs (256x256 tiles) when they give every pair of SMs a tile or
   // the contraction is long (each tile then runs long enough for the pair's
   // per-tile efficiency to win); otherwise single CTAs (128x256 tiles)
+  // int8 operands always take the CTA-pair kernel (the only one that widens)
   const int64_t pair_tiles = ((M + 255) / 256) * ((N + kBN - 1) / kBN);
-  const bool pair = M > kBM && (pair_tiles >= dev.sms / 2 || K >= 8192) && !dbg.single_cta;
+  const bool pair =
+      s8 || (M > kBM && (pair_tiles >= dev.sms / 2 || K >= 8192) && !dbg.single_cta);
+  const bool plain = mode == GemmOut::kBf16Plain;
   CUtensorMap mapA, mapB, mapO;
-  if (!make_operand_map(&mapA, A, a_mn, M, K, kBM) ||
-      !make_operand_map(&mapB, B, b_mn, N, K, pair ? 128 : kBN) ||
-      !make_output_map(&mapO, out, mode == GemmOut::kS32, M, N, ldo))
+  const bool maps_ok =
+      s8 ? make_raw_map(&mapA, A, a_mn, M, K) && make_raw_map(&mapB, B, b_mn, N, K)
+         : make_operand_map(&mapA, A, a_mn, M, K, kBM, plain) &&
+               make_operand_map(&mapB, B, b_mn, N, K, pair ? 128 : kBN, plain);
+  if (!maps_ok || !make_output_map(&mapO, out, mode == GemmOut::kS32, M, N, ldo))
     return cudaErrorInvalidValue;
   GemmParams p;
   p.sA = sA;
@@ -963,7 +1234,10 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
   p.m_fastest = M < N ? 1 : 0;
   p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
-  p.mode = mode == GemmOut::kS32 ? 1 : 0;
+  p.mode = mode == GemmOut::kS32 ? 1 : plain ? 2 : 0;
+  p.ab_format = plain ? kFormatBf16 : 0u;
+  // integer codes: exact fp32 chunks of 1024 terms; bf16: all of K at once
+  p.chunk_blocks = plain ? p.k_blocks : kChunkBlocks;
   p.status = dev.status_word;
   p.wait_limit_ns = dbg.wait_limit_ns;
   p.drop_first_load = dbg.drop_first_load;
@@ -1003,9 +1277,10 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   const int units = grid / (pair ? 2 : 1);
   const bool reg_scales = static_cast<int64_t>(p.dp_tiles) <= 2 * units;
   if (!a_mn && !b_mn)
-    return launch_layout<false, false>(pair, reg_scales, grid, mapA, mapB, mapO, p, stream);
-  if (!a_mn) return launch_layout<false, true>(pair, reg_scales, grid, mapA, mapB, mapO, p, stream);
-  return launch_layout<true, true>(pair, reg_scales, grid, mapA, mapB, mapO, p, stream);
+    return launch_layout<false, false>(pair, s8, reg_scales, grid, mapA, mapB, mapO, p, stream);
+  if (!a_mn)
+    return launch_layout<false, true>(pair, s8, reg_scales, grid, mapA, mapB, mapO, p, stream);
+  return launch_layout<true, true>(pair, s8, reg_scales, grid, mapA, mapB, mapO, p, stream);
 }
 
 }  // namespace int8mp

@@ -31,23 +31,28 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 struct ScratchSlot {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
-  void* ptr = nullptr;
+  std::mutex mu;
+  void* ptr = nullptr;  // set once a lookup has succeeded
 };
 ScratchSlot g_slots[kMaxDevices];
 
-// Device address of the scratch array on the current device, looked up once
-// per device with that device current.
+// Device address of the scratch array on the current device, looked up with
+// that device current.  Only a successful lookup is kept: a first call made
+// in a state where the lookup fails (inside a stream capture, or with an
+// error pending from earlier work) returns INT8MP_ERR_CUDA, and the next
+// call tries again.
 int8mp_status scratch_on_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return INT8MP_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return INT8MP_ERR_UNSUPPORTED_DEVICE;
   ScratchSlot& slot = g_slots[dev];
-  std::call_once(slot.once, [&slot] {
-    slot.err = cudaGetSymbolAddress(&slot.ptr, g_noalloc_scratch);
-  });
-  if (slot.err != cudaSuccess || slot.ptr == nullptr) return INT8MP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(slot.mu);
+  if (slot.ptr == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return INT8MP_ERR_CUDA;
+    slot.ptr = p;
+  }
   *out = slot.ptr;
   return INT8MP_OK;
 }
@@ -59,10 +64,8 @@ inline uint64_t round256(uint64_t v) { return (v + 255u) / 256u * 256u; }
 extern "C" int8mp_status int8mp_linear_fwd_noalloc(const void* X, const void* W, void* Y,
                                                    int64_t T, int64_t N, int64_t K,
                                                    const int8mp_linear_cfg* cfg, void* stream) {
-  if (T < 0 || N < 0 || K < 0 || T > INT8MP_MAX_K || N > INT8MP_MAX_K || K > INT8MP_MAX_K)
+  if (!cfg || T < 0 || N < 0 || K < 0 || T > INT8MP_MAX_K || N > INT8MP_MAX_K || K > INT8MP_MAX_K)
     return INT8MP_ERR_INVALID_ARG;
-  // the BF16 forward pass runs in a library GEMM that may allocate: not here
-  if (cfg && cfg->int8_fwd != 1) return INT8MP_ERR_INVALID_ARG;
   // the forward pass's workspace: codes (2 bytes each) and scales of X and W
   const uint64_t need = round256(2ull * T * K) + round256(4ull * T) + round256(2ull * N * K) +
                         round256(4ull * N);
@@ -70,5 +73,8 @@ extern "C" int8mp_status int8mp_linear_fwd_noalloc(const void* X, const void* W,
   void* scratch = nullptr;
   const int8mp_status st = scratch_on_current_device(&scratch);
   if (st != INT8MP_OK) return st;
-  return int8mp_linear_fwd(X, W, Y, T, N, K, cfg, scratch, INT8MP_NOALLOC_SCRATCH_BYTES, stream);
+  // Exactly the codes and scales: with no room past them the matmul runs
+  // whole tiles only (no split last wave, whose counters it would read
+  // before writing), so every byte a call reads it has written first.
+  return int8mp_linear_fwd(X, W, Y, T, N, K, cfg, scratch, static_cast<size_t>(need), stream);
 }

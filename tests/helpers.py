@@ -113,3 +113,18 @@ def curand_host_philox_words(seed, n):
     finally:
         cur.curandDestroyGenerator(g)
     return out
+
+
+# ---- BF16 passes: tolerance of an fp32-accumulated bf16 product ----------
+def bf16_pass_close(got_t, ref_bits, a, b, what):
+    """A BF16 pass (plain bf16 product, fp32 accumulation in the tensor
+    core's order) against the oracle's (fp64 sum, rounded to fp32 then
+    bf16): within two bf16 ulps of the reference plus the fp32 accumulation
+    bound K 2^-23 sum_k |a_ik||b_jk| per output.  a [M, K], b [N, K] as
+    float tensors (CPU); got_t bf16 [M, N]."""
+    got = got_t.cpu().float().double()
+    ref = torch.from_numpy(bits_to_f32(ref_bits).astype(np.float64))
+    K = a.shape[1]
+    bound = 2.0 ** -7 * ref.abs() + K * 2.0 ** -23 * (a.abs().double() @ b.abs().double().T)
+    bad = (got - ref).abs() > bound
+    assert not bool(bad.any()), f"{what}: {int(bad.sum())} of {bad.numel()} outputs outside the bound"

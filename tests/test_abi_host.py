@@ -120,7 +120,9 @@ def _mm(lib, M, N, K, layout=0, codes=1, A=16, B=16, out=16, ldo=None):
 
 def test_matmul_host_validation(lib):
     assert _mm(lib, 8, 8, 16, layout=3) == m.INT8MP_ERR_INVALID_ARG       # no such layout
-    assert _mm(lib, 8, 8, 16, codes=0) == m.INT8MP_ERR_INVALID_ARG        # tensor core: f16 containers
+    assert _mm(lib, 8, 8, 16, codes=2) == m.INT8MP_ERR_INVALID_ARG        # no such code container
+    assert _mm(lib, 8, 24, 16, layout=1, codes=0) == m.INT8MP_ERR_ALIGNMENT   # int8 [K,N] rows: N % 16
+    assert _mm(lib, 24, 16, 16, layout=2, codes=0) == m.INT8MP_ERR_ALIGNMENT  # int8 [K,M] rows: M % 16
     assert _mm(lib, 12, 8, 16, layout=2) == m.INT8MP_ERR_ALIGNMENT        # A.T@B: rows of A^T, M % 8
     assert _mm(lib, 8, 12, 16, layout=1) == m.INT8MP_ERR_ALIGNMENT        # A@B: rows of B, N % 8
     assert _mm(lib, 8, 8, m.INT8MP_MAX_K + 1) == m.INT8MP_ERR_INVALID_ARG
@@ -141,8 +143,8 @@ def test_matmul_workspace_host_validation(lib):
     g = lib.int8mp_scaled_mm_ws
     assert g(P(16), P(16), P(16), P(16), 8, 8, 16, 0, 1, P(16), 8, P(256), 16, None) == \
         m.INT8MP_ERR_WORKSPACE
-    assert g(P(16), P(16), P(16), P(16), 8, 8, 16, 0, 0, P(16), 8, P(256), need, None) == \
-        m.INT8MP_ERR_INVALID_ARG                                          # codes must be f16
+    assert g(P(16), P(16), P(16), P(16), 8, 8, 16, 0, 2, P(16), 8, P(256), need, None) == \
+        m.INT8MP_ERR_INVALID_ARG                                          # no such code container
 
 
 def test_linear_host_validation(lib):
@@ -155,9 +157,8 @@ def test_linear_host_validation(lib):
     bad = m.int8mp_linear_cfg(2, 1, 1, 0, 0, 0)   # a pass switch is 0 (BF16) or 1 (INT8)
     assert f(P(16), P(16), P(16), 32, 32, 32, ctypes.byref(bad), P(256), 1 << 20, None) == \
         m.INT8MP_ERR_INVALID_ARG
-    bf16_fwd = m.int8mp_linear_cfg(0, 1, 1, 0, 0, 0)  # the no-alloc forward is INT8 only
-    assert lib.int8mp_linear_fwd_noalloc(P(16), P(16), P(16), 32, 32, 32, ctypes.byref(bf16_fwd),
-                                         None) == m.INT8MP_ERR_INVALID_ARG
+    assert lib.int8mp_linear_fwd_noalloc(P(16), P(16), P(16), 32, 32, 32, None,
+                                         None) == m.INT8MP_ERR_INVALID_ARG   # no cfg
     need = m.int8mp_linear_workspace_size(32, 48, 64, cfg)
     assert need >= 2 * (32 * 64 + 48 * 64) + m.int8mp_mm_workspace_size() and need % 256 == 0
     assert m.int8mp_linear_workspace_size(32, 48, 24, cfg) == 0

@@ -2,7 +2,8 @@
 compute is checked against its buffer before the access.  Run the paths of
 the library through it -- row and column quantization in every variant, the
 column maxima, two matrices' rows in one launch, the GEMM in three layouts
-with and without the split last wave, the linear layer -- on ragged sizes: no
+with and without the split last wave (f16 containers and int8 codes), the
+linear layer in INT8 and in BF16 -- on ragged sizes: no
 check may fail, and every result must equal the ordinary build's bit for
 bit."""
 import pytest
@@ -57,6 +58,11 @@ def _codes_and_gemms():
         out.append(m.int8mp_mm_s32(a, b, layout=lay))
         out.append(m.int8mp_mm_s32(a, b, layout=lay, workspace=True))
         out.append(m.int8mp_scaled_mm(a, sa, b, sb, layout=lay, workspace=True))
+        if (lay == m.INT8MP_AxBT or N % 16 == 0) and (lay != m.INT8MP_ATxB or M % 16 == 0):
+            # int8 operands (widened in the CTA-pair kernel)
+            a8, b8 = a.to(torch.int8), b.to(torch.int8)
+            out.append(m.int8mp_mm_s32(a8, b8, layout=lay, workspace=True))
+            out.append(m.int8mp_scaled_mm(a8, sa, b8, sb, layout=lay))
     T, N, K = 1040, 2048, 2048
     X = synth.bf16_normal((T, K), 1).to(DEV)
     W = synth.bf16_normal((N, K), 2, std=0.02).to(DEV)
@@ -66,6 +72,9 @@ def _codes_and_gemms():
     out.append(m.int8mp_linear_fwd_save(X, W, absmax, cfg))
     out += list(m.int8mp_linear_bwd_saved(dY, X, W, absmax, cfg))
     out += list(m.int8mp_linear_bwd(dY, X, W, cfg))
+    bf16 = m.linear_cfg(int8_fwd=0, int8_grad_in=0, int8_grad_w=0)  # the BF16 passes
+    out.append(m.int8mp_linear_fwd(X, W, bf16))
+    out += list(m.int8mp_linear_bwd(dY, X, W, bf16))
     torch.cuda.synchronize()
     return out
 

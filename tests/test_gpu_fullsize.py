@@ -15,7 +15,7 @@ import torch
 
 import int8_mixed_precision_row_gb300 as m
 import oracle
-from helpers import bf16_bits
+from helpers import bf16_bits, bf16_pass_close
 from int8_mixed_precision_row_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -117,3 +117,34 @@ def test_square_4096_sampled_rows(layout):
     rows = _sample(S, 8, 3)
     ref = oracle.scaled_mm(qar[rows], sar[rows], qbr, sbr, len(rows), S, S)  # K-major codes
     _rows_equal(out, rows, ref, f"square 4096 {layout}")
+
+
+@pytest.mark.parametrize("name", ["q", "down"])
+def test_full_size_bf16_passes_sampled_rows(name):
+    """The pages' BF16 training-table row at full size: all three passes in
+    BF16 (bf16 operands, fp32 accumulation in the tcgen05 kernels; the down
+    projection's forward pass splits its last wave), sampled output rows
+    against the oracle's bf16 product within the fp32 accumulation bound."""
+    X, W, dY = synth.linear_inputs(synth.LLAMA2_1B, name)
+    T, K = X.shape
+    N = W.shape[0]
+    cfg = m.linear_cfg(int8_fwd=0, int8_grad_in=0, int8_grad_w=0)
+    Xd, Wd, dYd = X.to(DEV), W.to(DEV), dY.to(DEV)
+    Y = m.int8mp_linear_fwd(Xd, Wd, cfg)
+    dX, dW = m.int8mp_linear_bwd(dYd, Xd, Wd, cfg)
+    torch.cuda.synchronize()
+    assert m.int8mp_poll_device_status() == m.INT8MP_OK
+    del Xd, Wd, dYd
+    xb, wb, gb = bf16_bits(X), bf16_bits(W), bf16_bits(dY)
+    rows_t = _sample(T, 8, 5)
+    rows_n = _sample(N, 4, 6)
+    it, in_ = torch.from_numpy(rows_t), torch.from_numpy(rows_n)
+    ref = oracle.matmul_bf16(xb[rows_t], wb, len(rows_t), N, K, layout=oracle.AxBT)
+    bf16_pass_close(Y[it.to(DEV)], ref, X[it].float(), W.float(), f"{name} BF16 forward")
+    ref = oracle.matmul_bf16(gb[rows_t], wb, len(rows_t), K, N, layout=oracle.AxB)
+    bf16_pass_close(dX[it.to(DEV)], ref, dY[it].float(), W.float().T.contiguous(),
+                    f"{name} BF16 grad input")
+    ref = oracle.matmul_bf16(np.ascontiguousarray(gb[:, rows_n]), xb, len(rows_n), K, T,
+                             layout=oracle.ATxB)
+    bf16_pass_close(dW[in_.to(DEV)], ref, dY[:, in_].float().T.contiguous(),
+                    X.float().T.contiguous(), f"{name} BF16 grad weight")
