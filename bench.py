@@ -9,6 +9,10 @@ matmul in INT8 with dynamic row-wise quantization along its contraction axis
 excluded).  Activations N(0,1), weights N(0,0.02), output gradients
 N(0,1e-3), round to nearest even.  Inputs are resident in HBM before the
 timed region; every step touches about 5 GB, far more than the 129 MB L2.
+Under torchrun with N ranks (one GPU each) the step is data parallel over
+tokens: every rank runs its own 16 x 2048 tokens (weak scaling), and the
+grad-weight pass forms fp32 partials that one NCCL all-reduce per linear sums
+before a single bf16 rounding (int8_mixed_precision_row_gb300/dp.py).
 
 Output: one JSON line (rank 0).  `value` is whole-job tokens/s; `e2e` is the
 same metric through the layer API (int8mp_linear_fwd_save /
@@ -54,7 +58,45 @@ def parse_args():
                     help="profiling cases only: comma-separated subset of q,k,v,o,gate,up,down")
     ap.add_argument("--rounding", choices=["rne", "sr"], default="rne",
                     help="profiling cases only: round to nearest even or stochastically")
+    ap.add_argument("--case", choices=sorted(PROFILE_CASES), default=None,
+                    help="profiling: run one matmul case three times and exit (no timing)")
     return ap.parse_args()
+
+
+# Single-call cases for a profiler (each runs its call three times, so that
+# `ncu -s 2 -c 1` captures a warm launch): the square 4096^3 A @ B.T matmul
+# on int8 codes and on f16 containers of the same codes, and the BF16
+# forward pass of a q projection at T = 16384.
+PROFILE_CASES = ("square-int8-4096", "square-f16-4096", "bf16-forward-q-T16384")
+
+
+def run_profile_case(case, device):
+    import torch
+    import int8_mixed_precision_row_gb300 as m
+    from int8_mixed_precision_row_gb300 import synth
+    g = torch.Generator(device=device).manual_seed(0)
+    if case.startswith("square"):
+        S = 4096
+        a = torch.randint(-127, 128, (S, S), device=device, generator=g, dtype=torch.int32)
+        b = torch.randint(-127, 128, (S, S), device=device, generator=g, dtype=torch.int32)
+        dt = torch.int8 if case == "square-int8-4096" else torch.float16
+        a, b = a.to(dt), b.to(dt)
+        sa = torch.rand(S, device=device, generator=g)
+        sb = torch.rand(S, device=device, generator=g)
+        out = torch.empty((S, S), dtype=torch.bfloat16, device=device)
+        for _ in range(3):
+            m.int8mp_scaled_mm(a, sa, b, sb, out=out)
+    else:
+        X = synth.bf16_normal((16384, 2048), 10).to(device)
+        W = synth.bf16_normal((2048, 2048), 20, std=0.02).to(device)
+        cfg = m.linear_cfg(int8_fwd=0, int8_grad_in=0, int8_grad_w=0)
+        Y = torch.empty((16384, 2048), dtype=torch.bfloat16, device=device)
+        for _ in range(3):
+            m.int8mp_linear_fwd(X, W, cfg, Y=Y)
+    torch.cuda.synchronize()
+    if m.int8mp_poll_device_status() != m.INT8MP_OK:
+        raise RuntimeError("a bounded device wait ran out")
+    print(f"profile case {case}: done")
 
 
 # ------------------------------------------------------------- distributed
@@ -161,11 +203,13 @@ class LayerStep:
     """Device-resident inputs, outputs and code/scale buffers of one decoder
     layer's linears, and the step composed of the public C-ABI calls."""
 
-    def __init__(self, spec, mode, device, T=None, only=None):
+    def __init__(self, spec, mode, device, T=None, only=None, world=1, rank=0):
         import torch
-        from int8_mixed_precision_row_gb300 import synth
+        from int8_mixed_precision_row_gb300 import dp, synth
         import int8_mixed_precision_row_gb300 as m
         self.m = m
+        self.dp = dp
+        self.world, self.rank = world, rank
         self.spec = spec
         self.T = spec["T"] if T is None else T
         self.mode = mode
@@ -211,6 +255,10 @@ class LayerStep:
             at += n
         # the matmuls' scratch for splitting their last wave of tiles
         self.mm_ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
+        # data parallel (world > 1): each rank's fp32 part of dW, summed by an
+        # all-reduce and rounded once
+        self.dw_f32 = (torch.empty(nmax * kmax, dtype=torch.float32, device=device)
+                       if world > 1 else None)
         self.flops = 6.0 * T * sum(l["N"] * l["K"] for l in self.linears)
         # GEMM operands read once (f16 codes) and bf16 outputs written, per step
         self.gemm_bytes = 6.0 * sum(T * l["K"] + T * l["N"] + l["N"] * l["K"] for l in self.linears)
@@ -219,7 +267,7 @@ class LayerStep:
         # launches (X and W together, then dY; each also recording column
         # absmax), three column quantizations (codes from that absmax), three
         # GEMMs
-        self.kernels_per_step = len(self.linears) * (2 + 3 + 3)
+        self.kernels_per_step = len(self.linears) * (2 + 3 + 3 + (1 if world > 1 else 0))
         # algorithmic quantize bytes: bf16 read once, code (f16 container) and scale written
         self.quant_elems = sum(2 * (T * l["K"] + l["N"] * l["K"] + T * l["N"]) for l in self.linears)
 
@@ -265,6 +313,9 @@ class LayerStep:
             b.record()
             timers.setdefault(kind, []).append((a, b))
             return r
+        # data parallel: rank r's stochastic-rounding counters start at
+        # offset + r * 2^40 (disjoint streams); rank 0 (and one GPU) as given
+        offset = self.dp.shard_offset(offset, self.rank)
         self.colmax_all.zero_()
         for l in self.linears:
             X, W, dY = l["X"], l["W"], l["dY"]
@@ -283,8 +334,17 @@ class LayerStep:
             # grad weight: dY and X along T (columns, codes [T, N], [T, K]): A.T @ B
             qgc, sgc = rec("quant_cols", lambda: self._q(dY, 2, m.INT8MP_STREAM_GW_DY, self.qa, self.sa, seed, offset, cg))
             qxc, sxc = rec("quant_cols", lambda: self._q(X, 2, m.INT8MP_STREAM_GW_X, self.qb, self.sb, seed, offset, cx))
-            rec("gemm", lambda: m.int8mp_scaled_mm(qgc, sgc, qxc, sxc, layout=m.INT8MP_ATxB, out=l["dW"],
-                                                   workspace=self.mm_ws))
+            if self.world == 1:
+                rec("gemm", lambda: m.int8mp_scaled_mm(qgc, sgc, qxc, sxc, layout=m.INT8MP_ATxB,
+                                                       out=l["dW"], workspace=self.mm_ws))
+            else:
+                # this rank's fp32 part of dW, the all-reduce, one rounding
+                N = l["N"]
+                part = self.dw_f32[:N * K].view(N, K)
+                rec("gemm", lambda: m.int8mp_scaled_mm_f32(qgc, sgc, qxc, sxc, layout=m.INT8MP_ATxB,
+                                                           out=part, workspace=self.mm_ws))
+                rec("allreduce", lambda: self.dp.reduce_partials(part))
+                rec("round", lambda: m.int8mp_round_bf16(part.view(-1), l["dW"].view(-1)))
 
 
 def time_steps(step, steps, warmup, world, device):
@@ -719,8 +779,11 @@ def main():
     if (args.tokens or only or args.rounding != "rne") and not args.profile_steps:
         raise SystemExit("--tokens/--linears/--rounding select profiling cases and need "
                          "--profile-steps")
+    if args.case:
+        run_profile_case(args.case, device)
+        return
     mode = m.INT8MP_SR if args.rounding == "sr" else m.INT8MP_RNE
-    step = LayerStep(spec, mode, device, T=args.tokens, only=only)
+    step = LayerStep(spec, mode, device, T=args.tokens, only=only, world=world, rank=rank)
     with ClockSampler(local) as clk:
         elapsed_ms, per_kind, counts = time_steps(step, args.steps, args.warmup, world, device)
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)
@@ -744,7 +807,9 @@ def main():
                    "intermediate": spec["inter"], "linears": len(step.linears),
                    "rounding": "SR" if mode == m.INT8MP_SR else "RNE",
                    "l2": "inputs larger than L2 (about 5 GB touched per step, L2 129 MB)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": (f"data parallel x{world}: {step.T} tokens per rank, dW as "
+                                   f"fp32 partials all-reduced then rounded once")
+                   if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor",
                      "kernel": "gemm_s8f16_pair_kernel (CTA-pair tcgen05 kind::f16, exact int32)",
                      "achieved": round(gemm_tflops, 1), "peak": bf16_burst, "unit": "TFLOP/s",

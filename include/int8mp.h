@@ -270,6 +270,34 @@ int8mp_status int8mp_mm_s32_ws(const void* A, const void* B, int64_t M, int64_t 
                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * int8mp_scaled_mm_f32 -- the scaled matmul with an fp32 result that is not
+ * rounded to bf16:
+ *   out[i,j] = (fp32_RN(sum_k a(i,k) b(j,k)) * sA[i]) * sB[j]     (fp32)
+ * i.e. int8mp_scaled_mm before its final rounding.  This is the partial
+ * grad-weight of one token shard in data-parallel training: each rank
+ * quantizes its own rows of dY and X by columns (its own column scales),
+ * multiplies them here, the ranks sum their partials (e.g. an all-reduce),
+ * and int8mp_round_bf16 rounds the sum once ("Integrate INT8 mixed-precision
+ * from torchao 0.7", discussion: FSDP2 training on two A100s; torchao issue
+ * 1887: gradients reduce-scattered across ranks).
+ *   out     fp32 [M, N], row stride ldo elements.
+ *   workspace, ws_bytes   as for int8mp_scaled_mm_ws (NULL allowed).
+ * Requirements and codes: those of int8mp_scaled_mm_ws.
+ */
+int8mp_status int8mp_scaled_mm_f32(const void* A, const float* sA, const void* B, const float* sB,
+                                   int64_t M, int64_t N, int64_t K, int8mp_layout layout,
+                                   int8mp_codes codes, float* out, int64_t ldo, void* workspace,
+                                   size_t ws_bytes, void* stream);
+
+/*
+ * int8mp_round_bf16 -- y[i] = bf16_RNE(x[i]) for n fp32 values (round to
+ * nearest, ties to even; the last step of a grad-weight whose fp32 partials
+ * were summed across ranks).  x fp32 [n], y bf16 [n], both 16-byte aligned
+ * (INT8MP_ERR_ALIGNMENT); n >= 0.
+ */
+int8mp_status int8mp_round_bf16(const float* x, void* y, int64_t n, void* stream);
+
+/*
  * Per-pass configuration of a linear layer (the pages' per-matmul INT8
  * switches and stochastic-rounding switch; "Quantized model training"
  * README, INT8 mixed precision training table).  int8_* = 1 runs that pass

@@ -40,6 +40,7 @@ EXPORTED = (
     "int8mp_debug_check_division", "int8mp_quantize_rows_colmax", "int8mp_quantize_cols_absmax",
     "int8mp_linear_fwd_save", "int8mp_linear_bwd_saved", "int8mp_mm_workspace_size",
     "int8mp_scaled_mm_ws", "int8mp_mm_s32_ws", "int8mp_quantize_rows_batch",
+    "int8mp_scaled_mm_f32", "int8mp_round_bf16",
 )
 INT8MP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -140,7 +141,11 @@ def load(path=None):
     L.int8mp_scaled_mm_ws.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _I64, _P,
                                       _SZ, _P]
     L.int8mp_mm_s32_ws.argtypes = [_P, _P, _I64, _I64, _I64, _INT, _INT, _P, _I64, _P, _SZ, _P]
-    for name in ("int8mp_scaled_mm_ws", "int8mp_mm_s32_ws",
+    L.int8mp_scaled_mm_f32.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _I64, _P,
+                                       _SZ, _P]
+    L.int8mp_round_bf16.argtypes = [_P, _P, _I64, _P]
+    for name in ("int8mp_scaled_mm_ws", "int8mp_mm_s32_ws", "int8mp_scaled_mm_f32",
+                 "int8mp_round_bf16",
                  "int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
                  "int8mp_linear_fwd", "int8mp_linear_bwd", "int8mp_poll_device_status",
                  "int8mp_version", "int8mp_debug_mm_s32_drop_first_load",
@@ -348,6 +353,35 @@ def int8mp_mm_s32(A, B, layout=INT8MP_AxBT, codes=None, out=None, stream=None,
                                        _ptr(out), ldo, _ptr(ws), nbytes, _stream(stream)),
                "int8mp_mm_s32_ws")
     return out
+
+
+def int8mp_scaled_mm_f32(A, sA, B, sB, layout=INT8MP_AxBT, codes=None, out=None, stream=None,
+                         workspace=None):
+    """The scaled matmul of codes A, B (layouts as int8mp_scaled_mm) with an
+    fp32 result [M, N] that is not rounded to bf16 (a token shard's partial
+    grad-weight)."""
+    codes = _mm_codes(A, B, codes)
+    M, N, K = _mm_sizes(A, B, layout)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _check_out(out, M, N, torch.float32)
+    ldo = out.stride(0) if M > 0 else N
+    ws, nbytes = _mm_ws(workspace, A.device)
+    _check(load().int8mp_scaled_mm_f32(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), M, N, K, int(layout),
+                                       int(codes), _ptr(out), ldo, _ptr(ws), nbytes,
+                                       _stream(stream)), "int8mp_scaled_mm_f32")
+    return out
+
+
+def int8mp_round_bf16(x, y=None, stream=None):
+    """bf16 round-to-nearest-even of a contiguous fp32 CUDA tensor."""
+    assert x.dtype == torch.float32 and x.is_cuda and x.is_contiguous()
+    if y is None:
+        y = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    assert y.dtype == torch.bfloat16 and y.is_contiguous() and y.numel() == x.numel()
+    _check(load().int8mp_round_bf16(_ptr(x), _ptr(y), x.numel(), _stream(stream)),
+           "int8mp_round_bf16")
+    return y
 
 
 def int8mp_linear_workspace_size(T, N, K, cfg=None):

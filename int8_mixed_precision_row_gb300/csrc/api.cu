@@ -343,6 +343,42 @@ int8mp_status int8mp_mm_s32_ws(const void* A, const void* B, int64_t M, int64_t 
                 workspace, int8mp::GemmDebug{}, as_stream(stream), codes == INT8MP_CODES_S8);
 }
 
+int8mp_status int8mp_scaled_mm_f32(const void* A, const float* sA, const void* B, const float* sB,
+                                   int64_t M, int64_t N, int64_t K, int8mp_layout layout,
+                                   int8mp_codes codes, float* out, int64_t ldo, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  int8mp_status st = check_mm(A, B, M, N, K, layout, codes, out, ldo);
+  if (st != INT8MP_OK) return st;
+  st = check_mm_workspace(workspace, ws_bytes);
+  if (st != INT8MP_OK) return st;
+  if (M > 0 && N > 0 && K > 0) {
+    if (!sA || !sB) return INT8MP_ERR_INVALID_ARG;
+    if (!aligned(sA, 4) || !aligned(sB, 4)) return INT8MP_ERR_ALIGNMENT;
+  }
+  if (M == 0 || N == 0) return INT8MP_OK;
+  if (K == 0) {  // an empty contraction: every product is 0 (the memset writes +0.0f)
+    DeviceInfo dev;
+    st = current_device(&dev, as_stream(stream));
+    if (st != INT8MP_OK) return st;
+    return from_cuda(cudaMemset2DAsync(out, static_cast<size_t>(ldo) * 4, 0,
+                                       static_cast<size_t>(N) * 4, static_cast<size_t>(M),
+                                       as_stream(stream)));
+  }
+  return run_mm(A, sA, B, sB, M, N, K, layout, int8mp::GemmOut::kF32Scaled, out, ldo, workspace,
+                int8mp::GemmDebug{}, as_stream(stream), codes == INT8MP_CODES_S8);
+}
+
+int8mp_status int8mp_round_bf16(const float* x, void* y, int64_t n, void* stream) {
+  if (n < 0) return INT8MP_ERR_INVALID_ARG;
+  if (n == 0) return INT8MP_OK;
+  if (!x || !y) return INT8MP_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return INT8MP_ERR_ALIGNMENT;
+  DeviceInfo dev;
+  int8mp_status st = current_device(&dev, as_stream(stream));
+  if (st != INT8MP_OK) return st;
+  return from_cuda(int8mp::launch_round_bf16(x, y, n, dev, as_stream(stream)));
+}
+
 size_t int8mp_linear_workspace_size(int64_t T, int64_t N, int64_t K, const int8mp_linear_cfg* cfg) {
   if (check_linear(T, N, K, cfg) != INT8MP_OK) return 0;
   const size_t f = fwd_bytes(T, N, K), b = bwd_bytes(T, N, K);

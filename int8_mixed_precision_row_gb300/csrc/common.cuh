@@ -100,6 +100,9 @@ cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int6
                                  const DeviceInfo& dev, cudaStream_t stream);
 // n 32-bit words at p set to 0 (a kernel: keeps dependent launches going).
 cudaError_t launch_zero_words(void* p, int64_t n, const DeviceInfo& dev, cudaStream_t stream);
+// y[i] = bf16_RNE(x[i]) for n fp32 values (x, y 16-byte aligned).
+cudaError_t launch_round_bf16(const float* x, void* y, int64_t n, const DeviceInfo& dev,
+                              cudaStream_t stream);
 // colmax[c] = max(colmax[c], max_r |x[r,c]|) (fp32 [cols]), one pass.
 cudaError_t launch_column_absmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                  float* colmax, const DeviceInfo& dev, cudaStream_t stream);
@@ -120,8 +123,9 @@ cudaError_t launch_quantize_cols(const void* x, int64_t rows, int64_t cols, int6
 // ---- GEMM (gemm.cu) ---------------------------------------------------------
 // kBf16Scaled: integer codes in f16 containers, out = bf16((acc * sA) * sB);
 // kS32: the same codes, out = the int32 accumulator; kBf16Plain: bf16
-// operands, out = bf16_RNE of their fp32-accumulated product (sA, sB unused).
-enum class GemmOut { kBf16Scaled = 0, kS32 = 1, kBf16Plain = 2 };
+// operands, out = bf16_RNE of their fp32-accumulated product (sA, sB unused);
+// kF32Scaled: integer codes, out = the fp32 (acc * sA) * sB itself.
+enum class GemmOut { kBf16Scaled = 0, kS32 = 1, kBf16Plain = 2, kF32Scaled = 3 };
 
 struct GemmDebug {
   int drop_first_load = 0;        // test only: never issue the first TMA load

@@ -76,7 +76,8 @@ struct GemmParams {
   int64_t ldo;
   int M, N, K;
   int m_tiles, n_tiles, k_blocks;
-  int mode;  // 0: bf16 scaled, 1: int32 accumulators, 2: plain bf16 (fp32 accumulator)
+  int mode;  // 0: bf16 scaled, 1: int32 accumulators, 2: plain bf16 (fp32 accumulator),
+             // 3: fp32 scaled (not rounded to bf16)
   uint32_t ab_format;   // operand-format bits of the instruction descriptor (bf16 or f16)
   int chunk_blocks;     // k-blocks per accumulator hand-off (exact chunks, or all of K)
   unsigned int* status;
@@ -148,7 +149,8 @@ __host__ __device__ constexpr uint64_t k_step() {
 
 // Eight outputs of row `row`, columns col .. col+7 (N % 8 == 0, so all or
 // none are inside), from their int32 totals.  bf16: (fp32(acc) * sA[row]) *
-// sB[col], round to nearest even; int32: the totals themselves.
+// sB[col], round to nearest even; fp32: the same product, not rounded to
+// bf16; int32: the totals themselves.
 __device__ __forceinline__ void store_vec8(const GemmParams& p, int64_t row, int64_t col, float sa,
                                            const int32_t* t) {
   if (col >= p.N) return;
@@ -157,6 +159,16 @@ __device__ __forceinline__ void store_vec8(const GemmParams& p, int64_t row, int
     int4* o = reinterpret_cast<int4*>(static_cast<int32_t*>(p.out) + row * p.ldo + col);
     o[0] = make_int4(t[0], t[1], t[2], t[3]);
     o[1] = make_int4(t[4], t[5], t[6], t[7]);
+    return;
+  }
+  if (p.mode == 3) {
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      o[e] = __fmul_rn(__fmul_rn(__int2float_rn(t[e]), sa), __ldg(p.sB + col + e));
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * p.ldo + col);
+    d[0] = make_float4(o[0], o[1], o[2], o[3]);
+    d[1] = make_float4(o[4], o[5], o[6], o[7]);
     return;
   }
   uint32_t w[4];
@@ -226,7 +238,7 @@ template <bool kRegScales>
 __device__ __forceinline__ TileScales load_tile_scales(const GemmParams& p, int64_t row0,
                                                        int64_t col0) {
   TileScales t{0.0f, {0.0f, 0.0f, 0.0f, 0.0f}};
-  if (!kRegScales || p.mode != 0) return t;
+  if (!kRegScales || (p.mode != 0 && p.mode != 3)) return t;
   const int lane = threadIdx.x & 31;
   if (row0 + lane < p.M) t.sa = __ldg(p.sA + row0 + lane);
 #pragma unroll
@@ -277,6 +289,36 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
       for (int c = 0; c < 8; ++c) {
         const int32_t* t = tot + 32 * j + 4 * c;
         ptx::st_shared_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), t[0], t[1], t[2], t[3]);
+      }
+      publish(c0);
+    }
+    return;
+  }
+  if (p.mode == 3) {  // fp32 scaled: boxes of 32 columns, like the int32 totals
+    const float sa = kRegScales ? ts.sa : row < p.M ? __ldg(p.sA + row) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t c0 = col0 + 32 * j;
+      if (c0 >= p.N) break;
+      reuse();
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int k0 = 32 * j + 4 * c;  // columns col0 + k0 .. col0 + k0 + 3
+        float sb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (kRegScales) {
+            sb[e] = __shfl_sync(0xFFFFFFFFu, ts.sb[j], 4 * c + e);
+          } else {
+            const int64_t col = col0 + k0 + e;
+            sb[e] = col < p.N ? __ldg(p.sB + col) : 0.0f;
+          }
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(tot[k0 + e]), sa), sb[e]));
+        ptx::st_shared_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), w[0], w[1], w[2], w[3]);
       }
       publish(c0);
     }
@@ -563,16 +605,23 @@ constexpr int kPairSmemBytes =
     1024 + kPairStages * kPairStageBytes + kStagingBytes + kBarrierBytes;
 static_assert(kPairSmemBytes <= 227 * 1024, "pair kernel shared memory");
 // int8 operands (kS8): TMA brings each CTA's int8 k-block (128 x 64 codes of
-// A and of B, 16 KB) into a ring of its own, and two converter warps widen it
+// A and of B, 16 KB) into a ring of its own, and six converter warps widen it
 // into the f16 stage the tensor core reads -- fewer f16 stages, more raw ones
 // (the raw ring covers the DRAM latency, the f16 ring only decouples the
-// converters from the MMA).
-constexpr int kS8Stages = 3;
-constexpr int kRawStages = 6;
+// converters from the MMA).  The kernel runs four warpgroups: warpgroup 0
+// (producer, MMA, converters 0-1) and 3 (converters 2-5) give up registers,
+// warpgroups 1-2 (the epilogue, warps 4-11) take them:
+// 256 x kS8RegsEpi + 256 x kS8RegsOther = 65,536, the launch's registers.
+constexpr int kS8Stages = 4;
+constexpr int kRawStages = 4;
 constexpr int kRawOperandBytes = 128 * kBK;  // 128 rows x 64 k, one byte each
 constexpr int kRawStageBytes = 2 * kRawOperandBytes;
-constexpr int kConvWarps = 2;
-constexpr int kS8Threads = kThreads + kConvWarps * 32;
+constexpr int kConvWarps = 6;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kS8Threads = 512;
+constexpr int kS8RegsEpi = 184, kS8RegsOther = 72;
+static_assert(256 * kS8RegsEpi + 256 * kS8RegsOther <= 65536, "register split of the S8 kernel");
+static_assert(kS8Threads * 128 == 65536, "the S8 kernel launches with 128 registers a thread");
 constexpr int kS8SmemBytes = 1024 + kS8Stages * kPairStageBytes + kRawStages * kRawStageBytes +
                              kStagingBytes + kBarrierBytes;
 static_assert(kS8SmemBytes <= 227 * 1024, "int8-operand pair kernel shared memory");
@@ -613,8 +662,9 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
 // tile at `dst`, in the 128-byte swizzled layout a TMA load would have
 // written: K-major, row m (128 bytes: 64 k) at m * 128; MN-major, 64-wide
 // block b, row k at b * 8192 + k * 128; 16-byte chunk c of row r at
-// (c ^ (r % 8)) * 16.  Converter thread ct (of 64) takes 16-byte raw chunks
-// ct, ct + 64, ...; each becomes 32 bytes (two chunks) of one f16 row.
+// (c ^ (r % 8)) * 16.  Converter thread ct (of kConvThreads) takes 16-byte
+// raw chunks ct, ct + kConvThreads, ...; each becomes 32 bytes (two chunks)
+// of one f16 row.
 // Bank conflicts: eight consecutive raw chunks (a quarter warp) are 128
 // contiguous bytes.  K-major, they fill two f16 rows with different
 // swizzles, so the first (and the second) stores of the quarter warp land in
@@ -622,10 +672,10 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
 // (same swizzle): the threads of block 1 store their second chunk first.
 template <bool kMN>
 __device__ __forceinline__ void widen_tile(uint32_t raw, uint32_t dst, int ct) {
+  static_assert(kConvThreads % 8 == 0, "a thread's chunks keep their bit 2");
   const int swap = kMN ? (ct >> 2) & 1 : 0;  // the same for every chunk of this thread
-#pragma unroll 4
-  for (int i = 0; i < kRawOperandBytes / 16 / (kConvWarps * 32); ++i) {
-    const int c = ct + kConvWarps * 32 * i;
+#pragma unroll 3
+  for (int c = ct; c < kRawOperandBytes / 16; c += kConvThreads) {
     const int row = kMN ? ((c >> 2) & 1) * 64 + (c >> 3) : c >> 2;
     const int chunk = (c & 3) * 2;  // first of the row's two 16-byte chunks
     uint4 v = ptx::ld_shared_v4(raw + static_cast<uint32_t>(c) * 16u);
@@ -743,7 +793,7 @@ __device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int e
   }
   if (r == 0 || row >= p.M) return;
   __threadfence();
-  const float sa = p.mode != 0 ? 0.0f : __ldg(p.sA + row);
+  const float sa = (p.mode == 0 || p.mode == 3) ? __ldg(p.sA + row) : 0.0f;
   // 32 columns at a time: each part's 8 vectors are loaded together
   for (int h = 0; h < 4; ++h) {
     int32_t acc[32];
@@ -779,10 +829,11 @@ __device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int e
 
 // kS8: the operands are int8 codes (INT8MP_CODES_S8).  Each CTA's producer
 // brings its int8 k-blocks into a raw ring (its own barriers); converter
-// warps 10-11 of both CTAs widen them into the f16 stages and arrive on the
-// even CTA's full barrier (release at cluster scope, after a proxy fence so
-// that the tensor core sees the stores), which the MMA thread waits on at
-// cluster scope.  Everything else is the f16 kernel.
+// warps 2-3 and 12-15 of both CTAs widen them into the f16 stages and arrive
+// on the even CTA's full barrier (release at cluster scope, after a proxy
+// fence so that the tensor core sees the stores), which the MMA thread waits
+// on at cluster scope; the epilogue is warps 4-11.  Everything else is the
+// f16 kernel.
 template <bool kAmn, bool kBmn, bool kRegScales, bool kS8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : kThreads, 1)
     gemm_s8f16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -853,8 +904,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : k
 
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const uint64_t limit = p.wait_limit_ns;
+  constexpr int kEpiFirst = kS8 ? 4 : 2;  // first epilogue warp
 
-  if (warp == 0 && kS8) {
+  auto s8_producer = [&]() {
     if (lane == 0) {
       // ------------------------------------------ producer (int8 operands)
       // each CTA fills its own raw ring with its 128 rows of A and of B
@@ -894,9 +946,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : k
           if (!ptx::mbar_wait_bounded(rfull_bar(s), (armed_par >> s) & 1u, never, limit))
             raise_abort(abort, p.status);
     }
-  } else if (kS8 && warp >= 2 + kEpiWarps) {
+  };
+  auto converters = [&]() {
     // ------------------------------------------- converters (int8 operands)
-    const int ct = threadIdx.x - (2 + kEpiWarps) * 32;
+    const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 320;  // 0 .. kConvThreads-1
     uint32_t rstage = 0, rphase = 0, stage = 0, phase = 0;
     bool ok = true;
     FragIter it(p, pair);
@@ -931,7 +984,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : k
       }
     }
     if (!ok && lane == 0) raise_abort(abort, p.status);
-  } else if (warp == 0) {
+  };
+  auto producer = [&]() {
     if (lane == 0) {
       // ------------------------------------------------------ producer
       uint32_t stage = 0, phase = 0;
@@ -974,7 +1028,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : k
           if (!ptx::mbar_wait_bounded(full_bar(s), (armed_par >> s) & 1u, never, limit))
             raise_abort(abort, p.status);
     }
-  } else if (warp == 1) {
+  };
+  auto mma = [&]() {
     if (lane == 0 && even) {
       // ----------------------------------------------------------- MMA
       const uint32_t idesc = ptx::idesc_f16_f32(256, 256, kAmn, kBmn) | p.ab_format;
@@ -1021,10 +1076,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : k
       ptx::mma_commit_pair(drain_bar, 0x1);
       if (!ptx::mbar_wait_bounded(drain_bar, 0u, never, limit)) raise_abort(abort, p.status);
     }
-  } else {
+  };
+  auto epilogue = [&]() {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - kEpiFirst) >> 2;
     uint32_t chunk = 0;
     bool ok = true;
     FragIter it(p, pair);
@@ -1064,15 +1120,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : k
       const int64_t row = static_cast<int64_t>(m0) + quad * 32 + lane;
       const int64_t col0 = static_cast<int64_t>(n0) + half * 128;
       if (whole) {
-        store_tile_tma<kRegScales>(p, &tmO, staging + (warp - 2) * kStoreBoxBytes, row - lane,
+        store_tile_tma<kRegScales>(p, &tmO, staging + (warp - kEpiFirst) * kStoreBoxBytes, row - lane,
                                    col0, ts, tot);
       } else {
-        sk_store_part(p, pair, static_cast<int>(rank), warp - 2, tot);
-        sk_complete(p, static_cast<int>(rank), warp - 2, tile, row, col0, abort);
+        sk_store_part(p, pair, static_cast<int>(rank), warp - kEpiFirst, tot);
+        sk_complete(p, static_cast<int>(rank), warp - kEpiFirst, tile, row, col0, abort);
       }
     }
     if (!ok && lane == 0) raise_abort(abort, p.status);
     if (lane == 0) ptx::bulk_wait_group0();  // the tile stores are complete
+  };
+
+  if constexpr (kS8) {
+    // register split by warpgroup: each warpgroup's four warps execute the
+    // same adjustment at the top of their branch
+    if (warp >= 4 && warp < 12) {
+      ptx::setmaxnreg_inc<kS8RegsEpi>();
+      epilogue();
+    } else {
+      ptx::setmaxnreg_dec<kS8RegsOther>();
+      if (warp == 0)
+        s8_producer();
+      else if (warp == 1)
+        mma();
+      else
+        converters();
+    }
+  } else {
+    if (warp == 0)
+      producer();
+    else if (warp == 1)
+      mma();
+    else
+      epilogue();
   }
 
   // ------------------------------------------------------------ teardown
@@ -1130,6 +1210,14 @@ cudaError_t set_smem_attrs() {
   if (err == cudaSuccess)
     err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kS8SmemBytes);
+  if (err == cudaSuccess) {
+    // the int8-operand kernel's register split assumes 128 registers a
+    // thread at launch; with fewer, its setmaxnreg.inc could never be
+    // satisfied, so such a build is refused instead of launched
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, true>);
+    if (err == cudaSuccess && fa.numRegs != 128) err = cudaErrorInvalidDeviceFunction;
+  }
   return err;
 }
 
@@ -1147,11 +1235,15 @@ uint64_t next_epoch() {
   return e == 0 ? 1 : e;
 }
 
-// Output map for the pair kernel's tile stores: boxes of 128 bytes x 32 rows,
-// 128-byte swizzle (bf16: 64 columns; int32: 32).
-bool make_output_map(CUtensorMap* map, void* out, bool s32, int64_t M, int64_t N, int64_t ldo) {
-  if (s32)
+// Output map for the tile stores: boxes of 128 bytes x 32 rows, 128-byte
+// swizzle (bf16: 64 columns; int32 and fp32: 32).
+bool make_output_map(CUtensorMap* map, void* out, GemmOut mode, int64_t M, int64_t N,
+                     int64_t ldo) {
+  if (mode == GemmOut::kS32)
     return encode_tensor_map_2d(map, out, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, M, N, ldo, 32, 32,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (mode == GemmOut::kF32Scaled)
+    return encode_tensor_map_2d(map, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, ldo, 32, 32,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
   return encode_tensor_map_2d(map, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, N, ldo, 64, 32,
                               CU_TENSOR_MAP_SWIZZLE_128B);
@@ -1220,7 +1312,7 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
       s8 ? make_raw_map(&mapA, A, a_mn, M, K) && make_raw_map(&mapB, B, b_mn, N, K)
          : make_operand_map(&mapA, A, a_mn, M, K, kBM, plain) &&
                make_operand_map(&mapB, B, b_mn, N, K, pair ? 128 : kBN, plain);
-  if (!maps_ok || !make_output_map(&mapO, out, mode == GemmOut::kS32, M, N, ldo))
+  if (!maps_ok || !make_output_map(&mapO, out, mode, M, N, ldo))
     return cudaErrorInvalidValue;
   GemmParams p;
   p.sA = sA;
@@ -1234,7 +1326,7 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
   p.m_fastest = M < N ? 1 : 0;
   p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
-  p.mode = mode == GemmOut::kS32 ? 1 : plain ? 2 : 0;
+  p.mode = mode == GemmOut::kS32 ? 1 : plain ? 2 : mode == GemmOut::kF32Scaled ? 3 : 0;
   p.ab_format = plain ? kFormatBf16 : 0u;
   // integer codes: exact fp32 chunks of 1024 terms; bf16: all of K at once
   p.chunk_blocks = plain ? p.k_blocks : kChunkBlocks;

@@ -188,6 +188,18 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Register split between warpgroups: every thread of a warpgroup executes
+// the same adjustment.  inc waits until the registers that other warpgroups
+// release with dec are free, so the launch's total must cover the split.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ----------------------------------------------------------------- tcgen05
 // Tensor memory allocation: executed by one whole warp.  The allocated base
 // address is written to shared memory at `dst`.

@@ -540,6 +540,31 @@ __global__ void zero_words_kernel(unsigned int* __restrict__ p, int64_t n) {
     p[i] = 0u;
 }
 
+// y[i] = bf16_RNE(x[i]): eight values per thread and step (two 16-byte
+// loads, one 16-byte store), the remainder one at a time.
+__global__ void round_bf16_kernel(const float* __restrict__ x, uint16_t* __restrict__ y,
+                                  int64_t n) {
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t n8 = n / 8;
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  uint4* y8 = reinterpret_cast<uint4*>(y);
+  auto pack = [](float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  };
+  for (int64_t i = t; i < n8; i += stride) {
+    const float4 a = __ldg(x4 + 2 * i), b = __ldg(x4 + 2 * i + 1);
+    y8[i] = make_uint4(pack(a.x, a.y), pack(a.z, a.w), pack(b.x, b.y), pack(b.z, b.w));
+  }
+  for (int64_t i = n8 * 8 + t; i < n; i += stride) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x[i]);
+    y[i] = *reinterpret_cast<const uint16_t*>(&h);
+  }
+}
+
 // Pass 2: scale = absmax / 127, in place, before any code is computed.
 __global__ void col_scale_kernel(unsigned int* __restrict__ amax_bits, int64_t cols) {
   ptx::grid_dependency_wait();  // the previous kernel in the stream is done
@@ -1106,6 +1131,17 @@ cudaError_t launch_zero_words(void* p, int64_t n, const DeviceInfo& dev, cudaStr
   if (blocks > 4 * sms) blocks = 4 * sms;
   return launch_overlapped(zero_words_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
                            stream, static_cast<unsigned int*>(p), n);
+}
+
+cudaError_t launch_round_bf16(const float* x, void* y, int64_t n, const DeviceInfo& dev,
+                              cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const int sms = dev.sms > 0 ? dev.sms : 148;
+  int64_t blocks = (n / 8 + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 8 * sms) blocks = 8 * sms;
+  return launch_overlapped(round_bf16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                           stream, x, static_cast<uint16_t*>(y), n);
 }
 
 cudaError_t launch_column_absmax(const void* x, int64_t rows, int64_t cols, int64_t ld,

@@ -44,11 +44,15 @@ def _load(path):
     L.orc_linear_fwd_cfg.argtypes = [_p, _p, _i64, _i64, _i64, _int, _int, _u64, _u64, _p, _int]
     L.orc_linear_bwd_cfg.argtypes = [_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _u64, _u64,
                                      _p, _p, _int]
+    L.orc_rescale_f32.argtypes = [_p, _p, _p, _i64, _i64, _p]
+    L.orc_scaled_mm_f32.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _int, _p, _int]
+    L.orc_grad_weight_sharded.argtypes = [_p, _p, _i64, _i64, _i64, _int, _int, _u64, _p, _p, _int]
     L.orc_f32_to_bf16_rne.argtypes = [ctypes.c_float]
     L.orc_f32_to_bf16_rne.restype = ctypes.c_uint16
     for name in ("orc_quantize", "orc_mm_s32", "orc_rescale_bf16", "orc_scaled_mm",
                  "orc_linear_fwd", "orc_linear_bwd", "orc_matmul_bf16", "orc_linear_fwd_cfg",
-                 "orc_linear_bwd_cfg"):
+                 "orc_linear_bwd_cfg", "orc_rescale_f32", "orc_scaled_mm_f32",
+                 "orc_grad_weight_sharded"):
         getattr(L, name).restype = _int
     return L
 
@@ -166,6 +170,41 @@ def linear_bwd(dY, X, W, mode=RNE, seed=0, offset=0, nthreads=None, want_dx=True
     _check(lib().orc_linear_bwd(_ptr(dY), _ptr(X), _ptr(W), T, N, K, mode, seed, offset,
                                 _ptr(dX), _ptr(dW), nthreads or default_threads()), "linear_bwd")
     return dX, dW
+
+
+def rescale_f32(acc, sA, sB):
+    acc = _c(acc, np.int32)
+    M, N = acc.shape
+    out = np.zeros((M, N), dtype=np.float32)
+    _check(lib().orc_rescale_f32(_ptr(acc), _ptr(_c(sA, np.float32)), _ptr(_c(sB, np.float32)),
+                                 M, N, _ptr(out)), "rescale_f32")
+    return out
+
+
+def scaled_mm_f32(A, sA, B, sB, M, N, K, layout=AxBT, nthreads=None):
+    """The scaled matmul's fp32 value before the bf16 rounding."""
+    out = np.zeros((M, N), dtype=np.float32)
+    _check(lib().orc_scaled_mm_f32(_ptr(_c(A, np.int8)), _ptr(_c(sA, np.float32)),
+                                   _ptr(_c(B, np.int8)), _ptr(_c(sB, np.float32)),
+                                   M, N, K, layout, _ptr(out), nthreads or default_threads()),
+           "scaled_mm_f32")
+    return out
+
+
+def grad_weight_sharded(dY, X, nshards, offsets, mode=RNE, seed=0, nthreads=None):
+    """dW [N,K] of token-sharded data parallelism: per-shard fp32 partials
+    summed in shard order, rounded once to bf16 (bits)."""
+    dY = _c(dY, np.uint16)
+    X = _c(X, np.uint16)
+    T, N = dY.shape
+    K = X.shape[1]
+    offs = _c(np.asarray(offsets, dtype=np.uint64), np.uint64)
+    assert len(offs) == nshards
+    out = np.zeros((N, K), dtype=np.uint16)
+    _check(lib().orc_grad_weight_sharded(_ptr(dY), _ptr(X), T, N, K, nshards, mode, seed,
+                                         _ptr(offs), _ptr(out), nthreads or default_threads()),
+           "grad_weight_sharded")
+    return out
 
 
 def matmul_bf16(A, B, M, N, K, layout=AxBT, nthreads=None):

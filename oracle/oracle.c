@@ -222,6 +222,36 @@ int orc_scaled_mm(const int8_t* A, const float* sA, const int8_t* B, const float
   return rc;
 }
 
+/* Step 5 without its final rounding: the fp32 value (acc * sA) * sB that a
+ * token shard contributes to a data-parallel grad-weight before the shards'
+ * values are summed. */
+int orc_rescale_f32(const int32_t* acc, const float* sA, const float* sB, int64_t M, int64_t N,
+                    float* out) {
+  if (M < 0 || N < 0) return -1;
+  if (M == 0 || N == 0) return 0;
+  if (!acc || !sA || !sB || !out) return -1;
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      float f = (float)acc[i * N + j]; /* int32 -> fp32, round to nearest */
+      float t = f * sA[i];
+      out[i * N + j] = t * sB[j];
+    }
+  }
+  return 0;
+}
+
+int orc_scaled_mm_f32(const int8_t* A, const float* sA, const int8_t* B, const float* sB,
+                      int64_t M, int64_t N, int64_t K, int layout, float* out, int nthreads) {
+  if (M < 0 || N < 0 || K < 0) return -1;
+  if (M == 0 || N == 0) return 0;
+  int32_t* acc = (int32_t*)malloc((size_t)(M * N) * sizeof(int32_t));
+  if (!acc) return -2;
+  int rc = orc_mm_s32(A, B, M, N, K, layout, acc, nthreads);
+  if (rc == 0) rc = orc_rescale_f32(acc, sA, sB, M, N, out);
+  free(acc);
+  return rc;
+}
+
 /* ---------------------------------------------------------------- linear */
 
 /* quantize X [R,C] along axis, multiply as A @ B.T with the codes, rescale */
@@ -346,5 +376,43 @@ int orc_linear_bwd_cfg(const uint16_t* dY, const uint16_t* X, const uint16_t* W,
              ? orc_linear_bwd(dY, X, W, T, N, K, mode, seed, offset, NULL, dW, nthreads)
              : orc_matmul_bf16(dY, X, N, K, T, ORC_ATxB, dW, nthreads); /* dW = dY^T . X */
   }
+  return rc;
+}
+
+/* ------------------------------------------------- data-parallel grad weight */
+
+/* Grad-weight of a linear layer whose T tokens are split into `nshards`
+ * equal shards of consecutive rows (T % nshards == 0): shard r quantizes
+ * its own rows of dY and X by columns (along T, its own column scales; SR
+ * counters from offsets[r]), forms its fp32 partial with orc_scaled_mm_f32,
+ * the partials are summed in fp32 in shard order, and the sum is rounded to
+ * bf16 once:  dW = bf16_RNE(P_0 + P_1 + ... + P_{n-1}). */
+int orc_grad_weight_sharded(const uint16_t* dY, const uint16_t* X, int64_t T, int64_t N, int64_t K,
+                            int nshards, int mode, uint64_t seed, const uint64_t* offsets,
+                            uint16_t* dW, int nthreads) {
+  if (T < 0 || N < 0 || K < 0 || nshards < 1 || T % nshards != 0) return -1;
+  if (N == 0 || K == 0) return 0;
+  if (!dY || !X || !dW || !offsets) return -1;
+  const int64_t Ts = T / nshards;
+  float* sum = (float*)calloc((size_t)(N * K), sizeof(float));
+  float* part = (float*)malloc((size_t)(N * K) * sizeof(float));
+  int8_t* qg = (int8_t*)malloc((size_t)(N * Ts) + 1);
+  int8_t* qx = (int8_t*)malloc((size_t)(K * Ts) + 1);
+  float* sg = (float*)malloc((size_t)N * sizeof(float));
+  float* sx = (float*)malloc((size_t)K * sizeof(float));
+  int rc = (sum && part && qg && qx && sg && sx) ? 0 : -2;
+  for (int r = 0; r < nshards && rc == 0; ++r) {
+    const uint16_t* g = dY + (size_t)(r * Ts) * (size_t)N;
+    const uint16_t* x = X + (size_t)(r * Ts) * (size_t)K;
+    /* dY and X of this shard along T: column groups, codes [N, Ts] and [K, Ts] */
+    rc = orc_quantize(g, Ts, N, N, 1, mode, seed, offsets[r], ORC_STREAM_GW_DY, qg, sg);
+    if (rc == 0) rc = orc_quantize(x, Ts, K, K, 1, mode, seed, offsets[r], ORC_STREAM_GW_X, qx, sx);
+    if (rc == 0) rc = orc_scaled_mm_f32(qg, sg, qx, sx, N, K, Ts, ORC_AxBT, part, nthreads);
+    if (rc == 0)
+      for (int64_t i = 0; i < N * K; ++i) sum[i] = sum[i] + part[i];
+  }
+  if (rc == 0)
+    for (int64_t i = 0; i < N * K; ++i) dW[i] = orc_f32_to_bf16_rne(sum[i]);
+  free(sum); free(part); free(qg); free(qx); free(sg); free(sx);
   return rc;
 }

@@ -112,6 +112,24 @@ int orc_linear_bwd_cfg(const uint16_t* dY, const uint16_t* X, const uint16_t* W,
                        uint64_t seed, uint64_t offset, uint16_t* dX, uint16_t* dW,
                        int nthreads);
 
+/* Step 5 without the final bf16 rounding: out[i,j] = fp32 (fp32_RN(acc) *
+ * sA[i]) * sB[j].  orc_scaled_mm_f32 = orc_mm_s32 + orc_rescale_f32. */
+int orc_rescale_f32(const int32_t* acc, const float* sA, const float* sB, int64_t M, int64_t N,
+                    float* out);
+int orc_scaled_mm_f32(const int8_t* A, const float* sA, const int8_t* B, const float* sB,
+                      int64_t M, int64_t N, int64_t K, int layout, float* out, int nthreads);
+
+/* Grad-weight under token-sharded data parallelism (the reading of the
+ * FSDP2 runs in "Integrate INT8 mixed-precision from torchao 0.7" and the
+ * reduce-scatter of torchao issue 1887): shard r of nshards equal blocks of
+ * consecutive token rows quantizes its dY and X rows by columns with its own
+ * column scales (SR counters from offsets[r]), forms its fp32 partial
+ * (orc_scaled_mm_f32), the partials are summed in fp32 in shard order and the
+ * sum is rounded once: dW = bf16_RNE(P_0 + ... + P_{n-1}). */
+int orc_grad_weight_sharded(const uint16_t* dY, const uint16_t* X, int64_t T, int64_t N, int64_t K,
+                            int nshards, int mode, uint64_t seed, const uint64_t* offsets,
+                            uint16_t* dW, int nthreads);
+
 #ifdef __cplusplus
 }
 #endif
