@@ -67,7 +67,8 @@ def parse_args():
 # `ncu -s 2 -c 1` captures a warm launch): the square 4096^3 A @ B.T matmul
 # on int8 codes and on f16 containers of the same codes, and the BF16
 # forward pass of a q projection at T = 16384.
-PROFILE_CASES = ("square-int8-4096", "square-f16-4096", "bf16-forward-q-T16384")
+PROFILE_CASES = ("square-int8-4096", "square-f16-4096", "square-f16-2048", "square-f16-1024",
+                 "bf16-forward-q-T16384")
 
 
 def run_profile_case(case, device):
@@ -76,7 +77,7 @@ def run_profile_case(case, device):
     from int8_mixed_precision_row_gb300 import synth
     g = torch.Generator(device=device).manual_seed(0)
     if case.startswith("square"):
-        S = 4096
+        S = int(case.rsplit("-", 1)[1])
         a = torch.randint(-127, 128, (S, S), device=device, generator=g, dtype=torch.int32)
         b = torch.randint(-127, 128, (S, S), device=device, generator=g, dtype=torch.int32)
         dt = torch.int8 if case == "square-int8-4096" else torch.float16
@@ -84,8 +85,9 @@ def run_profile_case(case, device):
         sa = torch.rand(S, device=device, generator=g)
         sb = torch.rand(S, device=device, generator=g)
         out = torch.empty((S, S), dtype=torch.bfloat16, device=device)
+        ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
         for _ in range(3):
-            m.int8mp_scaled_mm(a, sa, b, sb, out=out)
+            m.int8mp_scaled_mm(a, sa, b, sb, out=out, workspace=ws)
     else:
         X = synth.bf16_normal((16384, 2048), 10).to(device)
         W = synth.bf16_normal((2048, 2048), 20, std=0.02).to(device)

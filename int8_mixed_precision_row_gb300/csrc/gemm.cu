@@ -238,7 +238,7 @@ template <bool kRegScales>
 __device__ __forceinline__ TileScales load_tile_scales(const GemmParams& p, int64_t row0,
                                                        int64_t col0) {
   TileScales t{0.0f, {0.0f, 0.0f, 0.0f, 0.0f}};
-  if (!kRegScales || (p.mode != 0 && p.mode != 3)) return t;
+  if (!kRegScales || p.mode != 0) return t;
   const int lane = threadIdx.x & 31;
   if (row0 + lane < p.M) t.sa = __ldg(p.sA + row0 + lane);
 #pragma unroll
@@ -294,8 +294,11 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
     }
     return;
   }
-  if (p.mode == 3) {  // fp32 scaled: boxes of 32 columns, like the int32 totals
-    const float sa = kRegScales ? ts.sa : row < p.M ? __ldg(p.sA + row) : 0.0f;
+  if (!kRegScales && p.mode == 3) {  // fp32 scaled: 32-column boxes, like the int32 totals
+    // (a data-parallel partial, off the training step's hot path: launched
+    // without tile-start scales, and the column scales come from global
+    // memory, which keeps this branch out of the other epilogues' registers)
+    const float sa = row < p.M ? __ldg(p.sA + row) : 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int64_t c0 = col0 + 32 * j;
@@ -307,12 +310,8 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
         float sb[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          if (kRegScales) {
-            sb[e] = __shfl_sync(0xFFFFFFFFu, ts.sb[j], 4 * c + e);
-          } else {
-            const int64_t col = col0 + k0 + e;
-            sb[e] = col < p.N ? __ldg(p.sB + col) : 0.0f;
-          }
+          const int64_t col = col0 + k0 + e;
+          sb[e] = col < p.N ? __ldg(p.sB + col) : 0.0f;
         }
         uint32_t w[4];
 #pragma unroll
@@ -1367,7 +1366,8 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   }
   // at most two tiles per CTA (pair): the scales are loaded when a tile starts
   const int units = grid / (pair ? 2 : 1);
-  const bool reg_scales = static_cast<int64_t>(p.dp_tiles) <= 2 * units;
+  const bool reg_scales =
+      mode != GemmOut::kF32Scaled && static_cast<int64_t>(p.dp_tiles) <= 2 * units;
   if (!a_mn && !b_mn)
     return launch_layout<false, false>(pair, s8, reg_scales, grid, mapA, mapB, mapO, p, stream);
   if (!a_mn)
