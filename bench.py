@@ -68,7 +68,8 @@ def parse_args():
 # on int8 codes and on f16 containers of the same codes, and the BF16
 # forward pass of a q projection at T = 16384.
 PROFILE_CASES = ("square-int8-4096", "square-f16-4096", "square-f16-2048", "square-f16-1024",
-                 "bf16-forward-q-T16384")
+                 "bf16-forward-q-T16384", "forward-q-T16384-w-codes",
+                 "forward-q-T16384-w-quantized-in-prologue")
 
 
 def run_profile_case(case, device):
@@ -88,6 +89,19 @@ def run_profile_case(case, device):
         ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
         for _ in range(3):
             m.int8mp_scaled_mm(a, sa, b, sb, out=out, workspace=ws)
+    elif case.startswith("forward-q-T16384"):
+        # the forward matmul of a q projection on X's codes, with W's codes
+        # from the row pass, or W quantized in the GEMM's prologue from its
+        # row scales (the row pass's scales)
+        X = synth.bf16_normal((16384, 2048), 10).to(device)
+        W = synth.bf16_normal((2048, 2048), 20, std=0.02).to(device)
+        (qx, sx), (qw, sw) = m.int8mp_quantize_rows_batch([X, W], codes=m.INT8MP_CODES_F16)
+        Y = torch.empty((16384, 2048), dtype=torch.bfloat16, device=device)
+        for _ in range(3):
+            if case.endswith("in-prologue"):
+                m.int8mp_debug_scaled_mm_quant_b(qx, sx, W, sw, out=Y)
+            else:
+                m.int8mp_scaled_mm(qx, sx, qw, sw, out=Y)
     else:
         X = synth.bf16_normal((16384, 2048), 10).to(device)
         W = synth.bf16_normal((2048, 2048), 20, std=0.02).to(device)

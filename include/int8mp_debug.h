@@ -1,7 +1,8 @@
 /*
  * int8mp_debug.h -- test-only entry points of libint8mp.so.  Not needed to
  * use the library; they exist so that the failure paths can be exercised
- * without faulting or hanging a GPU.
+ * without faulting or hanging a GPU, and so that a design choice can be
+ * measured against its alternative.
  */
 #ifndef INT8MP_DEBUG_H
 #define INT8MP_DEBUG_H
@@ -45,6 +46,25 @@ int8mp_status int8mp_debug_mm_s32_drop_first_load(const void* A, const void* B, 
  * codes differ.  Synchronizes the device.  Test use only.
  */
 int8mp_status int8mp_debug_check_division(uint64_t* results, uint32_t* first_bad);
+
+/*
+ * The scaled matmul A @ B.T with the B operand quantized inside the GEMM's
+ * prologue instead of by a separate pass ("Integrate INT8 mixed-precision
+ * from torchao 0.7", limitations: the quantization must be compiled code to
+ * pay off; here the alternative to the library's separate row pass, kept so
+ * that the choice can be measured).  A: codes as f16 containers [M, K]
+ * (INT8MP_GROUP_ROWS), sA fp32 [M].  B: the bf16 values [N, K] themselves,
+ * with sB fp32 [N] their row scales (as int8mp_quantize_rowwise computes
+ * them); six converter warps of the CTA-pair kernel quantize each bf16 tile
+ * of B (nearest even) with its row scales as the row quantizer would, in
+ * shared memory, before the tensor core reads it.  out: bf16 [M, N], row
+ * stride ldo.  Results are those of int8mp_scaled_mm on B's codes, bit for
+ * bit.  Requirements: those of int8mp_scaled_mm with INT8MP_AxBT and
+ * INT8MP_CODES_F16.  Test use only.
+ */
+int8mp_status int8mp_debug_scaled_mm_quant_b(const void* A, const float* sA, const void* B,
+                                             const float* sB, int64_t M, int64_t N, int64_t K,
+                                             void* out, int64_t ldo, void* stream);
 
 #ifdef __cplusplus
 }

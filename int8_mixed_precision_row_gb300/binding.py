@@ -40,7 +40,7 @@ EXPORTED = (
     "int8mp_debug_check_division", "int8mp_quantize_rows_colmax", "int8mp_quantize_cols_absmax",
     "int8mp_linear_fwd_save", "int8mp_linear_bwd_saved", "int8mp_mm_workspace_size",
     "int8mp_scaled_mm_ws", "int8mp_mm_s32_ws", "int8mp_quantize_rows_batch",
-    "int8mp_scaled_mm_f32", "int8mp_round_bf16",
+    "int8mp_scaled_mm_f32", "int8mp_round_bf16", "int8mp_debug_scaled_mm_quant_b",
 )
 INT8MP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -144,8 +144,9 @@ def load(path=None):
     L.int8mp_scaled_mm_f32.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _I64, _P,
                                        _SZ, _P]
     L.int8mp_round_bf16.argtypes = [_P, _P, _I64, _P]
+    L.int8mp_debug_scaled_mm_quant_b.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P]
     for name in ("int8mp_scaled_mm_ws", "int8mp_mm_s32_ws", "int8mp_scaled_mm_f32",
-                 "int8mp_round_bf16",
+                 "int8mp_round_bf16", "int8mp_debug_scaled_mm_quant_b",
                  "int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
                  "int8mp_linear_fwd", "int8mp_linear_bwd", "int8mp_poll_device_status",
                  "int8mp_version", "int8mp_debug_mm_s32_drop_first_load",
@@ -478,6 +479,22 @@ def int8mp_debug_mm_s32_drop_first_load(A, B, out, wait_limit_ms=200, stream=Non
     return load().int8mp_debug_mm_s32_drop_first_load(_ptr(A), _ptr(B), M, N, K, _ptr(out),
                                                       out.stride(0), int(wait_limit_ms),
                                                       _stream(stream))
+
+
+def int8mp_debug_scaled_mm_quant_b(A, sA, B, sB, out=None, stream=None):
+    """Test only: A (f16 codes [M,K]) @ B.T with B bf16 [N,K] quantized in
+    the GEMM's prologue from its row scales sB -> bf16 [M,N]."""
+    M, K = A.shape
+    N = B.shape[0]
+    assert A.dtype == torch.float16 and B.dtype == torch.bfloat16
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _check_out(out, M, N, torch.bfloat16)
+    _check(load().int8mp_debug_scaled_mm_quant_b(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), M, N, K,
+                                                 _ptr(out), out.stride(0) if M > 0 else N,
+                                                 _stream(stream)),
+           "int8mp_debug_scaled_mm_quant_b")
+    return out
 
 
 def int8mp_linear_fwd_noalloc(X, W, cfg=None, Y=None, stream=None):

@@ -25,7 +25,7 @@ CHECK_DIR = os.path.join(HERE, "_build_check")
 CHECK_LIB = os.path.join(CHECK_DIR, "libint8mp.so")
 
 SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "tma.cu", "noalloc.cu", "debug.cu"]
-HEADERS = ["common.cuh", "ptx.cuh", "philox.cuh", "divide.cuh", "check.cuh"]
+HEADERS = ["common.cuh", "ptx.cuh", "philox.cuh", "divide.cuh", "check.cuh", "codes.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -618,4 +618,18 @@ int8mp_status int8mp_debug_mm_s32_drop_first_load(const void* A, const void* B, 
                 nullptr, dbg, as_stream(stream));
 }
 
+int8mp_status int8mp_debug_scaled_mm_quant_b(const void* A, const float* sA, const void* B,
+                                             const float* sB, int64_t M, int64_t N, int64_t K,
+                                             void* out, int64_t ldo, void* stream) {
+  int8mp_status st = check_mm(A, B, M, N, K, INT8MP_AxBT, INT8MP_CODES_F16, out, ldo);
+  if (st != INT8MP_OK) return st;
+  if (M == 0 || N == 0 || K == 0) return INT8MP_ERR_INVALID_ARG;
+  if (!sA || !sB) return INT8MP_ERR_INVALID_ARG;
+  if (!aligned(sA, 4) || !aligned(sB, 4)) return INT8MP_ERR_ALIGNMENT;
+  int8mp::GemmDebug dbg;
+  dbg.quant_b = 1;
+  return run_mm(A, sA, B, sB, M, N, K, INT8MP_AxBT, int8mp::GemmOut::kBf16Scaled, out, ldo,
+                nullptr, dbg, as_stream(stream));
+}
+
 }  // extern "C"

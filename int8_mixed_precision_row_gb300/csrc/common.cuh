@@ -131,6 +131,7 @@ struct GemmDebug {
   int drop_first_load = 0;        // test only: never issue the first TMA load
   int single_cta = 0;             // test only: use the single-CTA kernel for any M
   int no_split_tail = 0;            // test only: no split last wave even with scratch
+  int quant_b = 0;  // test only: B is bf16, quantized in the GEMM's prologue with its scales sB
   uint64_t wait_limit_ns = kWaitLimitNs;
 };
 

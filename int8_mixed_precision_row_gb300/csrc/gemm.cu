@@ -46,7 +46,9 @@
 #include <mutex>
 
 #include "check.cuh"
+#include "codes.cuh"
 #include "common.cuh"
+#include "divide.cuh"
 #include "ptx.cuh"
 
 namespace int8mp {
@@ -603,14 +605,19 @@ constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairSmemBytes =
     1024 + kPairStages * kPairStageBytes + kStagingBytes + kBarrierBytes;
 static_assert(kPairSmemBytes <= 227 * 1024, "pair kernel shared memory");
-// int8 operands (kS8): TMA brings each CTA's int8 k-block (128 x 64 codes of
-// A and of B, 16 KB) into a ring of its own, and six converter warps widen it
-// into the f16 stage the tensor core reads -- fewer f16 stages, more raw ones
-// (the raw ring covers the DRAM latency, the f16 ring only decouples the
-// converters from the MMA).  The kernel runs four warpgroups: warpgroup 0
-// (producer, MMA, converters 0-1) and 3 (converters 2-5) give up registers,
-// warpgroups 1-2 (the epilogue, warps 4-11) take them:
-// 256 x kS8RegsEpi + 256 x kS8RegsOther = 65,536, the launch's registers.
+// Converter stage (kConv != 0): TMA brings each CTA's raw k-block into a
+// ring of its own, and six converter warps turn it into the f16 stage the
+// tensor core reads -- fewer f16 stages, more raw ones (the raw ring covers
+// the DRAM latency, the f16 ring only decouples the converters from the MMA).
+//   kConvWiden (1): int8 codes of A and of B (128 x 64 each, 16 KB), widened.
+//   kConvQuantB (2): the bf16 B operand (128 x 64, 16 KB) quantized with its
+//                    given row scales, as the row quantizer would (A arrives
+//                    as f16 codes by TMA, as in the plain kernel).
+// The kernel runs four warpgroups: warpgroup 0 (producer, MMA, converters
+// 0-1) and 3 (converters 2-5) give up registers, warpgroups 1-2 (the
+// epilogue, warps 4-11) take them: 256 x kConvRegsEpi + 256 x kConvRegsOther
+// = 65,536, the launch's registers.
+constexpr int kConvNone = 0, kConvWiden = 1, kConvQuantB = 2;
 constexpr int kS8Stages = 4;
 constexpr int kRawStages = 4;
 constexpr int kRawOperandBytes = 128 * kBK;  // 128 rows x 64 k, one byte each
@@ -669,6 +676,46 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
 // swizzles, so the first (and the second) stores of the quarter warp land in
 // complementary chunk sets.  MN-major, they are one k of both 64-wide blocks
 // (same swizzle): the threads of block 1 store their second chunk first.
+// Quantize one CTA's bf16 B k-block (128 rows x 64 k at `raw`, unswizzled
+// 128-byte rows) into its f16 stage tile at `dst` (K-major, 128-byte
+// swizzle): row n's codes with its scale sB[n] (rows at or past `nrows` are
+// the zero fill, code 0), exactly as the row quantizer forms them -- the
+// certified three-operation quotient when the scale allows it, else IEEE
+// division; nearest even by the packed magic-number add when the scale is
+// normal, else rint and clamp.  Each 16-byte raw chunk (eight values of one
+// row) becomes one 16-byte chunk of codes; a quarter warp covers one row.
+__device__ __forceinline__ void quant_tile_b(uint32_t raw, uint32_t dst, int ct,
+                                             const float* __restrict__ sB, int nrows) {
+#pragma unroll 2
+  for (int c = ct; c < 128 * 8; c += kConvThreads) {
+    const int row = c >> 3, j = c & 7;
+    const uint4 v = ptx::ld_shared_v4(raw + static_cast<uint32_t>(c) * 16u);
+    const float sc = row < nrows ? __ldg(sB + row) : 0.0f;
+    const ScaleDiv d = make_scale_div(sc);
+    float f[8], q[8];
+    unpack8(v, f);
+    if (!div8_try(f, d, q)) div8_ieee(f, sc, q);
+    uint32_t h[4];
+    if (scale_is_normal(sc)) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 cc = code_rne_normal_scale2(make_float2(q[2 * i], q[2 * i + 1]));
+        const __half2 hh = __floats2half2_rn(cc.x, cc.y);
+        h[i] = *reinterpret_cast<const uint32_t*>(&hh);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 hh = __floats2half2_rn(code_rne(q[2 * i]), code_rne(q[2 * i + 1]));
+        h[i] = *reinterpret_cast<const uint32_t*>(&hh);
+      }
+    }
+    const uint32_t sw = static_cast<uint32_t>(row & 7);
+    ptx::st_shared_v4(dst + static_cast<uint32_t>(row) * 128u + ((static_cast<uint32_t>(j) ^ sw) << 4),
+                      h[0], h[1], h[2], h[3]);
+  }
+}
+
 template <bool kMN>
 __device__ __forceinline__ void widen_tile(uint32_t raw, uint32_t dst, int ct) {
   static_assert(kConvThreads % 8 == 0, "a thread's chunks keep their bit 2");
@@ -826,18 +873,22 @@ __device__ __forceinline__ void sk_complete(const GemmParams& p, int rank, int e
   }
 }
 
-// kS8: the operands are int8 codes (INT8MP_CODES_S8).  Each CTA's producer
-// brings its int8 k-blocks into a raw ring (its own barriers); converter
-// warps 2-3 and 12-15 of both CTAs widen them into the f16 stages and arrive
-// on the even CTA's full barrier (release at cluster scope, after a proxy
-// fence so that the tensor core sees the stores), which the MMA thread waits
-// on at cluster scope; the epilogue is warps 4-11.  Everything else is the
+// kConv != 0: a converter stage.  Each CTA's producer brings its raw
+// k-blocks into a raw ring (its own barriers); converter warps 2-3 and 12-15
+// of both CTAs turn them into the f16 stages and arrive on the even CTA's
+// full barrier (release at cluster scope, after a proxy fence so that the
+// tensor core sees the stores), which the MMA thread waits on at cluster
+// scope; the epilogue is warps 4-11.  kConvWiden: both operands are int8
+// codes (INT8MP_CODES_S8).  kConvQuantB: A is f16 codes loaded by TMA into
+// the f16 stage as in the plain kernel (the even CTA's arrive carries their
+// bytes), B is bf16, quantized by the converters.  Everything else is the
 // f16 kernel.
-template <bool kAmn, bool kBmn, bool kRegScales, bool kS8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : kThreads, 1)
+template <bool kAmn, bool kBmn, bool kRegScales, int kConv>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kConv != kConvNone ? kS8Threads : kThreads, 1)
     gemm_s8f16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
+  constexpr bool kS8 = kConv != kConvNone;  // a converter stage (any kind)
   constexpr int kStagesHere = kS8 ? kS8Stages : kPairStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -868,8 +919,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : k
   const bool even = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesHere; ++s) {
-      // int8 operands: both CTAs' converter warps arrive; f16: the TMA bytes
-      ptx::mbar_init(full_bar(s), kS8 ? 2 * kConvWarps : 1);
+      // converters: both CTAs' converter warps arrive (and, quantizing B,
+      // the even producer with A's bytes); f16: the TMA bytes
+      ptx::mbar_init(full_bar(s), kConv == kConvWiden    ? 2 * kConvWarps
+                                  : kConv == kConvQuantB ? 1 + 2 * kConvWarps
+                                                         : 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -946,6 +1000,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : k
             raise_abort(abort, p.status);
     }
   };
+  auto qb_producer = [&]() {
+    if (lane == 0) {
+      // ------------------------------- producer (quantizing B in the prologue)
+      // A's f16 codes by TMA into the f16 stage, completing on the even
+      // CTA's full barrier (as in the plain kernel); B's bf16 rows into this
+      // CTA's raw ring for the converters
+      uint32_t stage = 0, phase = 0, rstage = 0, rphase = 0;
+      uint32_t armed = 0u, armed_par = 0u, rarmed = 0u, rarmed_par = 0u;
+      bool ok = true;
+      FragIter it(p, pair);
+      int tile, kb0, kb1;
+      while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
+        int mb, nb;
+        tile_mn(p, tile, mb, nb);
+        const int m0 = mb * 256 + static_cast<int>(rank) * 128;
+        const int n0 = nb * 256 + static_cast<int>(rank) * 128;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort, limit) ||
+              !ptx::mbar_wait_bounded(rempty_bar(rstage), rphase ^ 1u, abort, limit)) {
+            ok = false;
+            break;
+          }
+          armed &= ~(1u << stage);
+          const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0);
+          if (even) {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * kPairABytes);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          }
+          load_operand_pair<kAmn, 128>(a_base + stage * kPairABytes, &tmA, fb, kb, m0);
+          ptx::mbar_arrive_expect_tx(rfull_bar(rstage), kRawStageBytes);
+          ptx::tma_load_2d(rawring + rstage * kRawStageBytes, &tmB, rfull_bar(rstage), kb * kBK,
+                           n0);
+          rarmed |= 1u << rstage;
+          rarmed_par = (rarmed_par & ~(1u << rstage)) | (rphase << rstage);
+          if (++stage == kStagesHere) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++rstage == kRawStages) {
+            rstage = 0;
+            rphase ^= 1u;
+          }
+        }
+      }
+      if (!ok) raise_abort(abort, p.status);
+      // never leave a copy in flight into shared memory of an exiting CTA
+      for (int s = 0; s < kRawStages; ++s)
+        if (rarmed & (1u << s))
+          if (!ptx::mbar_wait_bounded(rfull_bar(s), (rarmed_par >> s) & 1u, never, limit))
+            raise_abort(abort, p.status);
+      for (int s = 0; s < kStagesHere; ++s)
+        if (armed & (1u << s))
+          if (!ptx::mbar_wait_bounded_cluster(full_bar(s), (armed_par >> s) & 1u, never, limit))
+            raise_abort(abort, p.status);
+    }
+  };
   auto converters = [&]() {
     // ------------------------------------------- converters (int8 operands)
     const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 320;  // 0 .. kConvThreads-1
@@ -964,8 +1075,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : k
           break;
         }
         const uint32_t raw = rawring + rstage * kRawStageBytes;
-        widen_tile<kAmn>(raw, a_base + stage * kPairABytes, ct);
-        widen_tile<kBmn>(raw + kRawOperandBytes, b_base + stage * kPairBBytes, ct);
+        if constexpr (kConv == kConvQuantB) {
+          int mb, nb;
+          tile_mn(p, tile, mb, nb);
+          const int n0 = nb * 256 + static_cast<int>(rank) * 128;
+          quant_tile_b(raw, b_base + stage * kPairBBytes, ct, p.sB + n0, p.N - n0);
+        } else {
+          widen_tile<kAmn>(raw, a_base + stage * kPairABytes, ct);
+          widen_tile<kBmn>(raw + kRawOperandBytes, b_base + stage * kPairBBytes, ct);
+        }
         ptx::fence_proxy_async_smem();  // the tensor core reads these stores
         __syncwarp();
         if (lane == 0) {
@@ -1138,9 +1256,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kS8 ? kS8Threads : k
       epilogue();
     } else {
       ptx::setmaxnreg_dec<kS8RegsOther>();
-      if (warp == 0)
-        s8_producer();
-      else if (warp == 1)
+      if (warp == 0) {
+        if constexpr (kConv == kConvQuantB)
+          qb_producer();
+        else
+          s8_producer();
+      } else if (warp == 1)
         mma();
       else
         converters();
@@ -1199,24 +1320,32 @@ bool make_raw_map(CUtensorMap* map, const void* base, bool mn_major, int64_t mn,
                               CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// Shared-memory size of a converter-stage kernel, and its launch register
+// count: the register split assumes 128 registers a thread at launch; with
+// fewer, its setmaxnreg.inc could never be satisfied, so such a build is
+// refused instead of launched.
+template <typename Kernel>
+cudaError_t set_conv_attrs(Kernel kernel) {
+  cudaError_t err =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kS8SmemBytes);
+  if (err != cudaSuccess) return err;
+  cudaFuncAttributes fa;
+  err = cudaFuncGetAttributes(&fa, kernel);
+  if (err == cudaSuccess && fa.numRegs != 128) err = cudaErrorInvalidDeviceFunction;
+  return err;
+}
+
 template <bool kAmn, bool kBmn, bool kRegScales>
 cudaError_t set_smem_attrs() {
   cudaError_t err = cudaFuncSetAttribute(gemm_s8f16_kernel<kAmn, kBmn, kRegScales>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, false>,
+    err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, kConvNone>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
   if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kS8SmemBytes);
-  if (err == cudaSuccess) {
-    // the int8-operand kernel's register split assumes 128 registers a
-    // thread at launch; with fewer, its setmaxnreg.inc could never be
-    // satisfied, so such a build is refused instead of launched
-    cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, true>);
-    if (err == cudaSuccess && fa.numRegs != 128) err = cudaErrorInvalidDeviceFunction;
-  }
+    err = set_conv_attrs(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, kConvWiden>);
+  if (err == cudaSuccess && !kAmn && !kBmn)
+    err = set_conv_attrs(gemm_s8f16_pair_kernel<false, false, kRegScales, kConvQuantB>);
   return err;
 }
 
@@ -1249,26 +1378,35 @@ bool make_output_map(CUtensorMap* map, void* out, GemmOut mode, int64_t M, int64
 }
 
 template <bool kAmn, bool kBmn, bool kRegScales>
-cudaError_t launch_kernel(bool pair, bool s8, int grid, const CUtensorMap& mapA,
+cudaError_t launch_kernel(bool pair, int conv, int grid, const CUtensorMap& mapA,
                           const CUtensorMap& mapB, const CUtensorMap& mapO, const GemmParams& p,
                           cudaStream_t stream) {
-  if (s8)
-    return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, true>, dim3(grid),
-                             dim3(kS8Threads), kS8SmemBytes, stream, mapA, mapB, mapO, p);
+  if (conv == kConvWiden)
+    return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, kConvWiden>,
+                             dim3(grid), dim3(kS8Threads), kS8SmemBytes, stream, mapA, mapB, mapO,
+                             p);
+  if (conv == kConvQuantB) {
+    if constexpr (!kAmn && !kBmn)
+      return launch_overlapped(gemm_s8f16_pair_kernel<false, false, kRegScales, kConvQuantB>,
+                               dim3(grid), dim3(kS8Threads), kS8SmemBytes, stream, mapA, mapB,
+                               mapO, p);
+    return cudaErrorInvalidValue;  // B quantized in the prologue: A @ B.T only
+  }
   if (pair)
-    return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, false>, dim3(grid),
-                             dim3(kThreads), kPairSmemBytes, stream, mapA, mapB, mapO, p);
+    return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, kConvNone>,
+                             dim3(grid), dim3(kThreads), kPairSmemBytes, stream, mapA, mapB, mapO,
+                             p);
   return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn, kRegScales>, dim3(grid), dim3(kThreads),
                            kSmemBytes, stream, mapA, mapB, mapO, p);
 }
 
 template <bool kAmn, bool kBmn>
-cudaError_t launch_layout(bool pair, bool s8, bool reg_scales, int grid, const CUtensorMap& mapA,
-                          const CUtensorMap& mapB, const CUtensorMap& mapO, const GemmParams& p,
-                          cudaStream_t stream) {
+cudaError_t launch_layout(bool pair, int conv, bool reg_scales, int grid,
+                          const CUtensorMap& mapA, const CUtensorMap& mapB,
+                          const CUtensorMap& mapO, const GemmParams& p, cudaStream_t stream) {
   return reg_scales
-             ? launch_kernel<kAmn, kBmn, true>(pair, s8, grid, mapA, mapB, mapO, p, stream)
-             : launch_kernel<kAmn, kBmn, false>(pair, s8, grid, mapA, mapB, mapO, p, stream);
+             ? launch_kernel<kAmn, kBmn, true>(pair, conv, grid, mapA, mapB, mapO, p, stream)
+             : launch_kernel<kAmn, kBmn, false>(pair, conv, grid, mapA, mapB, mapO, p, stream);
 }
 
 }  // namespace
@@ -1279,6 +1417,11 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
                         const GemmDebug& dbg, cudaStream_t stream) {
   if (a_mn && !b_mn) return cudaErrorInvalidValue;  // no layout of the API needs it
   if (s8 && mode == GemmOut::kBf16Plain) return cudaErrorInvalidValue;
+  // the converter stage: int8 codes widened, or (test only) the bf16 B
+  // operand quantized in the prologue from its row scales sB
+  const int conv = s8 ? kConvWiden : dbg.quant_b ? kConvQuantB : kConvNone;
+  if (conv == kConvQuantB && (s8 || a_mn || b_mn || mode == GemmOut::kBf16Plain || !sB))
+    return cudaErrorInvalidValue;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int device = 0;
@@ -1303,14 +1446,19 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   // per-tile efficiency to win); otherwise single CTAs (128x256 tiles)
   // int8 operands always take the CTA-pair kernel (the only one that widens)
   const int64_t pair_tiles = ((M + 255) / 256) * ((N + kBN - 1) / kBN);
-  const bool pair =
-      s8 || (M > kBM && (pair_tiles >= dev.sms / 2 || K >= 8192) && !dbg.single_cta);
+  const bool pair = conv != kConvNone ||
+                    (M > kBM && (pair_tiles >= dev.sms / 2 || K >= 8192) && !dbg.single_cta);
   const bool plain = mode == GemmOut::kBf16Plain;
   CUtensorMap mapA, mapB, mapO;
   const bool maps_ok =
-      s8 ? make_raw_map(&mapA, A, a_mn, M, K) && make_raw_map(&mapB, B, b_mn, N, K)
-         : make_operand_map(&mapA, A, a_mn, M, K, kBM, plain) &&
-               make_operand_map(&mapB, B, b_mn, N, K, pair ? 128 : kBN, plain);
+      conv == kConvWiden
+          ? make_raw_map(&mapA, A, a_mn, M, K) && make_raw_map(&mapB, B, b_mn, N, K)
+      : conv == kConvQuantB
+          ? make_operand_map(&mapA, A, false, M, K, kBM, false) &&
+                encode_tensor_map_2d(&mapB, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, K, kBK,
+                                     128, CU_TENSOR_MAP_SWIZZLE_NONE)
+          : make_operand_map(&mapA, A, a_mn, M, K, kBM, plain) &&
+                make_operand_map(&mapB, B, b_mn, N, K, pair ? 128 : kBN, plain);
   if (!maps_ok || !make_output_map(&mapO, out, mode, M, N, ldo))
     return cudaErrorInvalidValue;
   GemmParams p;
@@ -1369,10 +1517,10 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   const bool reg_scales =
       mode != GemmOut::kF32Scaled && static_cast<int64_t>(p.dp_tiles) <= 2 * units;
   if (!a_mn && !b_mn)
-    return launch_layout<false, false>(pair, s8, reg_scales, grid, mapA, mapB, mapO, p, stream);
+    return launch_layout<false, false>(pair, conv, reg_scales, grid, mapA, mapB, mapO, p, stream);
   if (!a_mn)
-    return launch_layout<false, true>(pair, s8, reg_scales, grid, mapA, mapB, mapO, p, stream);
-  return launch_layout<true, true>(pair, s8, reg_scales, grid, mapA, mapB, mapO, p, stream);
+    return launch_layout<false, true>(pair, conv, reg_scales, grid, mapA, mapB, mapO, p, stream);
+  return launch_layout<true, true>(pair, conv, reg_scales, grid, mapA, mapB, mapO, p, stream);
 }
 
 }  // namespace int8mp
