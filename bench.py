@@ -534,17 +534,20 @@ def cpu_baseline(spec):
 def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
     """Square quant+scaled-mm in the three layouts: quantize A and B along K
     (by columns, codes left in place, for the operands stored K-first), then
-    the matmul in the stored layout.  L2 flushed between iterations: a 256 MB
-    write, then a read of another 256 MB buffer, so that the flush's dirty
-    lines are written back before the timed kernels start (they would
-    otherwise pay for them).  The iterations are queued back to back and the
-    events read after one synchronize at the end, so that the host's launch
-    overhead does not leave the device idle inside the timed intervals."""
+    the matmul in the stored layout.  Each of quantize, matmul and both is
+    captured in a CUDA graph and replayed (device time, no host gaps), the
+    L2 flushed before every replay: a 256 MB write, then a read of another
+    256 MB buffer, so that the flush's dirty lines are written back before
+    the timed kernels start."""
     import torch
     import int8_mixed_precision_row_gb300 as m
     from int8_mixed_precision_row_gb300 import synth
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     clean = torch.zeros(64 << 20, dtype=torch.float32, device=device)  # 256 MB, read
+
+    def flush(it):
+        flush_buf.fill_(it & 0xFF)
+        clean.max()
     out = {}
     for S in sizes:
         A, B = synth.square_inputs(S, "AxBT")
@@ -557,13 +560,7 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
         mm_ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
         for layout, (ax_a, ax_b, lay) in (("A@B.T", (0, 0, m.INT8MP_AxBT)), ("A@B", (0, 2, m.INT8MP_AxB)),
                                           ("A.T@B", (2, 2, m.INT8MP_ATxB))):
-            events = []
-            torch.cuda.synchronize()
-            for it in range(iters + 3):
-                flush.fill_(it & 0xFF)
-                clean.max()
-                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-                e[0].record()
+            def quant():
                 if ax_a == 0 and ax_b == 0:  # both by rows: one launch
                     m.int8mp_quantize_rows_batch([A, B], codes=m.INT8MP_CODES_F16, qs=[qa, qb],
                                                  scales=[sa, sb])
@@ -572,28 +569,29 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
                                               scale=sa)
                     m.int8mp_quantize_rowwise(B, axis=ax_b, codes=m.INT8MP_CODES_F16, q=qb,
                                               scale=sb)
-                e[1].record()
+
+            def mm():
                 m.int8mp_scaled_mm(qa, sa, qb, sb, layout=lay, out=Y, workspace=mm_ws)
-                e[2].record()
-                if it >= 3:
-                    events.append(e)
-            torch.cuda.synchronize()
-            tq = [e[0].elapsed_time(e[1]) for e in events]
-            tm = [e[1].elapsed_time(e[2]) for e in events]
-            q_ms, mm_ms = statistics.median(tq), statistics.median(tm)
+
+            def both():
+                quant()
+                mm()
+            q_us = graph_replay_us(quant, device, iters, flush)
+            mm_us = graph_replay_us(mm, device, iters, flush)
+            both_us = graph_replay_us(both, device, iters, flush)
             ops = 2.0 * S ** 3
             out[f"{S}:{layout}"] = {
-                "quant_mm_tops": round(ops / ((q_ms + mm_ms) * 1e-3) / 1e12, 1),
-                "mm_tops": round(ops / (mm_ms * 1e-3) / 1e12, 1),
-                "quant_ms": round(q_ms, 4), "mm_ms": round(mm_ms, 4),
-                "quant_gbs_f16codes": round(2 * S * S * 4 / (q_ms * 1e-3) / 1e9, 1)}
+                "quant_mm_tops": round(ops / (both_us * 1e-6) / 1e12, 1),
+                "mm_tops": round(ops / (mm_us * 1e-6) / 1e12, 1),
+                "quant_us": round(q_us, 2), "mm_us": round(mm_us, 2), "quant_mm_us": round(both_us, 2),
+                "quant_gbs_f16codes": round(2 * S * S * 4 / (q_us * 1e-6) / 1e9, 1)}
     return out
 
 
-def single_matmul_latency(device, iters=200):
+def single_matmul_latency(device, reps=200):
     """The 256x512 single forward matmul (X and W quantized by rows in one
-    launch, then the scaled matmul): median device time per call, from
-    events around each call, inputs resident."""
+    launch, then the scaled matmul): device time per call, the two launches
+    replayed from a CUDA graph (inputs resident; 0.5 MB, L2-resident)."""
     import torch
     import int8_mixed_precision_row_gb300 as m
     from int8_mixed_precision_row_gb300 import synth
@@ -604,19 +602,13 @@ def single_matmul_latency(device, iters=200):
     sx = torch.empty(256, dtype=torch.float32, device=device)
     sw = torch.empty(256, dtype=torch.float32, device=device)
     Y = torch.empty((256, 256), dtype=torch.bfloat16, device=device)
-    ev = []
-    for it in range(iters + 10):
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        e[0].record()
+
+    def one():
         m.int8mp_quantize_rows_batch([X, W], codes=m.INT8MP_CODES_F16, qs=[qx, qw], scales=[sx, sw])
         m.int8mp_scaled_mm(qx, sx, qw, sw, out=Y)
-        e[1].record()
-        if it >= 10:
-            ev.append(e)
-    torch.cuda.synchronize()
-    us = statistics.median([a.elapsed_time(b) for a, b in ev]) * 1e3
+    us = graph_replay_us(one, device, reps)
     return {"us_per_call": round(us, 2), "tops": round(2.0 * 256 * 256 * 512 / (us * 1e-6) / 1e12, 2),
-            "launches_per_call": 2}
+            "launches_per_call": 2, "timing": "CUDA-graph replays, device time, median"}
 
 
 def decoder_module_tok_s(spec, device, steps=5, warmup=2):
