@@ -631,7 +631,7 @@ static_assert(kS8Threads * 128 == 65536, "the S8 kernel launches with 128 regist
 constexpr int kS8SmemBytes = 1024 + kS8Stages * kPairStageBytes + kRawStages * kRawStageBytes +
                              kStagingBytes + kBarrierBytes;
 static_assert(kS8SmemBytes <= 227 * 1024, "int8-operand pair kernel shared memory");
-static_assert((2 * kS8Stages + 5 + 2 * kRawStages) * 8 + 12 <= kBarrierBytes, "barrier area");
+static_assert((3 * kS8Stages + 5 + 2 * kRawStages) * 8 + 12 <= kBarrierBytes, "barrier area");
 constexpr int kCasLimit = 4096;  // bound on the counter's compare-and-swap retries
 constexpr int kMaxSplit = 4;     // most parts a tile of the last wave is split into
 static_assert(static_cast<size_t>(kSplitTailMaxPairs) * 256 * 256 * 4 +
@@ -909,7 +909,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kConv != kConvNone ?
   const uint32_t drain_bar = bar0 + 8u * (2 * kStagesHere + 4);
   auto rfull_bar = [&](int s) { return bar0 + 8u * (2 * kStagesHere + 5 + s); };
   auto rempty_bar = [&](int s) { return bar0 + 8u * (2 * kStagesHere + 5 + kRawStages + s); };
-  constexpr int kBarsHere = 2 * kStagesHere + 5 + (kS8 ? 2 * kRawStages : 0);
+  // odd CTA: its converters' stage done, forwarded to the even CTA by one thread
+  auto cdone_bar = [&](int s) { return bar0 + 8u * (2 * kStagesHere + 5 + 2 * kRawStages + s); };
+  constexpr int kBarsHere = 2 * kStagesHere + 5 + (kS8 ? 2 * kRawStages + kStagesHere : 0);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarsHere);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -919,10 +921,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kConv != kConvNone ?
   const bool even = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesHere; ++s) {
-      // converters: both CTAs' converter warps arrive (and, quantizing B,
-      // the even producer with A's bytes); f16: the TMA bytes
-      ptx::mbar_init(full_bar(s), kConv == kConvWiden    ? 2 * kConvWarps
-                                  : kConv == kConvQuantB ? 1 + 2 * kConvWarps
+      // converters: the even CTA's converter warps arrive, and one thread of
+      // the odd CTA for all of its converters (and, quantizing B, the even
+      // producer with A's bytes); f16: the TMA bytes
+      ptx::mbar_init(full_bar(s), kConv == kConvWiden    ? kConvWarps + 1
+                                  : kConv == kConvQuantB ? 1 + kConvWarps + 1
                                                          : 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
@@ -936,6 +939,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kConv != kConvNone ?
         ptx::mbar_init(rfull_bar(s), 1);
         ptx::mbar_init(rempty_bar(s), kConvWarps);
       }
+      for (int s = 0; s < kStagesHere; ++s) ptx::mbar_init(cdone_bar(s), kConvWarps);
     }
     *abort = 0;
     *never = 0;
@@ -1087,8 +1091,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kConv != kConvNone ?
         ptx::fence_proxy_async_smem();  // the tensor core reads these stores
         __syncwarp();
         if (lane == 0) {
+          // CTA-scope arrivals only: on the even CTA's full barrier, or on
+          // the odd CTA's stage-done barrier that its forwarder passes on
           ptx::mbar_arrive(rempty_bar(rstage));
-          ptx::mbar_arrive_cluster(ptx::mapa_shared(full_bar(stage), 0));
+          ptx::mbar_arrive(even ? full_bar(stage) : cdone_bar(stage));
         }
         if (++rstage == kRawStages) {
           rstage = 0;
@@ -1192,6 +1198,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kConv != kConvNone ?
       if (!ok) raise_abort(abort, p.status);
       ptx::mma_commit_pair(drain_bar, 0x1);
       if (!ptx::mbar_wait_bounded(drain_bar, 0u, never, limit)) raise_abort(abort, p.status);
+    }
+    if constexpr (kS8) {
+      if (lane == 0 && !even) {
+        // -------------------------- forwarder (odd CTA, converter stages)
+        // once this CTA's converters are done with a stage, one arrival at
+        // cluster scope on the even CTA's full barrier carries them all
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        FragIter it(p, pair);
+        int tile, kb0, kb1;
+        while (ok && it.next(p, pair, npairs, tile, kb0, kb1)) {
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!ptx::mbar_wait_bounded(cdone_bar(stage), phase, abort, limit)) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(full_bar(stage), 0));
+            if (++stage == kStagesHere) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (!ok) raise_abort(abort, p.status);
+      }
     }
   };
   auto epilogue = [&]() {
