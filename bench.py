@@ -531,6 +531,34 @@ def cpu_baseline(spec):
 
 
 # ------------------------------------------------------------------ extras
+def graph_replay_us(fn, device, reps, flush=None):
+    """Median device time (us) of `fn`'s launches captured once in a CUDA
+    graph and replayed `reps` times, events around each replay (one host
+    call per replay, so no host gaps inside the timed interval); `flush`, if
+    given, runs before each replay outside the timed interval."""
+    import torch
+    s = torch.cuda.Stream(device=device)
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    torch.cuda.synchronize()
+    ev = []
+    for it in range(reps + 3):
+        if flush is not None:
+            flush(it)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        if it >= 3:
+            ev.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median([x.elapsed_time(y) for x, y in ev]) * 1e3
+
+
 def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
     """Square quant+scaled-mm in the three layouts: quantize A and B along K
     (by columns, codes left in place, for the operands stored K-first), then
@@ -701,7 +729,7 @@ def pass_switch_table(spec, device, steps=5, warmup=2):
 # `python bench.py --steps 2 --warmup 3 --profile-steps` (one pass per
 # launch), valid for the GEMM sources whose digest is given (reported as null
 # once they change).
-GEMM_TRAFFIC = {"bytes_per_launch": 406591612, "sources_sha256_16": "06409c425d389f84"}
+GEMM_TRAFFIC = {"bytes_per_launch": 406362163, "sources_sha256_16": "410e9bef792f97dd"}
 GEMM_SOURCES = ("gemm.cu", "ptx.cuh")
 
 
