@@ -231,8 +231,15 @@ int8mp_status int8mp_quantize_cols_absmax(const void* x, int64_t rows, int64_t c
  * Requirements: M, N >= 0; 16 <= K <= INT8MP_MAX_K; K % 16 == 0 (when M or N
  * is 0 nothing is launched); A, B 16-byte aligned; N % 8 == 0, ldo % 8 == 0
  * and out 16-byte aligned (128-bit stores); for ATxB also M % 8 == 0.  M and
- * N need not be tile multiples.  codes must be INT8MP_CODES_F16 (the
- * tensor-core container; INT8MP_CODES_S8 returns INT8MP_ERR_INVALID_ARG).
+ * N need not be tile multiples.
+ * codes: INT8MP_CODES_F16 containers are loaded by TMA straight into the
+ * tensor core's operand tiles (the fast path: the linear entry points use
+ * it).  INT8MP_CODES_S8 (`const int8_t*` codes in [-127, 127]) are loaded as
+ * int8 and widened to f16 in shared memory inside the CTA-pair kernel; the
+ * results are the same bit for bit, at roughly half the f16 path's speed.
+ * With int8 codes an operand stored [K, N] (AxB, ATxB) also needs
+ * N % 16 == 0 and one stored [K, M] (ATxB) M % 16 == 0 (16-byte row strides);
+ * otherwise INT8MP_ERR_ALIGNMENT.  A code of -128 is outside the contract.
  */
 int8mp_status int8mp_scaled_mm(const void* A, const float* sA, const void* B, const float* sB,
                                int64_t M, int64_t N, int64_t K, int8mp_layout layout,
