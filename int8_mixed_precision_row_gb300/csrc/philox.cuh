@@ -1,4 +1,4 @@
-// philox.cuh -- device Philox4x32-10 and the stochastic-rounding draw.
+// philox.cuh -- device Philox4x32-10: the random words of stochastic rounding.
 //
 // Philox4x32 with 10 rounds as published by Salmon, Moraes, Dror and Shaw,
 // "Parallel random numbers: as easy as 1, 2, 3" (SC'11): each round
@@ -115,11 +115,6 @@ __device__ __forceinline__ void philox_words8x2(const PhiloxKeys& pk, PhiloxStre
   wa[4] = c[1].x, wa[5] = c[1].y, wa[6] = c[1].z, wa[7] = c[1].w;
   wb[0] = c[2].x, wb[1] = c[2].y, wb[2] = c[2].z, wb[3] = c[2].w;
   wb[4] = c[3].x, wb[5] = c[3].y, wb[6] = c[3].z, wb[7] = c[3].w;
-}
-
-// u in [0, 1) carrying the word's top 24 bits (exact in fp32).
-__device__ __forceinline__ float sr_uniform(uint32_t word) {
-  return __uint2float_rn(word >> 8) * 0x1p-24f;
 }
 
 }  // namespace int8mp

@@ -75,28 +75,45 @@ __device__ __forceinline__ float absmax8(float m, const uint4& v) {
 }
 
 
+// Stochastic codes of two quotients v from their random words w:
+// floor(v) + (u < v - floor(v)) with u = (w >> 8) 2^-24, computed as
+// ceil(v - u).  With f = floor(v) and fr = v - f in [0, 1), fr - u lies in
+// (-1, 1) and its ceiling is 1 exactly when u < fr, so ceil(v - u) =
+// f + (u < fr).  One fused multiply-add rounded upwards gives y = RU(v - u)
+// (u's product is exact), and ceil(y) = ceil(v - u) because that integer is
+// a float at least v - u, and rounding upwards never passes it.  The ceiling
+// itself is y + 1.5 * 2^23 rounded upwards (for |y| < 2^22 the sum lies in
+// [2^23, 2^24), where floats are the integers) minus the constant again,
+// exactly; a zero code comes out as +0.  |v| stays below 128 for every group
+// scale, so the codes lie in [-128, 128] before the clamp.
 // kClamp false: the caller clamps afterwards (f16 codes, as packed half2
-// min/max: every unclamped code is an integer or +-inf after the f16
-// conversion, which is monotonic, so clamping after it gives the same codes).
+// min/max: every unclamped code is an integer in [-128, 128], exact in f16).
 template <bool kClamp>
-__device__ __forceinline__ float code_sr(float v, uint32_t word) {
-  const float f = floorf(v);
-  const float fr = __fsub_rn(v, f);
-  const float q = (sr_uniform(word) < fr) ? __fadd_rn(f, 1.0f) : f;
-  return kClamp ? fminf(fmaxf(q, -127.0f), 127.0f) : q;
+__device__ __forceinline__ float2 code_sr2(float v0, float v1, uint32_t w0, uint32_t w1) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  const float2 k = make_float2(__uint2float_rn(w0 >> 8), __uint2float_rn(w1 >> 8));
+  const float2 y = __ffma2_ru(k, make_float2(-0x1p-24f, -0x1p-24f), make_float2(v0, v1));
+  const float2 t = __fadd2_ru(y, make_float2(kMagic, kMagic));
+  const float2 q = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
+  if (!kClamp) return q;
+  return make_float2(fminf(fmaxf(q.x, -127.0f), 127.0f), fminf(fmaxf(q.y, -127.0f), 127.0f));
 }
 
-// Eight codes from eight quotients (elements n0 .. n0+7 of the SR stream).
-// normal_scales: every element's group scale is at least 2^-126.
-// kSrClamp false: stochastic codes are left unclamped for a later half2 clamp.
 // Eight stochastic codes from eight quotients and their random words.
 template <bool kSrClamp>
 __device__ __forceinline__ void codes_sr8(const float (&v)[8], const uint32_t (&w)[8],
                                           float (&c)[8]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) c[i] = code_sr<kSrClamp>(v[i], w[i]);
+  for (int i = 0; i < 4; ++i) {
+    const float2 q = code_sr2<kSrClamp>(v[2 * i], v[2 * i + 1], w[2 * i], w[2 * i + 1]);
+    c[2 * i] = q.x;
+    c[2 * i + 1] = q.y;
+  }
 }
 
+// Eight codes from eight quotients (elements n0 .. n0+7 of the SR stream).
+// normal_scales: every element's group scale is at least 2^-126.
+// kSrClamp false: stochastic codes are left unclamped for a later half2 clamp.
 template <bool SR, bool kSrClamp = true>
 __device__ __forceinline__ void codes_of(const float (&v)[8], const PhiloxKeys& keys,
                                          PhiloxStream st, uint64_t n0, bool normal_scales,
@@ -104,8 +121,7 @@ __device__ __forceinline__ void codes_of(const float (&v)[8], const PhiloxKeys& 
   if (SR) {
     uint32_t w[8];
     philox_words8(keys, st, n0, w);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = code_sr<kSrClamp>(v[i], w[i]);
+    codes_sr8<kSrClamp>(v, w, c);
   } else if (normal_scales) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
