@@ -81,6 +81,23 @@ __device__ __forceinline__ bool div8_each_try(const float (&x)[8], const float (
   return all_fast;
 }
 
+// The same with the two-lane instructions, pairing the scales of columns
+// 2i and 2i+1 (for the stochastic column codes, whose kernels are bound by
+// instruction issue rather than memory).
+__device__ __forceinline__ bool div8_each_try2(const float (&x)[8], const float (&s)[8],
+                                               const float (&r)[8], bool all_fast,
+                                               float (&v)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 q = div2_fast(make_float2(x[2 * i], x[2 * i + 1]),
+                               make_float2(s[2 * i], s[2 * i + 1]),
+                               make_float2(r[2 * i], r[2 * i + 1]));
+    v[2 * i] = q.x;
+    v[2 * i + 1] = q.y;
+  }
+  return all_fast;
+}
+
 // IEEE quotients (a zero scale gives 0: the group is all zero).
 __device__ __forceinline__ void div8_ieee(const float (&x)[8], float s, float (&v)[8]) {
 #pragma unroll

@@ -609,21 +609,68 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
     for (int j = 0; j < 8; ++j) scale_out[c + j] = s[j];
   }
   const uint16_t* xc = x + c;
+  auto put = [&](int64_t row, const float (&cd)[8]) {
+    typename P::Vec out = P::pack(cd);
+    if (kHalfClamp) out = clamp_half8(out);
+    if (in_bounds(row < rows, status))
+      *reinterpret_cast<typename P::Vec*>(q + row * cols + c) = out;
+  };
+  auto load_row = [&](int64_t row) {
+    return row < r1 && in_bounds(row < rows, status)
+               ? __ldg(reinterpret_cast<const uint4*>(xc + row * ld))
+               : make_uint4(0u, 0u, 0u, 0u);
+  };
+  if (SR && (sr.offset & 3u) == 0) {
+    // Stochastic codes, every group of eight starting a Philox block: two
+    // rows at a time, the next two rows' loads issued before this pair's
+    // generator and codes, so that the long computation per pair hides the
+    // load latency instead of waiting for it.  Input and code pointers and
+    // the element counter of row rr advance by additions.
+    const int64_t row0 = r0 + warp;
+    const uint16_t* xp = xc + row0 * ld;
+    typename P::Vec* qp = reinterpret_cast<typename P::Vec*>(q + row0 * cols + c);
+    uint64_t n = sr.offset + static_cast<uint64_t>(row0 * cols + c);
+    const int64_t xstep = 8 * ld, qstep = cols;  // 8 rows of input; 8 rows of codes, in vectors
+    const uint64_t nstep = 8u * static_cast<uint64_t>(cols);
+    auto ld_at = [&](const uint16_t* ptr, int64_t row) {
+      return row < r1 && in_bounds(row < rows, status)
+                 ? __ldg(reinterpret_cast<const uint4*>(ptr))
+                 : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto put_at = [&](typename P::Vec* dst, int64_t row, const float (&cd)[8]) {
+      typename P::Vec out = P::pack(cd);
+      if (kHalfClamp) out = clamp_half8(out);
+      if (in_bounds(row < rows, status)) *dst = out;
+    };
+    uint4 cur0 = ld_at(xp, row0), cur1 = ld_at(xp + xstep, row0 + 8);
+#pragma unroll 2
+    for (int64_t rr = row0; rr < r1; rr += 16) {
+      const uint4 nxt0 = ld_at(xp + 2 * xstep, rr + 16), nxt1 = ld_at(xp + 3 * xstep, rr + 24);
+      uint32_t w_a[8], w_b[8];
+      philox_words8x2(sr.keys, sr.stream, n, n + nstep, w_a, w_b);
+      float f[8], v[8], cd[8];
+      unpack8(cur0, f);
+      if (!div8_each_try2(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
+      codes_sr8<!kHalfClamp>(v, w_a, cd);
+      put_at(qp, rr, cd);
+      if (rr + 8 < r1) {
+        unpack8(cur1, f);
+        if (!div8_each_try2(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
+        codes_sr8<!kHalfClamp>(v, w_b, cd);
+        put_at(qp + qstep, rr + 8, cd);
+      }
+      cur0 = nxt0;
+      cur1 = nxt1;
+      xp += 2 * xstep;
+      qp += 2 * qstep;
+      n += 2 * nstep;
+    }
+    return;
+  }
   for (int64_t rr = r0 + warp; rr < r1; rr += kNatUnroll * 8) {
     uint4 a[kNatUnroll];
 #pragma unroll
-    for (int u = 0; u < kNatUnroll; ++u) {
-      const int64_t row = rr + u * 8;
-      a[u] = row < r1 && in_bounds(row < rows, status)
-                 ? __ldg(reinterpret_cast<const uint4*>(xc + row * ld))
-                 : make_uint4(0u, 0u, 0u, 0u);
-    }
-    auto put = [&](int64_t row, const float (&cd)[8]) {
-      typename P::Vec out = P::pack(cd);
-      if (kHalfClamp) out = clamp_half8(out);
-      if (in_bounds(row < rows, status))
-        *reinterpret_cast<typename P::Vec*>(q + row * cols + c) = out;
-    };
+    for (int u = 0; u < kNatUnroll; ++u) a[u] = load_row(rr + u * 8);
 #pragma unroll
     for (int u = 0; u < kNatUnroll; u += 2) {
       const int64_t row_a = rr + u * 8, row_b = row_a + 8;
