@@ -110,15 +110,18 @@ COL_NAT_SHAPES = [(256, 512), (8, 8), (77, 136), (1032, 64), (520, 2048), (16, 4
                   (3001, 264), (1, 5632)]
 
 
+@pytest.mark.parametrize("off", [2**35 + 3, 2**35 + 4])
 @pytest.mark.parametrize("codes", [m.INT8MP_CODES_S8, m.INT8MP_CODES_F16])
 @pytest.mark.parametrize("mode", [m.INT8MP_RNE, m.INT8MP_SR])
 @pytest.mark.parametrize("shape", COL_NAT_SHAPES)
-def test_quantize_cols_in_input_layout_bit_exact(shape, mode, codes):
+def test_quantize_cols_in_input_layout_bit_exact(shape, mode, codes, off):
     # column groups with the codes left in x's layout: the same numbers as
-    # the oracle's column quantization, which it returns transposed
+    # the oracle's column quantization, which it returns transposed (an
+    # offset that is a multiple of 4 starts every group of eight at a Philox
+    # block, the stochastic kernel's two-rows-at-a-time path)
     rows, cols = shape
     x = _edge_input(rows, cols, seed=5 * rows + cols)
-    seed, off, sid = 4242, 2**35 + 3, 4
+    seed, sid = 4242, 4
     q, s = m.int8mp_quantize_rowwise(_dev(x), axis=m.INT8MP_GROUP_COLS, mode=mode, seed=seed,
                                      offset=off, stream_id=sid, codes=codes)
     assert tuple(q.shape) == (rows, cols)
