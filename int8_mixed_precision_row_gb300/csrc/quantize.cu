@@ -236,6 +236,51 @@ __device__ __forceinline__ void quantize_two(const uint4& a, const uint4& b, boo
   }
 }
 
+// The same for a row whose scale is in the fast range of the division (so
+// also a normal number), with the stochastic words' blocks aligned (na, nb
+// multiples of 4): no branch inside, so that the generator, the divisions
+// and the codes of the two vectors form one block of independent work.
+template <typename CodeT, bool SR>
+__device__ __forceinline__ void quantize_two_fast(const uint4& a, const uint4& b, bool has_b,
+                                                  const ScaleDiv& d, const PhiloxKeys& keys,
+                                                  PhiloxStream st, uint64_t na, uint64_t nb,
+                                                  typename Pack8<CodeT>::Vec* qa,
+                                                  typename Pack8<CodeT>::Vec* qb) {
+  constexpr bool kHalfClamp = SR && std::is_same<CodeT, __half>::value;
+  float fa[8], fb[8], va[8], vb[8], c[8];
+  uint32_t wa[8], wb[8];
+  if (SR) philox_words8x2(keys, st, na, nb, wa, wb);
+  unpack8(a, fa);
+  unpack8(b, fb);
+  (void)div8_try(fa, d, va);
+  (void)div8_try(fb, d, vb);
+  if (SR) {
+    codes_sr8<!kHalfClamp>(va, wa, c);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 qv = code_rne_normal_scale2(make_float2(va[2 * i], va[2 * i + 1]));
+      c[2 * i] = qv.x;
+      c[2 * i + 1] = qv.y;
+    }
+  }
+  *qa = Pack8<CodeT>::pack(c);
+  if (kHalfClamp) *qa = clamp_half8(*qa);
+  if (SR) {
+    codes_sr8<!kHalfClamp>(vb, wb, c);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 qv = code_rne_normal_scale2(make_float2(vb[2 * i], vb[2 * i + 1]));
+      c[2 * i] = qv.x;
+      c[2 * i + 1] = qv.y;
+    }
+  }
+  typename Pack8<CodeT>::Vec pb = Pack8<CodeT>::pack(c);
+  if (kHalfClamp) pb = clamp_half8(pb);
+  if (has_b) *qb = pb;
+}
+
 // Column absmax alongside the row groups (kColMax): each thread owns the same
 // vectors first + k*step, k < kColVecs, of every row it sees and keeps their
 // running |x| maxima as packed bf16 pairs (|x| of a bf16 is a bf16, and
@@ -380,6 +425,20 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
     const bool normal = scale_is_normal(s);
     typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + r * cols);
     const uint64_t nrow = sr_offset + static_cast<uint64_t>(r * cols);
+    if (d.fast && (nrow & 3u) == 0) {
+      for (int v = first; v < nvec; v += 2 * step) {
+        const int v2 = v + step;
+        const bool has2 = v2 < nvec;
+        if (!in_bounds(r < rows && (has2 ? v2 : v) < nvec &&
+                           ((has2 ? v2 : v) + 1) * 16u <= slot_bytes, status))
+          continue;
+        const uint4 a = rowv[v];
+        const uint4 bb = has2 ? rowv[v2] : make_uint4(0u, 0u, 0u, 0u);
+        quantize_two_fast<CodeT, SR>(a, bb, has2, d, sr.keys, sr_stream, nrow + 8u * v,
+                                     nrow + 8u * v2, qr + v, qr + (has2 ? v2 : v));
+      }
+      continue;
+    }
     for (int v = first; v < nvec; v += 2 * step) {
       const int v2 = v + step;
       const bool has2 = v2 < nvec;
@@ -642,29 +701,44 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
       if (kHalfClamp) out = clamp_half8(out);
       if (in_bounds(row < rows, status)) *dst = out;
     };
-    uint4 cur0 = ld_at(xp, row0), cur1 = ld_at(xp + xstep, row0 + 8);
+    // (every scale in the division's fast range, the usual case: a loop with
+    // no fallback branch in it)
+    auto run = [&](auto fast_tag) {
+      constexpr bool kFast = decltype(fast_tag)::value;
+      auto divide = [&](const float (&f)[8], float (&v)[8]) {
+        if (kFast)
+          (void)div8_each_try2(f, s, r, true, v);
+        else if (!div8_each_try2(f, s, r, all_fast, v))
+          div8_each_ieee(f, s, v);
+      };
+      uint4 cur0 = ld_at(xp, row0), cur1 = ld_at(xp + xstep, row0 + 8);
 #pragma unroll 2
-    for (int64_t rr = row0; rr < r1; rr += 16) {
-      const uint4 nxt0 = ld_at(xp + 2 * xstep, rr + 16), nxt1 = ld_at(xp + 3 * xstep, rr + 24);
-      uint32_t w_a[8], w_b[8];
-      philox_words8x2(sr.keys, sr.stream, n, n + nstep, w_a, w_b);
-      float f[8], v[8], cd[8];
-      unpack8(cur0, f);
-      if (!div8_each_try2(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
-      codes_sr8<!kHalfClamp>(v, w_a, cd);
-      put_at(qp, rr, cd);
-      if (rr + 8 < r1) {
-        unpack8(cur1, f);
-        if (!div8_each_try2(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
-        codes_sr8<!kHalfClamp>(v, w_b, cd);
-        put_at(qp + qstep, rr + 8, cd);
+      for (int64_t rr = row0; rr < r1; rr += 16) {
+        const uint4 nxt0 = ld_at(xp + 2 * xstep, rr + 16), nxt1 = ld_at(xp + 3 * xstep, rr + 24);
+        uint32_t w_a[8], w_b[8];
+        philox_words8x2(sr.keys, sr.stream, n, n + nstep, w_a, w_b);
+        float f[8], v[8], cd[8];
+        unpack8(cur0, f);
+        divide(f, v);
+        codes_sr8<!kHalfClamp>(v, w_a, cd);
+        put_at(qp, rr, cd);
+        if (rr + 8 < r1) {
+          unpack8(cur1, f);
+          divide(f, v);
+          codes_sr8<!kHalfClamp>(v, w_b, cd);
+          put_at(qp + qstep, rr + 8, cd);
+        }
+        cur0 = nxt0;
+        cur1 = nxt1;
+        xp += 2 * xstep;
+        qp += 2 * qstep;
+        n += 2 * nstep;
       }
-      cur0 = nxt0;
-      cur1 = nxt1;
-      xp += 2 * xstep;
-      qp += 2 * qstep;
-      n += 2 * nstep;
-    }
+    };
+    if (all_fast)
+      run(std::true_type{});
+    else
+      run(std::false_type{});
     return;
   }
   for (int64_t rr = r0 + warp; rr < r1; rr += kNatUnroll * 8) {
