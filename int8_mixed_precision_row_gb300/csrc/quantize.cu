@@ -636,7 +636,7 @@ constexpr int kNatUnroll = 4;
 static_assert(kNatUnroll % 2 == 0, "stochastic codes go two rows at a time");
 
 template <typename CodeT, bool SR, bool kFromAbsmax>
-__global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
+__global__ void __launch_bounds__(kThreads, SR ? 2 : 3) quant_cols_nat_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
     int64_t rows_per_block, const float* __restrict__ in, float* __restrict__ scale_out,
     CodeT* __restrict__ q, SrArgs sr, unsigned int* status) {
@@ -739,6 +739,32 @@ __global__ void __launch_bounds__(kThreads) quant_cols_nat_kernel(
       run(std::true_type{});
     else
       run(std::false_type{});
+    return;
+  }
+  if (!SR && all_fast && normal) {
+    // nearest-even codes, every scale in the division's fast range (and a
+    // normal number): no branch per row
+    for (int64_t rr = r0 + warp; rr < r1; rr += kNatUnroll * 8) {
+      uint4 a[kNatUnroll];
+#pragma unroll
+      for (int u = 0; u < kNatUnroll; ++u) a[u] = load_row(rr + u * 8);
+#pragma unroll
+      for (int u = 0; u < kNatUnroll; ++u) {
+        const int64_t row = rr + u * 8;
+        if (row < r1) {
+          float f[8], v[8], cd[8];
+          unpack8(a[u], f);
+          (void)div8_each_try(f, s, r, true, v);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 qv = code_rne_normal_scale2(make_float2(v[2 * i], v[2 * i + 1]));
+            cd[2 * i] = qv.x;
+            cd[2 * i + 1] = qv.y;
+          }
+          put(row, cd);
+        }
+      }
+    }
     return;
   }
   for (int64_t rr = r0 + warp; rr < r1; rr += kNatUnroll * 8) {
