@@ -559,6 +559,50 @@ def graph_replay_us(fn, device, reps, flush=None):
     return statistics.median([x.elapsed_time(y) for x, y in ev]) * 1e3
 
 
+def graph_sequence_us(fn, device, n=20, reps=5, flush=None):
+    """Device time (us) per call of `fn` when n calls run back to back: n
+    calls (each after `flush`, if given) captured in one CUDA graph and
+    replayed, the time of a graph of the n flushes alone subtracted, divided
+    by n (median of `reps` replays each).  Unlike graph_replay_us, one call's
+    launch overlaps the end of the work before it, as in a stream of calls."""
+    import torch
+    s = torch.cuda.Stream(device=device)
+
+    def graph_of(body):
+        body()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            body()
+        torch.cuda.synchronize()
+        return g
+
+    def timed(g):
+        ts = []
+        for _ in range(reps + 1):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts[1:])
+
+    def calls():
+        for i in range(n):
+            if flush is not None:
+                flush(i)
+            fn()
+
+    def flushes():
+        for i in range(n):
+            flush(i)
+    full = timed(graph_of(calls))
+    base = timed(graph_of(flushes)) if flush is not None else 0.0
+    return (full - base) / n
+
+
 def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
     """Square quant+scaled-mm in the three layouts: quantize A and B along K
     (by columns, codes left in place, for the operands stored K-first), then
@@ -607,12 +651,18 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
             q_us = graph_replay_us(quant, device, iters, flush)
             mm_us = graph_replay_us(mm, device, iters, flush)
             both_us = graph_replay_us(both, device, iters, flush)
+            seq_us = graph_sequence_us(both, device, flush=flush)
             ops = 2.0 * S ** 3
             out[f"{S}:{layout}"] = {
                 "quant_mm_tops": round(ops / (both_us * 1e-6) / 1e12, 1),
                 "mm_tops": round(ops / (mm_us * 1e-6) / 1e12, 1),
                 "quant_us": round(q_us, 2), "mm_us": round(mm_us, 2), "quant_mm_us": round(both_us, 2),
-                "quant_gbs_f16codes": round(2 * S * S * 4 / (q_us * 1e-6) / 1e9, 1)}
+                "quant_gbs_f16codes": round(2 * S * S * 4 / (q_us * 1e-6) / 1e9, 1),
+                "quant_mm_us_in_sequence": round(seq_us, 2),
+                "quant_mm_tops_in_sequence": round(ops / (seq_us * 1e-6) / 1e12, 1)}
+    out["timing"] = ("each of quantize, matmul and both replayed alone from a CUDA graph after "
+                     "an L2 flush (median device time); *_in_sequence: 20 flushed calls in one "
+                     "graph, the flushes' own time subtracted, per call")
     return out
 
 
@@ -635,8 +685,14 @@ def single_matmul_latency(device, reps=200):
         m.int8mp_quantize_rows_batch([X, W], codes=m.INT8MP_CODES_F16, qs=[qx, qw], scales=[sx, sw])
         m.int8mp_scaled_mm(qx, sx, qw, sw, out=Y)
     us = graph_replay_us(one, device, reps)
-    return {"us_per_call": round(us, 2), "tops": round(2.0 * 256 * 256 * 512 / (us * 1e-6) / 1e12, 2),
-            "launches_per_call": 2, "timing": "CUDA-graph replays, device time, median"}
+    seq = graph_sequence_us(one, device)
+    ops = 2.0 * 256 * 256 * 512
+    return {"us_per_call": round(us, 2), "tops": round(ops / (us * 1e-6) / 1e12, 2),
+            "us_per_call_in_sequence": round(seq, 2),
+            "tops_in_sequence": round(ops / (seq * 1e-6) / 1e12, 2),
+            "launches_per_call": 2,
+            "timing": "CUDA-graph replays of one call, device time, median; *_in_sequence: 20 "
+                      "calls in one graph, per call"}
 
 
 def decoder_module_tok_s(spec, device, steps=5, warmup=2):

@@ -757,127 +757,6 @@ def _bf16_pass_close(got_t, ref_bits, a, b, what):
     bf16_pass_close(got_t, ref_bits, a, b, what)
 
 
-@pytest.mark.parametrize("flags", [(1, 1, 1), (1, 0, 1), (1, 1, 0), (0, 1, 1)])
-@pytest.mark.parametrize("shape", [(256, 256, 512), (1040, 64, 48), (48, 5632, 2048)])
-def test_linear_with_saved_absmax_matches_plain_passes(shape, flags):
-    T, N, K = shape
-    X = synth.bf16_normal((T, K), 14, outlier_frac=0.005, outlier_scale=30.0)
-    W = synth.bf16_normal((N, K), 24, std=0.02)
-    dY = synth.bf16_normal((T, N), 34, std=1e-3)
-    f, gi, gw = flags
-    cfg = m.linear_cfg(mode=m.INT8MP_SR, seed=9, offset=3, int8_fwd=f, int8_grad_in=gi,
-                       int8_grad_w=gw)
-    Xd, Wd, dYd = _dev(X), _dev(W), _dev(dY)
-    absmax = torch.full((2 * K,), -1.0, dtype=torch.float32, device=DEV)  # overwritten
-    Y1 = m.int8mp_linear_fwd_save(Xd, Wd, absmax, cfg)
-    dX1, dW1 = m.int8mp_linear_bwd_saved(dYd, Xd, Wd, absmax, cfg)
-    Y0 = m.int8mp_linear_fwd(Xd, Wd, cfg)
-    dX0, dW0 = m.int8mp_linear_bwd(dYd, Xd, Wd, cfg)
-    assert m.int8mp_poll_device_status() == m.INT8MP_OK
-    zero = np.zeros(K, dtype=np.int32)
-    np.testing.assert_array_equal(_f32_bits(absmax[:K]), _col_absmax_bits(X) if gw else zero)
-    np.testing.assert_array_equal(_f32_bits(absmax[K:]), _col_absmax_bits(W) if gi else zero)
-    for a, b, what in ((Y1, Y0, "Y"), (dX1, dX0, "dX"), (dW1, dW0, "dW")):
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), what
-    if f and gi and gw:
-        Yr = oracle.linear_fwd(bf16_bits(X), bf16_bits(W), mode=oracle.SR, seed=9, offset=3)
-        dXr, dWr = oracle.linear_bwd(bf16_bits(dY), bf16_bits(X), bf16_bits(W), mode=oracle.SR,
-                                     seed=9, offset=3)
-        assert_bf16_equal(Y1, Yr, "saved forward")
-        assert_bf16_equal(dX1, dXr, "saved grad input")
-        assert_bf16_equal(dW1, dWr, "saved grad weight")
-
-
-def test_single_forward_matmul_256x512():
-    X, W = synth.single_matmul_inputs()
-    Y = m.int8mp_linear_fwd(_dev(X), _dev(W))
-    assert_bf16_equal(Y, oracle.linear_fwd(bf16_bits(X), bf16_bits(W)), "256x512 forward")
-
-
-def test_bwd_skips_passes_on_null_outputs():
-    T, N, K = 64, 48, 32
-    X = synth.bf16_normal((T, K), 1)
-    W = synth.bf16_normal((N, K), 2, std=0.02)
-    dY = synth.bf16_normal((T, N), 3, std=1e-3)
-    dX, dW = m.int8mp_linear_bwd(_dev(dY), _dev(X), _dev(W), want_dw=False)
-    assert dW is None
-    dXr, _ = oracle.linear_bwd(bf16_bits(dY), bf16_bits(X), bf16_bits(W), want_dw=False)
-    assert_bf16_equal(dX, dXr, "grad_input only")
-
-
-def test_empty_and_zero_contraction():
-    z = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
-    q, s = m.int8mp_quantize_rowwise(z, axis=0)
-    assert q.shape == (0, 64)
-    a = torch.empty((32, 0), dtype=torch.float16, device=DEV)
-    b = torch.empty((16, 0), dtype=torch.float16, device=DEV)
-    out = torch.full((32, 16), 7.0, dtype=torch.bfloat16, device=DEV)
-    sa = torch.ones(32, device=DEV)
-    sb = torch.ones(16, device=DEV)
-    m.int8mp_scaled_mm(a, sa, b, sb, out=out)
-    assert torch.count_nonzero(out) == 0
-
-
-def test_bounded_wait_reports_timeout_and_context_survives():
-    M, N, K = 256, 512, 256
-    a, b = _rand_codes(M, K, 5), _rand_codes(N, K, 6)
-    ad, bd = _dev(a.half()), _dev(b.half())
-    out = torch.zeros((M, N), dtype=torch.int32, device=DEV)
-    assert m.int8mp_poll_device_status() == m.INT8MP_OK
-    st = m.int8mp_debug_mm_s32_drop_first_load(ad, bd, out, wait_limit_ms=100)
-    assert st == m.INT8MP_OK
-    assert m.int8mp_poll_device_status() == m.INT8MP_ERR_TIMEOUT
-    assert m.int8mp_poll_device_status() == m.INT8MP_OK  # the word was cleared
-    # the CUDA context is intact: a normal launch still runs and is exact
-    acc = m.int8mp_mm_s32(ad, bd).cpu().numpy()
-    np.testing.assert_array_equal(acc, oracle.mm_s32(a.numpy(), b.numpy(), M, N, K))
-    assert m.int8mp_poll_device_status() == m.INT8MP_OK
-
-
-def test_division_gives_ieee_codes_for_every_bf16_pair():
-    # codes from the quantizers' reciprocal-and-FMA quotient against codes
-    # from __fdiv_rn on every (absmax, x) pair of bf16 values with absmax > 0
-    # finite and |x| <= absmax: nearest-even bit for bit, stochastic for
-    # every possible draw
-    bad, pairs, fast, qdiff, first = m.int8mp_debug_check_division()
-    print(f"division check: {pairs} pairs, {fast} on the fast path, {qdiff} quotients differ "
-          f"in some bit, {bad} codes differ")
-    assert pairs > 1_000_000_000
-    assert fast > 200_000_000  # the fast path is exercised (scales in [2^-60, 2^10])
-    assert bad == 0, f"{bad} codes differ; first at bf16 bits (absmax, x) = {first}"
-
-
-@pytest.mark.parametrize("axis", [0, 1])
-def test_quantize_division_ties_bit_exact(axis):
-    # bf16 pairs where x / s sits on (or within rounding of) k + 1/2 and a
-    # reciprocal multiply would round the other way than IEEE division
-    from test_oracle_quantize import DIVISION_TIES
-    rows = np.zeros((len(DIVISION_TIES), 8), dtype=np.float32)
-    for i, (amax, xv) in enumerate(DIVISION_TIES):
-        rows[i, 0], rows[i, 1] = amax, xv
-        rows[i, 2:] = np.float32(xv) * np.array([1, -1, 0.5, -0.5, 0.25, 3], dtype=np.float32)
-    x = torch.from_numpy(rows).to(torch.bfloat16)
-    if axis == 1:
-        x = x.t().contiguous()
-    for codes in (m.INT8MP_CODES_S8, m.INT8MP_CODES_F16):
-        q, s = m.int8mp_quantize_rowwise(_dev(x), axis=axis, codes=codes)
-        qr, sr = oracle.quantize(bf16_bits(x), axis=axis)
-        np.testing.assert_array_equal(_f32_bits(s), sr.view(np.int32))
-        np.testing.assert_array_equal(_codes_np(q), qr)
-
-
-def _bf16_pass_close(got_t, ref_bits, a, b, what):
-    """BF16 pass: the tensor core accumulates in fp32 in its own order, the
-    oracle in fp64; allow two bf16 ulps plus the fp32 accumulation bound
-    K 2^-23 sum |a||b| per output."""
-    got = got_t.cpu().float().double()
-    ref = torch.from_numpy(bits_to_f32(ref_bits).astype(np.float64))
-    K = a.shape[1]
-    bound = 2.0 ** -7 * ref.abs() + K * 2.0 ** -23 * (a.abs().double() @ b.abs().double().T)
-    bad = (got - ref).abs() > bound
-    assert not bool(bad.any()), f"{what}: {int(bad.sum())} outputs outside the bound"
-
-
 @pytest.mark.parametrize("flags", [(0, 0, 0), (1, 0, 0), (1, 1, 0), (0, 1, 1), (1, 0, 1)])
 def test_linear_per_pass_switches(flags):
     T, N, K = 256, 192, 320
