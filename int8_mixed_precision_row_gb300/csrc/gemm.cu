@@ -24,16 +24,18 @@
 // 64-column TMA boxes and is described to the tensor core as such, so that
 // column-grouped codes need no transposition.
 //
-// Structure (one persistent CTA per SM, 320 threads):
+// Structure (one persistent CTA per SM, 320 threads; tiles of 128 x 256, or
+// 128 x 128 for launches with few tiles):
 //   warp 0      TMA producer (one thread): 4-stage ring of 128x64 A and
-//               256x64 B f16 tiles, 128-byte swizzled, one mbarrier per stage
+//               256x64 B f16 tiles (6 stages with 128x64 B tiles), 128-byte
+//               swizzled, one mbarrier per stage
 //   warp 1      TMEM allocator + MMA issuer (one thread): 4 MMAs of
-//               128x256x16 per stage, commit frees the stage; commit after
-//               each K-chunk hands the accumulator to the epilogue
+//               128x256x16 (128x128x16) per stage, commit frees the stage;
+//               commit after each K-chunk hands the accumulator to the epilogue
 //   warps 2-9   epilogue: warp w reads TMEM lanes 32*(w%4).. and one half
-//               (128 columns) of the tile, keeps 128 int32 totals per thread,
-//               and writes the finished tile through a 4 KB shared-memory
-//               staging buffer with TMA tensor stores
+//               of the tile's columns, keeps an int32 total per column and
+//               thread, and writes the finished tile through a 4 KB
+//               shared-memory staging buffer with TMA tensor stores
 // Every mbarrier wait is bounded (wall clock); a wait that runs out raises
 // the CTA abort flag and the device status word, every role winds down,
 // outstanding copies and MMAs are waited for (bounded), TMEM is freed.
@@ -55,21 +57,16 @@ namespace int8mp {
 namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;  // kBK f16 = 128 bytes per row
-constexpr int kStages = 4;
 constexpr int kChunkBlocks = 16;  // 16 * 64 = 1024 terms per exact fp32 chunk
 constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBN * kBK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-constexpr uint32_t kTmemCols = 512;  // two 128x256 fp32 accumulators
+constexpr uint32_t kTmemCols = 512;  // CTA pair: two 128x256 fp32 accumulators per CTA
 constexpr int kBarrierBytes = 256;
 constexpr int kMnBlockBytes = 64 * kBK * 2;  // one 64 (M or N) x 64 (K) MN-major box
 // each epilogue warp stages its outputs in 4 KB: one 32-row x 128-byte box
 constexpr int kStoreBoxBytes = 32 * 128;
 constexpr int kStagingBytes = kEpiWarps * kStoreBoxBytes;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kBarrierBytes;
-static_assert(kSmemBytes <= 227 * 1024, "single-CTA kernel shared memory");
 
 struct GemmParams {
   const float* sA;
@@ -201,10 +198,11 @@ __device__ __forceinline__ void store_vec8(const GemmParams& p, int64_t row, int
 // from tensor memory into the int32 totals; every fp32 value is an exact
 // integer below 2^24 in magnitude.  Plain bf16 launches (one chunk per tile)
 // keep the fp32 bit patterns themselves.
-__device__ __forceinline__ void drain_chunk(uint32_t taddr, int32_t (&tot)[128], bool plain) {
+template <int kCols>
+__device__ __forceinline__ void drain_chunk(uint32_t taddr, int32_t (&tot)[kCols], bool plain) {
   if (plain) {
 #pragma unroll
-    for (int sub = 0; sub < 8; ++sub) {
+    for (int sub = 0; sub < kCols / 16; ++sub) {
       uint32_t r[16];
       ptx::tmem_ld_16cols(taddr + sub * 16, r);
       ptx::tmem_wait_ld();
@@ -214,7 +212,7 @@ __device__ __forceinline__ void drain_chunk(uint32_t taddr, int32_t (&tot)[128],
     return;
   }
 #pragma unroll
-  for (int sub = 0; sub < 8; ++sub) {
+  for (int sub = 0; sub < kCols / 16; ++sub) {
     uint32_t r[16];
     ptx::tmem_ld_16cols(taddr + sub * 16, r);
     ptx::tmem_wait_ld();
@@ -236,7 +234,7 @@ struct TileScales {
   float sa;
   float sb[4];
 };
-template <bool kRegScales>
+template <bool kRegScales, int kCols = 128>
 __device__ __forceinline__ TileScales load_tile_scales(const GemmParams& p, int64_t row0,
                                                        int64_t col0) {
   TileScales t{0.0f, {0.0f, 0.0f, 0.0f, 0.0f}};
@@ -244,7 +242,7 @@ __device__ __forceinline__ TileScales load_tile_scales(const GemmParams& p, int6
   const int lane = threadIdx.x & 31;
   if (row0 + lane < p.M) t.sa = __ldg(p.sA + row0 + lane);
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
+  for (int q = 0; q < kCols / 32; ++q)
     if (col0 + 32 * q + lane < p.N) t.sb[q] = __ldg(p.sB + col0 + 32 * q + lane);
   return t;
 }
@@ -260,10 +258,10 @@ __device__ __forceinline__ TileScales load_tile_scales(const GemmParams& p, int6
 // and columns outside the output; a box that starts at or past column N is
 // not stored.  Before the buffer is rewritten, lane 0 waits until the
 // previous store has read it.
-template <bool kRegScales>
+template <bool kRegScales, int kCols>
 __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtensorMap* map,
                                                uint32_t buf, int64_t row0, int64_t col0,
-                                               const TileScales& ts, const int32_t (&tot)[128]) {
+                                               const TileScales& ts, const int32_t (&tot)[kCols]) {
   if (row0 >= p.M) return;
   const int lane = threadIdx.x & 31;
   const int64_t row = row0 + lane;
@@ -283,7 +281,7 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
   };
   if (p.mode == 1) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kCols / 32; ++j) {
       const int64_t c0 = col0 + 32 * j;
       if (c0 >= p.N) break;
       reuse();
@@ -302,7 +300,7 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
     // memory, which keeps this branch out of the other epilogues' registers)
     const float sa = row < p.M ? __ldg(p.sA + row) : 0.0f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kCols / 32; ++j) {
       const int64_t c0 = col0 + 32 * j;
       if (c0 >= p.N) break;
       reuse();
@@ -327,7 +325,7 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
   }
   if (p.mode == 2) {  // plain bf16: tot holds fp32 bit patterns
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < kCols / 64; ++j) {
       const int64_t c0 = col0 + 64 * j;
       if (c0 >= p.N) break;
       reuse();
@@ -350,7 +348,7 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
   const float sa = kRegScales ? ts.sa : row < p.M ? __ldg(p.sA + row) : 0.0f;
   const bool sb_vec4 = (reinterpret_cast<uintptr_t>(p.sB) & 15u) == 0;
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
+  for (int j = 0; j < kCols / 64; ++j) {
     const int64_t c0 = col0 + 64 * j;
     if (c0 >= p.N) break;
     reuse();
@@ -388,11 +386,31 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
   }
 }
 
-template <bool kAmn, bool kBmn, bool kRegScales>
+// Single-CTA tiles of 128 x kTileN: 256 (four stages of 48 KB, two 256-column
+// accumulators) or, for launches with few tiles, 128 (six stages of 32 KB,
+// two 128-column accumulators), so that twice as many SMs share the work.
+template <int kTileN>
+struct SingleTile {
+  static constexpr int kStages = kTileN == 256 ? 4 : 6;
+  static constexpr int kBBytes = kTileN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = 2u * kTileN;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kBarrierBytes;
+  static_assert(kSmemBytes <= 227 * 1024, "single-CTA kernel shared memory");
+  static_assert((2 * kStages + 5) * 8 + 12 <= kBarrierBytes, "barrier area");
+};
+
+template <bool kAmn, bool kBmn, bool kRegScales, int kTileN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_s8f16_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
+  using Cfg = SingleTile<kTileN>;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int kBBytes = Cfg::kBBytes;
+  constexpr int kStageBytes = Cfg::kStageBytes;
+  constexpr uint32_t kTmemCols = Cfg::kTmemCols;
+  constexpr int kCols = kTileN / 2;  // columns of a tile per epilogue warp
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -453,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mb, nb;
         tile_mn(p, tile, mb, nb);
         const int m0 = mb * kBM;
-        const int n0 = nb * kBN;
+        const int n0 = nb * kTileN;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort, limit)) {
             ok = false;
@@ -464,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!drop) {
             ptx::mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
             load_operand<kAmn, kBM>(a_base + stage * kABytes, &tmA, full_bar(stage), kb, m0);
-            load_operand<kBmn, kBN>(b_base + stage * kBBytes, &tmB, full_bar(stage), kb, n0);
+            load_operand<kBmn, kTileN>(b_base + stage * kBBytes, &tmB, full_bar(stage), kb, n0);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
@@ -484,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ----------------------------------------------------------- MMA
-      const uint32_t idesc = ptx::idesc_f16_f32(kBM, kBN, kAmn, kBmn) | p.ab_format;
+      const uint32_t idesc = ptx::idesc_f16_f32(kBM, kTileN, kAmn, kBmn) | p.ab_format;
       uint32_t stage = 0, phase = 0, chunk = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -495,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t d_tmem = tmem_base + buf * kBN;
+          const uint32_t d_tmem = tmem_base + buf * kTileN;
           const int kb_end = min(kb0 + p.chunk_blocks, p.k_blocks);
           for (int kb = kb0; kb < kb_end; ++kb) {
             if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort, limit)) {
@@ -528,19 +546,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;           // TMEM lanes this warp may access
-    const int half = (warp - 2) >> 2;    // which 128 columns of the tile
+    const int half = (warp - 2) >> 2;    // which half of the tile's columns
     uint32_t chunk = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       int mb, nb;
       tile_mn(p, tile, mb, nb);
       const int m0 = mb * kBM;
-      const int n0 = nb * kBN;
-      const TileScales ts = load_tile_scales<kRegScales>(
-          p, static_cast<int64_t>(m0) + quad * 32, static_cast<int64_t>(n0) + half * 128);
-      int32_t tot[128];
+      const int n0 = nb * kTileN;
+      const TileScales ts = load_tile_scales<kRegScales, kCols>(
+          p, static_cast<int64_t>(m0) + quad * 32, static_cast<int64_t>(n0) + half * kCols);
+      int32_t tot[kCols];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) tot[i] = 0;
+      for (int i = 0; i < kCols; ++i) tot[i] = 0;
       for (int kb0 = 0; kb0 < p.k_blocks; kb0 += p.chunk_blocks) {
         const uint32_t buf = chunk & 1u, aph = (chunk >> 1) & 1u;
         int got = 1;
@@ -551,8 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kBN +
-                               static_cast<uint32_t>(half * 128);
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kTileN +
+                               static_cast<uint32_t>(half * kCols);
         drain_chunk(taddr, tot, p.mode == 2);
         ptx::tc_fence_before();
         __syncwarp();
@@ -560,9 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++chunk;
       }
       if (!ok) break;
-      store_tile_tma<kRegScales>(p, &tmO, staging + (warp - 2) * kStoreBoxBytes,
-                                 static_cast<int64_t>(m0) + quad * 32,
-                                 static_cast<int64_t>(n0) + half * 128, ts, tot);
+      store_tile_tma<kRegScales, kCols>(p, &tmO, staging + (warp - 2) * kStoreBoxBytes,
+                                        static_cast<int64_t>(m0) + quad * 32,
+                                        static_cast<int64_t>(n0) + half * kCols, ts, tot);
     }
     if (!ok && lane == 0) raise_abort(abort, p.status);
     if (lane == 0) ptx::bulk_wait_group0();  // the tile stores are complete
@@ -1368,8 +1386,13 @@ cudaError_t set_conv_attrs(Kernel kernel) {
 
 template <bool kAmn, bool kBmn, bool kRegScales>
 cudaError_t set_smem_attrs() {
-  cudaError_t err = cudaFuncSetAttribute(gemm_s8f16_kernel<kAmn, kBmn, kRegScales>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t err =
+      cudaFuncSetAttribute(gemm_s8f16_kernel<kAmn, kBmn, kRegScales, 256>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, SingleTile<256>::kSmemBytes);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(gemm_s8f16_kernel<kAmn, kBmn, kRegScales, 128>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SingleTile<128>::kSmemBytes);
   if (err == cudaSuccess)
     err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, kConvNone>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
@@ -1409,7 +1432,7 @@ bool make_output_map(CUtensorMap* map, void* out, GemmOut mode, int64_t M, int64
 }
 
 template <bool kAmn, bool kBmn, bool kRegScales>
-cudaError_t launch_kernel(bool pair, int conv, int grid, const CUtensorMap& mapA,
+cudaError_t launch_kernel(bool pair, int conv, int tile_n, int grid, const CUtensorMap& mapA,
                           const CUtensorMap& mapB, const CUtensorMap& mapO, const GemmParams& p,
                           cudaStream_t stream) {
   if (conv == kConvWiden)
@@ -1427,17 +1450,23 @@ cudaError_t launch_kernel(bool pair, int conv, int grid, const CUtensorMap& mapA
     return launch_overlapped(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, kConvNone>,
                              dim3(grid), dim3(kThreads), kPairSmemBytes, stream, mapA, mapB, mapO,
                              p);
-  return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn, kRegScales>, dim3(grid), dim3(kThreads),
-                           kSmemBytes, stream, mapA, mapB, mapO, p);
+  if (tile_n == 128)
+    return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn, kRegScales, 128>, dim3(grid),
+                             dim3(kThreads), SingleTile<128>::kSmemBytes, stream, mapA, mapB, mapO,
+                             p);
+  return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn, kRegScales, 256>, dim3(grid),
+                           dim3(kThreads), SingleTile<256>::kSmemBytes, stream, mapA, mapB, mapO,
+                           p);
 }
 
 template <bool kAmn, bool kBmn>
-cudaError_t launch_layout(bool pair, int conv, bool reg_scales, int grid,
+cudaError_t launch_layout(bool pair, int conv, int tile_n, bool reg_scales, int grid,
                           const CUtensorMap& mapA, const CUtensorMap& mapB,
                           const CUtensorMap& mapO, const GemmParams& p, cudaStream_t stream) {
-  return reg_scales
-             ? launch_kernel<kAmn, kBmn, true>(pair, conv, grid, mapA, mapB, mapO, p, stream)
-             : launch_kernel<kAmn, kBmn, false>(pair, conv, grid, mapA, mapB, mapO, p, stream);
+  return reg_scales ? launch_kernel<kAmn, kBmn, true>(pair, conv, tile_n, grid, mapA, mapB, mapO,
+                                                      p, stream)
+                    : launch_kernel<kAmn, kBmn, false>(pair, conv, tile_n, grid, mapA, mapB, mapO,
+                                                       p, stream);
 }
 
 }  // namespace
@@ -1480,6 +1509,14 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   const bool pair = conv != kConvNone ||
                     (M > kBM && (pair_tiles >= dev.sms / 2 || K >= 8192) && !dbg.single_cta);
   const bool plain = mode == GemmOut::kBf16Plain;
+  // single CTAs: 128-column tiles when the 256-column ones would leave more
+  // than half of the SMs idle and the narrower tiles still fit in one wave
+  int tile_n = kBN;
+  if (!pair) {
+    const int64_t t256 = ((M + kBM - 1) / kBM) * ((N + 255) / 256);
+    const int64_t t128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
+    if (t256 * 2 <= dev.sms && t128 <= dev.sms && t128 > t256) tile_n = 128;
+  }
   CUtensorMap mapA, mapB, mapO;
   const bool maps_ok =
       conv == kConvWiden
@@ -1489,7 +1526,7 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
                 encode_tensor_map_2d(&mapB, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, K, kBK,
                                      128, CU_TENSOR_MAP_SWIZZLE_NONE)
           : make_operand_map(&mapA, A, a_mn, M, K, kBM, plain) &&
-                make_operand_map(&mapB, B, b_mn, N, K, pair ? 128 : kBN, plain);
+                make_operand_map(&mapB, B, b_mn, N, K, pair ? 128 : tile_n, plain);
   if (!maps_ok || !make_output_map(&mapO, out, mode, M, N, ldo))
     return cudaErrorInvalidValue;
   GemmParams p;
@@ -1501,7 +1538,7 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.m_tiles = static_cast<int>((M + (pair ? 255 : kBM - 1)) / (pair ? 256 : kBM));
-  p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
+  p.n_tiles = static_cast<int>((N + (pair ? kBN : tile_n) - 1) / (pair ? kBN : tile_n));
   p.m_fastest = M < N ? 1 : 0;
   p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
   p.mode = mode == GemmOut::kS32 ? 1 : plain ? 2 : mode == GemmOut::kF32Scaled ? 3 : 0;
@@ -1548,10 +1585,13 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   const bool reg_scales =
       mode != GemmOut::kF32Scaled && static_cast<int64_t>(p.dp_tiles) <= 2 * units;
   if (!a_mn && !b_mn)
-    return launch_layout<false, false>(pair, conv, reg_scales, grid, mapA, mapB, mapO, p, stream);
+    return launch_layout<false, false>(pair, conv, tile_n, reg_scales, grid, mapA, mapB, mapO, p,
+                                       stream);
   if (!a_mn)
-    return launch_layout<false, true>(pair, conv, reg_scales, grid, mapA, mapB, mapO, p, stream);
-  return launch_layout<true, true>(pair, conv, reg_scales, grid, mapA, mapB, mapO, p, stream);
+    return launch_layout<false, true>(pair, conv, tile_n, reg_scales, grid, mapA, mapB, mapO, p,
+                                      stream);
+  return launch_layout<true, true>(pair, conv, tile_n, reg_scales, grid, mapA, mapB, mapO, p,
+                                   stream);
 }
 
 }  // namespace int8mp
