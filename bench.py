@@ -271,10 +271,11 @@ class LayerStep:
             at += n
         # the matmuls' scratch for splitting their last wave of tiles
         self.mm_ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
-        # data parallel (world > 1): each rank's fp32 part of dW, summed by an
-        # all-reduce and rounded once
-        self.dw_f32 = (torch.empty(nmax * kmax, dtype=torch.float32, device=device)
-                       if world > 1 else None)
+        # data parallel (world > 1): each rank's fp32 part of dW per linear,
+        # summed by an all-reduce and rounded once; the all-reduces run while
+        # the later linears compute, and the roundings end the step
+        self.dw_f32 = ([torch.empty((l["N"], l["K"]), dtype=torch.float32, device=device)
+                        for l in self.linears] if world > 1 else None)
         self.flops = 6.0 * T * sum(l["N"] * l["K"] for l in self.linears)
         # GEMM operands read once (f16 codes) and bf16 outputs written, per step
         self.gemm_bytes = 6.0 * sum(T * l["K"] + T * l["N"] + l["N"] * l["K"] for l in self.linears)
@@ -333,7 +334,8 @@ class LayerStep:
         # offset + r * 2^40 (disjoint streams); rank 0 (and one GPU) as given
         offset = self.dp.shard_offset(offset, self.rank)
         self.colmax_all.zero_()
-        for l in self.linears:
+        pending = []  # data parallel: (all-reduce in flight, fp32 part, dW)
+        for i, l in enumerate(self.linears):
             X, W, dY = l["X"], l["W"], l["dY"]
             K = l["K"]
             cm = l["colmax"]
@@ -354,13 +356,16 @@ class LayerStep:
                 rec("gemm", lambda: m.int8mp_scaled_mm(qgc, sgc, qxc, sxc, layout=m.INT8MP_ATxB,
                                                        out=l["dW"], workspace=self.mm_ws))
             else:
-                # this rank's fp32 part of dW, the all-reduce, one rounding
-                N = l["N"]
-                part = self.dw_f32[:N * K].view(N, K)
+                # this rank's fp32 part of dW, its all-reduce started (it runs
+                # while the next linears compute), one rounding at the end
+                part = self.dw_f32[i]
                 rec("gemm", lambda: m.int8mp_scaled_mm_f32(qgc, sgc, qxc, sxc, layout=m.INT8MP_ATxB,
                                                            out=part, workspace=self.mm_ws))
-                rec("allreduce", lambda: self.dp.reduce_partials(part))
-                rec("round", lambda: m.int8mp_round_bf16(part.view(-1), l["dW"].view(-1)))
+                work = self.dp.reduce_partials(part, async_op=True)
+                pending.append((work, part, l["dW"]))
+        for work, part, dW in pending:
+            rec("allreduce", work.wait)
+            rec("round", lambda: m.int8mp_round_bf16(part.view(-1), dW.view(-1)))
 
 
 def time_steps(step, steps, warmup, world, device):

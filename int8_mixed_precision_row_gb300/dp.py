@@ -65,12 +65,15 @@ def grad_weight_partial(dY, X, cfg, colmax_dy=None, colmax_x=None, workspace=Non
                                   stream=stream)
 
 
-def reduce_partials(partial, group=None):
+def reduce_partials(partial, group=None, async_op=False):
     """The ranks' fp32 partials summed in place on every rank (one
-    all-reduce of the [N, K] buffer)."""
+    all-reduce of the [N, K] buffer).  async_op: start it and return its
+    handle (the sum is in place once handle.wait() returns; on the GPU, work
+    queued after wait() on the current stream sees it), so that it runs
+    while later work is computed."""
     import torch.distributed as dist
-    dist.all_reduce(partial, op=dist.ReduceOp.SUM, group=group)
-    return partial
+    work = dist.all_reduce(partial, op=dist.ReduceOp.SUM, group=group, async_op=async_op)
+    return work if async_op else partial
 
 
 def grad_weight_data_parallel(dY, X, cfg, group=None, dW=None, workspace=None, stream=None):

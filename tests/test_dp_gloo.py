@@ -32,7 +32,7 @@ def _inputs():
     return dY, X
 
 
-def _worker(rank, world, port, mode, out):
+def _worker(rank, world, port, mode, async_op, out):
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     sys.path.insert(0, root)
@@ -54,20 +54,24 @@ def _worker(rank, world, port, mode, out):
     qx, sx = oracle.quantize(x, 1, mode=mode, seed=9, offset=off, stream_id=oracle.STREAM_GW_X)
     mine = oracle.scaled_mm_f32(qg, sg, qx, sx, N, K, t1 - t0)
     part = torch.from_numpy(mine.copy())
-    dp.reduce_partials(part)
+    if async_op:  # started, then waited for (the bench step overlaps it with later linears)
+        dp.reduce_partials(part, async_op=True).wait()
+    else:
+        dp.reduce_partials(part)
     out[rank] = (mine, part.numpy().copy())
     dist.destroy_process_group()
 
 
+@pytest.mark.parametrize("async_op", [False, True])
 @pytest.mark.parametrize("mode", [0, 1])
-def test_two_rank_grad_weight_is_the_sum_of_shard_oracles(mode):
+def test_two_rank_grad_weight_is_the_sum_of_shard_oracles(mode, async_op):
     import oracle
     from helpers import bf16_bits
     from int8_mixed_precision_row_gb300 import dp
     ctx = mp.get_context("spawn")
     out = ctx.Manager().dict()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, mode, out)) for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, mode, async_op, out)) for r in range(2)]
     for p in procs:
         p.start()
     for p in procs:
