@@ -476,7 +476,18 @@ def time_e2e(step, steps, warmup):
     torch.cuda.synchronize()
     if m.int8mp_poll_device_status() != m.INT8MP_OK:
         raise RuntimeError("device status reported a timeout during the e2e run")
-    return a.elapsed_time(b), h2d, d2h
+    # the host link alone on this machine: the largest input copied in, nothing else running
+    host, dev = max(pinned.values(), key=lambda hd: hd[0].numel())
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    dev.copy_(host, non_blocking=True)
+    c0.record(comp)
+    for _ in range(3):
+        dev.copy_(host, non_blocking=True)
+    c1.record(comp)
+    torch.cuda.synchronize()
+    link_gbs = 3 * host.numel() * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    return a.elapsed_time(b), h2d, d2h, link_gbs
 
 
 # ------------------------------------------------------------------ oracle
@@ -941,12 +952,14 @@ def main():
     }
     if not args.profile_steps:
         e2e_steps = max(3, min(args.steps, 10))
-        e2e_ms, h2d, d2h = time_e2e(step, e2e_steps, 1)
+        e2e_ms, h2d, d2h, link_gbs = time_e2e(step, e2e_steps, 1)
         e2e_ms = max_over_ranks(e2e_ms, world, device)
         line["e2e"] = {"value": round(step.T * e2e_steps * world / (e2e_ms * 1e-3), 1), "unit": "tok/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "copies": "pinned host <-> device on their own streams, overlapping the "
-                                 "compute of other linears"}
+                                 "compute of other linears",
+                       "host_link_h2d_gbs": round(link_gbs, 1),
+                       "h2d_bound_tok_s": round(step.T * world / (h2d / (link_gbs * 1e9)), 1)}
     del step
     torch.cuda.empty_cache()
     if rank == 0 and not args.profile_steps and not args.no_extra:
