@@ -12,6 +12,7 @@ timed region; every step touches about 5 GB, far more than the 129 MB L2.
 Under torchrun with N ranks (one GPU each) the step is data parallel over
 tokens: every rank runs its own 16 x 2048 tokens (weak scaling), and the
 grad-weight pass forms fp32 partials that one NCCL all-reduce per linear sums
+(started when the part is formed, running while the later linears compute)
 before a single bf16 rounding (int8_mixed_precision_row_gb300/dp.py).
 
 Output: one JSON line (rank 0).  `value` is whole-job tokens/s; `e2e` is the
