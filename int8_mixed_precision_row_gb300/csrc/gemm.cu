@@ -388,10 +388,15 @@ __device__ __forceinline__ void store_tile_tma(const GemmParams& p, const CUtens
 
 // Single-CTA tiles of 128 x kTileN: 256 (four stages of 48 KB, two 256-column
 // accumulators) or, for launches with few tiles, 128 (six stages of 32 KB,
-// two 128-column accumulators), so that twice as many SMs share the work.
+// two 128-column accumulators) or 64 (eight stages of 24 KB, two 64-column
+// accumulators), so that more SMs share the work.  kEpi epilogue warps drain
+// a tile, each 32 rows x kCols columns: all eight with two column halves, or
+// the first four with whole 64-column tiles.
 template <int kTileN>
 struct SingleTile {
-  static constexpr int kStages = kTileN == 256 ? 4 : 6;
+  static constexpr int kStages = kTileN == 256 ? 4 : kTileN == 128 ? 6 : 8;
+  static constexpr int kCols = kTileN == 64 ? 64 : kTileN / 2;
+  static constexpr int kEpi = kTileN == 64 ? kEpiWarps / 2 : kEpiWarps;
   static constexpr int kBBytes = kTileN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2u * kTileN;
@@ -410,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kBBytes = Cfg::kBBytes;
   constexpr int kStageBytes = Cfg::kStageBytes;
   constexpr uint32_t kTmemCols = Cfg::kTmemCols;
-  constexpr int kCols = kTileN / 2;  // columns of a tile per epilogue warp
+  constexpr int kCols = Cfg::kCols;  // columns of a tile per epilogue warp
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull_bar(b), 1);
-      ptx::mbar_init(tempty_bar(b), kEpiWarps);
+      ptx::mbar_init(tempty_bar(b), Cfg::kEpi);
     }
     ptx::mbar_init(drain_bar, 1);
     *abort = 0;
@@ -543,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mma_commit(drain_bar);
       if (!ptx::mbar_wait_bounded(drain_bar, 0u, never, limit)) raise_abort(abort, p.status);
     }
-  } else {
+  } else if (warp - 2 < Cfg::kEpi) {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;           // TMEM lanes this warp may access
     const int half = (warp - 2) >> 2;    // which half of the tile's columns
@@ -1394,6 +1399,10 @@ cudaError_t set_smem_attrs() {
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SingleTile<128>::kSmemBytes);
   if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(gemm_s8f16_kernel<kAmn, kBmn, kRegScales, 64>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SingleTile<64>::kSmemBytes);
+  if (err == cudaSuccess)
     err = cudaFuncSetAttribute(gemm_s8f16_pair_kernel<kAmn, kBmn, kRegScales, kConvNone>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
   if (err == cudaSuccess)
@@ -1454,6 +1463,10 @@ cudaError_t launch_kernel(bool pair, int conv, int tile_n, int grid, const CUten
     return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn, kRegScales, 128>, dim3(grid),
                              dim3(kThreads), SingleTile<128>::kSmemBytes, stream, mapA, mapB, mapO,
                              p);
+  if (tile_n == 64)
+    return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn, kRegScales, 64>, dim3(grid),
+                             dim3(kThreads), SingleTile<64>::kSmemBytes, stream, mapA, mapB, mapO,
+                             p);
   return launch_overlapped(gemm_s8f16_kernel<kAmn, kBmn, kRegScales, 256>, dim3(grid),
                            dim3(kThreads), SingleTile<256>::kSmemBytes, stream, mapA, mapB, mapO,
                            p);
@@ -1513,9 +1526,11 @@ cudaError_t launch_gemm(const void* A, bool a_mn, const float* sA, const void* B
   // than half of the SMs idle and the narrower tiles still fit in one wave
   int tile_n = kBN;
   if (!pair) {
-    const int64_t t256 = ((M + kBM - 1) / kBM) * ((N + 255) / 256);
-    const int64_t t128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
+    const int64_t mt = (M + kBM - 1) / kBM;
+    const int64_t t256 = mt * ((N + 255) / 256), t128 = mt * ((N + 127) / 128);
+    const int64_t t64 = mt * ((N + 63) / 64);
     if (t256 * 2 <= dev.sms && t128 <= dev.sms && t128 > t256) tile_n = 128;
+    if (tile_n == 128 && t128 * 2 <= dev.sms && t64 <= dev.sms && t64 > t128) tile_n = 64;
   }
   CUtensorMap mapA, mapB, mapO;
   const bool maps_ok =
