@@ -25,17 +25,18 @@
 // column-grouped codes need no transposition.
 //
 // Structure (one persistent CTA per SM, 320 threads; tiles of 128 x 256, or
-// 128 x 128 for launches with few tiles):
+// 128 x 128 or 128 x 64 for launches with few tiles):
 //   warp 0      TMA producer (one thread): 4-stage ring of 128x64 A and
-//               256x64 B f16 tiles (6 stages with 128x64 B tiles), 128-byte
-//               swizzled, one mbarrier per stage
+//               256x64 B f16 tiles (6 and 8 stages with 128- and 64-row B
+//               tiles), 128-byte swizzled, one mbarrier per stage
 //   warp 1      TMEM allocator + MMA issuer (one thread): 4 MMAs of
-//               128x256x16 (128x128x16) per stage, commit frees the stage;
-//               commit after each K-chunk hands the accumulator to the epilogue
+//               128 x N x 16 per stage, commit frees the stage; commit after
+//               each K-chunk hands the accumulator to the epilogue
 //   warps 2-9   epilogue: warp w reads TMEM lanes 32*(w%4).. and one half
-//               of the tile's columns, keeps an int32 total per column and
-//               thread, and writes the finished tile through a 4 KB
-//               shared-memory staging buffer with TMA tensor stores
+//               of the tile's columns (warps 2-5 the whole of a 64-column
+//               tile), keeps an int32 total per column and thread, and writes
+//               the finished tile through a 4 KB shared-memory staging
+//               buffer with TMA tensor stores
 // Every mbarrier wait is bounded (wall clock); a wait that runs out raises
 // the CTA abort flag and the device status word, every role winds down,
 // outstanding copies and MMAs are waited for (bounded), TMEM is freed.
