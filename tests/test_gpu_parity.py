@@ -363,6 +363,52 @@ def _stored(codes, layout, which, M, N, K, seed):
     return _rand_codes(N, K, seed) if layout == m.INT8MP_AxBT else _rand_codes(K, N, seed)
 
 
+# Shapes that take each tile width of the single-CTA GEMM (on 152 SMs): 128 x
+# 256 when its tiles fill half of the SMs or more, else 128 x 128, else
+# 128 x 64 (the CTA-pair kernel takes neither: fewer than 76 pair tiles and
+# K < 8192).  Every width in every layout and output mode.
+SINGLE_TILE_SHAPES = [(2048, 2048, 256),    # 128 tiles of 128 x 256
+                      (1024, 1280, 1040),   # 80 tiles of 128 x 128 (40 of 128 x 256)
+                      (512, 528, 1040)]     # 36 tiles of 128 x 64 (20 of 128 x 128)
+
+
+@pytest.mark.parametrize("layout", [m.INT8MP_AxBT, m.INT8MP_AxB, m.INT8MP_ATxB])
+@pytest.mark.parametrize("shape", SINGLE_TILE_SHAPES)
+def test_single_cta_tile_widths_all_outputs(shape, layout):
+    M, N, K = shape
+    a = _stored(None, layout, "A", M, N, K, 31)
+    b = _stored(None, layout, "B", M, N, K, 32)
+    g = torch.Generator().manual_seed(33)
+    sa = (torch.rand(M, generator=g) * 2.0 ** -6).float()
+    sb = (torch.rand(N, generator=g) * 2.0 ** -3).float()
+    ad, bd = _dev(a.half()), _dev(b.half())
+    acc = m.int8mp_mm_s32(ad, bd, layout=layout)
+    y = m.int8mp_scaled_mm(ad, _dev(sa), bd, _dev(sb), layout=layout)
+    y32 = m.int8mp_scaled_mm_f32(ad, _dev(sa), bd, _dev(sb), layout=layout)
+    torch.cuda.synchronize()
+    assert m.int8mp_poll_device_status() == m.INT8MP_OK
+    an, bn = a.numpy(), b.numpy()
+    np.testing.assert_array_equal(acc.cpu().numpy(), oracle.mm_s32(an, bn, M, N, K, layout=layout))
+    assert_bf16_equal(y, oracle.scaled_mm(an, sa.numpy(), bn, sb.numpy(), M, N, K, layout=layout),
+                      "scaled_mm")
+    np.testing.assert_array_equal(
+        y32.cpu().numpy().view(np.int32),
+        oracle.scaled_mm_f32(an, sa.numpy(), bn, sb.numpy(), M, N, K, layout=layout).view(np.int32))
+
+
+@pytest.mark.parametrize("shape", SINGLE_TILE_SHAPES)
+def test_single_cta_tile_widths_bf16_pass(shape):
+    # the plain-bf16 mode of the same kernels: the forward matmul of a linear
+    # layer with its pass in BF16
+    T, N, K = shape
+    X = synth.bf16_normal((T, K), 41)
+    W = synth.bf16_normal((N, K), 42, std=0.02)
+    Y = m.int8mp_linear_fwd(_dev(X), _dev(W), cfg=m.linear_cfg(int8_fwd=0))
+    torch.cuda.synchronize()
+    ref = oracle.matmul_bf16(bf16_bits(X), bf16_bits(W), T, N, K)
+    _bf16_pass_close(Y, ref, X.float(), W.float(), "BF16 forward")
+
+
 @pytest.mark.parametrize("shape", SPLIT_TAIL_SHAPES)
 def test_mm_s32_split_tail_bit_exact(shape):
     M, N, K, layout = shape
