@@ -106,8 +106,10 @@ def test_quantize_cols_bit_exact(shape, mode, codes):
     np.testing.assert_array_equal(_codes_np(q), qr)
 
 
+# up to 2048 rows: the one-launch kernel (1024 or 2048 rows per register
+# share); more rows: the absmax, scale and code passes
 COL_NAT_SHAPES = [(256, 512), (8, 8), (77, 136), (1032, 64), (520, 2048), (16, 4096),
-                  (3001, 264), (1, 5632)]
+                  (3001, 264), (1, 5632), (2048, 40), (2056, 72), (8200, 24)]
 
 
 @pytest.mark.parametrize("off", [2**35 + 3, 2**35 + 4])
@@ -125,6 +127,26 @@ def test_quantize_cols_in_input_layout_bit_exact(shape, mode, codes, off):
     q, s = m.int8mp_quantize_rowwise(_dev(x), axis=m.INT8MP_GROUP_COLS, mode=mode, seed=seed,
                                      offset=off, stream_id=sid, codes=codes)
     assert tuple(q.shape) == (rows, cols)
+    qr, sr = oracle.quantize(bf16_bits(x), axis=1, mode=mode, seed=seed, offset=off, stream_id=sid)
+    np.testing.assert_array_equal(_f32_bits(s), sr.view(np.int32))
+    np.testing.assert_array_equal(_codes_np(q), np.ascontiguousarray(qr.T))
+
+
+# Plain inputs (every column's scale in the division's fast range, as in a
+# real operand), on both sides of the one-launch kernel's 2048-row limit
+COL_NAT_PLAIN_SHAPES = [(1024, 1024), (2048, 264), (2049, 64), (4096, 136), (9, 8)]
+
+
+@pytest.mark.parametrize("off", [3, 2**20])
+@pytest.mark.parametrize("codes", [m.INT8MP_CODES_S8, m.INT8MP_CODES_F16])
+@pytest.mark.parametrize("mode", [m.INT8MP_RNE, m.INT8MP_SR])
+@pytest.mark.parametrize("shape", COL_NAT_PLAIN_SHAPES)
+def test_quantize_cols_in_input_layout_plain_inputs(shape, mode, codes, off):
+    rows, cols = shape
+    x = synth.bf16_normal((rows, cols), 3 * rows + cols, outlier_frac=0.01, outlier_scale=20.0)
+    seed, sid = 31337, 2
+    q, s = m.int8mp_quantize_rowwise(_dev(x), axis=m.INT8MP_GROUP_COLS, mode=mode, seed=seed,
+                                     offset=off, stream_id=sid, codes=codes)
     qr, sr = oracle.quantize(bf16_bits(x), axis=1, mode=mode, seed=seed, offset=off, stream_id=sid)
     np.testing.assert_array_equal(_f32_bits(s), sr.view(np.int32))
     np.testing.assert_array_equal(_codes_np(q), np.ascontiguousarray(qr.T))
