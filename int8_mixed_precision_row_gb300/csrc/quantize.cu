@@ -489,6 +489,78 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(
   }
 }
 
+// Rows of at most 256 kV columns with no column maxima: one warp per row,
+// the row in registers (kV 16-byte vectors per lane, loaded right after the
+// grid dependency wait), no shared memory, no barrier and no bulk copy to
+// set up -- for the small matrices whose launches are latency-bound.
+// Blocks job2.split .. gridDim.x - 1 take the second matrix, as in
+// quant_rows_kernel.  Faster than the ring of bulk copies at every size it
+// takes (A and B of 1024^2: 3.5 -> 2.8 us; X of 32768 x 2048: 38.0 -> 36.4
+// us), slower at 4096 columns (16 vectors per lane), which keep the ring.
+// (Blocks of 128 threads capped at 85 registers, small enough to sit beside
+// a GEMM CTA, measured slower: 2048^2 A and B 10.6 -> 12.2 us.)
+constexpr int kRegMaxV = 8;
+constexpr int kRegThreads = kThreads;
+
+template <typename CodeT, bool SR, int kV>
+__global__ void __launch_bounds__(kRegThreads) quant_rows_reg_kernel(
+    const uint16_t* __restrict__ x1, int64_t rows1, int64_t cols, int64_t ld1,
+    CodeT* __restrict__ q1, float* __restrict__ scale1, SrArgs sr, unsigned int* status,
+    RowsJob2 job2) {
+  const bool second = static_cast<int>(blockIdx.x) >= job2.split;
+  const uint16_t* __restrict__ x = second ? job2.x : x1;
+  const int64_t rows = second ? job2.rows : rows1;
+  const int64_t ld = second ? job2.ld : ld1;
+  CodeT* __restrict__ q = second ? static_cast<CodeT*>(job2.q) : q1;
+  float* __restrict__ scale = second ? job2.scale : scale1;
+  const uint64_t sr_offset = second ? job2.offset : sr.offset;
+  const PhiloxStream sr_stream = second ? job2.stream : sr.stream;
+  const int64_t block = second ? blockIdx.x - job2.split : blockIdx.x;
+  const int64_t blocks = second ? gridDim.x - job2.split : job2.split;
+  constexpr int kWarps = kRegThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = static_cast<int>(cols >> 3);
+  using P = Pack8<CodeT>;
+  ptx::grid_dependency_wait();  // the previous kernel in the stream is done
+  ptx::allow_dependents();
+  if (!in_bounds(nvec <= 32 * kV && cols <= ld, status)) return;
+  for (int64_t r = block * kWarps + warp; r < rows; r += blocks * kWarps) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + r * ld);
+    uint4 a[kV];
+    uint32_t am2 = 0u;  // packed pair of |x| maxima
+#pragma unroll
+    for (int i = 0; i < kV; ++i) {
+      const int v = lane + 32 * i;
+      a[i] = v < nvec ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+      am2 = absmax8_bits(am2, abs_bits8(a[i]));
+    }
+    float amax = unpack_max(am2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (lane == 0) scale[r] = s;
+    const ScaleDiv d = make_scale_div(s);
+    const bool normal = scale_is_normal(s);
+    typename P::Vec* qr = reinterpret_cast<typename P::Vec*>(q + r * cols);
+    const uint64_t nrow = sr_offset + static_cast<uint64_t>(r * cols);
+    const bool fast = d.fast && (nrow & 3u) == 0;
+#pragma unroll
+    for (int i = 0; i < kV; i += 2) {
+      const int v = lane + 32 * i, v2 = v + 32;
+      if (v < nvec) {
+        const bool has2 = i + 1 < kV && v2 < nvec;
+        const uint4 b = i + 1 < kV ? a[i + 1 < kV ? i + 1 : i] : make_uint4(0u, 0u, 0u, 0u);
+        if (fast)
+          quantize_two_fast<CodeT, SR>(a[i], b, has2, d, sr.keys, sr_stream, nrow + 8u * v,
+                                       nrow + 8u * v2, qr + v, qr + (has2 ? v2 : v));
+        else
+          quantize_two<CodeT, SR>(a[i], b, has2, d, normal, sr.keys, sr_stream, nrow + 8u * v,
+                                  nrow + 8u * v2, qr + v, qr + (has2 ? v2 : v));
+      }
+    }
+  }
+}
+
 // Rows too long for two shared-memory slots: one block per row, two sweeps
 // over global memory (the second hits L2).
 template <typename CodeT, bool SR>
@@ -1232,6 +1304,50 @@ cudaError_t rows_dispatch(const RowsJob* jobs, int njobs, int64_t cols, const Sr
     return launch_col_absmax(static_cast<const uint16_t*>(j.x), j.rows, cols, j.ld,
                              reinterpret_cast<unsigned int*>(j.colmax), dev, stream);
   };
+  // blocks [0, split) take job 0 and [split, blocks) job 1, in proportion
+  // to their rows when the two need more than one wave of blocks (`per`:
+  // rows a block takes at a time; `cap`: blocks of one wave)
+  auto plan = [&](int64_t per, int64_t cap, int64_t* split, int64_t* blocks) {
+    auto need = [&](const RowsJob& j) { return (j.rows + per - 1) / per; };
+    if (njobs == 1) {
+      *split = *blocks = need(jobs[0]) < cap ? need(jobs[0]) : cap;
+    } else if (need(jobs[0]) + need(jobs[1]) <= cap) {
+      *split = need(jobs[0]);
+      *blocks = *split + need(jobs[1]);
+    } else {
+      *blocks = cap;
+      const double share = static_cast<double>(jobs[0].rows) / (jobs[0].rows + jobs[1].rows);
+      *split = static_cast<int64_t>(share * cap + 0.5);
+      if (*split < 1) *split = 1;
+      if (*split > cap - 1) *split = cap - 1;
+    }
+  };
+  auto second_job = [&](int64_t split, bool with_colmax) {
+    RowsJob2 j2{nullptr, 0, 0, nullptr, nullptr, nullptr, 0, PhiloxStream{0u, 0u},
+                static_cast<int>(split)};
+    if (njobs > 1) {
+      const RowsJob& j1 = jobs[1];
+      j2 = RowsJob2{static_cast<const uint16_t*>(j1.x), j1.rows, j1.ld, j1.q, j1.scale,
+                    with_colmax ? reinterpret_cast<unsigned int*>(j1.colmax) : nullptr,
+                    j1.offset, philox_stream(j1.stream_id), static_cast<int>(split)};
+    }
+    return j2;
+  };
+  if (!cm && cols <= 256 * kRegMaxV) {
+    // short rows, no column maxima: one warp per row, the row in registers
+    auto kernel = cols <= 256   ? quant_rows_reg_kernel<CodeT, SR, 1>
+                  : cols <= 512 ? quant_rows_reg_kernel<CodeT, SR, 2>
+                  : cols <= 1024 ? quant_rows_reg_kernel<CodeT, SR, 4>
+                                 : quant_rows_reg_kernel<CodeT, SR, kRegMaxV>;
+    const int occ = blocks_per_sm(kernel, kRegThreads, 0);
+    int64_t split, blocks;
+    plan(kRegThreads / 32, static_cast<int64_t>(sms) * occ, &split, &blocks);
+    const RowsJob& j0 = jobs[0];
+    return launch_overlapped(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kRegThreads), 0,
+                             stream, static_cast<const uint16_t*>(j0.x), j0.rows, cols, j0.ld,
+                             static_cast<CodeT*>(j0.q), j0.scale, sr_of(j0), dev.status_word,
+                             second_job(split, false));
+  }
   if (2ull * slot > kMaxDynSmem) {
     for (int i = 0; i < njobs; ++i) {
       const RowsJob& j = jobs[i];
@@ -1269,37 +1385,15 @@ cudaError_t rows_dispatch(const RowsJob* jobs, int njobs, int64_t cols, const Sr
   if (S < 2) S = 2;
   const size_t smem = team_bytes * S;
   const int64_t teams = warps / T;
-  auto need = [&](const RowsJob& j) { return (j.rows + teams - 1) / teams; };
   auto kernel = fused ? quant_rows_kernel<CodeT, SR, true> : quant_rows_kernel<CodeT, SR, false>;
   static bool attr_fused[64] = {}, attr_plain[64] = {};
   cudaError_t e = allow_smem(kernel, fused ? attr_fused : attr_plain);
   if (e != cudaSuccess) return e;
   const int occ = blocks_per_sm(kernel, kThreads, smem);
-  const int64_t cap = static_cast<int64_t>(sms) * occ;
-  // blocks [0, split) take job 0 and [split, blocks) job 1, in proportion
-  // to their rows when the two need more than one wave of blocks
   int64_t split, blocks;
-  if (njobs == 1) {
-    split = blocks = need(jobs[0]) < cap ? need(jobs[0]) : cap;
-  } else if (need(jobs[0]) + need(jobs[1]) <= cap) {
-    split = need(jobs[0]);
-    blocks = split + need(jobs[1]);
-  } else {
-    blocks = cap;
-    const double share = static_cast<double>(jobs[0].rows) / (jobs[0].rows + jobs[1].rows);
-    split = static_cast<int64_t>(share * cap + 0.5);
-    if (split < 1) split = 1;
-    if (split > cap - 1) split = cap - 1;
-  }
+  plan(teams, static_cast<int64_t>(sms) * occ, &split, &blocks);
   const RowsJob& j0 = jobs[0];
-  RowsJob2 j2{nullptr, 0, 0, nullptr, nullptr, nullptr, 0, PhiloxStream{0u, 0u},
-              static_cast<int>(split)};
-  if (njobs > 1) {
-    const RowsJob& j1 = jobs[1];
-    j2 = RowsJob2{static_cast<const uint16_t*>(j1.x), j1.rows, j1.ld, j1.q, j1.scale,
-                  fused ? reinterpret_cast<unsigned int*>(j1.colmax) : nullptr, j1.offset,
-                  philox_stream(j1.stream_id), static_cast<int>(split)};
-  }
+  const RowsJob2 j2 = second_job(split, fused);
   e = launch_overlapped(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem, stream,
                         static_cast<const uint16_t*>(j0.x), j0.rows, cols, j0.ld,
                         static_cast<CodeT*>(j0.q), j0.scale, sr_of(j0), slot, T, S,
