@@ -435,7 +435,9 @@ def time_e2e(step, steps, warmup):
         e.record(stream)
         return e
 
-    def one():
+    copies = []      # (bytes, start, end) of each timed step's input copies
+
+    def one(timed=False):
         ready = {}
         for i, l in enumerate(step.linears):
             for hid in l["inputs"]:
@@ -444,7 +446,14 @@ def time_e2e(step, steps, warmup):
                     if hid in last_read:
                         cin.wait_event(last_read[hid])
                     with torch.cuda.stream(cin):
+                        if timed:
+                            c0 = torch.cuda.Event(enable_timing=True)
+                            c0.record(cin)
                         dev.copy_(host, non_blocking=True)
+                        if timed:
+                            c1 = torch.cuda.Event(enable_timing=True)
+                            c1.record(cin)
+                            copies.append((host.numel() * 2, c0, c1))
                     ready[hid] = event(cin)
                 comp.wait_event(ready[hid])
             if i in dw_back:
@@ -469,14 +478,19 @@ def time_e2e(step, steps, warmup):
     a.record(comp)
     cin.wait_event(a)
     cout.wait_event(a)
+    t0 = time.perf_counter()
     for _ in range(steps):
-        one()
+        one(timed=True)
     comp.wait_event(event(cin))
     comp.wait_event(event(cout))
     b.record(comp)
+    host_ms = (time.perf_counter() - t0) * 1e3  # enqueueing the steps, no wait
     torch.cuda.synchronize()
     if m.int8mp_poll_device_status() != m.INT8MP_OK:
         raise RuntimeError("device status reported a timeout during the e2e run")
+    # the input copies' own rate inside the run (busy time of the copy stream)
+    copy_gbs = (sum(n for n, _, _ in copies) /
+                (sum(c0.elapsed_time(c1) for _, c0, c1 in copies) * 1e-3) / 1e9)
     # the host link alone on this machine: the largest input copied in, nothing else running
     host, dev = max(pinned.values(), key=lambda hd: hd[0].numel())
     c0 = torch.cuda.Event(enable_timing=True)
@@ -488,7 +502,7 @@ def time_e2e(step, steps, warmup):
     c1.record(comp)
     torch.cuda.synchronize()
     link_gbs = 3 * host.numel() * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9
-    return a.elapsed_time(b), h2d, d2h, link_gbs
+    return a.elapsed_time(b), h2d, d2h, link_gbs, copy_gbs, host_ms / steps
 
 
 # ------------------------------------------------------------------ oracle
@@ -953,13 +967,15 @@ def main():
     }
     if not args.profile_steps:
         e2e_steps = max(3, min(args.steps, 10))
-        e2e_ms, h2d, d2h, link_gbs = time_e2e(step, e2e_steps, 1)
+        e2e_ms, h2d, d2h, link_gbs, copy_gbs, host_ms = time_e2e(step, e2e_steps, 1)
         e2e_ms = max_over_ranks(e2e_ms, world, device)
         line["e2e"] = {"value": round(step.T * e2e_steps * world / (e2e_ms * 1e-3), 1), "unit": "tok/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "copies": "pinned host <-> device on their own streams, overlapping the "
                                  "compute of other linears",
                        "host_link_h2d_gbs": round(link_gbs, 1),
+                       "h2d_gbs_in_run": round(copy_gbs, 1),
+                       "host_enqueue_ms_per_step": round(host_ms, 3),
                        "h2d_bound_tok_s": round(step.T * world / (h2d / (link_gbs * 1e9)), 1)}
     del step
     torch.cuda.empty_cache()
