@@ -67,10 +67,12 @@ def parse_args():
 # Single-call cases for a profiler (each runs its call three times, so that
 # `ncu -s 2 -c 1` captures a warm launch): the square 4096^3 A @ B.T matmul
 # on int8 codes and on f16 containers of the same codes, and the BF16
-# forward pass of a q projection at T = 16384.
+# forward pass of a q projection at T = 16384; quantize-AxB-2048: the two
+# quantizations of a 2048^3 A @ B (A by rows, B by columns in place; two
+# launches per call).
 PROFILE_CASES = ("square-int8-4096", "square-f16-4096", "square-f16-2048", "square-f16-1024",
                  "bf16-forward-q-T16384", "forward-q-T16384-w-codes",
-                 "forward-q-T16384-w-quantized-in-prologue")
+                 "forward-q-T16384-w-quantized-in-prologue", "quantize-AxB-2048")
 
 
 def run_profile_case(case, device):
@@ -90,6 +92,18 @@ def run_profile_case(case, device):
         ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=device)
         for _ in range(3):
             m.int8mp_scaled_mm(a, sa, b, sb, out=out, workspace=ws)
+    elif case.startswith("quantize-AxB"):
+        S = int(case.rsplit("-", 1)[1])
+        A = synth.bf16_normal((S, S), 1).to(device)
+        B = synth.bf16_normal((S, S), 2).to(device)
+        qa = torch.empty((S, S), dtype=torch.float16, device=device)
+        qb = torch.empty((S, S), dtype=torch.float16, device=device)
+        sa = torch.empty(S, dtype=torch.float32, device=device)
+        sb = torch.empty(S, dtype=torch.float32, device=device)
+        for _ in range(3):
+            m.int8mp_quantize_rowwise(A, axis=0, codes=m.INT8MP_CODES_F16, q=qa, scale=sa)
+            m.int8mp_quantize_rowwise(B, axis=m.INT8MP_GROUP_COLS, codes=m.INT8MP_CODES_F16, q=qb,
+                                      scale=sb)
     elif case.startswith("forward-q-T16384"):
         # the forward matmul of a q projection on X's codes, with W's codes
         # from the row pass, or W quantized in the GEMM's prologue from its
