@@ -1428,11 +1428,18 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
     const dim3 grid(static_cast<unsigned>((cols + 8 * kClVecs - 1) / (8 * kClVecs)), kClCtas);
     CodeT* qc = static_cast<CodeT*>(q);
     const int64_t per_u = static_cast<int64_t>(kClCtas) * kClRows;  // 256 rows
-    if (rows <= per_u * 4)
-      return launch_overlapped(quant_cols_cluster_kernel<CodeT, SR, 4>, grid, dim3(kThreads), 0,
-                               stream, xp, rows, cols, ld, scale, qc, sr, dev.status_word);
-    return launch_overlapped(quant_cols_cluster_kernel<CodeT, SR, kClMaxU>, grid, dim3(kThreads),
-                             0, stream, xp, rows, cols, ld, scale, qc, sr, dev.status_word);
+    const cudaError_t e =
+        rows <= per_u * 4
+            ? launch_overlapped(quant_cols_cluster_kernel<CodeT, SR, 4>, grid, dim3(kThreads), 0,
+                                stream, xp, rows, cols, ld, scale, qc, sr, dev.status_word)
+            : launch_overlapped(quant_cols_cluster_kernel<CodeT, SR, kClMaxU>, grid,
+                                dim3(kThreads), 0, stream, xp, rows, cols, ld, scale, qc, sr,
+                                dev.status_word);
+    if (e == cudaSuccess) return e;
+    // the cluster launch was refused (e.g. no eight-CTA cluster fits the
+    // stream's SM partition): clear that error and take the passes, whose
+    // launches report any error that persists
+    (void)cudaGetLastError();
   }
   unsigned int* amax = reinterpret_cast<unsigned int*>(scale);
   cudaError_t err = launch_zero_words(amax, cols, dev, stream);

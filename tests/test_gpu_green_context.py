@@ -62,6 +62,8 @@ def test_gemm_and_quantizers_on_a_partition(partition):
     B = synth.bf16_normal((K, N), 52).to(DEV)
     ws = torch.empty(m.int8mp_mm_workspace_size(), dtype=torch.uint8, device=DEV)
 
+    C = synth.bf16_normal((1024, 2048), 56).to(DEV)   # the one-launch kernels of small operands
+
     def run(s):
         with torch.cuda.stream(s):
             cm = torch.zeros(K, dtype=torch.float32, device=DEV)
@@ -70,8 +72,12 @@ def test_gemm_and_quantizers_on_a_partition(partition):
                                                seed=7, codes=m.INT8MP_CODES_F16)
             out = m.int8mp_scaled_mm(qa, sa, qb, sb, layout=m.INT8MP_AxB, workspace=ws)
             acc = m.int8mp_mm_s32(qa, qb, layout=m.INT8MP_AxB, workspace=ws)
+            qr, sr = m.int8mp_quantize_rowwise(C, mode=m.INT8MP_SR, seed=8,
+                                               codes=m.INT8MP_CODES_F16)
+            qc, sc = m.int8mp_quantize_rowwise(C, axis=m.INT8MP_GROUP_COLS, mode=m.INT8MP_SR,
+                                               seed=9, codes=m.INT8MP_CODES_F16)
         s.synchronize()
-        return qa, sa, qb, sb, out, acc, cm
+        return qa, sa, qb, sb, out, acc, cm, qr, sr, qc, sc
 
     ref = run(torch.cuda.current_stream())
     got = run(stream)
