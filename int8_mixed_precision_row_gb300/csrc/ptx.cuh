@@ -289,26 +289,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// The two halves of a cluster-wide barrier, for threads that need not be
-// converged: arrive (ordering this thread's earlier shared-memory accesses
-// before the peers' later ones) and wait for every thread of the cluster.
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_acquire() {
-  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// 16 bytes from a shared::cluster address (any CTA of the cluster).
-__device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
 // Arrive on an mbarrier given by a shared::cluster address (any CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
