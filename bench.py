@@ -169,7 +169,8 @@ class ClockSampler:
     """nvidia-smi samples every 200 ms while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "temperature.gpu,clocks.mem")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
@@ -223,9 +224,13 @@ class ClockSampler:
         power = [num(r[3]) for r in rows if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        temp = [num(r[9]) for r in rows if len(r) > 9 and num(r[9]) is not None]
+        mem = [num(r[10]) for r in rows if len(r) > 10 and num(r[10]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
+                "temp_c_max": max(temp) if temp else None,
+                "mem_mhz": statistics.median(mem) if mem else None,
                 "samples": len(rows), "reasons": reasons}
 
 
@@ -981,7 +986,8 @@ def main():
     }
     if not args.profile_steps:
         e2e_steps = max(3, min(args.steps, 10))
-        e2e_ms, h2d, d2h, link_gbs, copy_gbs, host_ms = time_e2e(step, e2e_steps, 1)
+        with ClockSampler(local) as eclk:
+            e2e_ms, h2d, d2h, link_gbs, copy_gbs, host_ms = time_e2e(step, e2e_steps, 1)
         e2e_ms = max_over_ranks(e2e_ms, world, device)
         line["e2e"] = {"value": round(step.T * e2e_steps * world / (e2e_ms * 1e-3), 1), "unit": "tok/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -990,7 +996,8 @@ def main():
                        "host_link_h2d_gbs": round(link_gbs, 1),
                        "h2d_gbs_in_run": round(copy_gbs, 1),
                        "host_enqueue_ms_per_step": round(host_ms, 3),
-                       "h2d_bound_tok_s": round(step.T * world / (h2d / (link_gbs * 1e9)), 1)}
+                       "h2d_bound_tok_s": round(step.T * world / (h2d / (link_gbs * 1e9)), 1),
+                       "clocks": eclk.summary()}
     del step
     torch.cuda.empty_cache()
     if rank == 0 and not args.profile_steps and not args.no_extra:
