@@ -686,6 +686,9 @@ def square_sweep(device, sizes=(1024, 2048, 4096), iters=20):
                 if ax_a == 0 and ax_b == 0:  # both by rows: one launch
                     m.int8mp_quantize_rows_batch([A, B], codes=m.INT8MP_CODES_F16, qs=[qa, qb],
                                                  scales=[sa, sb])
+                elif ax_a == 2 and ax_b == 2:  # both by columns: one launch up to 2048 rows
+                    m.int8mp_quantize_cols_batch([A, B], codes=m.INT8MP_CODES_F16, qs=[qa, qb],
+                                                 scales=[sa, sb])
                 else:
                     m.int8mp_quantize_rowwise(A, axis=ax_a, codes=m.INT8MP_CODES_F16, q=qa,
                                               scale=sa)

@@ -199,6 +199,25 @@ int8mp_status int8mp_quantize_rows_batch(const int8mp_rows_job* jobs, int njobs,
                                          void* stream);
 
 /*
+ * int8mp_quantize_cols_batch -- column groups with the codes in the input's
+ * layout (INT8MP_GROUP_COLS) of up to two matrices with the same number of
+ * columns, e.g. both K-first operands of A.T @ B.  The codes and scales are
+ * those of one int8mp_quantize_rowwise call with INT8MP_GROUP_COLS per job,
+ * with the mode, seed and codes given here and each job's own offset and
+ * stream_id.  When every job has at most 2048 rows the jobs share one
+ * launch; otherwise each job takes the passes of that call.
+ *   jobs    as for int8mp_quantize_rows_batch, with scale fp32 [cols] and
+ *           colmax NULL (INT8MP_ERR_INVALID_ARG otherwise).
+ *   njobs   1 .. INT8MP_MAX_ROWS_JOBS.
+ *   cols    the number of columns of every job.
+ * Requirements: every job those of int8mp_quantize_rowwise with
+ * INT8MP_GROUP_COLS; a job with rows == 0 is skipped.
+ */
+int8mp_status int8mp_quantize_cols_batch(const int8mp_rows_job* jobs, int njobs, int64_t cols,
+                                         int8mp_round mode, uint64_t seed, int8mp_codes codes,
+                                         void* stream);
+
+/*
  * int8mp_quantize_cols_absmax -- column groups with the codes in the input's
  * layout (as INT8MP_GROUP_COLS), given each column's absmax (fp32 [cols],
  * e.g. from int8mp_quantize_rows_colmax over the same x): scale[c] =

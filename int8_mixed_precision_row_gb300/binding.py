@@ -41,6 +41,7 @@ EXPORTED = (
     "int8mp_linear_fwd_save", "int8mp_linear_bwd_saved", "int8mp_mm_workspace_size",
     "int8mp_scaled_mm_ws", "int8mp_mm_s32_ws", "int8mp_quantize_rows_batch",
     "int8mp_scaled_mm_f32", "int8mp_round_bf16", "int8mp_debug_scaled_mm_quant_b",
+    "int8mp_quantize_cols_batch",
 )
 INT8MP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -136,6 +137,8 @@ def load(path=None):
                                           ctypes.POINTER(int8mp_linear_cfg), _P, _P, _SZ, _P]
     L.int8mp_quantize_rows_batch.argtypes = [ctypes.POINTER(int8mp_rows_job), _INT, _I64, _INT, _U64,
                                              _INT, _P]
+    L.int8mp_quantize_cols_batch.argtypes = [ctypes.POINTER(int8mp_rows_job), _INT, _I64, _INT, _U64,
+                                             _INT, _P]
     L.int8mp_mm_workspace_size.argtypes = []
     L.int8mp_mm_workspace_size.restype = _SZ
     L.int8mp_scaled_mm_ws.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _I64, _P,
@@ -145,7 +148,7 @@ def load(path=None):
                                        _SZ, _P]
     L.int8mp_round_bf16.argtypes = [_P, _P, _I64, _P]
     L.int8mp_debug_scaled_mm_quant_b.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P]
-    for name in ("int8mp_scaled_mm_ws", "int8mp_mm_s32_ws", "int8mp_scaled_mm_f32",
+    for name in ("int8mp_quantize_cols_batch", "int8mp_scaled_mm_ws", "int8mp_mm_s32_ws", "int8mp_scaled_mm_f32",
                  "int8mp_round_bf16", "int8mp_debug_scaled_mm_quant_b",
                  "int8mp_quantize_rowwise", "int8mp_scaled_mm", "int8mp_mm_s32",
                  "int8mp_linear_fwd", "int8mp_linear_bwd", "int8mp_poll_device_status",
@@ -268,6 +271,35 @@ def int8mp_quantize_rows_batch(xs, mode=INT8MP_RNE, seed=0, offsets=None, stream
         out.append((q, sc))
     _check(load().int8mp_quantize_rows_batch(arr, n, cols, int(mode), int(seed), int(codes),
                                              _stream(stream)), "int8mp_quantize_rows_batch")
+    return out
+
+
+def int8mp_quantize_cols_batch(xs, mode=INT8MP_RNE, seed=0, offsets=None, stream_ids=None,
+                               codes=INT8MP_CODES_S8, qs=None, scales=None, stream=None):
+    """Column groups (codes in x's layout) of up to two bf16 matrices with the
+    same number of columns, as one int8mp_quantize_rowwise(axis=
+    INT8MP_GROUP_COLS) call per matrix.  Returns the list of (codes, scale)."""
+    n = len(xs)
+    cols = xs[0].shape[1]
+    offsets = offsets or [0] * n
+    stream_ids = stream_ids or [0] * n
+    qs = qs or [None] * n
+    scales = scales or [None] * n
+    arr = (int8mp_rows_job * max(n, 1))()
+    out = []
+    for i, x in enumerate(xs):
+        assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_cuda and x.shape[1] == cols
+        rows = x.shape[0]
+        q = qs[i] if qs[i] is not None else torch.empty((rows, cols), dtype=_code_dtype(codes),
+                                                        device=x.device)
+        sc = scales[i] if scales[i] is not None else torch.empty((cols,), dtype=torch.float32,
+                                                                 device=x.device)
+        arr[i] = int8mp_rows_job(x.data_ptr(), rows, x.stride(0) if rows > 0 else cols,
+                                 int(offsets[i]), int(stream_ids[i]), q.data_ptr(), sc.data_ptr(),
+                                 None)
+        out.append((q, sc))
+    _check(load().int8mp_quantize_cols_batch(arr, n, cols, int(mode), int(seed), int(codes),
+                                             _stream(stream)), "int8mp_quantize_cols_batch")
     return out
 
 

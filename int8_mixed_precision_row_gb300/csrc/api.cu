@@ -285,6 +285,29 @@ int8mp_status int8mp_quantize_rows_batch(const int8mp_rows_job* jobs, int njobs,
                                                      as_stream(stream)));
 }
 
+int8mp_status int8mp_quantize_cols_batch(const int8mp_rows_job* jobs, int njobs, int64_t cols,
+                                         int8mp_round mode, uint64_t seed, int8mp_codes codes,
+                                         void* stream) {
+  if (!jobs || njobs < 1 || njobs > INT8MP_MAX_ROWS_JOBS) return INT8MP_ERR_INVALID_ARG;
+  int8mp::RowsJob run[INT8MP_MAX_ROWS_JOBS];
+  int nrun = 0;
+  for (int i = 0; i < njobs; ++i) {
+    const int8mp_rows_job& j = jobs[i];
+    int8mp_status st = check_quantize(j.x, j.rows, cols, j.ld, 2, mode, j.q, codes, j.scale);
+    if (st != INT8MP_OK) return st;
+    if (j.colmax != nullptr) return INT8MP_ERR_INVALID_ARG;
+    if (j.rows > 0 && cols > 0)
+      run[nrun++] = int8mp::RowsJob{j.x, j.rows, j.ld, j.q, j.scale, nullptr, j.offset,
+                                    j.stream_id};
+  }
+  if (nrun == 0) return INT8MP_OK;
+  DeviceInfo dev;
+  int8mp_status st = current_device(&dev, as_stream(stream));
+  if (st != INT8MP_OK) return st;
+  return from_cuda(int8mp::launch_quantize_cols_jobs(run, nrun, cols, mode, seed, codes, dev,
+                                                     as_stream(stream)));
+}
+
 int8mp_status int8mp_quantize_cols_absmax(const void* x, int64_t rows, int64_t cols, int64_t ld,
                                           const float* colmax, int8mp_round mode, uint64_t seed,
                                           uint64_t offset, uint32_t stream_id, void* q,

@@ -119,6 +119,12 @@ cudaError_t launch_quantize_cols(const void* x, int64_t rows, int64_t cols, int6
                                  int8mp_round mode, const SrArgs& sr, void* q,
                                  int8mp_codes codes, float* scale, bool transposed,
                                  const DeviceInfo& dev, cudaStream_t stream);
+// Column groups (codes in the input's layout) of up to kMaxRowsJobs matrices
+// with the same number of columns: one launch when every job has at most 2048
+// rows, else each job's own passes.  Job colmax is unused.
+cudaError_t launch_quantize_cols_jobs(const RowsJob* jobs, int njobs, int64_t cols,
+                                      int8mp_round mode, uint64_t seed, int8mp_codes codes,
+                                      const DeviceInfo& dev, cudaStream_t stream);
 
 // ---- GEMM (gemm.cu) ---------------------------------------------------------
 // kBf16Scaled: integer codes in f16 containers, out = bf16((acc * sA) * sB);

@@ -916,20 +916,42 @@ constexpr int kClRows = kThreads / kClVecs;         // rows per CTA and pass
 constexpr int kClMaxU = 8;                          // passes (16-byte loads) per thread
 constexpr int64_t kClMaxRows = static_cast<int64_t>(kClCtas) * kClRows * kClMaxU;  // 2048
 
+// One matrix of a launch of the kernel below (x bf16 [rows, cols], stride
+// ld; codes q [rows, cols]; scale [cols]; SR counters from offset on stream).
+struct ColsJob {
+  const uint16_t* x;
+  int64_t rows, ld;
+  void* q;
+  float* scale;
+  uint64_t offset;
+  PhiloxStream stream;
+};
+
+// Strips 0 .. split - 1 (blockIdx.x) belong to matrix j0, the rest to j1:
+// every CTA of a cluster shares blockIdx.x, so a cluster stays within one
+// matrix.
 template <typename CodeT, bool SR, int kU>
 __global__ void __cluster_dims__(1, kClCtas, 1) __launch_bounds__(kThreads)
-    quant_cols_cluster_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
-                              int64_t ld, float* __restrict__ scale, CodeT* __restrict__ q,
-                              SrArgs sr, unsigned int* status) {
+    quant_cols_cluster_kernel(ColsJob j0, ColsJob j1, int split, int64_t cols, PhiloxKeys keys,
+                              unsigned int* status) {
   using P = Pack8<CodeT>;
   __shared__ uint4 red[kThreads / 32][kClVecs];
   __shared__ uint4 part[kClVecs];  // this CTA's maxima of the strip's 64 columns
+  const bool second = static_cast<int>(blockIdx.x) >= split;
+  const uint16_t* __restrict__ x = second ? j1.x : j0.x;
+  const int64_t rows = second ? j1.rows : j0.rows;
+  const int64_t ld = second ? j1.ld : j0.ld;
+  CodeT* __restrict__ q = static_cast<CodeT*>(second ? j1.q : j0.q);
+  float* __restrict__ scale = second ? j1.scale : j0.scale;
+  const uint64_t offset = second ? j1.offset : j0.offset;
+  const PhiloxStream st = second ? j1.stream : j0.stream;
+  const int64_t strip = second ? blockIdx.x - split : blockIdx.x;
   ptx::grid_dependency_wait();  // the previous kernel in the stream is done
   ptx::allow_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int vec = threadIdx.x % kClVecs, rsub = threadIdx.x / kClVecs;
   const int64_t k = blockIdx.y;  // the CTA's rank in its cluster (grid y = kClCtas)
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * (8 * kClVecs) + 8 * vec;
+  const int64_t c = strip * (8 * kClVecs) + 8 * vec;
   // no thread leaves early: every one reaches the cluster barriers
   const bool col_ok =
       c + 8 <= cols && in_bounds(cols <= ld && rows <= static_cast<int64_t>(kClCtas) * kClRows * kU,
@@ -985,7 +1007,7 @@ __global__ void __cluster_dims__(1, kClCtas, 1) __launch_bounds__(kThreads)
   }
   // f16 stochastic codes are clamped as packed half2 after the conversion
   constexpr bool kHalfClamp = SR && std::is_same<CodeT, __half>::value;
-  const uint64_t n0 = sr.offset + static_cast<uint64_t>(c);  // SR counter of (row 0, column c)
+  const uint64_t n0 = offset + static_cast<uint64_t>(c);  // SR counter of (row 0, column c)
   auto put = [&](int64_t row, const float (&cd)[8]) {
     typename P::Vec out = P::pack(cd);
     if (kHalfClamp) out = clamp_half8(out);
@@ -998,14 +1020,14 @@ __global__ void __cluster_dims__(1, kClCtas, 1) __launch_bounds__(kThreads)
     if (!div8_each_try2(f, s, r, all_fast, v)) div8_each_ieee(f, s, v);
   };
   if (col_ok) {
-    if (SR && (sr.offset & 3u) == 0) {
+    if (SR && (offset & 3u) == 0) {
       // every group of eight starts a Philox block: two rows' blocks side by side
 #pragma unroll
       for (int u = 0; u < kU; u += 2) {
         const int64_t ra = row0 + u * pass_rows, rb = ra + pass_rows;
         if (ra < rows) {
           uint32_t wa[8], wb[8];
-          philox_words8x2(sr.keys, sr.stream, n0 + static_cast<uint64_t>(ra * cols),
+          philox_words8x2(keys, st, n0 + static_cast<uint64_t>(ra * cols),
                           n0 + static_cast<uint64_t>(rb * cols), wa, wb);
           float v[8], cd[8];
           divide(a[u], v);
@@ -1033,8 +1055,8 @@ __global__ void __cluster_dims__(1, kClCtas, 1) __launch_bounds__(kThreads)
               cd[2 * i + 1] = qv.y;
             }
           } else {
-            codes_of<SR, !kHalfClamp>(v, sr.keys, sr.stream,
-                                      n0 + static_cast<uint64_t>(row * cols), normal, cd);
+            codes_of<SR, !kHalfClamp>(v, keys, st, n0 + static_cast<uint64_t>(row * cols),
+                                      normal, cd);
           }
           put(row, cd);
         }
@@ -1438,6 +1460,25 @@ cudaError_t launch_cols_nat(const uint16_t* x, int64_t rows, int64_t cols, int64
                            scale_out, q, sr, dev.status_word);
 }
 
+// The cluster kernel over njobs (1 or 2) matrices of at most kClMaxRows rows
+// and `cols` columns each, in one launch.
+template <typename CodeT, bool SR>
+cudaError_t launch_cols_cluster(const ColsJob& j0, const ColsJob& j1, int njobs, int64_t cols,
+                                const PhiloxKeys& keys, const DeviceInfo& dev,
+                                cudaStream_t stream) {
+  const int64_t strips = (cols + 8 * kClVecs - 1) / (8 * kClVecs);
+  const dim3 grid(static_cast<unsigned>(strips * njobs), kClCtas);
+  const int64_t rows = njobs > 1 && j1.rows > j0.rows ? j1.rows : j0.rows;
+  const int64_t per_u = static_cast<int64_t>(kClCtas) * kClRows;  // 256 rows
+  const int split = static_cast<int>(strips);
+  return rows <= per_u * 4
+             ? launch_overlapped(quant_cols_cluster_kernel<CodeT, SR, 4>, grid, dim3(kThreads), 0,
+                                 stream, j0, j1, split, cols, keys, dev.status_word)
+             : launch_overlapped(quant_cols_cluster_kernel<CodeT, SR, kClMaxU>, grid,
+                                 dim3(kThreads), 0, stream, j0, j1, split, cols, keys,
+                                 dev.status_word);
+}
+
 template <typename CodeT, bool SR>
 cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
                           float* scale, bool transposed, const SrArgs& sr, const DeviceInfo& dev,
@@ -1447,16 +1488,8 @@ cudaError_t cols_dispatch(const void* x, int64_t rows, int64_t cols, int64_t ld,
     // up to 2048 rows: one launch, each column strip's rows held in the
     // registers of one cluster (at 4096 rows the three passes were faster:
     // 4096^2 operands 41 us instead of 37)
-    const dim3 grid(static_cast<unsigned>((cols + 8 * kClVecs - 1) / (8 * kClVecs)), kClCtas);
-    CodeT* qc = static_cast<CodeT*>(q);
-    const int64_t per_u = static_cast<int64_t>(kClCtas) * kClRows;  // 256 rows
-    const cudaError_t e =
-        rows <= per_u * 4
-            ? launch_overlapped(quant_cols_cluster_kernel<CodeT, SR, 4>, grid, dim3(kThreads), 0,
-                                stream, xp, rows, cols, ld, scale, qc, sr, dev.status_word)
-            : launch_overlapped(quant_cols_cluster_kernel<CodeT, SR, kClMaxU>, grid,
-                                dim3(kThreads), 0, stream, xp, rows, cols, ld, scale, qc, sr,
-                                dev.status_word);
+    const ColsJob j{xp, rows, ld, q, scale, sr.offset, sr.stream};
+    const cudaError_t e = launch_cols_cluster<CodeT, SR>(j, j, 1, cols, sr.keys, dev, stream);
     if (e == cudaSuccess) return e;
     // the cluster launch was refused (e.g. no eight-CTA cluster fits the
     // stream's SM partition): clear that error and take the passes, whose
@@ -1597,6 +1630,47 @@ cudaError_t launch_quantize_cols(const void* x, int64_t rows, int64_t cols, int6
              : cols_dispatch<int8_t, false>(x, rows, cols, ld, q, scale, t, sr, dev, stream);
   return s ? cols_dispatch<__half, true>(x, rows, cols, ld, q, scale, t, sr, dev, stream)
            : cols_dispatch<__half, false>(x, rows, cols, ld, q, scale, t, sr, dev, stream);
+}
+
+namespace {
+template <typename CodeT, bool SR>
+cudaError_t cols_jobs(const RowsJob* jobs, int njobs, int64_t cols, uint64_t seed,
+                      const DeviceInfo& dev, cudaStream_t stream) {
+  bool small = true;
+  for (int i = 0; i < njobs; ++i) small = small && jobs[i].rows <= kClMaxRows;
+  if (small) {
+    ColsJob cj[kMaxRowsJobs];
+    for (int i = 0; i < njobs; ++i) {
+      const RowsJob& j = jobs[i];
+      cj[i] = ColsJob{static_cast<const uint16_t*>(j.x), j.rows, j.ld, j.q, j.scale, j.offset,
+                      philox_stream(j.stream_id)};
+    }
+    const cudaError_t e = launch_cols_cluster<CodeT, SR>(cj[0], cj[njobs > 1 ? 1 : 0], njobs, cols,
+                                                         philox_keys(seed), dev, stream);
+    if (e == cudaSuccess) return e;
+    (void)cudaGetLastError();  // refused: the passes below
+  }
+  for (int i = 0; i < njobs; ++i) {
+    const RowsJob& j = jobs[i];
+    const cudaError_t e =
+        cols_dispatch<CodeT, SR>(j.x, j.rows, cols, j.ld, j.q, j.scale, false,
+                                 make_sr(seed, j.offset, j.stream_id), dev, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_quantize_cols_jobs(const RowsJob* jobs, int njobs, int64_t cols,
+                                      int8mp_round mode, uint64_t seed, int8mp_codes codes,
+                                      const DeviceInfo& dev, cudaStream_t stream) {
+  if (njobs < 1 || njobs > kMaxRowsJobs) return cudaErrorInvalidValue;
+  const bool s = mode == INT8MP_SR;
+  if (codes == INT8MP_CODES_S8)
+    return s ? cols_jobs<int8_t, true>(jobs, njobs, cols, seed, dev, stream)
+             : cols_jobs<int8_t, false>(jobs, njobs, cols, seed, dev, stream);
+  return s ? cols_jobs<__half, true>(jobs, njobs, cols, seed, dev, stream)
+           : cols_jobs<__half, false>(jobs, njobs, cols, seed, dev, stream);
 }
 
 }  // namespace int8mp

@@ -215,6 +215,33 @@ def test_rows_batch_matches_the_oracle_per_matrix(shapes, mode, codes, with_colm
             np.testing.assert_array_equal(_f32_bits(cms[i]), _col_absmax_bits(x), err_msg=str(i))
 
 
+# Two matrices' column groups in one launch (int8mp_quantize_cols_batch):
+# rows of each size class of the one-launch kernel (a different one per
+# matrix), ragged column strips, plain operands and edge rows; a pair with a
+# matrix over 2048 rows takes each matrix's passes.
+COLS_BATCH_SHAPES = [((1024, 1024), (1024, 1024)), ((77, 136), (2048, 136)),
+                     ((2048, 264), (9, 264)), ((3001, 64), (100, 64))]
+
+
+@pytest.mark.parametrize("codes", [m.INT8MP_CODES_S8, m.INT8MP_CODES_F16])
+@pytest.mark.parametrize("mode", [m.INT8MP_RNE, m.INT8MP_SR])
+@pytest.mark.parametrize("shapes", COLS_BATCH_SHAPES)
+def test_cols_batch_matches_the_oracle_per_matrix(shapes, mode, codes):
+    (r0, cols), (r1, _) = shapes
+    xs = [synth.bf16_normal((r0, cols), r0 + 7, outlier_frac=0.01, outlier_scale=20.0),
+          _edge_input(r1, cols, seed=r1 + 9)]
+    offs, sids, seed = [4, (1 << 33) + 1], [m.INT8MP_STREAM_GW_DY, m.INT8MP_STREAM_GW_X], 23
+    got = m.int8mp_quantize_cols_batch([_dev(x) for x in xs], mode=mode, seed=seed, offsets=offs,
+                                       stream_ids=sids, codes=codes)
+    assert m.int8mp_poll_device_status() == m.INT8MP_OK
+    for i, x in enumerate(xs):
+        q, sc = got[i]
+        qr, sr = oracle.quantize(bf16_bits(x), axis=1, mode=mode, seed=seed, offset=offs[i],
+                                 stream_id=sids[i])
+        np.testing.assert_array_equal(_f32_bits(sc), sr.view(np.int32), err_msg=str(i))
+        np.testing.assert_array_equal(_codes_np(q), np.ascontiguousarray(qr.T), err_msg=str(i))
+
+
 @pytest.mark.parametrize("mode", [m.INT8MP_RNE, m.INT8MP_SR])
 def test_columns_from_absmax_int8_codes(mode):
     rows, cols = 1000, 2056
