@@ -91,6 +91,27 @@ def test_absmax_entry_points_host_validation(lib):
                                        P(256), 1 << 20, None) == m.INT8MP_ERR_ALIGNMENT
 
 
+def test_cols_batch_host_validation(lib):
+    J = m.int8mp_rows_job
+
+    def run(*jobs, n=None, cols=8, mode=0, codes=1):
+        arr = (J * max(len(jobs), 1))(*jobs)
+        return lib.int8mp_quantize_cols_batch(arr if jobs else None, len(jobs) if n is None else n,
+                                              cols, mode, 0, codes, None)
+    plain = J(16, 8, 8, 0, 0, 16, 16, None)
+    assert run() == m.INT8MP_ERR_INVALID_ARG                               # no jobs
+    assert run(plain, n=0) == m.INT8MP_ERR_INVALID_ARG                     # njobs 0
+    assert run(plain, plain, plain) == m.INT8MP_ERR_INVALID_ARG            # more than two
+    assert run(J(16, 8, 8, 0, 1, 16, 16, 16)) == m.INT8MP_ERR_INVALID_ARG  # colmax given
+    assert run(plain, mode=3) == m.INT8MP_ERR_INVALID_ARG
+    assert run(plain, codes=4) == m.INT8MP_ERR_INVALID_ARG
+    assert run(J(24, 8, 8, 0, 0, 16, 16, None)) == m.INT8MP_ERR_ALIGNMENT  # x misaligned
+    assert run(J(16, 8, 8, 0, 0, 24, 16, None)) == m.INT8MP_ERR_ALIGNMENT  # q misaligned
+    assert run(plain, cols=12) == m.INT8MP_ERR_INVALID_ARG                 # ld < cols
+    assert run(J(16, 8, 16, 0, 0, 16, 16, None), cols=12) == m.INT8MP_ERR_ALIGNMENT  # cols % 8
+    assert run(J(16, 0, 8, 0, 0, 16, 16, None)) == m.INT8MP_OK             # empty: nothing launched
+
+
 def test_rows_batch_host_validation(lib):
     J = m.int8mp_rows_job
 
