@@ -806,9 +806,11 @@ __global__ void __launch_bounds__(kThreads, SR ? 2 : 3) quant_cols_nat_kernel(
           div8_each_ieee(f, s, v);
       };
       uint4 cur0 = ld_at(xp, row0), cur1 = ld_at(xp + xstep, row0 + 8);
+      uint4 nxt0 = ld_at(xp + 2 * xstep, row0 + 16), nxt1 = ld_at(xp + 3 * xstep, row0 + 24);
 #pragma unroll 2
       for (int64_t rr = row0; rr < r1; rr += 16) {
-        const uint4 nxt0 = ld_at(xp + 2 * xstep, rr + 16), nxt1 = ld_at(xp + 3 * xstep, rr + 24);
+        // the loads of the pair after next: two pairs of rows in flight
+        const uint4 nn0 = ld_at(xp + 4 * xstep, rr + 32), nn1 = ld_at(xp + 5 * xstep, rr + 40);
         uint32_t w_a[8], w_b[8];
         philox_words8x2(sr.keys, sr.stream, n, n + nstep, w_a, w_b);
         float f[8], v[8], cd[8];
@@ -824,6 +826,8 @@ __global__ void __launch_bounds__(kThreads, SR ? 2 : 3) quant_cols_nat_kernel(
         }
         cur0 = nxt0;
         cur1 = nxt1;
+        nxt0 = nn0;
+        nxt1 = nn1;
         xp += 2 * xstep;
         qp += 2 * qstep;
         n += 2 * nstep;
