@@ -1,7 +1,7 @@
 """The bounds-checked build (-DINT8MP_CHECK): every global index the kernels
 compute is checked against its buffer before the access.  Run the paths of
 the library through it -- row and column quantization in every variant, the
-column maxima, two matrices' rows in one launch, the GEMM in three layouts
+column maxima, two matrices' rows (and column groups) in one launch, the GEMM in three layouts
 with and without the split last wave (f16 containers and int8 codes), the
 linear layer in INT8 and in BF16 -- on ragged sizes: no
 check may fail, and every result must equal the ordinary build's bit for
@@ -44,6 +44,8 @@ def _codes_and_gemms():
                 for pair in m.int8mp_quantize_rows_batch([x, x2], **bkw):
                     out += list(pair)
                 for pair in m.int8mp_quantize_rows_batch([x, x2], colmaxes=cms, **bkw):
+                    out += list(pair)
+                for pair in m.int8mp_quantize_cols_batch([x, x2], **bkw):
                     out += list(pair)
                 out += cms
     g = torch.Generator().manual_seed(9)
