@@ -113,6 +113,28 @@ def test_fuzz_rows_batch(case):
             np.testing.assert_array_equal(_f32_bits(cms[i]), _col_absmax_bits(x))
 
 
+@pytest.mark.parametrize("case", range(CASES))
+def test_fuzz_cols_batch(case):
+    # two matrices' column groups in one call: one launch when both have at
+    # most 2048 rows (most cases here), each matrix's passes otherwise
+    g = _rng(70 + case)
+    cols = 8 * int(g.integers(1, 400))
+    r0, r1 = int(g.integers(1, 2600)), int(g.integers(1, 2100))
+    mode, codes = int(g.integers(0, 2)), int(g.integers(0, 2))
+    seed = int(g.integers(0, 1 << 40))
+    offs = [int(g.integers(0, 1 << 34)), int(g.integers(0, 1 << 34))]
+    sids = [int(g.integers(0, 6)), int(g.integers(0, 6))]
+    xs = [_input(r0, cols, 13 * case + 4), _input(r1, cols, 13 * case + 5)]
+    got = m.int8mp_quantize_cols_batch([x.to(DEV) for x in xs], mode=mode, seed=seed,
+                                       offsets=offs, stream_ids=sids, codes=codes)
+    assert m.int8mp_poll_device_status() == m.INT8MP_OK
+    for i, x in enumerate(xs):
+        qr, sr = oracle.quantize(bf16_bits(x), axis=1, mode=mode, seed=seed, offset=offs[i],
+                                 stream_id=sids[i])
+        np.testing.assert_array_equal(_f32_bits(got[i][1]), sr.view(np.int32))
+        np.testing.assert_array_equal(_codes_np(got[i][0]), np.ascontiguousarray(qr.T))
+
+
 def _rand_codes(shape, g):
     return torch.from_numpy(g.integers(-127, 128, size=shape).astype(np.int8))
 
