@@ -988,7 +988,7 @@ def main():
         "clocks": clk.summary(),
     }
     if not args.profile_steps:
-        e2e_steps = max(3, min(args.steps, 30))
+        e2e_steps = max(3, min(args.steps, 10))
         with ClockSampler(local) as eclk:
             e2e_ms, h2d, d2h, link_gbs, copy_gbs, host_ms = time_e2e(step, e2e_steps, 1)
         e2e_ms = max_over_ranks(e2e_ms, world, device)
